@@ -1,0 +1,443 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused ZeRO/FSDP sharded optimizer step on GB300.
+
+Default workload: N_d = 8 emulated data-parallel ranks on one GPU, the flat
+buffer of GPT-2-small's tensor shapes (124,439,808 parameters padded to
+124,440,064), seeded synthetic bf16 gradients ~N(0, 1e-3) and fp32 master
+weights ~N(0, 0.02).  One step = one pass of the fused reduce-scatter + AdamW +
+bf16 all-gather over the whole buffer (ZeRO-1: one launch); the ZeRO-2 step
+(25 MiB buckets, one launch per bucket, the same bits) is timed beside it.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+                    [--workload NAME]
+
+Prints one JSON line.  `value` is parameters updated per second over all GPUs
+with inputs resident in HBM; `e2e` is the same metric through the C ABI with
+the gradients copied from pinned host memory and the new bf16 weights copied
+back inside the timed region.  With --gpus N > 1 (torchrun) every rank runs an
+independent replica of the workload on its own GPU ("replicas only": the
+emulated ranks live in one GPU's HBM and the path has no inter-GPU exchange).
+`--impl reference` times the CPU oracle on a bounded sample of the same
+workload on the host cores.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused ZeRO step params/s & HBM GB/s vs GB300 peak (N_d=8, 1 GPU)"
+HP = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
+SIGMA_W, SIGMA_G = 0.02, 1e-3
+BUCKET_25MIB = 25 * 2**20 // 2  # bf16 elements in a 25 MiB gradient bucket
+L2_BYTES = 129e6
+
+WORKLOADS = {
+    # name: (unit sizes, N_d, description)
+    "gpt2-small-flat-n8": ([124_439_808], 8,
+                           "GPT-2-small tensor shapes (12 layers, d=768, ffn 3072, vocab 50257, "
+                           "ctx 1024) as one flat buffer padded to N_d*64"),
+    "flat-2p20-n2": ([2**20], 2, "flat P=2^20, N_d=2"),
+    "llama-1.1b-zero3-n8": ([44_044_288] * 22 + [131_074_048], 8,
+                            "Llama-shaped 1.1B (22 blocks d=2048 ffn 5632 32/4 heads, vocab 32000), "
+                            "one FSDP unit per block + root"),
+    "llama-7b-zero3-n8": ([202_383_360] * 32 + [262_148_096], 8,
+                          "Llama-7B shapes (32 blocks d=4096 ffn 11008, vocab 32000), one FSDP unit "
+                          "per block + root"),
+}
+DEFAULT_WORKLOAD = "gpt2-small-flat-n8"
+FUSED_SOURCES = ["fsdp_sharded_optimizer_gb300/csrc/fused_step.cu",
+                 "fsdp_sharded_optimizer_gb300/csrc/device.cuh"]
+
+
+def parse():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--e2e-steps", type=int, default=None,
+                    help="steps of the end-to-end (host buffers) measurement; default min(K, 50)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ environment
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "of measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "of fallback"
+
+
+def fused_source_sha():
+    h = hashlib.sha256()
+    for rel in FUSED_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload):
+    """DRAM bytes per launch of the fused kernel from the committed ncu summary,
+    if it was taken on this kernel source and workload; else None."""
+    path = os.path.join(ROOT, "profiles", "fused_step_traffic.txt")
+    try:
+        rows = [dict(kv.split("=", 1) for kv in line.split())
+                for line in open(path) if line.strip() and not line.startswith("#")]
+    except OSError:
+        return None
+    sha = fused_source_sha()
+    for r in rows:
+        if r.get("source_sha") == sha and r.get("workload") == workload:
+            return float(r["dram_bytes_per_launch"])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_uuid):
+        self.proc = None
+        try:
+            cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                   "-lms", "50"]
+            if device_uuid:
+                cmd += ["-i", device_uuid]
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                smax.append(float(f[1]))
+                power.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, f[4:8]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "power_w_max": max(power), "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ GPU arm
+class Zero12State:
+    """Device buffers of one emulated N_d-rank ZeRO-1/2 job."""
+
+    def __init__(self, Z, torch, unit_sizes, N, dev):
+        self.Z, self.torch = Z, torch
+        P = sum(unit_sizes)
+        (self.unit,), _ = Z.zero_layout([P], N)
+        u = self.unit
+        self.P, self.N, self.S = P, N, u.shard_len
+        self.grads = torch.empty((N, u.n_padded), dtype=torch.int16, device=dev)
+        self.master = torch.empty((N, u.shard_len), dtype=torch.float32, device=dev)
+        self.m = torch.zeros_like(self.master)
+        self.v = torch.zeros_like(self.master)
+        self.params = torch.empty(u.n_padded, dtype=torch.int16, device=dev)
+        Z.zero_gen_master(0, SIGMA_W, [u], self.master)
+        Z.zero_gen_grads_unit(0, 1, SIGMA_G, 0, u, self.grads)
+        self.t = 0
+
+    def step(self, stage, bucket=0, stream=None):
+        self.t += 1
+        self.Z.zero_step_stage12(stage, self.grads, self.master, self.m, self.v, self.params,
+                                 self.Z.hparams(**HP, step=self.t), bucket, stream=stream)
+
+
+def barrier_sync(torch, world):
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+
+
+def max_over_ranks(torch, world, x, dev):
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def timed(torch, world, dev, stream, fn, K, per_launch=False):
+    """Time exactly K calls of fn on `stream` with CUDA events; returns (total ms,
+    mean per-call ms from per-call event pairs or None)."""
+    barrier_sync(torch, world)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    pairs = []
+    start.record(stream)
+    for i in range(K):
+        if per_launch:
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            pairs.append((a, b))
+        else:
+            fn()
+    end.record(stream)
+    end.synchronize()
+    barrier_sync(torch, world)
+    total = start.elapsed_time(end)
+    mean = statistics.fmean(a.elapsed_time(b) for a, b in pairs) if pairs else None
+    return max_over_ranks(torch, world, total, dev), mean
+
+
+def run_gpu(args):
+    import torch
+
+    import fsdp_sharded_optimizer_gb300 as Z
+
+    world, rank, local = dist_env()
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    units, N, desc = WORKLOADS[args.workload]
+    if len(units) > 1:
+        return run_gpu_zero3(args, torch, Z, world, rank, dev)
+    K, W = args.steps, args.warmup
+    st = Zero12State(Z, torch, units, N, dev)
+    stream = torch.cuda.current_stream(dev)
+    P, Pp = st.P, st.unit.n_padded
+    bytes_per_step = (26 + 2 * N) * Pp  # the fused step's algorithmic HBM bytes
+
+    for _ in range(W):
+        st.step(1)
+        st.step(2, BUCKET_25MIB)
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    clocks = ClockSampler(uuid)
+    # headline: ZeRO-1, one fused launch per step, per-launch events for the roofline
+    ms1, launch_ms = timed(torch, world, dev, stream, lambda: st.step(1), K, per_launch=True)
+    clk = clocks.stop()
+    # ZeRO-2: 25 MiB buckets, one launch per bucket, identical results
+    ms2, _ = timed(torch, world, dev, stream, lambda: st.step(2, BUCKET_25MIB), K)
+    n_buckets = -(-Pp // BUCKET_25MIB)
+
+    # end to end through the C ABI with host buffers: H2D gradients, step, D2H weights
+    E = args.e2e_steps or min(K, 50)
+    host_g = torch.empty((N, Pp), dtype=torch.int16, pin_memory=True)
+    host_g.copy_(st.grads)
+    host_p = torch.empty(Pp, dtype=torch.int16, pin_memory=True)
+
+    def e2e_step():
+        st.grads.copy_(host_g, non_blocking=True)
+        st.step(1)
+        host_p.copy_(st.params, non_blocking=True)
+
+    for _ in range(min(W, 3)):
+        e2e_step()
+    ms_e2e, _ = timed(torch, world, dev, stream, e2e_step, E)
+
+    peak, peak_kind = measured_peak()
+    per_step_ms = ms1 / K
+    achieved = bytes_per_step / (launch_ms * 1e-3) / 1e9
+    traffic = ncu_traffic(args.workload)
+    result = {
+        "metric": METRIC,
+        "value": world * P * K / (ms1 * 1e-3),
+        "unit": "params/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": per_step_ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded SplitMix64 inputs; bf16 grads ~N(0,1e-3), fp32 master ~N(0,0.02))",
+        "config": {
+            "workload": args.workload, "description": desc, "N_d": N, "params": P,
+            "n_padded": Pp, "shard_len": st.S, "stage": 1, "storage":
+            "bf16 grads and weights, fp32 master/m/v", "parallelism": "replicas" if world > 1 else
+            "emulated dp%d on 1 GPU" % N,
+            "l2": "no flush: %.2f GB touched per step vs 129 MB L2" % (bytes_per_step / 1e9),
+            "hbm_bytes_per_step": bytes_per_step,
+        },
+        "hbm_gbs": bytes_per_step * K / (ms1 * 1e-3) / 1e9,
+        "roofline": {
+            "bound": "hbm", "kernel": "fused_step_kernel", "achieved": achieved, "peak": peak,
+            "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind,
+            "frac_of_8tbs_nominal": achieved / 8000.0,
+            "bytes_per_launch": bytes_per_step, "launch_ms": launch_ms,
+            "traffic": traffic,
+        },
+        "zero2": {
+            "ms_per_step": ms2 / K, "value": world * P * K / (ms2 * 1e-3),
+            "launches_per_step": n_buckets, "bucket_elems": BUCKET_25MIB,
+            "hbm_gbs": bytes_per_step * K / (ms2 * 1e-3) / 1e9,
+        },
+        "e2e": {
+            "value": world * P * E / (ms_e2e * 1e-3), "unit": "params/s", "steps": E,
+            "ms_per_step": ms_e2e / E,
+            "h2d_bytes_per_step": N * Pp * 2, "d2h_bytes_per_step": Pp * 2,
+        },
+        "clocks": clk,
+        "gpu_launches": K,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(args.workload, steps=20)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return result if rank == 0 else None
+
+
+def run_gpu_zero3(args, torch, Z, world, rank, dev):
+    from fsdp_sharded_optimizer_gb300.zero3 import CudaBackend, Zero3Schedule
+
+    unit_sizes, N, desc = WORKLOADS[args.workload]
+    K, W = args.steps, args.warmup
+    units, total = Z.zero_layout(unit_sizes, N)
+    P = sum(unit_sizes)
+    shard_total = total // N
+    max_unit = max(u.n_padded for u in units)
+    master = torch.empty((N, shard_total), dtype=torch.float32, device=dev)
+    m = torch.zeros_like(master)
+    v = torch.zeros_like(master)
+    shards = torch.empty((N, shard_total), dtype=torch.int16, device=dev)
+    grads = torch.empty((N, max_unit), dtype=torch.int16, device=dev)
+    full = [torch.empty(max_unit, dtype=torch.int16, device=dev) for _ in range(2)]
+    Z.zero_gen_master(0, SIGMA_W, units, master)
+    for k in range(N):
+        Z.zero_cast_bf16(master[k], shards[k])
+    be = CudaBackend(N, shards, master, m, v, device=dev)
+    sched = Zero3Schedule(units, be, full, [grads[k] for k in range(N)])
+    regen = []
+    t = [0]
+
+    def make_grads(ui, unit, gviews, stream):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        Z.zero_gen_grads_unit(0, t[0], SIGMA_G, 0, unit, gviews, stream=stream)
+        b.record(stream)
+        regen.append((a, b))
+
+    def step():
+        t[0] += 1
+        sched.step(Z.hparams(**HP, step=t[0]), make_grads)
+
+    for _ in range(W):
+        step()
+    regen.clear()
+    stream = be.main
+    ms, _ = timed(torch, world, dev, stream, step, K)
+    regen_ms = sum(a.elapsed_time(b) for a, b in regen) / K
+    fused_bytes = (26 + 2 * N) * total
+    gather_bytes = 2 * 4 * total
+    return {
+        "metric": METRIC, "value": world * P * K / (ms * 1e-3), "unit": "params/s",
+        "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": ms / K,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded SplitMix64 inputs)",
+        "config": {"workload": args.workload, "description": desc, "N_d": N, "params": P,
+                   "n_padded": total, "units": len(units), "stage": 3,
+                   "l2": "no flush: unit buffers exceed the 129 MB L2"},
+        "step_breakdown": {"regen_ms_per_step (harness, on the main stream)": regen_ms,
+                           "fused_bytes": fused_bytes, "gather_bytes": gather_bytes,
+                           "hbm_gbs_excl_regen": (fused_bytes + gather_bytes) /
+                           ((ms / K - regen_ms) * 1e-3) / 1e9},
+        "gpu_launches": K * len(units) * 4,
+    } if rank == 0 else None
+
+
+# ------------------------------------------------------------------ CPU oracle
+def cpu_baseline(workload, steps, sample_params=2**22):
+    """The oracle as it stands, single-threaded, on the first `sample_params`
+    parameters of the workload (same generator, same N_d), timed over `steps`
+    fused steps after the inputs are generated."""
+    import numpy as np
+
+    import oracle as orc
+
+    unit_sizes, N, _ = WORKLOADS[workload]
+    P = min(sample_params, sum(unit_sizes))
+    (u,), _ = orc.layout([P], N)
+    w = orc.gen_master(0, SIGMA_W, [u], N)
+    m, v = np.zeros_like(w), np.zeros_like(w)
+    p = np.zeros(u.n_padded, np.uint16)
+    g = orc.gen_grads_unit(0, 1, SIGMA_G, 0, u, N)
+    t0 = time.perf_counter()
+    for t in range(1, steps + 1):
+        orc.zero12_step(1, g, w, m, v, p, orc.hparams(**HP, step=t))
+    dt = time.perf_counter() - t0
+    return {"value": P * steps / dt, "unit": "params/s", "cores": 1, "kind": "oracle",
+            "sample": "first %d params of %s, N_d=%d, %d ZeRO-1 steps, inputs pre-generated"
+                      % (P, workload, N, steps), "seconds": dt}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    _, N, _ = WORKLOADS[args.workload]
+    per_step_params = 2**20
+    cb_w = cpu_baseline(args.workload, steps=max(1, args.warmup), sample_params=per_step_params)
+    cb = cpu_baseline(args.workload, steps=args.steps, sample_params=per_step_params)
+    value = cb["value"]
+    return {
+        "metric": METRIC, "value": value, "unit": "params/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * cb["seconds"] / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": args.workload, "N_d": N,
+                   "note": "the CPU oracle, one host core, each step a %d-parameter sample"
+                           % per_step_params},
+        "cpu_baseline": {"value": value, "unit": "params/s", "cores": 1, "kind": "oracle",
+                         "sample": cb["sample"]},
+        "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "warmup_seconds": cb_w["seconds"],
+    }
+
+
+def main():
+    args = parse()
+    res = run_reference(args) if args.impl == "reference" else run_gpu(args)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,17 @@
+"""GB300-native fused ZeRO/FSDP sharded optimizer step.
+
+The N_d data-parallel ranks of a job are emulated as separate buffers on one
+GPU; one CUDA kernel reduce-scatters their bf16 gradients (fixed-order fp32
+mean), applies AdamW to each owner's fp32 shard and writes the new bf16
+weights (the all-gather).  ZeRO-3 adds the per-unit gather and the per-unit
+reduce-scatter, scheduled with next-unit prefetch on a side stream
+(``zero3.Zero3Schedule``).
+
+The public calls carry the C ABI's names (include/zero.h); see ``_binding``.
+"""
+from ._binding import (ZERO_DEFAULT_ALIGN, ZERO_EALIGN, ZERO_ECUDA, ZERO_EINVAL,  # noqa: F401
+                       ZERO_ETIMEOUT, ZERO_MAX_RANKS, ZERO_OK, LIB_PATH, ZeroError, hparams,
+                       strerror, zero3_gather_unit, zero3_reduce_scatter_unit, zero_bytes_t,
+                       zero_cast_bf16, zero_gen_grads_unit, zero_gen_master, zero_hparams_t,
+                       zero_layout, zero_state_bytes, zero_step_stage12, zero_stream_wait,
+                       zero_unit_t)

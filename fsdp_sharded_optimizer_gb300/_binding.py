@@ -1,0 +1,197 @@
+"""Thin ctypes binding of ``libzero.so`` (the C ABI declared in include/zero.h).
+
+Argument marshalling only: torch tensors become device pointers and host
+pointer tables, the caller's current torch stream becomes the ``cudaStream_t``,
+and a negative return code becomes an exception.  Every step of the path runs
+in the library's CUDA kernels; there is no CPU or PyTorch fallback, and
+importing this module fails loudly if the library is missing.
+
+Per-rank buffers may be given as a list of tensors (one per rank) or as the
+rows of one 2-D tensor (row k = rank k).  bf16 buffers may be ``torch.bfloat16``
+or ``torch.int16``/``torch.uint16`` bit patterns.
+"""
+import ctypes as C
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libzero.so")
+
+ZERO_OK, ZERO_EINVAL, ZERO_EALIGN, ZERO_ECUDA, ZERO_ETIMEOUT = 0, -1, -2, -3, -4
+ZERO_MAX_RANKS = 64
+ZERO_DEFAULT_ALIGN = 64
+
+
+class ZeroError(RuntimeError):
+    """A negative return code of the C ABI."""
+
+    def __init__(self, fn, code):
+        self.code = code
+        super().__init__("%s failed: %s (%d)" % (fn, strerror(code), code))
+
+
+class zero_hparams_t(C.Structure):
+    _fields_ = [("lr", C.c_double), ("beta1", C.c_double), ("beta2", C.c_double),
+                ("eps", C.c_double), ("weight_decay", C.c_double), ("step", C.c_int64)]
+
+
+class zero_unit_t(C.Structure):
+    _fields_ = [(n, C.c_int64) for n in ("n_params", "n_padded", "shard_len", "offset",
+                                         "shard_offset", "param_offset", "pad")]
+
+    def as_dict(self):
+        return {n: getattr(self, n) for n, _ in self._fields_}
+
+    def __repr__(self):
+        return "zero_unit_t(%s)" % ", ".join("%s=%d" % kv for kv in self.as_dict().items())
+
+
+class zero_bytes_t(C.Structure):
+    _fields_ = [(n, C.c_double) for n in ("weight_bytes", "grad_bytes", "optim_bytes",
+                                          "state_bytes", "comm_volume", "comm_sent_elems",
+                                          "comm_sent_bytes", "hbm_bytes")]
+
+    def as_dict(self):
+        return {n: getattr(self, n) for n, _ in self._fields_}
+
+
+# name -> (restype, argtypes); the same names as include/zero.h
+_P, _I32, _I64, _U64, _F64 = C.c_void_p, C.c_int32, C.c_int64, C.c_uint64, C.c_double
+SIGNATURES = {
+    "zero_layout": (C.c_int, [_P, _I32, _I32, _I32, _P, _P]),
+    "zero_step_stage12": (C.c_int, [_I32, _I32, _I64, _P, _P, _P, _P, _P, _P, _I64, _P]),
+    "zero3_gather_unit": (C.c_int, [_P, _I32, _P, _P, _P]),
+    "zero3_reduce_scatter_unit": (C.c_int, [_P, _I32, _P, _P, _P, _P, _P, _P, _P]),
+    "zero_state_bytes": (C.c_int, [_I64, _I32, _I32, _I32, _P]),
+    "zero_gen_grads_unit": (C.c_int, [_U64, _I64, _F64, _I32, _P, _I32, _P, _P]),
+    "zero_gen_master": (C.c_int, [_U64, _F64, _P, _I32, _I32, _P, _P]),
+    "zero_cast_bf16": (C.c_int, [_P, _P, _I64, _P]),
+    "zero_stream_wait": (C.c_int, [_P, _I64]),
+    "zero_strerror": (C.c_char_p, [C.c_int]),
+}
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            "libzero.so is not built (%s). Run __graft_entry__.build() or "
+            "python -m fsdp_sharded_optimizer_gb300.build; there is no fallback path." % LIB_PATH)
+    lib = C.CDLL(LIB_PATH)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+lib = _load()
+
+
+def strerror(code):
+    return lib.zero_strerror(code).decode()
+
+
+def _check(fn, rc):
+    if rc != ZERO_OK:
+        raise ZeroError(fn, rc)
+
+
+def _rows(x, dtype_bytes, what):
+    """A host table of device pointers from a list of tensors or a 2-D tensor."""
+    rows = list(x) if isinstance(x, (list, tuple)) else [x[i] for i in range(x.shape[0])]
+    for t in rows:
+        if not t.is_cuda:
+            raise ValueError("%s must live on a CUDA device" % what)
+        if t.element_size() != dtype_bytes:
+            raise ValueError("%s: expected %d-byte elements, got %s" % (what, dtype_bytes, t.dtype))
+        if not t.is_contiguous():
+            raise ValueError("%s must be contiguous" % what)
+    return (C.c_void_p * len(rows))(*[t.data_ptr() for t in rows]), rows
+
+
+def _dev(t, dtype_bytes, what):
+    if not t.is_cuda or t.element_size() != dtype_bytes or not t.is_contiguous():
+        raise ValueError("%s must be a contiguous CUDA tensor of %d-byte elements" % (what, dtype_bytes))
+    return C.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return C.c_void_p(s.cuda_stream)
+
+
+def hparams(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01, step=1):
+    return zero_hparams_t(lr, beta1, beta2, eps, weight_decay, step)
+
+
+# ------------------------------------------------------------------ host calls
+def zero_layout(unit_sizes, n_ranks, align_elems=ZERO_DEFAULT_ALIGN):
+    """Layout of each unit and the total padded length (host only)."""
+    sizes = (C.c_int64 * len(unit_sizes))(*[int(s) for s in unit_sizes])
+    units = (zero_unit_t * len(unit_sizes))()
+    total = C.c_int64()
+    _check("zero_layout", lib.zero_layout(sizes, len(unit_sizes), n_ranks, align_elems, units,
+                                          C.byref(total)))
+    return list(units), total.value
+
+
+def zero_state_bytes(n_params, n_ranks, stage, K=12):
+    out = zero_bytes_t()
+    _check("zero_state_bytes", lib.zero_state_bytes(int(n_params), n_ranks, stage, K, C.byref(out)))
+    return out.as_dict()
+
+
+def zero_stream_wait(stream=None, timeout_ms=10_000):
+    """Wait for the stream with a wall-clock limit; raises ZeroError(ZERO_ETIMEOUT)."""
+    _check("zero_stream_wait", lib.zero_stream_wait(_stream(stream), int(timeout_ms)))
+
+
+# ------------------------------------------------------------------ device calls
+def zero_step_stage12(stage, grads, master, m, v, params_bf16, hp, bucket_elems=0, stream=None):
+    """The fused ZeRO-1/2 step: grads (N x P' bf16), master/m/v (N x S fp32),
+    params_bf16 (P' bf16), all on the device."""
+    g, grows = _rows(grads, 2, "grads")
+    w, wrows = _rows(master, 4, "master")
+    mm, _ = _rows(m, 4, "m")
+    vv, _ = _rows(v, 4, "v")
+    n_padded = grows[0].numel()
+    _check("zero_step_stage12", lib.zero_step_stage12(
+        stage, len(grows), n_padded, g, w, mm, vv, _dev(params_bf16, 2, "params_bf16"),
+        C.byref(hp), int(bucket_elems), _stream(stream)))
+
+
+def zero3_gather_unit(unit, shard_bf16, full_unit, stream=None):
+    s, rows = _rows(shard_bf16, 2, "shard_bf16")
+    _check("zero3_gather_unit", lib.zero3_gather_unit(
+        C.byref(unit), len(rows), s, _dev(full_unit, 2, "full_unit"), _stream(stream)))
+
+
+def zero3_reduce_scatter_unit(unit, unit_grads, master, m, v, shard_bf16, hp, stream=None):
+    g, grows = _rows(unit_grads, 2, "unit_grads")
+    w, _ = _rows(master, 4, "master")
+    mm, _ = _rows(m, 4, "m")
+    vv, _ = _rows(v, 4, "v")
+    s, _ = _rows(shard_bf16, 2, "shard_bf16")
+    _check("zero3_reduce_scatter_unit", lib.zero3_reduce_scatter_unit(
+        C.byref(unit), len(grows), g, w, mm, vv, s, C.byref(hp), _stream(stream)))
+
+
+# ------------------------------------------------------------------ harness calls
+def zero_gen_grads_unit(seed, step, sigma, outliers, unit, unit_grads, stream=None):
+    g, rows = _rows(unit_grads, 2, "unit_grads")
+    _check("zero_gen_grads_unit", lib.zero_gen_grads_unit(
+        int(seed), int(step), float(sigma), int(outliers), C.byref(unit), len(rows), g,
+        _stream(stream)))
+
+
+def zero_gen_master(seed, sigma, units, master, stream=None):
+    w, rows = _rows(master, 4, "master")
+    arr = (zero_unit_t * len(units))(*units)
+    _check("zero_gen_master", lib.zero_gen_master(
+        int(seed), float(sigma), arr, len(units), len(rows), w, _stream(stream)))
+
+
+def zero_cast_bf16(src, dst, stream=None):
+    _check("zero_cast_bf16", lib.zero_cast_bf16(
+        _dev(src, 4, "src"), _dev(dst, 2, "dst"), src.numel(), _stream(stream)))

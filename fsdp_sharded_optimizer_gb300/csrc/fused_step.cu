@@ -1,0 +1,222 @@
+// fused_step.cu -- the fused reduce-scatter + AdamW + bf16 all-gather kernel
+// and its two entry points, zero_step_stage12 and zero3_reduce_scatter_unit.
+//
+// Method ("Data parallelism, ZeRO and FSDP", lesson 8): "The communication is
+// already there" puts the optimizer step between the two halves of the
+// all-reduce; the Theorem's proof steps 2, 3 and 6 (ZeRO-1/2) and 7 (ZeRO-3);
+// the AdamW update of "5. In code", first block.
+//
+// One pass over HBM per element: read the N_d bf16 gradients and the owner's
+// fp32 master/m/v, write master/m/v and one bf16 weight -- 26 + 2*N_d bytes
+// per parameter.  The reduce-scatter is the owner's in-register fp32 sum in
+// rank order; the all-gather is the bf16 store.  The path is bound by HBM
+// bandwidth (about 0.5 flop per byte), so the kernel is a persistent
+// grid-stride stream of 16-byte vector accesses: each thread handles 8
+// consecutive elements (one 16-byte bf16 vector per rank, two 16-byte fp32
+// vectors per state array) and keeps all of a batch's loads in flight before
+// it sums.  No tensor cores: this is not a contraction.
+#include "device.cuh"
+#include "zero_internal.h"
+
+namespace zero {
+namespace {
+
+constexpr int kBlock = 256;
+constexpr int kRankBatch = 8; // gradient loads issued together before summing
+
+// Per-rank device pointers, passed by value in the kernel's parameter space
+// (5 x 64 x 8 B = 2.5 KB).  o[k] points at rank k's output slice: the
+// replicated buffer at k*S for ZeRO-1/2, the rank's shard for ZeRO-3.
+struct Tables {
+    const uint4* g[ZERO_MAX_RANKS];
+    float4* w[ZERO_MAX_RANKS];
+    float4* m[ZERO_MAX_RANKS];
+    float4* v[ZERO_MAX_RANKS];
+    uint4* o[ZERO_MAX_RANKS];
+};
+
+// The vectors [q0, q1) this launch covers (a vector = 8 elements), the shard
+// length in vectors, and the grid stride split into whole shards + remainder.
+struct Range {
+    int64_t q0, q1;
+    int64_t shard_vec;
+    int64_t step_k, step_j;
+    int32_t n_ranks;
+};
+
+__device__ __forceinline__ void adamw(float g, float& w, float& m, float& v,
+                                      const StepScalars& s)
+{
+    // The page's operand order; each operation is one rounded fp32 op.
+    const float m1 = __fadd_rn(__fmul_rn(s.b1, m), __fmul_rn(s.omb1, g));
+    const float v1 = __fadd_rn(__fmul_rn(s.b2, v), __fmul_rn(__fmul_rn(s.omb2, g), g));
+    const float mh = __fdiv_rn(m1, s.bc1);
+    const float vh = __fdiv_rn(v1, s.bc2);
+    const float upd = __fadd_rn(__fdiv_rn(mh, __fadd_rn(__fsqrt_rn(vh), s.eps)),
+                                __fmul_rn(s.wd, w));
+    w = __fsub_rn(w, __fmul_rn(s.lr, upd));
+    m = m1;
+    v = v1;
+}
+
+__global__ void __launch_bounds__(kBlock)
+fused_step_kernel(const __grid_constant__ Tables T, const StepScalars s, const Range R)
+{
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kBlock;
+    int64_t q = R.q0 + static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x;
+    if (q >= R.q1) return;
+    int64_t k = q / R.shard_vec;     // owner
+    int64_t j = q - k * R.shard_vec; // vector position inside the owner's shard
+    const int N = R.n_ranks;
+
+    for (; q < R.q1; q += stride) {
+        float4* wp = T.w[k] + 2 * j;
+        float4* mp = T.m[k] + 2 * j;
+        float4* vp = T.v[k] + 2 * j;
+        const float4 w0 = dev::ld_stream(wp), w1 = dev::ld_stream(wp + 1);
+        const float4 m0 = dev::ld_stream(mp), m1 = dev::ld_stream(mp + 1);
+        const float4 v0 = dev::ld_stream(vp), v1 = dev::ld_stream(vp + 1);
+
+        // reduce-scatter: fp32 sum from +0 over ranks 0..N-1, in order
+        float acc[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+        for (int r0 = 0; r0 < N; r0 += kRankBatch) {
+            uint4 G[kRankBatch];
+#pragma unroll
+            for (int i = 0; i < kRankBatch; ++i)
+                if (r0 + i < N) G[i] = dev::ld_stream(T.g[r0 + i] + q);
+#pragma unroll
+            for (int i = 0; i < kRankBatch; ++i) {
+                if (r0 + i < N) {
+                    acc[0] = __fadd_rn(acc[0], dev::bf16_lo(G[i].x));
+                    acc[1] = __fadd_rn(acc[1], dev::bf16_hi(G[i].x));
+                    acc[2] = __fadd_rn(acc[2], dev::bf16_lo(G[i].y));
+                    acc[3] = __fadd_rn(acc[3], dev::bf16_hi(G[i].y));
+                    acc[4] = __fadd_rn(acc[4], dev::bf16_lo(G[i].z));
+                    acc[5] = __fadd_rn(acc[5], dev::bf16_hi(G[i].z));
+                    acc[6] = __fadd_rn(acc[6], dev::bf16_lo(G[i].w));
+                    acc[7] = __fadd_rn(acc[7], dev::bf16_hi(G[i].w));
+                }
+            }
+        }
+
+        float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+        float m[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+        float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) adamw(__fmul_rn(acc[e], s.inv_n), w[e], m[e], v[e], s);
+
+        dev::st_stream(wp, make_float4(w[0], w[1], w[2], w[3]));
+        dev::st_stream(wp + 1, make_float4(w[4], w[5], w[6], w[7]));
+        dev::st_stream(mp, make_float4(m[0], m[1], m[2], m[3]));
+        dev::st_stream(mp + 1, make_float4(m[4], m[5], m[6], m[7]));
+        dev::st_stream(vp, make_float4(v[0], v[1], v[2], v[3]));
+        dev::st_stream(vp + 1, make_float4(v[4], v[5], v[6], v[7]));
+        // all-gather: the owner's new bf16 slice
+        dev::st_stream(T.o[k] + j,
+                       make_uint4(dev::pack_bf16x2(w[0], w[1]), dev::pack_bf16x2(w[2], w[3]),
+                                  dev::pack_bf16x2(w[4], w[5]), dev::pack_bf16x2(w[6], w[7])));
+
+        k += R.step_k;
+        j += R.step_j;
+        if (j >= R.shard_vec) {
+            j -= R.shard_vec;
+            ++k;
+        }
+    }
+}
+
+int launch(const Tables& T, const StepScalars& s, int64_t q0, int64_t q1, int64_t shard_vec,
+           int32_t n_ranks, cudaStream_t stream)
+{
+    if (q1 <= q0) return ZERO_OK;
+    const int max_blocks = persistent_blocks(reinterpret_cast<const void*>(fused_step_kernel),
+                                             kBlock, 0);
+    if (max_blocks <= 0) return ZERO_ECUDA;
+    const int64_t need = (q1 - q0 + kBlock - 1) / kBlock;
+    const int blocks = static_cast<int>(need < max_blocks ? need : max_blocks);
+    const int64_t stride = static_cast<int64_t>(blocks) * kBlock;
+    const StrideSplit sp = split_stride(stride, shard_vec);
+    const Range R{q0, q1, shard_vec, sp.k, sp.j, n_ranks};
+    fused_step_kernel<<<blocks, kBlock, 0, stream>>>(T, s, R);
+    return cuda_status(cudaGetLastError());
+}
+
+int check_state_tables(int32_t n, const uint16_t* const* grads, float* const* master,
+                       float* const* m, float* const* v)
+{
+    int rc;
+    if ((rc = check_table(grads, n)) != ZERO_OK) return rc;
+    if ((rc = check_table(master, n)) != ZERO_OK) return rc;
+    if ((rc = check_table(m, n)) != ZERO_OK) return rc;
+    return check_table(v, n);
+}
+
+} // namespace
+} // namespace zero
+
+using namespace zero;
+
+extern "C" int zero_step_stage12(int32_t stage, int32_t n_ranks, int64_t n_padded,
+                                 const uint16_t* const* grads, float* const* master,
+                                 float* const* m, float* const* v, uint16_t* params_bf16,
+                                 const zero_hparams_t* hp, int64_t bucket_elems,
+                                 cudaStream_t stream)
+{
+    if ((stage != 1 && stage != 2) || n_ranks < 1 || n_ranks > ZERO_MAX_RANKS ||
+        n_padded <= 0 || n_padded % (8 * static_cast<int64_t>(n_ranks)) != 0 ||
+        bucket_elems < 0 || bucket_elems % 8 != 0 || !valid_hparams(hp) || !params_bf16)
+        return ZERO_EINVAL;
+    int rc = check_state_tables(n_ranks, grads, master, m, v);
+    if (rc != ZERO_OK) return rc;
+    if (!aligned16(params_bf16)) return ZERO_EALIGN;
+
+    const int64_t S = n_padded / n_ranks;
+    Tables T = {};
+    for (int32_t r = 0; r < n_ranks; ++r) {
+        T.g[r] = reinterpret_cast<const uint4*>(grads[r]);
+        T.w[r] = reinterpret_cast<float4*>(master[r]);
+        T.m[r] = reinterpret_cast<float4*>(m[r]);
+        T.v[r] = reinterpret_cast<float4*>(v[r]);
+        T.o[r] = reinterpret_cast<uint4*>(params_bf16 + r * S);
+    }
+    const StepScalars s = make_scalars(hp, n_ranks);
+    const int64_t nvec = n_padded / 8, shard_vec = S / 8;
+    // ZeRO-2 reduces the gradient bucket by bucket as it becomes ready; the
+    // per-element arithmetic is the same, so stage 1 and 2 give equal bits.
+    const int64_t bucket_vec = (stage == 2 && bucket_elems > 0) ? bucket_elems / 8 : nvec;
+    for (int64_t q0 = 0; q0 < nvec; q0 += bucket_vec) {
+        const int64_t q1 = q0 + bucket_vec < nvec ? q0 + bucket_vec : nvec;
+        if ((rc = launch(T, s, q0, q1, shard_vec, n_ranks, stream)) != ZERO_OK) return rc;
+    }
+    return ZERO_OK;
+}
+
+extern "C" int zero3_reduce_scatter_unit(const zero_unit_t* unit, int32_t n_ranks,
+                                         const uint16_t* const* unit_grads,
+                                         float* const* master, float* const* m,
+                                         float* const* v, uint16_t* const* shard_bf16,
+                                         const zero_hparams_t* hp, cudaStream_t stream)
+{
+    if (!unit || n_ranks < 1 || n_ranks > ZERO_MAX_RANKS || unit->n_padded <= 0 ||
+        unit->shard_len <= 0 || unit->shard_len % 8 != 0 ||
+        unit->shard_len * n_ranks != unit->n_padded || unit->shard_offset < 0 ||
+        unit->shard_offset % 8 != 0 || !valid_hparams(hp))
+        return ZERO_EINVAL;
+    int rc = check_state_tables(n_ranks, unit_grads, master, m, v);
+    if (rc != ZERO_OK) return rc;
+    if ((rc = check_table(shard_bf16, n_ranks)) != ZERO_OK) return rc;
+
+    const int64_t off = unit->shard_offset;
+    Tables T = {};
+    for (int32_t r = 0; r < n_ranks; ++r) {
+        T.g[r] = reinterpret_cast<const uint4*>(unit_grads[r]);
+        T.w[r] = reinterpret_cast<float4*>(master[r] + off);
+        T.m[r] = reinterpret_cast<float4*>(m[r] + off);
+        T.v[r] = reinterpret_cast<float4*>(v[r] + off);
+        T.o[r] = reinterpret_cast<uint4*>(shard_bf16[r] + off);
+    }
+    const StepScalars s = make_scalars(hp, n_ranks);
+    return launch(T, s, 0, unit->n_padded / 8, unit->shard_len / 8, n_ranks, stream);
+}

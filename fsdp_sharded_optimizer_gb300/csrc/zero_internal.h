@@ -1,0 +1,55 @@
+// zero_internal.h -- host-side helpers shared by the library's translation
+// units (argument checks, per-device launch geometry, the fp32 step scalars).
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "zero.h"
+
+namespace zero {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Checks a host table of n device pointers: non-null and 16-byte aligned.
+// Returns ZERO_OK, ZERO_EINVAL or ZERO_EALIGN.
+template <typename T>
+int check_table(T const* table, int32_t n)
+{
+    if (!table) return ZERO_EINVAL;
+    for (int32_t i = 0; i < n; ++i) {
+        if (!table[i]) return ZERO_EINVAL;
+        if (!aligned16(table[i])) return ZERO_EALIGN;
+    }
+    return ZERO_OK;
+}
+
+// Hyper-parameters a step accepts: finite, step >= 1, betas in [0, 1),
+// lr and eps and weight decay >= 0 (eps > 0 keeps the division defined).
+bool valid_hparams(const zero_hparams_t* hp);
+
+// The fp32 constants of one AdamW step, each computed in double from the
+// double hyper-parameters and rounded once to fp32.
+struct StepScalars {
+    float b1, b2, omb1, omb2, bc1, bc2, lr, eps, wd, inv_n;
+};
+StepScalars make_scalars(const zero_hparams_t* hp, int32_t n_ranks);
+
+// Persistent-grid size for a kernel on the current device: the SM count
+// times the resident blocks per SM (computed once per device and kernel).
+int persistent_blocks(const void* kernel, int block_threads, size_t dyn_smem);
+
+// Splits a grid stride (in vectors) into whole shards and a remainder so
+// that a grid-stride loop can advance (owner, position) without dividing.
+struct StrideSplit {
+    int64_t k, j;
+};
+inline StrideSplit split_stride(int64_t stride, int64_t shard_vec)
+{
+    return {stride / shard_vec, stride % shard_vec};
+}
+
+int cuda_status(cudaError_t e);
+
+} // namespace zero

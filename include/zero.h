@@ -1,0 +1,220 @@
+/*
+ * zero.h -- C ABI of the GB300 fused ZeRO/FSDP sharded optimizer step.
+ *
+ * The N_d data-parallel ranks of one training job are emulated on ONE GPU:
+ * each rank is a separate set of device buffers (its bf16 gradient, its fp32
+ * master/m/v shard and, for ZeRO-3, its bf16 parameter shard).  The
+ * "collectives" are memory traffic inside one kernel: the reduce-scatter is
+ * each owner's fixed-order fp32 sum over the N_d gradient buffers, the
+ * all-gather is the owner writing its new bf16 slice into the replicated
+ * buffer (ZeRO-1/2) or into its shard that the unit gather later copies
+ * (ZeRO-3).
+ *
+ * Sources (page title and section; the method is theirs, the code is not):
+ *  [DZF] "Data parallelism, ZeRO and FSDP" (ML Systems, lesson 8):
+ *        "2. The picture" (what is redundant; the communication is already
+ *        there), "3. Definitions and main results" (Theorem: ZeRO memory and
+ *        communication; How FSDP implements ZeRO-3), "5. In code" (the
+ *        AdamW update of the ZeRO-1 simulator).
+ *  [DDF] "Distributed Training Basics -- DDP and FSDP": "Memory accounting:
+ *        derive the table from bytes", "Communication and a roofline sanity
+ *        check".
+ *  [COL] "Data parallelism, collectives and ZeRO/FSDP": "Collectives",
+ *        "ZeRO and FSDP" (the per-unit FSDP step figure).
+ *
+ * Conventions shared by every call:
+ *  - Return ZERO_OK (0) or a negative ZERO_E* code; no exception crosses the
+ *    ABI.  zero_strerror() names a code.
+ *  - Device calls are asynchronous on the caller's stream and allocate no
+ *    memory.  The caller owns every buffer.  Pointer tables ("n_ranks device
+ *    pointers") are HOST arrays holding DEVICE addresses; the library copies
+ *    them into the kernel's parameters, so the tables may be freed as soon as
+ *    the call returns.
+ *  - bf16 values travel as uint16_t bit patterns.  Every device pointer must
+ *    be 16-byte aligned (ZERO_EALIGN otherwise).
+ *  - Arguments are checked on the host before anything is launched; a bad
+ *    argument launches nothing.  ZERO_ECUDA reports a launch failure.
+ *  - Stateless and re-entrant.  1 <= n_ranks <= ZERO_MAX_RANKS.
+ *
+ * Layout (zero_layout): a unit of P true parameters is padded to
+ * P' = ceil(P / (n_ranks*align)) * n_ranks*align; S = P'/n_ranks; rank k owns
+ * [k*S, (k+1)*S).  Padding holds +0 gradients and +0 state and stays +0.
+ */
+#ifndef ZERO_H
+#define ZERO_H
+
+#include <stdint.h>
+
+#include <cuda_runtime_api.h> /* cudaStream_t */
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ZERO_OK 0
+#define ZERO_EINVAL (-1)   /* an argument is out of range or null */
+#define ZERO_EALIGN (-2)   /* a device pointer is not 16-byte aligned */
+#define ZERO_ECUDA (-3)    /* the CUDA runtime reported an error */
+#define ZERO_ETIMEOUT (-4) /* a bounded host wait ran out */
+
+#define ZERO_MAX_RANKS 64
+#define ZERO_DEFAULT_ALIGN 64 /* elements per shard granule */
+
+/* AdamW hyper-parameters ([DZF] "5. In code": lr, b1, b2, eps, wd) and the
+ * 1-based step counter t used by the bias correction 1 - b^t. */
+typedef struct {
+    double lr, beta1, beta2, eps, weight_decay;
+    int64_t step;
+} zero_hparams_t;
+
+/* One FSDP unit ([DZF] "How FSDP implements ZeRO-3", step 1): its parameters
+ * flattened, padded and cut into n_ranks equal chunks. */
+typedef struct {
+    int64_t n_params;     /* true parameters of the unit */
+    int64_t n_padded;     /* multiple of n_ranks*align */
+    int64_t shard_len;    /* n_padded / n_ranks */
+    int64_t offset;       /* start of the unit in the concatenated padded buffer */
+    int64_t shard_offset; /* start of the unit inside each rank's shard storage */
+    int64_t param_offset; /* start of the unit's true parameters in the model */
+    int64_t pad;          /* n_padded - n_params */
+} zero_unit_t;
+
+/* Per-rank accounting ([DZF] Theorem; [DDF] "Memory accounting"). */
+typedef struct {
+    double weight_bytes;    /* bf16 weights one rank keeps */
+    double grad_bytes;      /* bf16 gradients one rank keeps */
+    double optim_bytes;     /* optimizer state (K bytes per parameter) one rank keeps */
+    double state_bytes;     /* their sum: model states per GPU */
+    double comm_volume;     /* elements per step: 2P (DDP, ZeRO-1/2) or 3P (ZeRO-3) */
+    double comm_sent_elems; /* ring elements sent per rank: volume*(N-1)/N */
+    double comm_sent_bytes; /* the same at 2 bytes per element */
+    double hbm_bytes;       /* algorithmic HBM bytes of the one-GPU emulated step:
+                               (26 + 2N) per parameter, + 8 per parameter for
+                               ZeRO-3's two unit gathers */
+} zero_bytes_t;
+
+/* zero_layout -- host only.  [DZF] "What is redundant" (GPU k owns slice k);
+ * "How FSDP implements ZeRO-3", step 1 (equal chunks of the flat unit).
+ *   unit_sizes[n_units]  true parameter count of each unit (> 0)
+ *   n_ranks, align_elems shards are multiples of align_elems elements
+ *   out_units[n_units]   filled with each unit's layout; units are padded one
+ *                        by one and concatenated in order
+ *   out_total_padded     sum of the units' n_padded
+ * ZERO_EINVAL on a null pointer, n_units < 1, n_ranks outside [1, 64],
+ * align_elems < 1 or not a multiple of 8, or a unit size <= 0. */
+int zero_layout(const int64_t* unit_sizes, int32_t n_units, int32_t n_ranks,
+                int32_t align_elems, zero_unit_t* out_units,
+                int64_t* out_total_padded);
+
+/* zero_step_stage12 -- the fused ZeRO-1/ZeRO-2 step, one pass over HBM.
+ * [DZF] Theorem, proof steps 2, 3, 6; "The communication is already there".
+ * For every element i of the flat padded buffer, with owner k = i / S:
+ *   g   = (sum over r = 0..n_ranks-1, in that order, of fp32(grads[r][i]))
+ *         * (float)(1/n_ranks)                                [reduce-scatter]
+ *   AdamW on master[k], m[k], v[k] at i - k*S in fp32:          [update]
+ *     m = b1*m + (1-b1)*g;  v = b2*v + ((1-b2)*g)*g;
+ *     w = w - lr*((m/(1-b1^t)) / (sqrt(v/(1-b2^t)) + eps) + wd*w)
+ *   params_bf16[i] = bf16_round_nearest_even(w)                [all-gather]
+ * Every operation is one IEEE fp32 operation, none fused; the fp32 scalars
+ * are computed in double from *hp and rounded once.
+ *   stage          1 (ZeRO-1) or 2 (ZeRO-2); identical results
+ *   n_padded       P' (multiple of 8*n_ranks); S = n_padded / n_ranks
+ *   grads          n_ranks device pointers, each n_padded bf16 (read only)
+ *   master, m, v   n_ranks device pointers, each S fp32 (read and written)
+ *   params_bf16    device pointer, n_padded bf16 (written): the replicated
+ *                  weights every rank holds after the all-gather
+ *   bucket_elems   stage 2: reduce-scatter+update bucket by bucket, one launch
+ *                  per bucket of this many elements (multiple of 8; 0 = whole
+ *                  buffer); ignored for stage 1
+ * Buffers must not overlap.  ZERO_EINVAL / ZERO_EALIGN / ZERO_ECUDA. */
+int zero_step_stage12(int32_t stage, int32_t n_ranks, int64_t n_padded,
+                      const uint16_t* const* grads, float* const* master,
+                      float* const* m, float* const* v, uint16_t* params_bf16,
+                      const zero_hparams_t* hp, int64_t bucket_elems,
+                      cudaStream_t stream);
+
+/* zero3_gather_unit -- ZeRO-3 all-gather of one unit's bf16 parameters.
+ * [DZF] "How FSDP implements ZeRO-3", steps 2-3; [COL] "Collectives" (every
+ * rank gets all shards) and the per-unit step figure.
+ *   full_unit[k*S_u + j] = shard_bf16[k][unit->shard_offset + j]
+ *   for k < n_ranks, j < S_u = unit->shard_len.
+ *   unit        layout from zero_layout (host pointer)
+ *   shard_bf16  n_ranks device pointers: rank k's bf16 shard storage of ALL
+ *               units (unit u at shard_offset)
+ *   full_unit   device pointer, unit->n_padded bf16 (written)
+ * A bit copy.  ZERO_EINVAL / ZERO_EALIGN / ZERO_ECUDA. */
+int zero3_gather_unit(const zero_unit_t* unit, int32_t n_ranks,
+                      const uint16_t* const* shard_bf16, uint16_t* full_unit,
+                      cudaStream_t stream);
+
+/* zero3_reduce_scatter_unit -- ZeRO-3 gradient reduce-scatter of one unit,
+ * fused with each owner's AdamW and the write of its new bf16 shard.
+ * [DZF] "How FSDP implements ZeRO-3", steps 3-4; Theorem, proof step 7 (no
+ * all-gather follows the update).  Per element i < unit->n_padded with owner
+ * k = i / S_u and position p = unit->shard_offset + i - k*S_u: the same
+ * reduce-scatter mean and AdamW as zero_step_stage12, on master[k][p],
+ * m[k][p], v[k][p], then shard_bf16[k][p] = bf16_rne(new master).
+ *   unit_grads     n_ranks device pointers, each unit->n_padded bf16
+ *   master, m, v   n_ranks device pointers to each rank's fp32 shard storage
+ *   shard_bf16     n_ranks device pointers to each rank's bf16 shard storage
+ * ZERO_EINVAL / ZERO_EALIGN / ZERO_ECUDA. */
+int zero3_reduce_scatter_unit(const zero_unit_t* unit, int32_t n_ranks,
+                              const uint16_t* const* unit_grads,
+                              float* const* master, float* const* m,
+                              float* const* v, uint16_t* const* shard_bf16,
+                              const zero_hparams_t* hp, cudaStream_t stream);
+
+/* zero_state_bytes -- host only.  [DZF] Theorem (table and proof); [DDF]
+ * "Memory accounting" (state_bytes raises on params <= 0 or ranks < 1) and
+ * "Communication and a roofline sanity check" (ring bytes).
+ *   stage 0 = DDP, 1..3 = ZeRO-1..3; K = optimizer bytes per parameter (12
+ *   for mixed-precision AdamW).  Model states per rank: (4+K)P, 4P+KP/N,
+ *   2P+(2+K)P/N, (4+K)P/N.
+ * ZERO_EINVAL on n_params <= 0, n_ranks < 1, stage outside [0,3], K < 0 or a
+ * null out. */
+int zero_state_bytes(int64_t n_params, int32_t n_ranks, int32_t stage, int32_t K,
+                     zero_bytes_t* out);
+
+/* ---------------------------------------------------------------------
+ * Harness calls: seeded synthetic inputs and helpers.  They are not part
+ * of the method; the benchmark and the tests use them to fill device
+ * buffers without a host round trip.
+ * ------------------------------------------------------------------- */
+
+/* zero_gen_grads_unit -- rank r's bf16 gradient of one unit at step t.
+ * Element j < unit->n_params holds bf16_rne(z), z drawn by a SplitMix64
+ * counter stream keyed by (seed, stream 1, step, r) at the true parameter
+ * index unit->param_offset + j (an approximately normal value of standard
+ * deviation sigma; with outliers != 0 one value in a hundred is scaled by
+ * 100).  Padding elements are +0.
+ *   unit_grads  n_ranks device pointers, each unit->n_padded bf16 (written) */
+int zero_gen_grads_unit(uint64_t seed, int64_t step, double sigma, int32_t outliers,
+                        const zero_unit_t* unit, int32_t n_ranks,
+                        uint16_t* const* unit_grads, cudaStream_t stream);
+
+/* zero_gen_master -- initial fp32 master weights of every unit, written into
+ * each owner's shard storage: true parameter p draws from (seed, stream 0,
+ * step 0, rank 0) at index p with standard deviation sigma; padding is +0.
+ *   units[n_units]  layout from zero_layout (host array)
+ *   master          n_ranks device pointers to fp32 shard storage */
+int zero_gen_master(uint64_t seed, double sigma, const zero_unit_t* units,
+                    int32_t n_units, int32_t n_ranks, float* const* master,
+                    cudaStream_t stream);
+
+/* zero_cast_bf16 -- dst[i] = bf16_rne(src[i]) for i < n (n a multiple of 8):
+ * the initial bf16 replica or shard of fp32 master weights. */
+int zero_cast_bf16(const float* src, uint16_t* dst, int64_t n, cudaStream_t stream);
+
+/* zero_stream_wait -- host wait for all work on a stream, polling with a
+ * wall-clock limit instead of blocking forever.  ZERO_ETIMEOUT if the work
+ * has not finished after timeout_ms milliseconds (the work is left running),
+ * ZERO_ECUDA if the stream reports an error. */
+int zero_stream_wait(cudaStream_t stream, int64_t timeout_ms);
+
+/* zero_strerror -- a static string naming a return code. */
+const char* zero_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ZERO_H */

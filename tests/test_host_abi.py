@@ -1,0 +1,161 @@
+"""Host side of the C ABI, on the CPU: the library loads, exports every symbol
+include/zero.h declares, its host-only calls agree bit for bit with the oracle,
+and bad arguments are rejected before anything is launched."""
+import ctypes as C
+import os
+import re
+
+import numpy as np
+import pytest
+
+from conftest import ROOT
+
+
+@pytest.fixture(scope="module")
+def B():
+    from fsdp_sharded_optimizer_gb300 import build
+    build.build()
+    from fsdp_sharded_optimizer_gb300 import _binding
+    return _binding
+
+
+def _header_functions():
+    text = open(os.path.join(ROOT, "include", "zero.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(zero[0-9]*_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = _header_functions()
+    for n in ("zero_layout", "zero_step_stage12", "zero3_gather_unit",
+              "zero3_reduce_scatter_unit", "zero_state_bytes"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(B):
+    lib = C.CDLL(B.LIB_PATH)
+    missing = [n for n in _header_functions() if not hasattr(lib, n)]
+    assert not missing
+    # and the binding wires every one of them with the header's name
+    assert set(_header_functions()) == set(B.SIGNATURES)
+
+
+def test_library_is_built_for_sm_103a_only(B):
+    log = open(os.path.join(os.path.dirname(B.LIB_PATH), "build.log")).read()
+    assert "arch=compute_103a,code=sm_103a" in log
+    assert "sm_90" not in log and "sm_100" not in log
+
+
+@pytest.mark.parametrize("align", [8, 64])
+def test_layout_matches_oracle(B, orc, align):
+    for N in list(range(1, 9)) + [16, 64]:
+        for P in list(range(1, 70)) + [2**16 + 37, 2**20 + 5, 124_439_808]:
+            (u,), total = B.zero_layout([P], N, align)
+            (o,), ototal = orc.layout([P], N, align)
+            assert u.as_dict() == o.as_dict() and total == ototal
+
+
+def test_layout_multi_unit_matches_oracle(B, orc):
+    for sizes in ([44_044_288] * 22 + [131_074_048], [202_383_360] * 32 + [262_148_096],
+                  [5, 64, 1, 130, 63, 2**16 + 37]):
+        for N in (2, 8, 64):
+            units, total = B.zero_layout(sizes, N)
+            ounits, ototal = orc.layout(sizes, N)
+            assert [u.as_dict() for u in units] == [o.as_dict() for o in ounits]
+            assert total == ototal
+
+
+def test_workload_totals(B):
+    units, total = B.zero_layout([44_044_288] * 22 + [131_074_048], 8)
+    assert total == sum(u.n_params for u in units) == 1_100_048_384
+    units, total = B.zero_layout([202_383_360] * 32 + [262_148_096], 8)
+    assert total == sum(u.n_params for u in units) == 6_738_415_616
+
+
+def test_state_bytes_matches_oracle(B, orc):
+    for P in (1, 10, 7 * 10**9, 124_439_808, 2**40):
+        for N in (1, 2, 3, 8, 32, 128):
+            for stage in range(4):
+                for K in (0, 12, 16):
+                    assert B.zero_state_bytes(P, N, stage, K) == orc.state_bytes(P, N, stage, K)
+
+
+def test_state_bytes_rejects(B):
+    out = B.zero_bytes_t()
+    for args in ((0, 8, 1, 12), (-1, 8, 1, 12), (10, 0, 1, 12), (10, 8, -1, 12), (10, 8, 4, 12),
+                 (10, 8, 1, -1)):
+        assert B.lib.zero_state_bytes(*args, C.byref(out)) == B.ZERO_EINVAL
+    assert B.lib.zero_state_bytes(10, 8, 1, 12, None) == B.ZERO_EINVAL
+
+
+def test_layout_rejects(B):
+    units = (B.zero_unit_t * 2)()
+    total = C.c_int64()
+    sizes = (C.c_int64 * 2)(10, 20)
+    bad = [(sizes, 0, 8, 64), (sizes, 2, 0, 64), (sizes, 2, 65, 64), (sizes, 2, 8, 0),
+           (sizes, 2, 8, 12), ((C.c_int64 * 2)(10, 0), 2, 8, 64)]
+    for s, n_units, n_ranks, align in bad:
+        assert B.lib.zero_layout(s, n_units, n_ranks, align, units, C.byref(total)) == B.ZERO_EINVAL
+    assert B.lib.zero_layout(None, 2, 8, 64, units, C.byref(total)) == B.ZERO_EINVAL
+
+
+def _table(addrs):
+    return (C.c_void_p * len(addrs))(*addrs)
+
+
+# Fake device addresses: validation must reject before anything touches them.
+A16 = [0x10000 * (i + 1) for i in range(64)]
+
+
+def test_step_rejects_before_launch(B):
+    hp = B.hparams()
+    g = _table(A16[:8])
+    w, m, v = _table(A16[8:16]), _table(A16[16:24]), _table(A16[24:32])
+    p = C.c_void_p(0x900000)
+    call = lambda *a: B.lib.zero_step_stage12(*a)
+    assert call(3, 8, 1024, g, w, m, v, p, C.byref(hp), 0, None) == B.ZERO_EINVAL  # stage
+    assert call(1, 0, 1024, g, w, m, v, p, C.byref(hp), 0, None) == B.ZERO_EINVAL  # ranks
+    assert call(1, 65, 1024, g, w, m, v, p, C.byref(hp), 0, None) == B.ZERO_EINVAL
+    assert call(1, 8, 1000, g, w, m, v, p, C.byref(hp), 0, None) == B.ZERO_EINVAL  # not 8N-multiple
+    assert call(1, 8, 0, g, w, m, v, p, C.byref(hp), 0, None) == B.ZERO_EINVAL
+    assert call(2, 8, 1024, g, w, m, v, p, C.byref(hp), 12, None) == B.ZERO_EINVAL  # bucket % 8
+    assert call(2, 8, 1024, g, w, m, v, p, C.byref(hp), -8, None) == B.ZERO_EINVAL
+    assert call(1, 8, 1024, None, w, m, v, p, C.byref(hp), 0, None) == B.ZERO_EINVAL
+    assert call(1, 8, 1024, g, w, m, v, None, C.byref(hp), 0, None) == B.ZERO_EINVAL
+    assert call(1, 8, 1024, g, w, m, v, p, None, 0, None) == B.ZERO_EINVAL
+    for bad_hp in (B.hparams(step=0), B.hparams(eps=0.0), B.hparams(beta1=1.0),
+                   B.hparams(lr=float("nan")), B.hparams(weight_decay=-1.0)):
+        assert call(1, 8, 1024, g, w, m, v, p, C.byref(bad_hp), 0, None) == B.ZERO_EINVAL
+    nulls = _table(A16[:7] + [0])
+    assert call(1, 8, 1024, nulls, w, m, v, p, C.byref(hp), 0, None) == B.ZERO_EINVAL
+    odd = _table(A16[:7] + [A16[7] + 8])
+    assert call(1, 8, 1024, odd, w, m, v, p, C.byref(hp), 0, None) == B.ZERO_EALIGN
+    assert call(1, 8, 1024, g, w, m, v, C.c_void_p(0x900002), C.byref(hp), 0, None) == B.ZERO_EALIGN
+
+
+def test_zero3_calls_reject_before_launch(B):
+    (u,), _ = B.zero_layout([1000], 4)
+    hp = B.hparams()
+    t = _table(A16[:4])
+    full = C.c_void_p(0x900000)
+    assert B.lib.zero3_gather_unit(None, 4, t, full, None) == B.ZERO_EINVAL
+    assert B.lib.zero3_gather_unit(C.byref(u), 3, t, full, None) == B.ZERO_EINVAL  # layout mismatch
+    assert B.lib.zero3_gather_unit(C.byref(u), 4, t, None, None) == B.ZERO_EINVAL
+    assert B.lib.zero3_gather_unit(C.byref(u), 4, t, C.c_void_p(0x900004), None) == B.ZERO_EALIGN
+    bad = B.zero_unit_t(**{**u.as_dict(), "shard_offset": 4})
+    assert B.lib.zero3_gather_unit(C.byref(bad), 4, t, full, None) == B.ZERO_EINVAL
+    args = (t, t, t, t, t, C.byref(hp), None)
+    assert B.lib.zero3_reduce_scatter_unit(C.byref(u), 0, *args) == B.ZERO_EINVAL
+    assert B.lib.zero3_reduce_scatter_unit(C.byref(bad), 4, *args) == B.ZERO_EINVAL
+    assert B.lib.zero3_reduce_scatter_unit(C.byref(u), 4, t, t, t, t, None, C.byref(hp),
+                                           None) == B.ZERO_EINVAL
+    hp0 = B.hparams(step=0)
+    assert B.lib.zero3_reduce_scatter_unit(C.byref(u), 4, t, t, t, t, t, C.byref(hp0),
+                                           None) == B.ZERO_EINVAL
+
+
+def test_strerror_names_codes(B):
+    assert B.strerror(B.ZERO_OK) == "ok"
+    assert "align" in B.strerror(B.ZERO_EALIGN)
+    assert "timed out" in B.strerror(B.ZERO_ETIMEOUT)
+    assert B.strerror(-99) == "unknown error"
