@@ -7,11 +7,22 @@ weights (the all-gather).  ZeRO-3 adds the per-unit gather and the per-unit
 reduce-scatter, scheduled with next-unit prefetch on a side stream
 (``zero3.Zero3Schedule``).
 
-The public calls carry the C ABI's names (include/zero.h); see ``_binding``.
+The public calls carry the C ABI's names (include/zero.h) and live in
+``_binding``.  They are loaded on first use, so that ``build`` can be imported
+before the library exists; using any of them without a built library raises
+ImportError (there is no fallback).
 """
-from ._binding import (ZERO_DEFAULT_ALIGN, ZERO_EALIGN, ZERO_ECUDA, ZERO_EINVAL,  # noqa: F401
-                       ZERO_ETIMEOUT, ZERO_MAX_RANKS, ZERO_OK, LIB_PATH, ZeroError, hparams,
-                       strerror, zero3_gather_unit, zero3_reduce_scatter_unit, zero_bytes_t,
-                       zero_cast_bf16, zero_gen_grads_unit, zero_gen_master, zero_hparams_t,
-                       zero_layout, zero_state_bytes, zero_step_stage12, zero_stream_wait,
-                       zero_unit_t)
+_PUBLIC = ("ZERO_DEFAULT_ALIGN", "ZERO_EALIGN", "ZERO_ECUDA", "ZERO_EINVAL", "ZERO_ETIMEOUT",
+           "ZERO_MAX_RANKS", "ZERO_OK", "LIB_PATH", "ZeroError", "hparams", "strerror",
+           "zero3_gather_unit", "zero3_reduce_scatter_unit", "zero_bytes_t", "zero_cast_bf16",
+           "zero_gen_grads_unit", "zero_gen_master", "zero_hparams_t", "zero_layout",
+           "zero_state_bytes", "zero_step_stage12", "zero_stream_wait", "zero_unit_t")
+
+__all__ = list(_PUBLIC)
+
+
+def __getattr__(name):
+    if name in _PUBLIC:
+        from . import _binding
+        return getattr(_binding, name)
+    raise AttributeError("module %r has no attribute %r" % (__name__, name))

@@ -322,6 +322,9 @@ int or_sim_ddp(int32_t n_ranks, int64_t n_params, uint64_t seed, double sigma_w,
         Wb[r] = xcalloc((size_t)P, sizeof(uint16_t));
         G[r] = xcalloc((size_t)P, sizeof(uint16_t));
         or_gen_master(seed, sigma_w, &whole, 1, 1, &W[r]);
+        /* every replica starts from the bf16 rounding of the same master weights */
+        for (int64_t p = 0; p < P; ++p)
+            Wb[r][p] = or_bf16_rne(W[r][p]);
     }
     for (int32_t t = 0; t < n_steps; ++t) {
         or_hparams_t hp = *hp0;

@@ -342,6 +342,18 @@ def test_zero_stages_equal_ddp_bitwise(orc, N, P):
     assert not v.reshape(-1)[P:].view(np.uint32).any()
 
 
+def test_zero_steps_return_initial_replica(orc):
+    """With no step taken, every simulator returns the bf16 rounding of the
+    initial master weights (the replicas all start from the same weights)."""
+    hp0 = orc.hparams(**HP, step=1)
+    ddp = orc.sim_ddp(3, 100, 5, 0.02, 1e-3, 0, hp0, 0)
+    np.testing.assert_array_equal(ddp[0], orc.bf16_rne(ddp[1]))
+    assert ddp[0].any()
+    for stage in (1, 2, 3):
+        z = orc.sim_zero(stage, 3, [60, 40], 5, 0.02, 1e-3, 0, hp0, 0)
+        np.testing.assert_array_equal(z[0], ddp[0])
+
+
 def test_zero3_multi_unit_equals_ddp(orc):
     hp0 = orc.hparams(**HP, step=1)
     units = [37, 64, 1, 200, 9]
