@@ -23,6 +23,11 @@ namespace {
 
 constexpr int kBlock = 256;
 constexpr int kRankBatch = 8; // gradient loads issued together before summing
+// Three resident blocks per SM (an 80-register cap) instead of the two that
+// the unconstrained 94-102 registers allow: 24 warps per SM keep enough 16-byte
+// loads in flight to reach the HBM roofline (measured at N_d = 2..64 on GB300:
+// +12 % at N_d = 8 over two blocks per SM; four blocks per SM spill and lose).
+constexpr int kMinBlocksPerSM = 3;
 
 // Per-rank device pointers, passed by value in the kernel's parameter space
 // (5 x 64 x 8 B = 2.5 KB).  o[k] points at rank k's output slice: the
@@ -59,7 +64,7 @@ __device__ __forceinline__ void adamw(float g, float& w, float& m, float& v,
     v = v1;
 }
 
-__global__ void __launch_bounds__(kBlock)
+__global__ void __launch_bounds__(kBlock, kMinBlocksPerSM)
 fused_step_kernel(const __grid_constant__ Tables T, const StepScalars s, const Range R)
 {
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kBlock;
