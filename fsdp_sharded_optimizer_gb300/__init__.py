@@ -16,7 +16,8 @@ _PUBLIC = ("ZERO_DEFAULT_ALIGN", "ZERO_EALIGN", "ZERO_ECUDA", "ZERO_EINVAL", "ZE
            "ZERO_MAX_RANKS", "ZERO_OK", "LIB_PATH", "ZeroError", "hparams", "strerror",
            "zero3_gather_unit", "zero3_reduce_scatter_unit", "zero_bytes_t", "zero_cast_bf16",
            "zero_gen_grads_unit", "zero_gen_master", "zero_hparams_t", "zero_layout",
-           "zero_state_bytes", "zero_step_stage12", "zero_stream_wait", "zero_unit_t")
+           "zero_state_bytes", "zero_step_stage12", "zero_stream_wait", "zero_unit_t",
+           "zero3_plan", "zero3_step", "zero_op_t", "zero_regen_t")
 
 __all__ = list(_PUBLIC)
 

@@ -56,6 +56,18 @@ class zero_bytes_t(C.Structure):
         return {n: getattr(self, n) for n, _ in self._fields_}
 
 
+class zero_op_t(C.Structure):
+    _fields_ = [("kind", C.c_int32), ("stream", C.c_int32), ("unit", C.c_int32), ("arg", C.c_int32)]
+
+
+class zero_regen_t(C.Structure):
+    _fields_ = [("seed", C.c_uint64), ("sigma", C.c_double), ("outliers", C.c_int32)]
+
+
+ZERO_OP_RECORD, ZERO_OP_WAIT, ZERO_OP_GATHER = 1, 2, 3
+ZERO_OP_REDUCE_SCATTER, ZERO_OP_REGEN, ZERO_OP_USE = 4, 5, 6
+OP_NAMES = {1: "record", 2: "wait", 3: "gather", 4: "reduce_scatter", 5: "regen", 6: "use"}
+
 # name -> (restype, argtypes); the same names as include/zero.h
 _P, _I32, _I64, _U64, _F64 = C.c_void_p, C.c_int32, C.c_int64, C.c_uint64, C.c_double
 SIGNATURES = {
@@ -64,6 +76,8 @@ SIGNATURES = {
     "zero3_gather_unit": (C.c_int, [_P, _I32, _P, _P, _P]),
     "zero3_reduce_scatter_unit": (C.c_int, [_P, _I32, _P, _P, _P, _P, _P, _P, _P]),
     "zero_state_bytes": (C.c_int, [_I64, _I32, _I32, _I32, _P]),
+    "zero3_plan": (C.c_int, [_I32, _I32, _P, _I32, _P]),
+    "zero3_step": (C.c_int, [_P, _I32, _I32, _P, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "zero_gen_grads_unit": (C.c_int, [_U64, _I64, _F64, _I32, _P, _I32, _P, _P]),
     "zero_gen_master": (C.c_int, [_U64, _F64, _P, _I32, _I32, _P, _P]),
     "zero_cast_bf16": (C.c_int, [_P, _P, _I64, _P]),
@@ -175,6 +189,33 @@ def zero3_reduce_scatter_unit(unit, unit_grads, master, m, v, shard_bf16, hp, st
     s, _ = _rows(shard_bf16, 2, "shard_bf16")
     _check("zero3_reduce_scatter_unit", lib.zero3_reduce_scatter_unit(
         C.byref(unit), len(grows), g, w, mm, vv, s, C.byref(hp), _stream(stream)))
+
+
+def zero3_plan(n_units, regen=False):
+    """The operations of one ZeRO-3 step (host only): a list of
+    (kind name, stream 0=main/1=side, unit, arg)."""
+    cap = 14 * n_units + 2
+    ops = (zero_op_t * cap)()
+    n = C.c_int32()
+    _check("zero3_plan", lib.zero3_plan(n_units, 1 if regen else 0, ops, cap, C.byref(n)))
+    return [(OP_NAMES[o.kind], o.stream, o.unit, o.arg) for o in ops[:n.value]]
+
+
+def zero3_step(units, grads, master, m, v, shard_bf16, full_a, full_b, hp, grads_resident=True,
+               regen=None, main_stream=None, side_stream=None):
+    """One whole ZeRO-3 step issued by the native scheduler.  grads: per-rank
+    gradients (all units concatenated when grads_resident, else one unit-sized
+    buffer per rank refilled by `regen`, a zero_regen_t)."""
+    g, rows = _rows(grads, 2, "grads")
+    w, _ = _rows(master, 4, "master")
+    mm, _ = _rows(m, 4, "m")
+    vv, _ = _rows(v, 4, "v")
+    s, _ = _rows(shard_bf16, 2, "shard_bf16")
+    arr = (zero_unit_t * len(units))(*units)
+    _check("zero3_step", lib.zero3_step(
+        arr, len(units), len(rows), g, 1 if grads_resident else 0, w, mm, vv, s,
+        _dev(full_a, 2, "full_a"), _dev(full_b, 2, "full_b"), C.byref(hp),
+        C.byref(regen) if regen is not None else None, _stream(main_stream), _stream(side_stream)))
 
 
 # ------------------------------------------------------------------ harness calls

@@ -1,0 +1,184 @@
+// zero3_sched.cpp -- the native ZeRO-3 step scheduler (zero3_plan, zero3_step).
+//
+// Order ("Data parallelism, ZeRO and FSDP", "How FSDP implements ZeRO-3",
+// steps 2-5; "Data parallelism, collectives and ZeRO/FSDP", the per-unit
+// FSDP step figure): a forward pass that gathers every unit, a backward pass
+// in reverse unit order that gathers each unit again and reduce-scatters its
+// gradients, gathers on a separate stream, and the next unit's gather issued
+// before the current unit's work, with at most two units gathered at once.
+//
+// The plan is built on the host as a list of operations and then executed,
+// so the same plan can be checked on a machine without a GPU.  Executing it
+// costs one library call per gather / reduce-scatter and a handful of event
+// records and waits per unit -- microseconds of host time per unit, so small
+// units stay GPU-bound.
+#include <vector>
+
+#include "zero_internal.h"
+
+namespace zero {
+namespace {
+
+constexpr int kEvents = 5; // start, gathered[2], released[2]
+constexpr int kMaxDevices = 64;
+constexpr int kEvStart = 0, kEvGathered = 1, kEvReleased = 3;
+
+struct PlanBuilder {
+    std::vector<zero_op_t> ops;
+    bool released_recorded[2] = {false, false};
+
+    void add(int32_t kind, int32_t stream, int32_t unit, int32_t arg)
+    {
+        ops.push_back(zero_op_t{kind, stream, unit, arg});
+    }
+
+    // The side stream fills full buffer `slot` with unit `u` once the main
+    // stream has released that buffer, then marks the unit gathered.
+    void gather(int32_t u, int32_t pos, int32_t slot)
+    {
+        if (released_recorded[slot]) add(ZERO_OP_WAIT, 1, -1, kEvReleased + slot);
+        add(ZERO_OP_GATHER, 1, u, slot);
+        add(ZERO_OP_RECORD, 1, -1, kEvGathered + pos % 2);
+    }
+
+    void pass(int32_t n_units, bool backward, bool regen)
+    {
+        auto unit_at = [&](int32_t pos) { return backward ? n_units - 1 - pos : pos; };
+        gather(unit_at(0), 0, 0);
+        for (int32_t pos = 0; pos < n_units; ++pos) {
+            const int32_t slot = pos % 2;
+            const int32_t u = unit_at(pos);
+            if (pos + 1 < n_units) gather(unit_at(pos + 1), pos + 1, 1 - slot); // prefetch
+            add(ZERO_OP_WAIT, 0, -1, kEvGathered + pos % 2);
+            add(ZERO_OP_USE, 0, u, slot);
+            if (backward) {
+                if (regen) add(ZERO_OP_REGEN, 0, u, 0);
+                add(ZERO_OP_REDUCE_SCATTER, 0, u, 0);
+            }
+            add(ZERO_OP_RECORD, 0, -1, kEvReleased + slot);
+            released_recorded[slot] = true;
+        }
+    }
+
+    void step(int32_t n_units, bool regen)
+    {
+        // the step's first gather must see everything the main stream did before
+        add(ZERO_OP_RECORD, 0, -1, kEvStart);
+        add(ZERO_OP_WAIT, 1, -1, kEvStart);
+        pass(n_units, false, regen);
+        pass(n_units, true, regen);
+    }
+};
+
+// Five timing-free events per host thread and device, created on first use.
+struct EventCache {
+    int device = -1;
+    cudaEvent_t ev[kEvents] = {};
+};
+thread_local EventCache t_events[kMaxDevices];
+
+int events_for_current_device(cudaEvent_t** out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ZERO_ECUDA;
+    EventCache& c = t_events[dev];
+    if (c.device != dev) {
+        for (int i = 0; i < kEvents; ++i)
+            if (cudaEventCreateWithFlags(&c.ev[i], cudaEventDisableTiming) != cudaSuccess)
+                return ZERO_ECUDA;
+        c.device = dev;
+    }
+    *out = c.ev;
+    return ZERO_OK;
+}
+
+bool unit_consistent(const zero_unit_t& u, int32_t n_ranks)
+{
+    return u.n_params > 0 && u.n_params <= u.n_padded && u.shard_len > 0 &&
+           u.shard_len % 8 == 0 && u.shard_len * n_ranks == u.n_padded && u.offset >= 0 &&
+           u.offset % 8 == 0 && u.shard_offset >= 0 && u.shard_offset % 8 == 0;
+}
+
+} // namespace
+} // namespace zero
+
+using namespace zero;
+
+extern "C" int zero3_plan(int32_t n_units, int32_t regen, zero_op_t* ops, int32_t max_ops,
+                          int32_t* n_ops)
+{
+    if (n_units < 1 || !ops || !n_ops || max_ops < 0) return ZERO_EINVAL;
+    PlanBuilder b;
+    b.step(n_units, regen != 0);
+    if (static_cast<int64_t>(b.ops.size()) > max_ops) return ZERO_EINVAL;
+    for (size_t i = 0; i < b.ops.size(); ++i) ops[i] = b.ops[i];
+    *n_ops = static_cast<int32_t>(b.ops.size());
+    return ZERO_OK;
+}
+
+extern "C" int zero3_step(const zero_unit_t* units, int32_t n_units, int32_t n_ranks,
+                          const uint16_t* const* grads, int32_t grads_resident,
+                          float* const* master, float* const* m, float* const* v,
+                          uint16_t* const* shard_bf16, uint16_t* full_a, uint16_t* full_b,
+                          const zero_hparams_t* hp, const zero_regen_t* regen,
+                          cudaStream_t main_stream, cudaStream_t side_stream)
+{
+    if (!units || n_units < 1 || n_ranks < 1 || n_ranks > ZERO_MAX_RANKS || !valid_hparams(hp) ||
+        !full_a || !full_b || full_a == full_b || main_stream == side_stream ||
+        (!grads_resident && !regen))
+        return ZERO_EINVAL;
+    for (int32_t u = 0; u < n_units; ++u)
+        if (!unit_consistent(units[u], n_ranks)) return ZERO_EINVAL;
+    int rc;
+    if ((rc = check_table(grads, n_ranks)) != ZERO_OK) return rc;
+    if ((rc = check_table(master, n_ranks)) != ZERO_OK) return rc;
+    if ((rc = check_table(m, n_ranks)) != ZERO_OK) return rc;
+    if ((rc = check_table(v, n_ranks)) != ZERO_OK) return rc;
+    if ((rc = check_table(shard_bf16, n_ranks)) != ZERO_OK) return rc;
+    if (!aligned16(full_a) || !aligned16(full_b)) return ZERO_EALIGN;
+
+    cudaEvent_t* ev = nullptr;
+    if ((rc = events_for_current_device(&ev)) != ZERO_OK) return rc;
+    PlanBuilder plan;
+    plan.step(n_units, regen != nullptr);
+
+    const uint16_t* unit_grads[ZERO_MAX_RANKS];
+    uint16_t* unit_grads_w[ZERO_MAX_RANKS];
+    auto grads_of = [&](int32_t u) {
+        const int64_t off = grads_resident ? units[u].offset : 0;
+        for (int32_t r = 0; r < n_ranks; ++r) {
+            unit_grads[r] = grads[r] + off;
+            unit_grads_w[r] = const_cast<uint16_t*>(grads[r]) + off;
+        }
+    };
+    for (const zero_op_t& op : plan.ops) {
+        cudaStream_t s = op.stream == 0 ? main_stream : side_stream;
+        switch (op.kind) {
+        case ZERO_OP_RECORD:
+            rc = cuda_status(cudaEventRecord(ev[op.arg], s));
+            break;
+        case ZERO_OP_WAIT:
+            rc = cuda_status(cudaStreamWaitEvent(s, ev[op.arg], 0));
+            break;
+        case ZERO_OP_GATHER:
+            rc = zero3_gather_unit(&units[op.unit], n_ranks, shard_bf16,
+                                   op.arg == 0 ? full_a : full_b, s);
+            break;
+        case ZERO_OP_REGEN:
+            grads_of(op.unit);
+            rc = zero_gen_grads_unit(regen->seed, hp->step, regen->sigma, regen->outliers,
+                                     &units[op.unit], n_ranks, unit_grads_w, s);
+            break;
+        case ZERO_OP_REDUCE_SCATTER:
+            grads_of(op.unit);
+            rc = zero3_reduce_scatter_unit(&units[op.unit], n_ranks, unit_grads, master, m, v,
+                                           shard_bf16, hp, s);
+            break;
+        default: // ZERO_OP_USE: the unit's compute would run here
+            rc = ZERO_OK;
+            break;
+        }
+        if (rc != ZERO_OK) return rc;
+    }
+    return ZERO_OK;
+}

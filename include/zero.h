@@ -34,7 +34,8 @@
  *    be 16-byte aligned (ZERO_EALIGN otherwise).
  *  - Arguments are checked on the host before anything is launched; a bad
  *    argument launches nothing.  ZERO_ECUDA reports a launch failure.
- *  - Stateless and re-entrant.  1 <= n_ranks <= ZERO_MAX_RANKS.
+ *  - Stateless and re-entrant (zero3_step alone keeps a per-thread cache of
+ *    five CUDA events).  1 <= n_ranks <= ZERO_MAX_RANKS.
  *
  * Layout (zero_layout): a unit of P true parameters is padded to
  * P' = ceil(P / (n_ranks*align)) * n_ranks*align; S = P'/n_ranks; rank k owns
@@ -174,6 +175,80 @@ int zero3_reduce_scatter_unit(const zero_unit_t* unit, int32_t n_ranks,
  * null out. */
 int zero_state_bytes(int64_t n_params, int32_t n_ranks, int32_t stage, int32_t K,
                      zero_bytes_t* out);
+
+/* ---------------------------------------------------------------------
+ * ZeRO-3 step scheduler: the per-unit order of [DZF] "How FSDP implements
+ * ZeRO-3", steps 2-5 (and [COL]'s per-unit step figure), issued natively.
+ * ------------------------------------------------------------------- */
+
+/* One operation of a ZeRO-3 step plan.  stream: 0 = main (reduce-scatter,
+ * regeneration, unit use), 1 = side (gathers).  RECORD/WAIT name one of the
+ * plan's five reusable events in `arg` (0 = step start, 1..2 = "unit
+ * gathered", 3..4 = "full buffer released"); GATHER names the unit and in
+ * `arg` the full buffer (0 or 1) it fills; USE names the unit and in `arg`
+ * the full buffer it reads: it marks where the unit's forward or backward
+ * compute would run on the main stream (no work here); REDUCE_SCATTER and
+ * REGEN name the unit. */
+typedef struct {
+    int32_t kind;
+    int32_t stream;
+    int32_t unit;
+    int32_t arg;
+} zero_op_t;
+
+#define ZERO_OP_RECORD 1
+#define ZERO_OP_WAIT 2
+#define ZERO_OP_GATHER 3
+#define ZERO_OP_REDUCE_SCATTER 4
+#define ZERO_OP_REGEN 5
+#define ZERO_OP_USE 6
+
+/* zero3_plan -- host only.  The operations of one ZeRO-3 step over n_units
+ * units, in issue order: record "start" on main and make side wait for it;
+ * forward over units 0..U-1 and backward over U-1..0, each pass gathering
+ * unit p+1 into the other full buffer on the side stream (after the side
+ * stream waits for that buffer's release) before the main stream waits for
+ * unit p, uses it, and -- in the backward pass -- (optionally regenerates
+ * and) reduce-scatters it, then records the buffer's release.  Two gathers
+ * and one reduce-scatter per unit; at most two units gathered at a time.
+ *   regen      non-zero: a REGEN op precedes each REDUCE_SCATTER
+ *   ops        caller array of max_ops entries; *n_ops receives the count
+ *              (13*n_units + 2, plus n_units with regen, at most)
+ * ZERO_EINVAL on n_units < 1, null pointers or max_ops too small. */
+int zero3_plan(int32_t n_units, int32_t regen, zero_op_t* ops, int32_t max_ops,
+               int32_t* n_ops);
+
+/* Harness regeneration of a unit's gradients inside zero3_step (the
+ * stand-in for the backward compute that would produce them). */
+typedef struct {
+    uint64_t seed;
+    double sigma;
+    int32_t outliers;
+} zero_regen_t;
+
+/* zero3_step -- one whole ZeRO-3 step: executes zero3_plan's operations with
+ * zero3_gather_unit, zero3_reduce_scatter_unit and (if regen != NULL)
+ * zero_gen_grads_unit, on main_stream and side_stream, which must differ.
+ *   units[n_units]   layouts from one zero_layout call (host array)
+ *   grads            n_ranks device pointers.  grads_resident != 0: rank r's
+ *                    gradients of every unit, concatenated (unit u at
+ *                    units[u].offset, total padded length); == 0: one
+ *                    buffer of the largest unit's n_padded, reused per unit
+ *                    (requires regen, which fills it before each unit's
+ *                    reduce-scatter)
+ *   master, m, v, shard_bf16   as zero3_reduce_scatter_unit
+ *   full_a, full_b   two device buffers of the largest unit's n_padded bf16
+ *   hp               the step's hyper-parameters (the same t for all units)
+ * The library keeps five timing-free CUDA events per host thread and device
+ * (created on first use); no device memory is allocated.  Work is queued
+ * asynchronously; on return main_stream carries the end of the step.
+ * ZERO_EINVAL / ZERO_EALIGN / ZERO_ECUDA. */
+int zero3_step(const zero_unit_t* units, int32_t n_units, int32_t n_ranks,
+               const uint16_t* const* grads, int32_t grads_resident,
+               float* const* master, float* const* m, float* const* v,
+               uint16_t* const* shard_bf16, uint16_t* full_a, uint16_t* full_b,
+               const zero_hparams_t* hp, const zero_regen_t* regen,
+               cudaStream_t main_stream, cudaStream_t side_stream);
 
 /* ---------------------------------------------------------------------
  * Harness calls: seeded synthetic inputs and helpers.  They are not part

@@ -1,0 +1,93 @@
+"""Happens-before checks of a two-stream ZeRO-3 step trace (test helper).
+
+A trace is a list of entries in host issue order:
+  ("record", stream, event)   ("wait", stream, event)
+  ("gather", stream, unit, buffer)   ("use", stream, unit, buffer, ...)
+  ("rs", stream, unit)   ("regen", stream, unit)
+with stream "main" or "side".  A wait orders the waiting stream's later
+operations after the operation that preceded the event's most recent record
+at the time of the wait (CUDA's semantics for a re-recorded event)."""
+
+
+def happens_before_graph(trace):
+    pos, last_op, event_src, edges = {}, {}, {}, {}
+    count = {"main": 0, "side": 0}
+    pending = {"main": [], "side": []}
+    for e in trace:
+        kind, stream = e[0], e[1]
+        if kind == "record":
+            event_src[e[2]] = last_op.get(stream)
+            continue
+        if kind == "wait":
+            if event_src.get(e[2]) is not None:
+                pending[stream].append(event_src[e[2]])
+            continue
+        node = (stream, count[stream])
+        count[stream] += 1
+        pos[node] = e
+        preds = list(pending[stream])
+        pending[stream].clear()
+        if stream in last_op:
+            preds.append(last_op[stream])
+        edges[node] = preds
+        last_op[stream] = node
+    return pos, edges
+
+
+def hb(edges, a, b):
+    """True when operation a happens before operation b."""
+    stack, seen = [b], set()
+    while stack:
+        n = stack.pop()
+        for p in edges.get(n, []):
+            if p == a:
+                return True
+            if p not in seen:
+                seen.add(p)
+                stack.append(p)
+    return False
+
+
+def check_zero3_trace(trace, n_units, n_steps):
+    """Assert the ZeRO-3 schedule properties of "Data parallelism, ZeRO and FSDP",
+    "How FSDP implements ZeRO-3", steps 2-5, on a trace of n_steps steps."""
+    U = n_units
+    pos, edges = happens_before_graph(trace)
+    order_of = {id(e): i for i, e in enumerate(trace)}
+    by_issue = lambda nodes: sorted(nodes, key=lambda n: order_of[id(pos[n])])
+    gathers = by_issue([n for n, e in pos.items() if e[0] == "gather"])
+    uses = by_issue([n for n, e in pos.items() if e[0] == "use"])
+    rss = by_issue([n for n, e in pos.items() if e[0] == "rs"])
+    assert len(gathers) == 2 * U * n_steps and len(uses) == 2 * U * n_steps
+    assert len(rss) == U * n_steps
+    assert all(n[0] == "side" for n in gathers) and all(n[0] == "main" for n in uses + rss)
+    # forward 0..U-1, backward U-1..0, every step
+    assert [pos[n][2] for n in gathers] == (list(range(U)) + list(range(U - 1, -1, -1))) * n_steps
+    assert [pos[n][2] for n in uses] == (list(range(U)) + list(range(U - 1, -1, -1))) * n_steps
+    # two full buffers, alternating
+    assert len({pos[n][3] for n in gathers}) == (2 if U > 1 or n_steps > 1 else 1)
+    for g, u in zip(gathers, uses):
+        assert pos[g][2] == pos[u][2] and pos[g][3] == pos[u][3]
+        assert hb(edges, g, u), "unit %d used before it was gathered" % pos[u][2]
+        later = [h for h in gathers if order_of[id(pos[h])] > order_of[id(pos[g])]
+                 and pos[h][3] == pos[g][3]]
+        if later:
+            assert hb(edges, u, later[0]), "buffer of unit %d overwritten in use" % pos[u][2]
+    # each reduce-scatter follows its unit's backward use; backward prefetch:
+    # the gather of unit u-1 is issued before unit u's reduce-scatter and does
+    # not delay it
+    bwd_uses = [u for k, u in enumerate(uses) if (k // U) % 2 == 1]
+    for r, u in zip(rss, bwd_uses):
+        assert pos[r][2] == pos[u][2] and hb(edges, u, r)
+        unit = pos[r][2]
+        if unit > 0:
+            pre = [g for g in gathers if pos[g][2] == unit - 1
+                   and order_of[id(pos[g])] < order_of[id(pos[r])]]
+            assert pre, "no prefetch of unit %d before unit %d's reduce-scatter" % (unit - 1, unit)
+            assert not hb(edges, pre[-1], r)
+    # the next step's first gather sees the previous step's last reduce-scatter
+    for s in range(1, n_steps):
+        assert hb(edges, rss[s * U - 1], gathers[s * 2 * U])
+    # at most two units gathered and not yet released at any time is implied by
+    # the two buffers and the overwrite check above
+    return True

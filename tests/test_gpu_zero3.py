@@ -196,3 +196,75 @@ def test_llama_7b_shaped_zero3_full_size_sampled(orc):
     gradients regenerated from the seed in each unit's backward, 10 steps."""
     _sampled_zero3_check(orc, LLAMA_7B, 8, 10, 1_000_000)
     H.free()
+
+
+def _native_buffers(units, total, N, resident):
+    master, m, v, shards = _zero3_buffers(units, total, N)
+    max_unit = max(u.n_padded for u in units)
+    grads = H.Guarded(N, total if resident else max_unit, torch.int16)
+    full_a = H.Guarded(1, max_unit, torch.int16)
+    full_b = H.Guarded(1, max_unit, torch.int16)
+    return master, m, v, shards, grads, full_a, full_b
+
+
+@pytest.mark.parametrize("resident", [True, False])
+def test_native_zero3_step_matches_ddp(orc, resident):
+    """zero3_step (the native scheduler) over T steps equals T DDP steps bit for
+    bit, with every unit's gradients resident (refilled per step) or with one
+    unit-sized buffer per rank regenerated in each unit's backward."""
+    N, sizes, T, seed = 4, [70_000, 333, 200_000, 64, 90_001], 4, 2
+    units, total = B.zero_layout(sizes, N)
+    master, m, v, shards, grads, fa, fb = _native_buffers(units, total, N, resident)
+    side = torch.cuda.Stream()
+    regen = None if resident else B.zero_regen_t(seed, H.SIGMA_G, 1)
+    for t in range(1, T + 1):
+        if resident:
+            for u in units:
+                B.zero_gen_grads_unit(seed, t, H.SIGMA_G, 1, u,
+                                      [r[u.offset:u.offset + u.n_padded] for r in grads.rows])
+        B.zero3_step(units, grads.rows, master.rows, m.rows, v.rows, shards.rows, fa.rows[0],
+                     fb.rows[0], H.hp(t), grads_resident=resident, regen=regen, side_stream=side)
+    torch.cuda.synchronize()
+    for b in (master, m, v, shards, grads, fa, fb):
+        b.check()
+    ddp = orc.sim_ddp(N, sum(sizes), seed, H.SIGMA_W, H.SIGMA_G, 1, orc.hparams(**H.HP, step=1), T)
+    got = {k: [] for k in ("p", "w", "m", "v")}
+    sh, w, mm, vv = shards.numpy(), master.numpy(), m.numpy(), v.numpy()
+    for u in units:
+        for name, src in (("p", sh), ("w", w), ("m", mm), ("v", vv)):
+            rows = [src[k][u.shard_offset:u.shard_offset + u.shard_len] for k in range(N)]
+            got[name].append(np.concatenate(rows)[:u.n_params])
+    for (name, ref) in zip(("p", "w", "m", "v"), ddp):
+        H.assert_bitwise(np.concatenate(got[name]), ref, name)
+
+
+def test_native_zero3_step_rejects():
+    units, total = B.zero_layout([1000, 64], 2)
+    master, m, v, shards, grads, fa, fb = _native_buffers(units, total, 2, True)
+    cur = torch.cuda.current_stream()
+    with pytest.raises(B.ZeroError):  # main == side
+        B.zero3_step(units, grads.rows, master.rows, m.rows, v.rows, shards.rows, fa.rows[0],
+                     fb.rows[0], H.hp(1), side_stream=cur)
+    with pytest.raises(B.ZeroError):  # non-resident gradients need regeneration
+        B.zero3_step(units, grads.rows, master.rows, m.rows, v.rows, shards.rows, fa.rows[0],
+                     fb.rows[0], H.hp(1), grads_resident=False, side_stream=torch.cuda.Stream())
+    with pytest.raises(B.ZeroError):  # the two full buffers must differ
+        B.zero3_step(units, grads.rows, master.rows, m.rows, v.rows, shards.rows, fa.rows[0],
+                     fa.rows[0], H.hp(1), side_stream=torch.cuda.Stream())
+    torch.cuda.synchronize()
+
+
+def test_stream_wait_times_out_then_completes():
+    """zero_stream_wait returns ZERO_ETIMEOUT while queued work is still running
+    (no hang, the context stays usable) and ZERO_OK once it has finished."""
+    N = 8
+    (u,), _ = B.zero_layout([64 * 2**20], N)
+    g = torch.empty((N, u.n_padded), dtype=torch.int16, device="cuda")
+    torch.cuda.synchronize()
+    for _ in range(20):  # ~20 x 1 ms of generator work queued
+        B.zero_gen_grads_unit(0, 1, 1e-3, 1, u, g)
+    with pytest.raises(B.ZeroError) as e:
+        B.zero_stream_wait(timeout_ms=0)
+    assert e.value.code == B.ZERO_ETIMEOUT
+    B.zero_stream_wait(timeout_ms=60_000)
+    assert torch.cuda.current_stream().query()

@@ -9,6 +9,7 @@ import numpy as np
 import pytest
 
 from fsdp_sharded_optimizer_gb300.zero3 import Zero3Schedule
+from schedule_check import check_zero3_trace
 
 HP = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
 
@@ -90,50 +91,6 @@ def test_two_units_four_gathers_two_reduce_scatters(orc):
     assert ops.count("gather") == 4 and ops.count("rs") == 2
 
 
-def _happens_before_graph(trace):
-    """Ops per stream in program order, plus edges from each wait to the op just
-    before the awaited event's record on the other stream."""
-    pos = {}            # (stream, i) -> trace entry
-    last_op = {}        # stream -> (stream, i) of its latest op
-    event_src = {}      # event -> op that precedes its record (or None)
-    edges = {}
-    count = {"main": 0, "side": 0}
-    pending_wait = {"main": [], "side": []}
-    for e in trace:
-        kind, stream = e[0], e[1]
-        if kind == "record":
-            event_src[e[2]] = last_op.get(stream)
-            continue
-        if kind == "wait":
-            if event_src.get(e[2]) is not None:
-                pending_wait[stream].append(event_src[e[2]])
-            continue
-        node = (stream, count[stream])
-        count[stream] += 1
-        pos[node] = e
-        preds = list(pending_wait[stream])
-        pending_wait[stream].clear()
-        if stream in last_op:
-            preds.append(last_op[stream])
-        edges[node] = preds
-        last_op[stream] = node
-    return pos, edges
-
-
-def _hb(edges, a, b):
-    """True when op a happens before op b."""
-    stack, seen = [b], set()
-    while stack:
-        n = stack.pop()
-        for p in edges.get(n, []):
-            if p == a:
-                return True
-            if p not in seen:
-                seen.add(p)
-                stack.append(p)
-    return False
-
-
 def test_prefetch_order_and_buffer_safety(orc):
     units, be, sched, full = _setup(orc, [100, 200, 300, 400, 64], 2, 0)
     slot_of = lambda view: id(view.base) if view.base is not None else id(view)
@@ -141,39 +98,48 @@ def test_prefetch_order_and_buffer_safety(orc):
     for t in (1, 2):
         sched.step(orc.hparams(**HP, step=t), _make_grads(orc, 0, t, 2), forward=use("fwd"),
                    backward=use("bwd"))
-    pos, edges = _happens_before_graph(be.trace)
-    gathers = [n for n, e in pos.items() if e[0] == "gather"]
-    uses = [n for n, e in pos.items() if e[0] == "use"]
-    rss = [n for n, e in pos.items() if e[0] == "rs"]
-    U = len(units)
-    assert len(gathers) == 2 * 2 * U and len(uses) == 2 * 2 * U and len(rss) == 2 * U
-    # gathers on the side stream, uses and reduce-scatters on the main stream
-    assert all(n[0] == "side" for n in gathers) and all(n[0] == "main" for n in uses + rss)
-    # order: forward 0..U-1 then backward U-1..0, every step
-    order = [pos[n][2] for n in sorted(gathers, key=lambda n: n[1])]
-    assert order == (list(range(U)) + list(range(U - 1, -1, -1))) * 2
-    # only two full buffers exist
-    assert len({pos[n][3] for n in gathers}) == 2
-    # every use sees its own gather, and the buffer is not overwritten before the use
-    # ends: the next gather into the same buffer happens after the use
-    gathers_sorted = sorted(gathers, key=lambda n: n[1])
-    uses_sorted = sorted(uses, key=lambda n: n[1])
-    for g, u in zip(gathers_sorted, uses_sorted):
-        assert pos[g][2] == pos[u][2] and pos[g][3] == pos[u][3]
-        assert _hb(edges, g, u), "use of unit %d may run before its gather" % pos[u][2]
-        later = [h for h in gathers_sorted if h[1] > g[1] and pos[h][3] == pos[g][3]]
-        if later:
-            assert _hb(edges, u, later[0]), "buffer of unit %d overwritten while in use" % pos[u][2]
-    # backward prefetch: unit u-1's gather is issued before unit u's reduce-scatter,
-    # and the reduce-scatter of unit u does not wait for it
-    trace_index = {id(e): i for i, e in enumerate(be.trace)}
-    for r in rss:
-        u = pos[r][2]
-        if u == 0:
-            continue
-        pre = [g for g in gathers if pos[g][2] == u - 1 and trace_index[id(pos[g])] < trace_index[id(pos[r])]]
-        assert pre, "no prefetch of unit %d before the reduce-scatter of unit %d" % (u - 1, u)
-        assert not _hb(edges, pre[-1], r)
-    # a step's first gather happens after the previous step's last reduce-scatter
-    first_of_step2 = gathers_sorted[2 * U]
-    assert _hb(edges, sorted(rss, key=lambda n: n[1])[U - 1], first_of_step2)
+    check_zero3_trace(be.trace, len(units), 2)
+
+
+def _native_trace(n_units, n_steps, regen=False):
+    from fsdp_sharded_optimizer_gb300 import _binding as B
+    names = {0: "main", 1: "side"}
+    trace = []
+    for _ in range(n_steps):
+        for kind, stream, unit, arg in B.zero3_plan(n_units, regen):
+            st = names[stream]
+            if kind in ("record", "wait"):
+                trace.append((kind, st, "ev%d" % arg))
+            elif kind == "gather":
+                trace.append(("gather", st, unit, arg))
+            elif kind == "use":
+                trace.append(("use", st, unit, arg))
+            elif kind == "reduce_scatter":
+                trace.append(("rs", st, unit))
+            else:
+                trace.append((kind, st, unit))
+    return trace
+
+
+@pytest.mark.parametrize("n_units,n_steps,regen", [(1, 1, False), (2, 1, False), (5, 3, False),
+                                                   (33, 2, True), (23, 2, False)])
+def test_native_plan_is_safe(n_units, n_steps, regen):
+    """The native scheduler's plan (zero3_plan, the operations zero3_step
+    executes) obeys the same happens-before rules as the Python schedule."""
+    check_zero3_trace(_native_trace(n_units, n_steps, regen), n_units, n_steps)
+
+
+def test_native_plan_counts_and_regen():
+    from fsdp_sharded_optimizer_gb300 import _binding as B
+    ops = B.zero3_plan(2, False)
+    kinds = [o[0] for o in ops]
+    assert kinds.count("gather") == 4 and kinds.count("reduce_scatter") == 2
+    assert "regen" not in kinds and len(ops) <= 13 * 2 + 2
+    ops = B.zero3_plan(4, True)
+    kinds = [o[0] for o in ops]
+    assert kinds.count("regen") == 4 and len(ops) <= 14 * 4 + 2
+    # every regeneration immediately precedes its unit's reduce-scatter on the main stream
+    for i, o in enumerate(ops):
+        if o[0] == "regen":
+            assert ops[i + 1][0] == "reduce_scatter" and ops[i + 1][2] == o[2]
+            assert o[1] == 0
