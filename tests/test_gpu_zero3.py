@@ -38,13 +38,13 @@ def test_gather_unit_matches_oracle(orc, N, sizes):
     shards.check()
 
 
-def _zero3_buffers(units, total, N):
+def _zero3_buffers(units, total, N, seed=0):
     shard_total = total // N
     master = H.Guarded(N, shard_total, torch.float32)
     m = H.Guarded(N, shard_total, torch.float32).zero_()
     v = H.Guarded(N, shard_total, torch.float32).zero_()
     shards = H.Guarded(N, shard_total, torch.int16)
-    B.zero_gen_master(0, H.SIGMA_W, units, master.rows)
+    B.zero_gen_master(seed, H.SIGMA_W, units, master.rows)
     for k in range(N):
         B.zero_cast_bf16(master.rows[k], shards.rows[k])
     return master, m, v, shards
@@ -198,8 +198,8 @@ def test_llama_7b_shaped_zero3_full_size_sampled(orc):
     H.free()
 
 
-def _native_buffers(units, total, N, resident):
-    master, m, v, shards = _zero3_buffers(units, total, N)
+def _native_buffers(units, total, N, resident, seed=0):
+    master, m, v, shards = _zero3_buffers(units, total, N, seed)
     max_unit = max(u.n_padded for u in units)
     grads = H.Guarded(N, total if resident else max_unit, torch.int16)
     full_a = H.Guarded(1, max_unit, torch.int16)
@@ -214,7 +214,7 @@ def test_native_zero3_step_matches_ddp(orc, resident):
     unit-sized buffer per rank regenerated in each unit's backward."""
     N, sizes, T, seed = 4, [70_000, 333, 200_000, 64, 90_001], 4, 2
     units, total = B.zero_layout(sizes, N)
-    master, m, v, shards, grads, fa, fb = _native_buffers(units, total, N, resident)
+    master, m, v, shards, grads, fa, fb = _native_buffers(units, total, N, resident, seed)
     side = torch.cuda.Stream()
     regen = None if resident else B.zero_regen_t(seed, H.SIGMA_G, 1)
     for t in range(1, T + 1):
