@@ -85,6 +85,10 @@ def lib():
             "or_sim_zero": (i32, [i32, i32, P, i32, i32, u64, f64, f64, i32, P, i32,
                                   i64, P, P, P, P, P]),
             "or_sample": (None, [i32, u64, f64, f64, i32, P, i32, P, i64, P, P, P, P]),
+            "or_grad_sumsq": (f64, [i32, i64, P]),
+            "or_clip_coef": (f32, [f64, f64, P]),
+            "or_zero12_step_clip": (i32, [i32, i32, i64, P, P, P, P, P, P, i64, f64, P, P]),
+            "or_zero3_reduce_scatter_unit_coef": (i32, [P, i32, P, P, P, P, P, P, f32]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -180,6 +184,37 @@ def zero3_reduce_scatter_unit(unit, unit_grads, master, m, v, shards, hp):
     _check(lib().or_zero3_reduce_scatter_unit(
         C.byref(unit), unit_grads.shape[0], _rows(unit_grads), _rows(master), _rows(m),
         _rows(v), _rows(shards), C.byref(hp)), "or_zero3_reduce_scatter_unit")
+
+
+# ------------------------------------------------------------- clipping
+def grad_sumsq(grads):
+    g = np.ascontiguousarray(grads, dtype=np.uint16)
+    return lib().or_grad_sumsq(g.shape[0], g.shape[1], _rows(g))
+
+
+def clip_coef(sumsq, max_norm):
+    """(coef as numpy float32, norm as float)"""
+    norm = C.c_double()
+    c = lib().or_clip_coef(float(sumsq), float(max_norm), C.byref(norm))
+    return np.float32(c), norm.value
+
+
+def zero12_step_clip(stage, grads, master, m, v, params, hp, max_norm, bucket_elems=0):
+    """In place, like zero12_step, after clipping the mean gradient to max_norm.
+    Returns (norm, coef)."""
+    N, Pp = grads.shape
+    norm, coef = C.c_double(), C.c_float()
+    _check(lib().or_zero12_step_clip(stage, N, Pp, _rows(grads), _rows(master), _rows(m),
+                                     _rows(v), _ptr(params), C.byref(hp), bucket_elems,
+                                     float(max_norm), C.byref(norm), C.byref(coef)),
+           "or_zero12_step_clip")
+    return norm.value, np.float32(coef.value)
+
+
+def zero3_reduce_scatter_unit_coef(unit, unit_grads, master, m, v, shards, hp, coef):
+    _check(lib().or_zero3_reduce_scatter_unit_coef(
+        C.byref(unit), unit_grads.shape[0], _rows(unit_grads), _rows(master), _rows(m),
+        _rows(v), _rows(shards), C.byref(hp), float(coef)), "or_zero3_reduce_scatter_unit_coef")
 
 
 # ------------------------------------------------------------- accounting

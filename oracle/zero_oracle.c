@@ -245,6 +245,95 @@ int or_zero3_reduce_scatter_unit(const or_unit_t* unit, int32_t n_ranks,
 }
 
 /* ======================================================================
+ * Global gradient-norm clipping.  [DZF] "7. Common mistakes" (local
+ * gradient clipping): with sharded gradients the global norm needs an
+ * all-reduce of the squared shard norms.  [DDF] "A complete rank-aware DDP
+ * reference" clips with torch's clip_grad_norm_(params, 1.) before the
+ * optimizer step; its rule is used: norm = ||g||_2 over the whole averaged
+ * gradient, coef = max_norm / (norm + 1e-6) clamped to at most 1, and the
+ * gradient is multiplied by coef.  The norm is accumulated in double
+ * (each g is an fp32 value, so g*g is exact in double); coef is computed in
+ * double and rounded once to fp32; the scaled gradient is one fp32 multiply.
+ * ==================================================================== */
+double or_grad_sumsq(int32_t n_ranks, int64_t n, const uint16_t* const* grads)
+{
+    float inv_n = (float)(1.0 / (double)n_ranks);
+    double sum = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+        double g = (double)or_reduce_mean(grads, n_ranks, i, inv_n);
+        sum = sum + g * g;
+    }
+    return sum;
+}
+
+float or_clip_coef(double sumsq, double max_norm, double* out_norm)
+{
+    double norm = sqrt(sumsq);
+    double c = max_norm / (norm + 1e-6);
+    if (c > 1.0)
+        c = 1.0;
+    if (out_norm)
+        *out_norm = norm;
+    return (float)c;
+}
+
+int or_zero12_step_clip(int32_t stage, int32_t n_ranks, int64_t n_padded,
+                        const uint16_t* const* grads, float* const* master,
+                        float* const* m, float* const* v, uint16_t* params_bf16,
+                        const or_hparams_t* hp, int64_t bucket_elems, double max_norm,
+                        double* out_norm, float* out_coef)
+{
+    if ((stage != 1 && stage != 2) || n_ranks < 1 || n_padded <= 0 ||
+        n_padded % n_ranks != 0 || !grads || !master || !m || !v ||
+        !params_bf16 || bad_hp(hp) || bucket_elems < 0 || !(max_norm > 0))
+        return OR_EINVAL;
+    /* every owner's squared shard norm, summed over the owners: the global norm */
+    double coef_norm;
+    float coef = or_clip_coef(or_grad_sumsq(n_ranks, n_padded, grads), max_norm, &coef_norm);
+    if (out_norm)
+        *out_norm = coef_norm;
+    if (out_coef)
+        *out_coef = coef;
+    int64_t S = n_padded / n_ranks;
+    or_scalars_t s;
+    or_scalars(hp, n_ranks, &s);
+    int64_t bucket = (stage == 2 && bucket_elems > 0) ? bucket_elems : n_padded;
+    for (int64_t b0 = 0; b0 < n_padded; b0 += bucket) {
+        int64_t b1 = b0 + bucket < n_padded ? b0 + bucket : n_padded;
+        for (int64_t i = b0; i < b1; ++i) {
+            int64_t k = i / S;
+            int64_t j = i - k * S;
+            float g = or_reduce_mean(grads, n_ranks, i, s.inv_n) * coef;
+            or_adamw(g, &master[k][j], &m[k][j], &v[k][j], &s);
+            params_bf16[i] = or_bf16_rne(master[k][j]);
+        }
+    }
+    return OR_OK;
+}
+
+int or_zero3_reduce_scatter_unit_coef(const or_unit_t* unit, int32_t n_ranks,
+                                      const uint16_t* const* unit_grads,
+                                      float* const* master, float* const* m,
+                                      float* const* v, uint16_t* const* shard_bf16,
+                                      const or_hparams_t* hp, float coef)
+{
+    if (!unit || n_ranks < 1 || !unit_grads || !master || !m || !v ||
+        !shard_bf16 || bad_hp(hp) || unit->shard_len * n_ranks != unit->n_padded)
+        return OR_EINVAL;
+    or_scalars_t s;
+    or_scalars(hp, n_ranks, &s);
+    int64_t S = unit->shard_len;
+    for (int64_t i = 0; i < unit->n_padded; ++i) {
+        int64_t k = i / S;
+        int64_t j = unit->shard_offset + (i - k * S);
+        float g = or_reduce_mean(unit_grads, n_ranks, i, s.inv_n) * coef;
+        or_adamw(g, &master[k][j], &m[k][j], &v[k][j], &s);
+        shard_bf16[k][j] = or_bf16_rne(master[k][j]);
+    }
+    return OR_OK;
+}
+
+/* ======================================================================
  * Accounting.  [DZF] Theorem (ZeRO memory and communication), table and
  * proof steps 1-7; [DDF] "Memory accounting" (state_bytes raises on
  * params <= 0 or ranks < 1).  Bytes per parameter: bf16 weight 2, bf16

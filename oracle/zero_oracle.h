@@ -106,6 +106,20 @@ int or_zero3_reduce_scatter_unit(const or_unit_t* unit, int32_t n_ranks,
                                  float* const* v, uint16_t* const* shard_bf16,
                                  const or_hparams_t* hp);
 
+/* ------------------------------------------------ global grad-norm clipping */
+double or_grad_sumsq(int32_t n_ranks, int64_t n, const uint16_t* const* grads);
+float or_clip_coef(double sumsq, double max_norm, double* out_norm);
+int or_zero12_step_clip(int32_t stage, int32_t n_ranks, int64_t n_padded,
+                        const uint16_t* const* grads, float* const* master,
+                        float* const* m, float* const* v, uint16_t* params_bf16,
+                        const or_hparams_t* hp, int64_t bucket_elems, double max_norm,
+                        double* out_norm, float* out_coef);
+int or_zero3_reduce_scatter_unit_coef(const or_unit_t* unit, int32_t n_ranks,
+                                      const uint16_t* const* unit_grads,
+                                      float* const* master, float* const* m,
+                                      float* const* v, uint16_t* const* shard_bf16,
+                                      const or_hparams_t* hp, float coef);
+
 /* ------------------------------------------------------------- accounting */
 int or_state_bytes(int64_t n_params, int32_t n_ranks, int32_t stage, int32_t K,
                    or_bytes_t* out);

@@ -36,6 +36,12 @@ MUTANTS = [
     ("reverse_rank_order", "zero_oracle.c",
      "for (int32_t r = 0; r < n_ranks; ++r)\n        g = g + or_bf16_to_f32(grads[r][i]);",
      "for (int32_t r = n_ranks - 1; r >= 0; --r)\n        g = g + or_bf16_to_f32(grads[r][i]);"),
+    ("clip_coef_from_sumsq", "zero_oracle.c", "double norm = sqrt(sumsq);", "double norm = sumsq;"),
+    ("clip_not_clamped", "zero_oracle.c", "    if (c > 1.0)\n        c = 1.0;\n", ""),
+    ("clip_eps_dropped", "zero_oracle.c", "double c = max_norm / (norm + 1e-6);",
+     "double c = max_norm / norm;"),
+    ("clip_coef_unused", "zero_oracle.c", "float g = or_reduce_mean(grads, n_ranks, i, s.inv_n) * coef;",
+     "float g = or_reduce_mean(grads, n_ranks, i, s.inv_n);"),
     ("generator_lane_dropped", "gen_oracle.c", "(int32_t)(h >> 48) - 131070", "(int32_t)(h >> 48) * 0 - 131070"),
 ]
 

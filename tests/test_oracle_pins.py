@@ -502,3 +502,113 @@ def test_accounting_rejects_bad_arguments(orc):
     assert orc.state_bytes_rc(-5, 8, 1) == orc.OR_EINVAL
     assert orc.state_bytes_rc(10, 0, 1) == orc.OR_EINVAL
     assert orc.state_bytes_rc(10, 8, 4) == orc.OR_EINVAL
+
+
+# ------------------------------------------------------------------ clipping
+def _reduced_grad(orc, grads):
+    inv = np.float32(1.0 / grads.shape[0])
+    return np.array([orc.reduce_mean(grads, i, inv) for i in range(grads.shape[1])], np.float32)
+
+
+@pytest.mark.parametrize("max_norm", [1e-3, 0.02, 1.0])
+def test_clip_matches_torch_clip_grad_norm(orc, max_norm):
+    """torch.nn.utils.clip_grad_norm_ (the call the DDP reference makes before
+    the optimizer step) on the averaged gradient gives the same global norm and
+    the same scaled gradient."""
+    N, P = 4, 3000
+    rng = np.random.default_rng(7)
+    grads = orc.bf16_rne((rng.normal(size=(N, P)) * 1e-3).astype(np.float32))
+    g = _reduced_grad(orc, grads)
+    p = torch.nn.Parameter(torch.zeros(P, dtype=torch.float64))
+    p.grad = torch.from_numpy(g.astype(np.float64))
+    total = float(torch.nn.utils.clip_grad_norm_([p], max_norm, foreach=False))
+    sumsq = orc.grad_sumsq(grads)
+    coef, norm = orc.clip_coef(sumsq, max_norm)
+    assert norm == pytest.approx(total, rel=1e-12)
+    clipped = p.grad.numpy()
+    np.testing.assert_allclose(g.astype(np.float64) * float(coef), clipped, rtol=1e-7, atol=0)
+    # through the clipped step: m after t = 1 is (1 - b1) times the clipped gradient
+    master = np.zeros((N, P // N + 0), np.float32)
+    (u,), _ = orc.layout([P], N, 8)
+    gp = np.zeros((N, u.n_padded), np.uint16)
+    gp[:, :P] = grads
+    w = np.zeros((N, u.shard_len), np.float32)
+    m, v = np.zeros_like(w), np.zeros_like(w)
+    params = np.zeros(u.n_padded, np.uint16)
+    n2, c2 = orc.zero12_step_clip(1, gp, w, m, v, params, orc.hparams(**HP, step=1), max_norm)
+    assert n2 == norm and c2 == coef
+    np.testing.assert_allclose(m.reshape(-1)[:P], 0.1 * clipped, rtol=3e-7, atol=1e-30)
+    del master
+
+
+def test_clip_constant_gradient_closed_form(orc):
+    N, P, c = 8, 4096, 2.0**-7
+    grads = np.zeros((N, P + 64 * N), np.uint16)
+    grads[:, :P] = orc.bf16_rne(np.full(P, c, np.float32))
+    coef, norm = orc.clip_coef(orc.grad_sumsq(grads), 0.1)
+    assert norm == pytest.approx(c * math.sqrt(P), rel=1e-15)
+    assert float(coef) == pytest.approx(0.1 / (c * math.sqrt(P) + 1e-6), rel=6e-8)
+
+
+def test_clip_inactive_is_bitwise_unclipped(orc):
+    N, P, T = 4, 5000, 5
+    (u,), _ = orc.layout([P], N)
+    a = [orc.gen_master(1, 0.02, [u], N)]
+    a += [np.zeros_like(a[0]), np.zeros_like(a[0]), np.zeros(u.n_padded, np.uint16)]
+    b = [x.copy() for x in a]
+    for t in range(1, T + 1):
+        g = orc.gen_grads_unit(1, t, 1e-3, 1, u, N)
+        orc.zero12_step(2, g, a[0], a[1], a[2], a[3], orc.hparams(**HP, step=t), 512)
+        _, coef = orc.zero12_step_clip(2, g, b[0], b[1], b[2], b[3], orc.hparams(**HP, step=t),
+                                       1e6, 512)
+        assert coef == 1.0
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x.view(np.uint8), y.view(np.uint8))
+
+
+def test_clip_norm_is_the_sum_of_shard_norms(orc):
+    """The global squared norm equals the sum over owners of their squared shard
+    norms (the all-reduce the page calls for), and clipping with one owner's
+    local norm would give a different coefficient."""
+    N, P = 4, 4000
+    (u,), _ = orc.layout([P], N)
+    g = orc.gen_grads_unit(3, 1, 1e-3, 1, u, N)
+    S = u.shard_len
+    parts = [orc.grad_sumsq(np.ascontiguousarray(g[:, k * S:(k + 1) * S])) for k in range(N)]
+    whole = orc.grad_sumsq(g)
+    acc = 0.0
+    for x in parts:          # the all-reduce, in rank order
+        acc += x
+    assert acc == pytest.approx(whole, rel=1e-13)
+    local = orc.clip_coef(parts[0], 1e-3)[0]
+    assert local != orc.clip_coef(whole, 1e-3)[0]
+
+
+def test_zero3_unit_coef_equals_clipped_flat_step(orc):
+    """Clipping across units: the global norm is the sum of the units' squared
+    norms, and each unit's scaled update equals the flat ZeRO-1 clipped step."""
+    N, sizes, T = 4, [1000, 64, 3000], 3
+    units, total = orc.layout(sizes, N)
+    P = sum(sizes)
+    w3 = orc.gen_master(5, 0.02, units, N)
+    m3, v3 = np.zeros_like(w3), np.zeros_like(w3)
+    s3 = orc.bf16_rne(w3)
+    (u1,), _ = orc.layout([P], N)
+    w1 = orc.gen_master(5, 0.02, [u1], N)
+    m1, v1 = np.zeros_like(w1), np.zeros_like(w1)
+    p1 = np.zeros(u1.n_padded, np.uint16)
+    for t in range(1, T + 1):
+        hp = orc.hparams(**HP, step=t)
+        gs = [orc.gen_grads_unit(5, t, 1e-3, 1, u, N) for u in units]
+        coef, norm = orc.clip_coef(sum(orc.grad_sumsq(g) for g in gs), 2e-3)
+        for u, g in zip(units, gs):
+            orc.zero3_reduce_scatter_unit_coef(u, g, w3, m3, v3, s3, hp, coef)
+        g1 = orc.gen_grads_unit(5, t, 1e-3, 1, u1, N)
+        n1, c1 = orc.zero12_step_clip(1, g1, w1, m1, v1, p1, hp, 2e-3)
+        assert n1 == pytest.approx(norm, rel=1e-12)
+    flat = lambda a: a.reshape(-1)[:P]
+    got = []
+    for u in units:
+        rows = [w3[k][u.shard_offset:u.shard_offset + u.shard_len] for k in range(N)]
+        got.append(np.concatenate(rows)[:u.n_params])
+    np.testing.assert_allclose(np.concatenate(got), flat(w1), rtol=1e-6, atol=1e-9)
