@@ -259,6 +259,23 @@ def run_gpu(args):
     ms2, _ = timed(torch, world, dev, stream, lambda: st.step(2, BUCKET_25MIB), K)
     n_buckets = -(-Pp // BUCKET_25MIB)
 
+    # ZeRO-1 with global-norm clipping: norm pass + coefficient + clipped fused step
+    scratch = torch.empty(Z.zero_clip_scratch_bytes() // 8, dtype=torch.float64, device=dev)
+    norm_coef = torch.empty(4, dtype=torch.float32, device=dev)[:2]
+
+    def clipped_step():
+        st.t += 1
+        Z.zero_grad_sqnorm(st.grads, scratch)
+        Z.zero_clip_coef(scratch, 1.0, norm_coef)
+        Z.zero_step_stage12_clip(1, st.grads, st.master, st.m, st.v, st.params,
+                                 Z.hparams(**HP, step=st.t), norm_coef)
+
+    for _ in range(min(W, 3)):
+        clipped_step()
+    Kc = min(K, 200)
+    ms_c, _ = timed(torch, world, dev, stream, clipped_step, Kc)
+    clip_bytes = (26 + 4 * N) * Pp
+
     # end to end through the C ABI with host buffers: H2D gradients, step, D2H weights
     E = args.e2e_steps or min(K, 50)
     host_g = torch.empty((N, Pp), dtype=torch.int16, pin_memory=True)
@@ -311,6 +328,12 @@ def run_gpu(args):
             "ms_per_step": ms2 / K, "value": world * P * K / (ms2 * 1e-3),
             "launches_per_step": n_buckets, "bucket_elems": BUCKET_25MIB,
             "hbm_gbs": bytes_per_step * K / (ms2 * 1e-3) / 1e9,
+        },
+        "clip": {
+            "ms_per_step": ms_c / Kc, "value": world * P * Kc / (ms_c * 1e-3), "steps": Kc,
+            "hbm_gbs": clip_bytes * Kc / (ms_c * 1e-3) / 1e9, "bytes_per_step": clip_bytes,
+            "note": "ZeRO-1 with global-norm clipping (max_norm 1.0): norm pass (2N B/param) + "
+                    "coefficient + clipped fused step (26+2N B/param), 3 launches",
         },
         "e2e": {
             "value": world * P * E / (ms_e2e * 1e-3), "unit": "params/s", "steps": E,

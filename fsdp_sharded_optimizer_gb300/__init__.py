@@ -17,7 +17,9 @@ _PUBLIC = ("ZERO_DEFAULT_ALIGN", "ZERO_EALIGN", "ZERO_ECUDA", "ZERO_EINVAL", "ZE
            "zero3_gather_unit", "zero3_reduce_scatter_unit", "zero_bytes_t", "zero_cast_bf16",
            "zero_gen_grads_unit", "zero_gen_master", "zero_hparams_t", "zero_layout",
            "zero_state_bytes", "zero_step_stage12", "zero_stream_wait", "zero_unit_t",
-           "zero3_plan", "zero3_step", "zero_op_t", "zero_regen_t")
+           "zero3_plan", "zero3_step", "zero_op_t", "zero_regen_t", "zero_clip_scratch_bytes",
+           "zero_grad_sqnorm", "zero_clip_coef", "zero_step_stage12_clip",
+           "zero3_reduce_scatter_unit_clip", "zero_clip_t", "clip_args")
 
 __all__ = list(_PUBLIC)
 

@@ -66,7 +66,20 @@ class zero_regen_t(C.Structure):
 
 ZERO_OP_RECORD, ZERO_OP_WAIT, ZERO_OP_GATHER = 1, 2, 3
 ZERO_OP_REDUCE_SCATTER, ZERO_OP_REGEN, ZERO_OP_USE = 4, 5, 6
-OP_NAMES = {1: "record", 2: "wait", 3: "gather", 4: "reduce_scatter", 5: "regen", 6: "use"}
+OP_NAMES = {1: "record", 2: "wait", 3: "gather", 4: "reduce_scatter", 5: "regen", 6: "use",
+            7: "norm", 8: "clip_coef"}
+
+
+class zero_clip_t(C.Structure):
+    _fields_ = [("max_norm", C.c_double), ("scratch", C.c_void_p), ("scratch_bytes", C.c_int64),
+                ("norm_coef", C.c_void_p)]
+
+
+def clip_args(max_norm, scratch, norm_coef):
+    """A zero_clip_t for zero3_step from device tensors (scratch of
+    zero_clip_scratch_bytes(), norm_coef of 2 floats)."""
+    return zero_clip_t(float(max_norm), scratch.data_ptr(), scratch.numel() * scratch.element_size(),
+                       norm_coef.data_ptr())
 
 # name -> (restype, argtypes); the same names as include/zero.h
 _P, _I32, _I64, _U64, _F64 = C.c_void_p, C.c_int32, C.c_int64, C.c_uint64, C.c_double
@@ -76,8 +89,15 @@ SIGNATURES = {
     "zero3_gather_unit": (C.c_int, [_P, _I32, _P, _P, _P]),
     "zero3_reduce_scatter_unit": (C.c_int, [_P, _I32, _P, _P, _P, _P, _P, _P, _P]),
     "zero_state_bytes": (C.c_int, [_I64, _I32, _I32, _I32, _P]),
-    "zero3_plan": (C.c_int, [_I32, _I32, _P, _I32, _P]),
-    "zero3_step": (C.c_int, [_P, _I32, _I32, _P, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "zero_clip_scratch_bytes": (C.c_int64, []),
+    "zero_grad_sqnorm": (C.c_int, [_I32, _I64, _P, _I32, _P, _I64, _P]),
+    "zero_clip_coef": (C.c_int, [_P, _I64, _F64, _P, _P]),
+    "zero_step_stage12_clip": (C.c_int, [_I32, _I32, _I64, _P, _P, _P, _P, _P, _P, _I64, _P,
+                                         _P]),
+    "zero3_reduce_scatter_unit_clip": (C.c_int, [_P, _I32, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "zero3_plan": (C.c_int, [_I32, _I32, _I32, _P, _I32, _P]),
+    "zero3_step": (C.c_int, [_P, _I32, _I32, _P, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                             _P]),
     "zero_gen_grads_unit": (C.c_int, [_U64, _I64, _F64, _I32, _P, _I32, _P, _P]),
     "zero_gen_master": (C.c_int, [_U64, _F64, _P, _I32, _I32, _P, _P]),
     "zero_cast_bf16": (C.c_int, [_P, _P, _I64, _P]),
@@ -191,18 +211,62 @@ def zero3_reduce_scatter_unit(unit, unit_grads, master, m, v, shard_bf16, hp, st
         C.byref(unit), len(grows), g, w, mm, vv, s, C.byref(hp), _stream(stream)))
 
 
-def zero3_plan(n_units, regen=False):
+def zero_clip_scratch_bytes():
+    return lib.zero_clip_scratch_bytes()
+
+
+def zero_grad_sqnorm(grads, scratch, accumulate=False, stream=None):
+    """Add the squared norm of the averaged gradient of one buffer into the
+    per-block partials in `scratch` (a device tensor of zero_clip_scratch_bytes())."""
+    g, rows = _rows(grads, 2, "grads")
+    _check("zero_grad_sqnorm", lib.zero_grad_sqnorm(
+        len(rows), rows[0].numel(), g, 1 if accumulate else 0, C.c_void_p(scratch.data_ptr()),
+        scratch.numel() * scratch.element_size(), _stream(stream)))
+
+
+def zero_clip_coef(scratch, max_norm, norm_coef, stream=None):
+    """norm_coef (device float[2]) <- (global norm, clip coefficient)."""
+    _check("zero_clip_coef", lib.zero_clip_coef(
+        C.c_void_p(scratch.data_ptr()), scratch.numel() * scratch.element_size(), float(max_norm),
+        _dev(norm_coef, 4, "norm_coef"), _stream(stream)))
+
+
+def zero_step_stage12_clip(stage, grads, master, m, v, params_bf16, hp, norm_coef, bucket_elems=0,
+                           stream=None):
+    g, grows = _rows(grads, 2, "grads")
+    w, _ = _rows(master, 4, "master")
+    mm, _ = _rows(m, 4, "m")
+    vv, _ = _rows(v, 4, "v")
+    _check("zero_step_stage12_clip", lib.zero_step_stage12_clip(
+        stage, len(grows), grows[0].numel(), g, w, mm, vv, _dev(params_bf16, 2, "params_bf16"),
+        C.byref(hp), int(bucket_elems), _dev(norm_coef, 4, "norm_coef"), _stream(stream)))
+
+
+def zero3_reduce_scatter_unit_clip(unit, unit_grads, master, m, v, shard_bf16, hp, norm_coef,
+                                   stream=None):
+    g, grows = _rows(unit_grads, 2, "unit_grads")
+    w, _ = _rows(master, 4, "master")
+    mm, _ = _rows(m, 4, "m")
+    vv, _ = _rows(v, 4, "v")
+    s, _ = _rows(shard_bf16, 2, "shard_bf16")
+    _check("zero3_reduce_scatter_unit_clip", lib.zero3_reduce_scatter_unit_clip(
+        C.byref(unit), len(grows), g, w, mm, vv, s, C.byref(hp), _dev(norm_coef, 4, "norm_coef"),
+        _stream(stream)))
+
+
+def zero3_plan(n_units, regen=False, clip=False):
     """The operations of one ZeRO-3 step (host only): a list of
     (kind name, stream 0=main/1=side, unit, arg)."""
-    cap = 14 * n_units + 2
+    cap = 17 * n_units + 3
     ops = (zero_op_t * cap)()
     n = C.c_int32()
-    _check("zero3_plan", lib.zero3_plan(n_units, 1 if regen else 0, ops, cap, C.byref(n)))
+    _check("zero3_plan", lib.zero3_plan(n_units, 1 if regen else 0, 1 if clip else 0, ops, cap,
+                                        C.byref(n)))
     return [(OP_NAMES[o.kind], o.stream, o.unit, o.arg) for o in ops[:n.value]]
 
 
 def zero3_step(units, grads, master, m, v, shard_bf16, full_a, full_b, hp, grads_resident=True,
-               regen=None, main_stream=None, side_stream=None):
+               regen=None, clip=None, main_stream=None, side_stream=None):
     """One whole ZeRO-3 step issued by the native scheduler.  grads: per-rank
     gradients (all units concatenated when grads_resident, else one unit-sized
     buffer per rank refilled by `regen`, a zero_regen_t)."""
@@ -215,7 +279,8 @@ def zero3_step(units, grads, master, m, v, shard_bf16, full_a, full_b, hp, grads
     _check("zero3_step", lib.zero3_step(
         arr, len(units), len(rows), g, 1 if grads_resident else 0, w, mm, vv, s,
         _dev(full_a, 2, "full_a"), _dev(full_b, 2, "full_b"), C.byref(hp),
-        C.byref(regen) if regen is not None else None, _stream(main_stream), _stream(side_stream)))
+        C.byref(regen) if regen is not None else None, C.byref(clip) if clip is not None else None,
+        _stream(main_stream), _stream(side_stream)))
 
 
 # ------------------------------------------------------------------ harness calls

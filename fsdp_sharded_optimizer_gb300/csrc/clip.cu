@@ -1,0 +1,135 @@
+// clip.cu -- global gradient-norm clipping across the shards: the squared norm
+// of the averaged gradient (zero_grad_sqnorm) and the clip coefficient
+// (zero_clip_coef).
+//
+// Method ("Data parallelism, ZeRO and FSDP", "7. Common mistakes", local
+// gradient clipping): with sharded gradients the global norm needs an
+// all-reduce of the squared shard norms.  The rule is that of the
+// clip_grad_norm_ call in the DDP reference of "Distributed Training Basics --
+// DDP and FSDP": coef = max_norm / (norm + 1e-6), at most 1.
+//
+// On one GPU the squared shard norms are per-block partial sums in a scratch
+// array the caller provides; the "all-reduce" is one block summing them.  The
+// norm pass reads the N_d bf16 gradients once (2 N_d bytes per parameter,
+// HBM-bound) and rebuilds each mean gradient exactly as the fused step does.
+// The grid is fixed (kNormBlocks), so the partials and their order -- and with
+// them the result -- do not depend on the device's occupancy.  Accuracy: each
+// thread sums 8 squares pairwise in fp32 and accumulates with Kahan
+// compensation; the block and final sums run in fp64.  The relative error of
+// the squared norm stays within about 6 fp32 roundings (< 4e-7), whatever the
+// length.
+#include "device.cuh"
+#include "zero_internal.h"
+
+namespace zero {
+namespace {
+
+constexpr int kNormThreads = 256;
+
+struct GradTable {
+    const uint4* g[ZERO_MAX_RANKS];
+};
+
+__device__ __forceinline__ double block_sum(double d)
+{
+    __shared__ double warp_sums[kNormThreads / 32];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) d += __shfl_down_sync(0xFFFFFFFFu, d, off);
+    if ((threadIdx.x & 31) == 0) warp_sums[threadIdx.x >> 5] = d;
+    __syncthreads();
+    double total = 0.0;
+    if (threadIdx.x == 0)
+        for (int w = 0; w < kNormThreads / 32; ++w) total += warp_sums[w];
+    return total; // valid in thread 0
+}
+
+__global__ void __launch_bounds__(kNormThreads)
+grad_sqnorm_kernel(const __grid_constant__ GradTable T, int n_ranks, int64_t n_vec, float inv_n,
+                   int accumulate, double* __restrict__ partials)
+{
+    float sum = 0.0f, comp = 0.0f; // Kahan: true sum ~ sum - comp
+    for (int64_t q = static_cast<int64_t>(blockIdx.x) * kNormThreads + threadIdx.x; q < n_vec;
+         q += static_cast<int64_t>(gridDim.x) * kNormThreads) {
+        float acc[8];
+        dev::sum_ranks<8>(T.g, n_ranks, q, acc);
+        float sq[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float g = __fmul_rn(acc[e], inv_n);
+            sq[e] = __fmul_rn(g, g);
+        }
+        const float s8 = __fadd_rn(__fadd_rn(__fadd_rn(sq[0], sq[1]), __fadd_rn(sq[2], sq[3])),
+                                   __fadd_rn(__fadd_rn(sq[4], sq[5]), __fadd_rn(sq[6], sq[7])));
+        const float y = __fsub_rn(s8, comp);
+        const float t = __fadd_rn(sum, y);
+        comp = __fsub_rn(__fsub_rn(t, sum), y);
+        sum = t;
+    }
+    const double b = block_sum(static_cast<double>(sum) - static_cast<double>(comp));
+    if (threadIdx.x == 0) partials[blockIdx.x] = (accumulate ? partials[blockIdx.x] : 0.0) + b;
+}
+
+__global__ void __launch_bounds__(kNormThreads)
+clip_coef_kernel(const double* __restrict__ partials, int n, double max_norm,
+                 float* __restrict__ norm_coef)
+{
+    double s = 0.0;
+    for (int i = threadIdx.x; i < n; i += kNormThreads) s += partials[i];
+    const double total = block_sum(s);
+    if (threadIdx.x == 0) {
+        const double norm = sqrt(total);
+        double c = max_norm / (norm + 1e-6);
+        if (c > 1.0) c = 1.0;
+        norm_coef[0] = static_cast<float>(norm);
+        norm_coef[1] = static_cast<float>(c);
+    }
+}
+
+} // namespace
+
+int grad_sqnorm(int32_t n_ranks, int64_t n_elems, const uint16_t* const* grads, int32_t accumulate,
+                double* scratch, int64_t scratch_bytes, cudaStream_t stream)
+{
+    if (n_ranks < 1 || n_ranks > ZERO_MAX_RANKS || n_elems <= 0 || n_elems % 8 != 0 || !scratch ||
+        scratch_bytes < kNormScratchBytes)
+        return ZERO_EINVAL;
+    int rc = check_table(grads, n_ranks);
+    if (rc != ZERO_OK) return rc;
+    if (!aligned16(scratch)) return ZERO_EALIGN;
+    GradTable T = {};
+    for (int32_t r = 0; r < n_ranks; ++r) T.g[r] = reinterpret_cast<const uint4*>(grads[r]);
+    const float inv_n = static_cast<float>(1.0 / static_cast<double>(n_ranks));
+    grad_sqnorm_kernel<<<kNormBlocks, kNormThreads, 0, stream>>>(T, n_ranks, n_elems / 8, inv_n,
+                                                                accumulate ? 1 : 0, scratch);
+    return cuda_status(cudaGetLastError());
+}
+
+int clip_coef(const double* scratch, int64_t scratch_bytes, double max_norm, float* norm_coef,
+              cudaStream_t stream)
+{
+    if (!scratch || scratch_bytes < kNormScratchBytes || !norm_coef || !(max_norm > 0) ||
+        !std::isfinite(max_norm))
+        return ZERO_EINVAL;
+    if (!aligned16(scratch) || !aligned16(norm_coef)) return ZERO_EALIGN;
+    clip_coef_kernel<<<1, kNormThreads, 0, stream>>>(scratch, kNormBlocks, max_norm, norm_coef);
+    return cuda_status(cudaGetLastError());
+}
+
+} // namespace zero
+
+using namespace zero;
+
+extern "C" int64_t zero_clip_scratch_bytes(void) { return kNormScratchBytes; }
+
+extern "C" int zero_grad_sqnorm(int32_t n_ranks, int64_t n_elems, const uint16_t* const* grads,
+                                int32_t accumulate, double* scratch, int64_t scratch_bytes,
+                                cudaStream_t stream)
+{
+    return grad_sqnorm(n_ranks, n_elems, grads, accumulate, scratch, scratch_bytes, stream);
+}
+
+extern "C" int zero_clip_coef(const double* scratch, int64_t scratch_bytes, double max_norm,
+                              float* norm_coef, cudaStream_t stream)
+{
+    return clip_coef(scratch, scratch_bytes, max_norm, norm_coef, stream);
+}

@@ -36,5 +36,35 @@ __device__ __forceinline__ float4 ld_stream(const float4* p) { return __ldcs(p);
 __device__ __forceinline__ void st_stream(uint4* p, uint4 x) { __stcs(p, x); }
 __device__ __forceinline__ void st_stream(float4* p, float4 x) { __stcs(p, x); }
 
+// The reduce-scatter's sum for 8 consecutive elements of vector q: fp32 from
+// +0 over ranks 0..n_ranks-1 in order.  All loads of a batch of `kBatch`
+// ranks are issued before any of them is summed.
+template <int kBatch>
+__device__ __forceinline__ void sum_ranks(const uint4* const* g, int n_ranks, int64_t q,
+                                          float (&acc)[8])
+{
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+    for (int r0 = 0; r0 < n_ranks; r0 += kBatch) {
+        uint4 G[kBatch];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i)
+            if (r0 + i < n_ranks) G[i] = ld_stream(g[r0 + i] + q);
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            if (r0 + i < n_ranks) {
+                acc[0] = __fadd_rn(acc[0], bf16_lo(G[i].x));
+                acc[1] = __fadd_rn(acc[1], bf16_hi(G[i].x));
+                acc[2] = __fadd_rn(acc[2], bf16_lo(G[i].y));
+                acc[3] = __fadd_rn(acc[3], bf16_hi(G[i].y));
+                acc[4] = __fadd_rn(acc[4], bf16_lo(G[i].z));
+                acc[5] = __fadd_rn(acc[5], bf16_hi(G[i].z));
+                acc[6] = __fadd_rn(acc[6], bf16_lo(G[i].w));
+                acc[7] = __fadd_rn(acc[7], bf16_hi(G[i].w));
+            }
+        }
+    }
+}
+
 } // namespace dev
 } // namespace zero

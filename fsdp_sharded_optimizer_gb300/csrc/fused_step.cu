@@ -64,8 +64,12 @@ __device__ __forceinline__ void adamw(float g, float& w, float& m, float& v,
     v = v1;
 }
 
+// kClip: the mean gradient is multiplied by clip[1], the coefficient of the
+// global-norm clipping computed on the device by zero_clip_coef.
+template <bool kClip>
 __global__ void __launch_bounds__(kBlock, kMinBlocksPerSM)
-fused_step_kernel(const __grid_constant__ Tables T, const StepScalars s, const Range R)
+fused_step_kernel(const __grid_constant__ Tables T, const StepScalars s, const Range R,
+                  const float* __restrict__ clip)
 {
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kBlock;
     int64_t q = R.q0 + static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x;
@@ -73,6 +77,7 @@ fused_step_kernel(const __grid_constant__ Tables T, const StepScalars s, const R
     int64_t k = q / R.shard_vec;     // owner
     int64_t j = q - k * R.shard_vec; // vector position inside the owner's shard
     const int N = R.n_ranks;
+    const float coef = kClip ? clip[1] : 1.0f;
 
     for (; q < R.q1; q += stride) {
         float4* wp = T.w[k] + 2 * j;
@@ -84,33 +89,17 @@ fused_step_kernel(const __grid_constant__ Tables T, const StepScalars s, const R
 
         // reduce-scatter: fp32 sum from +0 over ranks 0..N-1, in order
         float acc[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
-        for (int r0 = 0; r0 < N; r0 += kRankBatch) {
-            uint4 G[kRankBatch];
-#pragma unroll
-            for (int i = 0; i < kRankBatch; ++i)
-                if (r0 + i < N) G[i] = dev::ld_stream(T.g[r0 + i] + q);
-#pragma unroll
-            for (int i = 0; i < kRankBatch; ++i) {
-                if (r0 + i < N) {
-                    acc[0] = __fadd_rn(acc[0], dev::bf16_lo(G[i].x));
-                    acc[1] = __fadd_rn(acc[1], dev::bf16_hi(G[i].x));
-                    acc[2] = __fadd_rn(acc[2], dev::bf16_lo(G[i].y));
-                    acc[3] = __fadd_rn(acc[3], dev::bf16_hi(G[i].y));
-                    acc[4] = __fadd_rn(acc[4], dev::bf16_lo(G[i].z));
-                    acc[5] = __fadd_rn(acc[5], dev::bf16_hi(G[i].z));
-                    acc[6] = __fadd_rn(acc[6], dev::bf16_lo(G[i].w));
-                    acc[7] = __fadd_rn(acc[7], dev::bf16_hi(G[i].w));
-                }
-            }
-        }
+        dev::sum_ranks<kRankBatch>(T.g, N, q, acc);
 
         float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
         float m[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
         float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
-        for (int e = 0; e < 8; ++e) adamw(__fmul_rn(acc[e], s.inv_n), w[e], m[e], v[e], s);
+        for (int e = 0; e < 8; ++e) {
+            float g = __fmul_rn(acc[e], s.inv_n);
+            if (kClip) g = __fmul_rn(g, coef);
+            adamw(g, w[e], m[e], v[e], s);
+        }
 
         dev::st_stream(wp, make_float4(w[0], w[1], w[2], w[3]));
         dev::st_stream(wp + 1, make_float4(w[4], w[5], w[6], w[7]));
@@ -133,18 +122,22 @@ fused_step_kernel(const __grid_constant__ Tables T, const StepScalars s, const R
 }
 
 int launch(const Tables& T, const StepScalars& s, int64_t q0, int64_t q1, int64_t shard_vec,
-           int32_t n_ranks, cudaStream_t stream)
+           int32_t n_ranks, const float* clip, cudaStream_t stream)
 {
     if (q1 <= q0) return ZERO_OK;
-    const int max_blocks = persistent_blocks(reinterpret_cast<const void*>(fused_step_kernel),
-                                             kBlock, 0);
+    const void* kernel = clip ? reinterpret_cast<const void*>(fused_step_kernel<true>)
+                              : reinterpret_cast<const void*>(fused_step_kernel<false>);
+    const int max_blocks = persistent_blocks(kernel, kBlock, 0);
     if (max_blocks <= 0) return ZERO_ECUDA;
     const int64_t need = (q1 - q0 + kBlock - 1) / kBlock;
     const int blocks = static_cast<int>(need < max_blocks ? need : max_blocks);
     const int64_t stride = static_cast<int64_t>(blocks) * kBlock;
     const StrideSplit sp = split_stride(stride, shard_vec);
     const Range R{q0, q1, shard_vec, sp.k, sp.j, n_ranks};
-    fused_step_kernel<<<blocks, kBlock, 0, stream>>>(T, s, R);
+    if (clip)
+        fused_step_kernel<true><<<blocks, kBlock, 0, stream>>>(T, s, R, clip);
+    else
+        fused_step_kernel<false><<<blocks, kBlock, 0, stream>>>(T, s, R, nullptr);
     return cuda_status(cudaGetLastError());
 }
 
@@ -158,16 +151,11 @@ int check_state_tables(int32_t n, const uint16_t* const* grads, float* const* ma
     return check_table(v, n);
 }
 
-} // namespace
-} // namespace zero
-
-using namespace zero;
-
-extern "C" int zero_step_stage12(int32_t stage, int32_t n_ranks, int64_t n_padded,
-                                 const uint16_t* const* grads, float* const* master,
-                                 float* const* m, float* const* v, uint16_t* params_bf16,
-                                 const zero_hparams_t* hp, int64_t bucket_elems,
-                                 cudaStream_t stream)
+// The two entry points with an optional device clip coefficient (nullptr = none).
+int step_stage12(int32_t stage, int32_t n_ranks, int64_t n_padded, const uint16_t* const* grads,
+                 float* const* master, float* const* m, float* const* v, uint16_t* params_bf16,
+                 const zero_hparams_t* hp, int64_t bucket_elems, const float* clip,
+                 cudaStream_t stream)
 {
     if ((stage != 1 && stage != 2) || n_ranks < 1 || n_ranks > ZERO_MAX_RANKS ||
         n_padded <= 0 || n_padded % (8 * static_cast<int64_t>(n_ranks)) != 0 ||
@@ -193,16 +181,14 @@ extern "C" int zero_step_stage12(int32_t stage, int32_t n_ranks, int64_t n_padde
     const int64_t bucket_vec = (stage == 2 && bucket_elems > 0) ? bucket_elems / 8 : nvec;
     for (int64_t q0 = 0; q0 < nvec; q0 += bucket_vec) {
         const int64_t q1 = q0 + bucket_vec < nvec ? q0 + bucket_vec : nvec;
-        if ((rc = launch(T, s, q0, q1, shard_vec, n_ranks, stream)) != ZERO_OK) return rc;
+        if ((rc = launch(T, s, q0, q1, shard_vec, n_ranks, clip, stream)) != ZERO_OK) return rc;
     }
     return ZERO_OK;
 }
 
-extern "C" int zero3_reduce_scatter_unit(const zero_unit_t* unit, int32_t n_ranks,
-                                         const uint16_t* const* unit_grads,
-                                         float* const* master, float* const* m,
-                                         float* const* v, uint16_t* const* shard_bf16,
-                                         const zero_hparams_t* hp, cudaStream_t stream)
+int rs_unit(const zero_unit_t* unit, int32_t n_ranks, const uint16_t* const* unit_grads,
+            float* const* master, float* const* m, float* const* v, uint16_t* const* shard_bf16,
+            const zero_hparams_t* hp, const float* clip, cudaStream_t stream)
 {
     if (!unit || n_ranks < 1 || n_ranks > ZERO_MAX_RANKS || unit->n_padded <= 0 ||
         unit->shard_len <= 0 || unit->shard_len % 8 != 0 ||
@@ -223,5 +209,59 @@ extern "C" int zero3_reduce_scatter_unit(const zero_unit_t* unit, int32_t n_rank
         T.o[r] = reinterpret_cast<uint4*>(shard_bf16[r] + off);
     }
     const StepScalars s = make_scalars(hp, n_ranks);
-    return launch(T, s, 0, unit->n_padded / 8, unit->shard_len / 8, n_ranks, stream);
+    return launch(T, s, 0, unit->n_padded / 8, unit->shard_len / 8, n_ranks, clip, stream);
+}
+
+int check_clip(const float* norm_coef)
+{
+    if (!norm_coef) return ZERO_EINVAL;
+    return aligned16(norm_coef) ? ZERO_OK : ZERO_EALIGN;
+}
+
+} // namespace
+} // namespace zero
+
+using namespace zero;
+
+extern "C" int zero_step_stage12(int32_t stage, int32_t n_ranks, int64_t n_padded,
+                                 const uint16_t* const* grads, float* const* master,
+                                 float* const* m, float* const* v, uint16_t* params_bf16,
+                                 const zero_hparams_t* hp, int64_t bucket_elems,
+                                 cudaStream_t stream)
+{
+    return step_stage12(stage, n_ranks, n_padded, grads, master, m, v, params_bf16, hp,
+                        bucket_elems, nullptr, stream);
+}
+
+extern "C" int zero_step_stage12_clip(int32_t stage, int32_t n_ranks, int64_t n_padded,
+                                      const uint16_t* const* grads, float* const* master,
+                                      float* const* m, float* const* v, uint16_t* params_bf16,
+                                      const zero_hparams_t* hp, int64_t bucket_elems,
+                                      const float* norm_coef, cudaStream_t stream)
+{
+    const int rc = check_clip(norm_coef);
+    if (rc != ZERO_OK) return rc;
+    return step_stage12(stage, n_ranks, n_padded, grads, master, m, v, params_bf16, hp,
+                        bucket_elems, norm_coef, stream);
+}
+
+extern "C" int zero3_reduce_scatter_unit(const zero_unit_t* unit, int32_t n_ranks,
+                                         const uint16_t* const* unit_grads,
+                                         float* const* master, float* const* m,
+                                         float* const* v, uint16_t* const* shard_bf16,
+                                         const zero_hparams_t* hp, cudaStream_t stream)
+{
+    return rs_unit(unit, n_ranks, unit_grads, master, m, v, shard_bf16, hp, nullptr, stream);
+}
+
+extern "C" int zero3_reduce_scatter_unit_clip(const zero_unit_t* unit, int32_t n_ranks,
+                                              const uint16_t* const* unit_grads,
+                                              float* const* master, float* const* m,
+                                              float* const* v, uint16_t* const* shard_bf16,
+                                              const zero_hparams_t* hp, const float* norm_coef,
+                                              cudaStream_t stream)
+{
+    const int rc = check_clip(norm_coef);
+    if (rc != ZERO_OK) return rc;
+    return rs_unit(unit, n_ranks, unit_grads, master, m, v, shard_bf16, hp, norm_coef, stream);
 }

@@ -41,7 +41,7 @@ struct PlanBuilder {
         add(ZERO_OP_RECORD, 1, -1, kEvGathered + pos % 2);
     }
 
-    void pass(int32_t n_units, bool backward, bool regen)
+    void pass(int32_t n_units, bool backward, bool regen, bool clip)
     {
         auto unit_at = [&](int32_t pos) { return backward ? n_units - 1 - pos : pos; };
         gather(unit_at(0), 0, 0);
@@ -53,20 +53,30 @@ struct PlanBuilder {
             add(ZERO_OP_USE, 0, u, slot);
             if (backward) {
                 if (regen) add(ZERO_OP_REGEN, 0, u, 0);
-                add(ZERO_OP_REDUCE_SCATTER, 0, u, 0);
+                add(ZERO_OP_REDUCE_SCATTER, 0, u, clip ? 1 : 0);
             }
             add(ZERO_OP_RECORD, 0, -1, kEvReleased + slot);
             released_recorded[slot] = true;
         }
     }
 
-    void step(int32_t n_units, bool regen)
+    void step(int32_t n_units, bool regen, bool clip)
     {
         // the step's first gather must see everything the main stream did before
         add(ZERO_OP_RECORD, 0, -1, kEvStart);
         add(ZERO_OP_WAIT, 1, -1, kEvStart);
-        pass(n_units, false, regen);
-        pass(n_units, true, regen);
+        if (clip) {
+            // the global norm before any unit's update: every unit's squared
+            // norm on the main stream (overlapping the forward gathers), then
+            // the coefficient
+            for (int32_t u = 0; u < n_units; ++u) {
+                if (regen) add(ZERO_OP_REGEN, 0, u, 0);
+                add(ZERO_OP_NORM, 0, u, u > 0 ? 1 : 0);
+            }
+            add(ZERO_OP_CLIP_COEF, 0, -1, 0);
+        }
+        pass(n_units, false, regen, clip);
+        pass(n_units, true, regen, clip);
     }
 };
 
@@ -104,12 +114,12 @@ bool unit_consistent(const zero_unit_t& u, int32_t n_ranks)
 
 using namespace zero;
 
-extern "C" int zero3_plan(int32_t n_units, int32_t regen, zero_op_t* ops, int32_t max_ops,
-                          int32_t* n_ops)
+extern "C" int zero3_plan(int32_t n_units, int32_t regen, int32_t clip, zero_op_t* ops,
+                          int32_t max_ops, int32_t* n_ops)
 {
     if (n_units < 1 || !ops || !n_ops || max_ops < 0) return ZERO_EINVAL;
     PlanBuilder b;
-    b.step(n_units, regen != 0);
+    b.step(n_units, regen != 0, clip != 0);
     if (static_cast<int64_t>(b.ops.size()) > max_ops) return ZERO_EINVAL;
     for (size_t i = 0; i < b.ops.size(); ++i) ops[i] = b.ops[i];
     *n_ops = static_cast<int32_t>(b.ops.size());
@@ -121,7 +131,8 @@ extern "C" int zero3_step(const zero_unit_t* units, int32_t n_units, int32_t n_r
                           float* const* master, float* const* m, float* const* v,
                           uint16_t* const* shard_bf16, uint16_t* full_a, uint16_t* full_b,
                           const zero_hparams_t* hp, const zero_regen_t* regen,
-                          cudaStream_t main_stream, cudaStream_t side_stream)
+                          const zero_clip_t* clip, cudaStream_t main_stream,
+                          cudaStream_t side_stream)
 {
     if (!units || n_units < 1 || n_ranks < 1 || n_ranks > ZERO_MAX_RANKS || !valid_hparams(hp) ||
         !full_a || !full_b || full_a == full_b || main_stream == side_stream ||
@@ -136,11 +147,17 @@ extern "C" int zero3_step(const zero_unit_t* units, int32_t n_units, int32_t n_r
     if ((rc = check_table(v, n_ranks)) != ZERO_OK) return rc;
     if ((rc = check_table(shard_bf16, n_ranks)) != ZERO_OK) return rc;
     if (!aligned16(full_a) || !aligned16(full_b)) return ZERO_EALIGN;
+    if (clip) {
+        if (!clip->scratch || clip->scratch_bytes < kNormScratchBytes || !clip->norm_coef ||
+            !(clip->max_norm > 0) || !std::isfinite(clip->max_norm))
+            return ZERO_EINVAL;
+        if (!aligned16(clip->scratch) || !aligned16(clip->norm_coef)) return ZERO_EALIGN;
+    }
 
     cudaEvent_t* ev = nullptr;
     if ((rc = events_for_current_device(&ev)) != ZERO_OK) return rc;
     PlanBuilder plan;
-    plan.step(n_units, regen != nullptr);
+    plan.step(n_units, regen != nullptr, clip != nullptr);
 
     const uint16_t* unit_grads[ZERO_MAX_RANKS];
     uint16_t* unit_grads_w[ZERO_MAX_RANKS];
@@ -171,8 +188,19 @@ extern "C" int zero3_step(const zero_unit_t* units, int32_t n_units, int32_t n_r
             break;
         case ZERO_OP_REDUCE_SCATTER:
             grads_of(op.unit);
-            rc = zero3_reduce_scatter_unit(&units[op.unit], n_ranks, unit_grads, master, m, v,
-                                           shard_bf16, hp, s);
+            rc = op.arg ? zero3_reduce_scatter_unit_clip(&units[op.unit], n_ranks, unit_grads,
+                                                         master, m, v, shard_bf16, hp,
+                                                         clip->norm_coef, s)
+                        : zero3_reduce_scatter_unit(&units[op.unit], n_ranks, unit_grads, master,
+                                                    m, v, shard_bf16, hp, s);
+            break;
+        case ZERO_OP_NORM:
+            grads_of(op.unit);
+            rc = grad_sqnorm(n_ranks, units[op.unit].n_padded, unit_grads, op.arg, clip->scratch,
+                             clip->scratch_bytes, s);
+            break;
+        case ZERO_OP_CLIP_COEF:
+            rc = clip_coef(clip->scratch, clip->scratch_bytes, clip->max_norm, clip->norm_coef, s);
             break;
         default: // ZERO_OP_USE: the unit's compute would run here
             rc = ZERO_OK;

@@ -2,6 +2,7 @@
 // units (argument checks, per-device launch geometry, the fp32 step scalars).
 #pragma once
 
+#include <cmath>
 #include <cstdint>
 
 #include <cuda_runtime.h>
@@ -51,5 +52,14 @@ inline StrideSplit split_stride(int64_t stride, int64_t shard_vec)
 }
 
 int cuda_status(cudaError_t e);
+
+// Global-norm clipping: a fixed grid of kNormBlocks blocks writes one fp64
+// partial sum each, so scratch holds kNormBlocks doubles (152 SMs x 8).
+constexpr int kNormBlocks = 1216;
+constexpr int64_t kNormScratchBytes = kNormBlocks * static_cast<int64_t>(sizeof(double));
+int grad_sqnorm(int32_t n_ranks, int64_t n_elems, const uint16_t* const* grads, int32_t accumulate,
+                double* scratch, int64_t scratch_bytes, cudaStream_t stream);
+int clip_coef(const double* scratch, int64_t scratch_bytes, double max_norm, float* norm_coef,
+              cudaStream_t stream);
 
 } // namespace zero

@@ -177,6 +177,59 @@ int zero_state_bytes(int64_t n_params, int32_t n_ranks, int32_t stage, int32_t K
                      zero_bytes_t* out);
 
 /* ---------------------------------------------------------------------
+ * Global gradient-norm clipping across the shards.  [DZF] "7. Common
+ * mistakes" (local gradient clipping: with sharded gradients the global norm
+ * needs an all-reduce of the squared shard norms); the rule of the
+ * clip_grad_norm_ call in [DDF]'s DDP reference: norm = ||g||_2 of the whole
+ * averaged gradient g, coef = max_norm / (norm + 1e-6), at most 1, and the
+ * update uses g * coef.  Sequence per step: zero_grad_sqnorm over every
+ * flat buffer or unit (accumulate = 0 for the first, 1 for the rest), then
+ * zero_clip_coef, then the *_clip step calls, all on one stream; nothing
+ * returns to the host.
+ * ------------------------------------------------------------------- */
+
+/* Bytes of device scratch the norm pass needs (1216 doubles, 9,728 B). */
+int64_t zero_clip_scratch_bytes(void);
+
+/* zero_grad_sqnorm -- adds the squared L2 norm of the averaged gradient of
+ * one buffer (g[i] = fp32 rank-order mean of grads[r][i], exactly as the
+ * fused step forms it) into per-block fp64 partials in scratch.
+ *   n_elems      length of each rank's buffer (multiple of 8)
+ *   grads        n_ranks device pointers (read only)
+ *   accumulate   0: overwrite the partials (first buffer of the step);
+ *                1: add to them (further units)
+ *   scratch      device, >= zero_clip_scratch_bytes(), 16-byte aligned; the
+ *                caller owns it; calls that share it must be ordered
+ * The partials and their summation order are fixed, so results repeat bit
+ * for bit.  ZERO_EINVAL / ZERO_EALIGN / ZERO_ECUDA. */
+int zero_grad_sqnorm(int32_t n_ranks, int64_t n_elems, const uint16_t* const* grads,
+                     int32_t accumulate, double* scratch, int64_t scratch_bytes,
+                     cudaStream_t stream);
+
+/* zero_clip_coef -- sums the partials (fp64, fixed order) and writes
+ * norm_coef[0] = (float)norm and norm_coef[1] = (float)coef on the device.
+ *   max_norm   > 0, finite
+ *   norm_coef  device float[2], 16-byte aligned */
+int zero_clip_coef(const double* scratch, int64_t scratch_bytes, double max_norm,
+                   float* norm_coef, cudaStream_t stream);
+
+/* zero_step_stage12_clip / zero3_reduce_scatter_unit_clip -- the two fused
+ * steps with the mean gradient multiplied (one fp32 multiply) by
+ * norm_coef[1] before AdamW.  norm_coef: device float[2] written by
+ * zero_clip_coef earlier on the same stream.  Other arguments as the
+ * unclipped calls. */
+int zero_step_stage12_clip(int32_t stage, int32_t n_ranks, int64_t n_padded,
+                           const uint16_t* const* grads, float* const* master,
+                           float* const* m, float* const* v, uint16_t* params_bf16,
+                           const zero_hparams_t* hp, int64_t bucket_elems,
+                           const float* norm_coef, cudaStream_t stream);
+int zero3_reduce_scatter_unit_clip(const zero_unit_t* unit, int32_t n_ranks,
+                                   const uint16_t* const* unit_grads, float* const* master,
+                                   float* const* m, float* const* v,
+                                   uint16_t* const* shard_bf16, const zero_hparams_t* hp,
+                                   const float* norm_coef, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------
  * ZeRO-3 step scheduler: the per-unit order of [DZF] "How FSDP implements
  * ZeRO-3", steps 2-5 (and [COL]'s per-unit step figure), issued natively.
  * ------------------------------------------------------------------- */
@@ -202,6 +255,8 @@ typedef struct {
 #define ZERO_OP_REDUCE_SCATTER 4
 #define ZERO_OP_REGEN 5
 #define ZERO_OP_USE 6
+#define ZERO_OP_NORM 7      /* unit's squared norm into the clip partials; arg = accumulate */
+#define ZERO_OP_CLIP_COEF 8 /* global norm and clip coefficient */
 
 /* zero3_plan -- host only.  The operations of one ZeRO-3 step over n_units
  * units, in issue order: record "start" on main and make side wait for it;
@@ -211,12 +266,17 @@ typedef struct {
  * unit p, uses it, and -- in the backward pass -- (optionally regenerates
  * and) reduce-scatters it, then records the buffer's release.  Two gathers
  * and one reduce-scatter per unit; at most two units gathered at a time.
- *   regen      non-zero: a REGEN op precedes each REDUCE_SCATTER
+ *   regen      non-zero: a REGEN op precedes each REDUCE_SCATTER (and each
+ *              NORM)
+ *   clip       non-zero: right after the start, NORM for every unit and one
+ *              CLIP_COEF on the main stream, and REDUCE_SCATTER ops carry
+ *              arg = 1 (scale by the coefficient)
  *   ops        caller array of max_ops entries; *n_ops receives the count
- *              (13*n_units + 2, plus n_units with regen, at most)
+ *              (13*n_units + 2, plus n_units with regen, plus n_units + 1
+ *              with clip, plus n_units with both, at most)
  * ZERO_EINVAL on n_units < 1, null pointers or max_ops too small. */
-int zero3_plan(int32_t n_units, int32_t regen, zero_op_t* ops, int32_t max_ops,
-               int32_t* n_ops);
+int zero3_plan(int32_t n_units, int32_t regen, int32_t clip, zero_op_t* ops,
+               int32_t max_ops, int32_t* n_ops);
 
 /* Harness regeneration of a unit's gradients inside zero3_step (the
  * stand-in for the backward compute that would produce them). */
@@ -225,6 +285,14 @@ typedef struct {
     double sigma;
     int32_t outliers;
 } zero_regen_t;
+
+/* Global-norm clipping inside zero3_step: the buffers of the clipping calls. */
+typedef struct {
+    double max_norm;
+    double* scratch;       /* device, >= zero_clip_scratch_bytes() */
+    int64_t scratch_bytes;
+    float* norm_coef;      /* device float[2]: norm and coefficient of this step */
+} zero_clip_t;
 
 /* zero3_step -- one whole ZeRO-3 step: executes zero3_plan's operations with
  * zero3_gather_unit, zero3_reduce_scatter_unit and (if regen != NULL)
@@ -239,6 +307,8 @@ typedef struct {
  *   master, m, v, shard_bf16   as zero3_reduce_scatter_unit
  *   full_a, full_b   two device buffers of the largest unit's n_padded bf16
  *   hp               the step's hyper-parameters (the same t for all units)
+ *   clip             NULL, or global-norm clipping over all units (the norm
+ *                    pre-pass reads every unit's gradients once more)
  * The library keeps five timing-free CUDA events per host thread and device
  * (created on first use); no device memory is allocated.  Work is queued
  * asynchronously; on return main_stream carries the end of the step.
@@ -248,7 +318,8 @@ int zero3_step(const zero_unit_t* units, int32_t n_units, int32_t n_ranks,
                float* const* master, float* const* m, float* const* v,
                uint16_t* const* shard_bf16, uint16_t* full_a, uint16_t* full_b,
                const zero_hparams_t* hp, const zero_regen_t* regen,
-               cudaStream_t main_stream, cudaStream_t side_stream);
+               const zero_clip_t* clip, cudaStream_t main_stream,
+               cudaStream_t side_stream);
 
 /* ---------------------------------------------------------------------
  * Harness calls: seeded synthetic inputs and helpers.  They are not part

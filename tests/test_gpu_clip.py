@@ -1,0 +1,196 @@
+"""GPU parity of global gradient-norm clipping across the shards against the
+oracle: the norm pass and coefficient, the clipped ZeRO-1/2 step, and the
+clipped ZeRO-3 step through the native scheduler.
+
+Bound on the norm: the GPU sums squares pairwise in fp32 with Kahan
+compensation and in fp64 across threads and blocks (relative error of the
+squared norm < 4e-7, of the norm < 2e-7, plus one fp32 rounding of the
+stored norm); the oracle sums in fp64.  Both are checked within 1e-6
+relative.  The clipped updates differ from the oracle only through the
+coefficient (1 fp32 ulp at most) and are checked with the acceptance
+tolerance (1e-6 relative on master/m/v, 1 bf16 ulp on weights)."""
+import numpy as np
+import pytest
+import torch
+
+import gpu_harness as H
+from fsdp_sharded_optimizer_gb300 import _binding as B
+
+pytestmark = pytest.mark.gpu
+
+
+def _scratch():
+    nbytes = B.zero_clip_scratch_bytes()
+    return torch.empty(nbytes // 8, dtype=torch.float64, device="cuda")
+
+
+def _norm_coef():
+    return torch.empty(4, dtype=torch.float32, device="cuda")[:2]
+
+
+def _gpu_norm(grads_rows, max_norm, scratch=None, out=None):
+    scratch = _scratch() if scratch is None else scratch
+    out = _norm_coef() if out is None else out
+    B.zero_grad_sqnorm(grads_rows, scratch)
+    B.zero_clip_coef(scratch, max_norm, out)
+    torch.cuda.synchronize()
+    return out.cpu().numpy(), scratch, out
+
+
+@pytest.mark.parametrize("N,P,outliers", [(2, 1000, 0), (8, 2**16 + 37, 1), (64, 70_000, 1),
+                                          (3, 123_457, 0), (8, 2**22, 1)])
+def test_norm_matches_oracle(orc, N, P, outliers):
+    (u,), _ = B.zero_layout([P], N)
+    g = H.Guarded(N, u.n_padded, torch.int16)
+    B.zero_gen_grads_unit(4, 1, H.SIGMA_G, outliers, u, g.rows)
+    torch.cuda.synchronize()
+    host = g.numpy()
+    for max_norm in (1e-4, 10.0):
+        nc, _, _ = _gpu_norm(g.rows, max_norm)
+        coef, norm = orc.clip_coef(orc.grad_sumsq(host), max_norm)
+        assert abs(float(nc[0]) - norm) <= 1e-6 * norm
+        assert abs(float(nc[1]) - float(coef)) <= 1e-6 * float(coef)
+    g.check()
+
+
+def test_norm_is_deterministic_and_accumulates_over_units(orc):
+    N, sizes = 8, [40_000, 1234, 77_777, 64]
+    units, total = B.zero_layout(sizes, N)
+    g = H.Guarded(N, total, torch.int16)
+    for u in units:
+        B.zero_gen_grads_unit(9, 2, H.SIGMA_G, 1, u, [r[u.offset:u.offset + u.n_padded] for r in g.rows])
+    a, b = _scratch(), _scratch()
+    outs = []
+    for sc in (a, b):
+        for i, u in enumerate(units):
+            B.zero_grad_sqnorm([r[u.offset:u.offset + u.n_padded] for r in g.rows], sc, accumulate=i > 0)
+        o = _norm_coef()
+        B.zero_clip_coef(sc, 1e-3, o)
+        outs.append(o)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1]) and torch.equal(a, b)
+    host = g.numpy()
+    ref = sum(orc.grad_sumsq(np.ascontiguousarray(host[:, u.offset:u.offset + u.n_padded]))
+              for u in units)
+    coef, norm = orc.clip_coef(ref, 1e-3)
+    got = outs[0].cpu().numpy()
+    assert abs(float(got[0]) - norm) <= 1e-6 * norm
+    assert abs(float(got[1]) - float(coef)) <= 1e-6 * float(coef)
+
+
+@pytest.mark.parametrize("stage,N,P,bucket,max_norm", [(1, 2, 2**20, 0, 1e-3), (2, 8, 300_001, 104, 2e-3),
+                                                       (2, 64, 2**16 + 37, 4096, 1e-4),
+                                                       (1, 3, 65, 0, 1e-5)])
+def test_clipped_zero12_step_matches_oracle(orc, stage, N, P, bucket, max_norm):
+    T, seed = 10, 6
+    (u,), _ = B.zero_layout([P], N)
+    grads = H.Guarded(N, u.n_padded, torch.int16)
+    master = H.Guarded(N, u.shard_len, torch.float32)
+    m = H.Guarded(N, u.shard_len, torch.float32).zero_()
+    v = H.Guarded(N, u.shard_len, torch.float32).zero_()
+    params = H.Guarded(1, u.n_padded, torch.int16)
+    B.zero_gen_master(seed, H.SIGMA_W, [u], master.rows)
+    (ou,), _ = orc.layout([P], N)
+    rw = orc.gen_master(seed, H.SIGMA_W, [ou], N)
+    rm, rv = np.zeros_like(rw), np.zeros_like(rw)
+    rp = np.zeros(ou.n_padded, np.uint16)
+    scratch, nc = _scratch(), _norm_coef()
+    clipped = 0
+    for t in range(1, T + 1):
+        B.zero_gen_grads_unit(seed, t, H.SIGMA_G, 1, u, grads.rows)
+        B.zero_grad_sqnorm(grads.rows, scratch)
+        B.zero_clip_coef(scratch, max_norm, nc)
+        B.zero_step_stage12_clip(stage, grads.rows, master.rows, m.rows, v.rows, params.rows[0],
+                                 H.hp(t), nc, bucket)
+        g = orc.gen_grads_unit(seed, t, H.SIGMA_G, 1, ou, N)
+        norm, coef = orc.zero12_step_clip(stage, g, rw, rm, rv, rp, orc.hparams(**H.HP, step=t),
+                                          max_norm, bucket)
+        got = nc.cpu().numpy()
+        assert abs(float(got[0]) - norm) <= 1e-6 * norm
+        clipped += coef < 1
+    assert clipped == T  # every step actually clipped
+    torch.cuda.synchronize()
+    for b_ in (grads, master, m, v, params):
+        b_.check()
+    H.assert_within_tolerance((master.numpy(), m.numpy(), v.numpy()), (rw, rm, rv),
+                              params.numpy()[0], rp)
+    assert not params.numpy()[0][P:].any()
+
+
+def test_inactive_clip_is_bitwise_unclipped():
+    N, P, T = 8, 300_001, 5
+    ref = H.run_zero12(2, N, P, T, seed=2, outliers=1, bucket=8 * 1001)
+    (u,), _ = B.zero_layout([P], N)
+    grads = H.Guarded(N, u.n_padded, torch.int16)
+    master = H.Guarded(N, u.shard_len, torch.float32)
+    m = H.Guarded(N, u.shard_len, torch.float32).zero_()
+    v = H.Guarded(N, u.shard_len, torch.float32).zero_()
+    params = H.Guarded(1, u.n_padded, torch.int16)
+    B.zero_gen_master(2, H.SIGMA_W, [u], master.rows)
+    scratch, nc = _scratch(), _norm_coef()
+    for t in range(1, T + 1):
+        B.zero_gen_grads_unit(2, t, H.SIGMA_G, 1, u, grads.rows)
+        B.zero_grad_sqnorm(grads.rows, scratch)
+        B.zero_clip_coef(scratch, 1e6, nc)
+        B.zero_step_stage12_clip(2, grads.rows, master.rows, m.rows, v.rows, params.rows[0],
+                                 H.hp(t), nc, 8 * 1001)
+    torch.cuda.synchronize()
+    assert float(nc[1]) == 1.0
+    for x, y, n in zip(ref[:4], (params.numpy()[0], master.numpy(), m.numpy(), v.numpy()),
+                       ("params", "master", "m", "v")):
+        H.assert_bitwise(y, x, n)
+
+
+def test_clipped_zero3_native_step_matches_oracle(orc):
+    N, sizes, T, seed, max_norm = 4, [70_000, 333, 200_000, 64, 90_001], 4, 3, 1e-3
+    units, total = B.zero_layout(sizes, N)
+    ounits, _ = orc.layout(sizes, N)
+    shard_total = total // N
+    master = H.Guarded(N, shard_total, torch.float32)
+    m = H.Guarded(N, shard_total, torch.float32).zero_()
+    v = H.Guarded(N, shard_total, torch.float32).zero_()
+    shards = H.Guarded(N, shard_total, torch.int16)
+    B.zero_gen_master(seed, H.SIGMA_W, units, master.rows)
+    for k in range(N):
+        B.zero_cast_bf16(master.rows[k], shards.rows[k])
+    max_unit = max(u.n_padded for u in units)
+    grads = H.Guarded(N, max_unit, torch.int16)
+    fa, fb = H.Guarded(1, max_unit, torch.int16), H.Guarded(1, max_unit, torch.int16)
+    scratch, nc = _scratch(), _norm_coef()
+    clip = B.clip_args(max_norm, scratch, nc)
+    side = torch.cuda.Stream()
+    rw = orc.gen_master(seed, H.SIGMA_W, ounits, N)
+    rm, rv = np.zeros_like(rw), np.zeros_like(rw)
+    rs = orc.bf16_rne(rw)
+    for t in range(1, T + 1):
+        B.zero3_step(units, grads.rows, master.rows, m.rows, v.rows, shards.rows, fa.rows[0],
+                     fb.rows[0], H.hp(t), grads_resident=False,
+                     regen=B.zero_regen_t(seed, H.SIGMA_G, 1), clip=clip, side_stream=side)
+        gs = [orc.gen_grads_unit(seed, t, H.SIGMA_G, 1, ou, N) for ou in ounits]
+        coef, norm = orc.clip_coef(sum(orc.grad_sumsq(g) for g in gs), max_norm)
+        for ou, g in zip(reversed(ounits), reversed(gs)):
+            orc.zero3_reduce_scatter_unit_coef(ou, g, rw, rm, rv, rs, orc.hparams(**H.HP, step=t),
+                                               coef)
+        got = nc.cpu().numpy()
+        assert abs(float(got[0]) - norm) <= 1e-6 * norm and coef < 1
+    torch.cuda.synchronize()
+    for b_ in (master, m, v, shards, grads, fa, fb):
+        b_.check()
+    H.assert_within_tolerance((master.numpy(), m.numpy(), v.numpy()), (rw, rm, rv),
+                              shards.numpy(), rs)
+
+
+def test_gpt2_shaped_norm_full_size(orc):
+    """The norm pass over the full GPT-2-small buffer at N_d = 8 (the benchmark's
+    workload) against the oracle's fp64 sum over the same gradients."""
+    N, P = 8, 124_439_808
+    (u,), _ = B.zero_layout([P], N)
+    g = torch.empty((N, u.n_padded), dtype=torch.int16, device="cuda")
+    B.zero_gen_grads_unit(0, 1, H.SIGMA_G, 0, u, g)
+    nc, _, _ = _gpu_norm(g, 1.0)
+    host = g.cpu().numpy().view(np.uint16)
+    coef, norm = orc.clip_coef(orc.grad_sumsq(host), 1.0)
+    assert abs(float(nc[0]) - norm) <= 1e-6 * norm
+    assert float(nc[1]) == float(coef)
+    del g
+    H.free()

@@ -104,9 +104,20 @@ def _table(addrs):
 
 
 # Fake device addresses: validation must reject before anything touches them.
+# These tests exercise host-side validation only; they never run where a GPU
+# is visible, so that a validation bug cannot launch a kernel on fake pointers.
 A16 = [0x10000 * (i + 1) for i in range(64)]
 
 
+def _no_gpu():
+    import torch
+    return not torch.cuda.is_available()
+
+
+host_only = pytest.mark.skipif(not _no_gpu(), reason="fake device addresses: CPU-only check")
+
+
+@host_only
 def test_step_rejects_before_launch(B):
     hp = B.hparams()
     g = _table(A16[:8])
@@ -133,6 +144,7 @@ def test_step_rejects_before_launch(B):
     assert call(1, 8, 1024, g, w, m, v, C.c_void_p(0x900002), C.byref(hp), 0, None) == B.ZERO_EALIGN
 
 
+@host_only
 def test_zero3_calls_reject_before_launch(B):
     (u,), _ = B.zero_layout([1000], 4)
     hp = B.hparams()
@@ -161,6 +173,7 @@ def test_strerror_names_codes(B):
     assert B.strerror(-99) == "unknown error"
 
 
+@host_only
 def test_zero3_step_rejects_before_launch(B):
     units, _ = B.zero_layout([1000, 64], 4)
     arr = (B.zero_unit_t * 2)(*units)
@@ -169,26 +182,57 @@ def test_zero3_step_rejects_before_launch(B):
     fa, fb = C.c_void_p(0x900000), C.c_void_p(0xA00000)
     s1, s2 = C.c_void_p(0x1), C.c_void_p(0x2)
     call = B.lib.zero3_step
-    ok_args = (arr, 2, 4, t, 1, t, t, t, t, fa, fb, C.byref(hp), None, s1, s2)
+    ok_args = (arr, 2, 4, t, 1, t, t, t, t, fa, fb, C.byref(hp), None, None, s1, s2)
     bad = [
-        (arr, 0, 4, t, 1, t, t, t, t, fa, fb, C.byref(hp), None, s1, s2),   # no units
-        (arr, 2, 3, t, 1, t, t, t, t, fa, fb, C.byref(hp), None, s1, s2),   # layout for 4 ranks
-        (arr, 2, 4, t, 1, t, t, t, t, fa, fa, C.byref(hp), None, s1, s2),   # one full buffer
-        (arr, 2, 4, t, 1, t, t, t, t, fa, fb, C.byref(hp), None, s1, s1),   # one stream
-        (arr, 2, 4, t, 0, t, t, t, t, fa, fb, C.byref(hp), None, s1, s2),   # nothing fills grads
-        (arr, 2, 4, t, 1, t, t, t, None, fa, fb, C.byref(hp), None, s1, s2),
-        (None, 2, 4, t, 1, t, t, t, t, fa, fb, C.byref(hp), None, s1, s2),
+        (arr, 0, 4, t, 1, t, t, t, t, fa, fb, C.byref(hp), None, None, s1, s2),   # no units
+        (arr, 2, 3, t, 1, t, t, t, t, fa, fb, C.byref(hp), None, None, s1, s2),   # layout for 4 ranks
+        (arr, 2, 4, t, 1, t, t, t, t, fa, fa, C.byref(hp), None, None, s1, s2),   # one full buffer
+        (arr, 2, 4, t, 1, t, t, t, t, fa, fb, C.byref(hp), None, None, s1, s1),   # one stream
+        (arr, 2, 4, t, 0, t, t, t, t, fa, fb, C.byref(hp), None, None, s1, s2),   # nothing fills grads
+        (arr, 2, 4, t, 1, t, t, t, None, fa, fb, C.byref(hp), None, None, s1, s2),
+        (None, 2, 4, t, 1, t, t, t, t, fa, fb, C.byref(hp), None, None, s1, s2),
     ]
     for args in bad:
         assert call(*args) == B.ZERO_EINVAL
-    mis = (arr, 2, 4, t, 1, t, t, t, t, C.c_void_p(0x900002), fb, C.byref(hp), None, s1, s2)
+    mis = (arr, 2, 4, t, 1, t, t, t, t, C.c_void_p(0x900002), fb, C.byref(hp), None, None, s1, s2)
     assert call(*mis) == B.ZERO_EALIGN
-    assert len(ok_args) == 15
+    assert len(ok_args) == 16
 
 
 def test_zero3_plan_rejects(B):
     ops = (B.zero_op_t * 10)()
     n = C.c_int32()
-    assert B.lib.zero3_plan(0, 0, ops, 10, C.byref(n)) == B.ZERO_EINVAL
-    assert B.lib.zero3_plan(3, 0, ops, 10, C.byref(n)) == B.ZERO_EINVAL   # too small
-    assert B.lib.zero3_plan(3, 0, None, 10, C.byref(n)) == B.ZERO_EINVAL
+    assert B.lib.zero3_plan(0, 0, 0, ops, 10, C.byref(n)) == B.ZERO_EINVAL
+    assert B.lib.zero3_plan(3, 0, 0, ops, 10, C.byref(n)) == B.ZERO_EINVAL   # too small
+    assert B.lib.zero3_plan(3, 0, 0, None, 10, C.byref(n)) == B.ZERO_EINVAL
+
+
+@host_only
+def test_clip_calls_reject_before_launch(B):
+    nbytes = B.zero_clip_scratch_bytes()
+    assert nbytes == 1216 * 8
+    t = _table(A16[:4])
+    sc = C.c_void_p(0x900000)
+    f = B.lib.zero_grad_sqnorm
+    assert f(4, 1004, t, 0, sc, nbytes, None) == B.ZERO_EINVAL       # n_elems % 8
+    assert f(4, 0, t, 0, sc, nbytes, None) == B.ZERO_EINVAL
+    assert f(0, 1024, t, 0, sc, nbytes, None) == B.ZERO_EINVAL
+    assert f(4, 1024, t, 0, sc, nbytes - 8, None) == B.ZERO_EINVAL   # scratch too small
+    assert f(4, 1024, t, 0, None, nbytes, None) == B.ZERO_EINVAL
+    assert f(4, 1024, t, 0, C.c_void_p(0x900008), nbytes, None) == B.ZERO_EALIGN
+    assert f(4, 1024, _table(A16[:3] + [0]), 0, sc, nbytes, None) == B.ZERO_EINVAL
+    g = B.lib.zero_clip_coef
+    nc = C.c_void_p(0xA00000)
+    assert g(sc, nbytes, 0.0, nc, None) == B.ZERO_EINVAL
+    assert g(sc, nbytes, float("inf"), nc, None) == B.ZERO_EINVAL
+    assert g(sc, nbytes, 1.0, None, None) == B.ZERO_EINVAL
+    assert g(sc, nbytes, 1.0, C.c_void_p(0xA00004), None) == B.ZERO_EALIGN
+    hp = B.hparams()
+    w = _table(A16[8:12])
+    p = C.c_void_p(0xB00000)
+    h = B.lib.zero_step_stage12_clip
+    assert h(1, 4, 1024, t, w, w, w, p, C.byref(hp), 0, None, None) == B.ZERO_EINVAL
+    assert h(1, 4, 1024, t, w, w, w, p, C.byref(hp), 0, C.c_void_p(0xA00004), None) == B.ZERO_EALIGN
+    (u,), _ = B.zero_layout([1000], 4)
+    k = B.lib.zero3_reduce_scatter_unit_clip
+    assert k(C.byref(u), 4, t, w, w, w, t, C.byref(hp), None, None) == B.ZERO_EINVAL

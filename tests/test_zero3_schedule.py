@@ -101,12 +101,12 @@ def test_prefetch_order_and_buffer_safety(orc):
     check_zero3_trace(be.trace, len(units), 2)
 
 
-def _native_trace(n_units, n_steps, regen=False):
+def _native_trace(n_units, n_steps, regen=False, clip=False):
     from fsdp_sharded_optimizer_gb300 import _binding as B
     names = {0: "main", 1: "side"}
     trace = []
     for _ in range(n_steps):
-        for kind, stream, unit, arg in B.zero3_plan(n_units, regen):
+        for kind, stream, unit, arg in B.zero3_plan(n_units, regen, clip):
             st = names[stream]
             if kind in ("record", "wait"):
                 trace.append((kind, st, "ev%d" % arg))
@@ -121,12 +121,24 @@ def _native_trace(n_units, n_steps, regen=False):
     return trace
 
 
-@pytest.mark.parametrize("n_units,n_steps,regen", [(1, 1, False), (2, 1, False), (5, 3, False),
-                                                   (33, 2, True), (23, 2, False)])
-def test_native_plan_is_safe(n_units, n_steps, regen):
+@pytest.mark.parametrize("n_units,n_steps,regen,clip", [(1, 1, False, False), (2, 1, False, True),
+                                                        (5, 3, False, False), (33, 2, True, True),
+                                                        (23, 2, False, True), (4, 2, True, False)])
+def test_native_plan_is_safe(n_units, n_steps, regen, clip):
     """The native scheduler's plan (zero3_plan, the operations zero3_step
     executes) obeys the same happens-before rules as the Python schedule."""
-    check_zero3_trace(_native_trace(n_units, n_steps, regen), n_units, n_steps)
+    trace = _native_trace(n_units, n_steps, regen, clip)
+    check_zero3_trace(trace, n_units, n_steps)
+    if clip:
+        # each step: every unit's norm, then the coefficient, before any reduce-scatter
+        per = len(trace) // n_steps
+        for s0 in range(0, len(trace), per):
+            st = trace[s0:s0 + per]
+            kinds = [e[0] for e in st]
+            first_rs, coef = kinds.index("rs"), kinds.index("clip_coef")
+            norms = [i for i, k in enumerate(kinds) if k == "norm"]
+            assert len(norms) == n_units and max(norms) < coef < first_rs
+            assert all(e[1] == "main" for e in st if e[0] in ("norm", "clip_coef"))
 
 
 def test_native_plan_counts_and_regen():
@@ -134,7 +146,13 @@ def test_native_plan_counts_and_regen():
     ops = B.zero3_plan(2, False)
     kinds = [o[0] for o in ops]
     assert kinds.count("gather") == 4 and kinds.count("reduce_scatter") == 2
-    assert "regen" not in kinds and len(ops) <= 13 * 2 + 2
+    assert "regen" not in kinds and "norm" not in kinds and len(ops) <= 13 * 2 + 2
+    assert all(o[3] == 0 for o in ops if o[0] == "reduce_scatter")
+    ops = B.zero3_plan(3, True, True)
+    assert len(ops) <= 13 * 3 + 2 + 3 + 3 + 1 + 3
+    assert all(o[3] == 1 for o in ops if o[0] == "reduce_scatter")
+    norms = [o for o in ops if o[0] == "norm"]
+    assert [o[3] for o in norms] == [0, 1, 1]  # the first unit overwrites the partials
     ops = B.zero3_plan(4, True)
     kinds = [o[0] for o in ops]
     assert kinds.count("regen") == 4 and len(ops) <= 14 * 4 + 2
