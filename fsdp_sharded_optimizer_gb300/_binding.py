@@ -95,6 +95,7 @@ SIGNATURES = {
     "zero_step_stage12_clip": (C.c_int, [_I32, _I32, _I64, _P, _P, _P, _P, _P, _P, _I64, _P,
                                          _P]),
     "zero3_reduce_scatter_unit_clip": (C.c_int, [_P, _I32, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "zero_clip_coef_units_noalloc": (C.c_int, [_P, _I32, _I32, _P, _F64, _P, _P, _P]),
     "zero3_plan": (C.c_int, [_I32, _I32, _I32, _P, _I32, _P]),
     "zero3_step": (C.c_int, [_P, _I32, _I32, _P, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                              _P]),
@@ -251,6 +252,23 @@ def zero3_reduce_scatter_unit_clip(unit, unit_grads, master, m, v, shard_bf16, h
     s, _ = _rows(shard_bf16, 2, "shard_bf16")
     _check("zero3_reduce_scatter_unit_clip", lib.zero3_reduce_scatter_unit_clip(
         C.byref(unit), len(grows), g, w, mm, vv, s, C.byref(hp), _dev(norm_coef, 4, "norm_coef"),
+        _stream(stream)))
+
+
+ZERO_NOALLOC_MAX_UNITS = 1024
+
+
+def zero_clip_coef_units_noalloc(units, grads, max_norm, norm_coef, unit_norms=None, stream=None):
+    """Global-norm clip coefficient over `units` (rank r's gradients of every
+    unit concatenated in grads[r]) using the library's fixed internal scratch
+    instead of caller memory: for callers that cannot allocate device memory.
+    norm_coef (device float[2]) <- (norm, coef); unit_norms (optional device
+    float[len(units)]) <- each unit's norm.  At most ZERO_NOALLOC_MAX_UNITS units."""
+    g, rows = _rows(grads, 2, "grads")
+    arr = (zero_unit_t * len(units))(*units)
+    un = _dev(unit_norms, 4, "unit_norms") if unit_norms is not None else None
+    _check("zero_clip_coef_units_noalloc", lib.zero_clip_coef_units_noalloc(
+        arr, len(units), len(rows), g, float(max_norm), _dev(norm_coef, 4, "norm_coef"), un,
         _stream(stream)))
 
 

@@ -229,6 +229,34 @@ int zero3_reduce_scatter_unit_clip(const zero_unit_t* unit, int32_t n_ranks,
                                    uint16_t* const* shard_bf16, const zero_hparams_t* hp,
                                    const float* norm_coef, cudaStream_t stream);
 
+/* zero_clip_coef_units_noalloc -- the same global-norm clip coefficient as
+ * zero_grad_sqnorm over each unit followed by zero_clip_coef, for callers that
+ * cannot allocate device memory (code running inside another framework whose
+ * memory pool owns the GPU, a monitoring thread that must not touch the
+ * training loop's allocator, a runtime held to a fixed memory budget).  The
+ * pages have no counterpart: this is a library convenience.
+ * The scratch is a fixed array inside the library (17,920 bytes of device
+ * memory, held on every GPU that loads the library until the process exits);
+ * no memory is allocated.  The caller passes inputs and outputs only:
+ *   units[n_units]  layouts (host array); unit u's gradients of rank r start
+ *                   at grads[r] + units[u].offset and span units[u].n_padded
+ *   n_units         1 .. ZERO_NOALLOC_MAX_UNITS (more: ZERO_EINVAL, the
+ *                   array's capacity)
+ *   grads           n_ranks device pointers (read only)
+ *   norm_coef       device float[2], 16-byte aligned: global norm, coefficient
+ *   unit_norms      NULL or device float[n_units], 16-byte aligned: each
+ *                   unit's gradient norm
+ * The global norm sums the units' squared norms in a different association
+ * than zero_clip_coef does, so the two agree within fp32 rounding, not bit for
+ * bit.  The first call on a device looks up the array's device address with
+ * that device current; make it before any stream capture.  All calls share the
+ * array: calls whose GPU work overlaps (two streams, two threads) race; order
+ * them on one stream. */
+#define ZERO_NOALLOC_MAX_UNITS 1024
+int zero_clip_coef_units_noalloc(const zero_unit_t* units, int32_t n_units, int32_t n_ranks,
+                                 const uint16_t* const* grads, double max_norm,
+                                 float* norm_coef, float* unit_norms, cudaStream_t stream);
+
 /* ---------------------------------------------------------------------
  * ZeRO-3 step scheduler: the per-unit order of [DZF] "How FSDP implements
  * ZeRO-3", steps 2-5 (and [COL]'s per-unit step figure), issued natively.
