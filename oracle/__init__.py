@@ -86,6 +86,9 @@ def lib():
                                   i64, P, P, P, P, P]),
             "or_sample": (None, [i32, u64, f64, f64, i32, P, i32, P, i64, P, P, P, P]),
             "or_grad_sumsq": (f64, [i32, i64, P]),
+            "or_zero2_accumulate": (i32, [i32, i64, P, P, i32]),
+            "or_zero2_step_accumulated": (i32, [i32, i64, P, P, i32, P, P, P, P, P]),
+            "or_comm_volume": (f64, [i32, i32, i32, f64]),
             "or_clip_coef": (f32, [f64, f64, P]),
             "or_zero12_step_clip": (i32, [i32, i32, i64, P, P, P, P, P, P, i64, f64, P, P]),
             "or_zero3_reduce_scatter_unit_coef": (i32, [P, i32, P, P, P, P, P, P, f32]),
@@ -215,6 +218,25 @@ def zero3_reduce_scatter_unit_coef(unit, unit_grads, master, m, v, shards, hp, c
     _check(lib().or_zero3_reduce_scatter_unit_coef(
         C.byref(unit), unit_grads.shape[0], _rows(unit_grads), _rows(master), _rows(m),
         _rows(v), _rows(shards), C.byref(hp), float(coef)), "or_zero3_reduce_scatter_unit_coef")
+
+
+# ------------------------------------------------------------- accumulation
+def zero2_accumulate(grads, grad_acc, first):
+    N, Pp = grads.shape
+    _check(lib().or_zero2_accumulate(N, Pp, _rows(grads), _rows(grad_acc), 1 if first else 0),
+           "or_zero2_accumulate")
+
+
+def zero2_step_accumulated(grads, grad_acc, micro_batches, master, m, v, params, hp):
+    N, Pp = grads.shape
+    _check(lib().or_zero2_step_accumulated(
+        N, Pp, _rows(grads), _rows(grad_acc) if grad_acc is not None else None, micro_batches,
+        _rows(master), _rows(m), _rows(v), _ptr(params), C.byref(hp)), "or_zero2_step_accumulated")
+
+
+def comm_volume(stage, micro_batches, reshard_after_forward, n_params):
+    return lib().or_comm_volume(stage, micro_batches, 1 if reshard_after_forward else 0,
+                                float(n_params))
 
 
 # ------------------------------------------------------------- accounting

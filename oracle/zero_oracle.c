@@ -334,6 +334,74 @@ int or_zero3_reduce_scatter_unit_coef(const or_unit_t* unit, int32_t n_ranks,
 }
 
 /* ======================================================================
+ * ZeRO-2 gradient accumulation.  [DZF] "Gradient accumulation": m
+ * micro-batches run one after the other and their gradients are added before
+ * one optimizer step; ZeRO-2 keeps no full gradient, so it reduce-scatters
+ * after every micro-batch (m*P + P elements per step).  Each owner keeps an
+ * fp32 accumulator of its slice: acc = +0, then acc = acc + mean_mu for every
+ * micro-batch mu (mean_mu = the reduce-scatter mean of that micro-batch); the
+ * step uses g = acc * (float)(1/m), the mean over the micro-batches (each
+ * micro-batch's gradient is that of its own mean loss, so the accumulated
+ * gradient is the gradient of the mean loss over all m*N micro-batches).
+ * or_zero2_accumulate handles micro-batches 1..m-1; the last micro-batch's
+ * reduce-scatter is folded into or_zero2_step_accumulated.
+ * ==================================================================== */
+int or_zero2_accumulate(int32_t n_ranks, int64_t n_padded, const uint16_t* const* grads,
+                        float* const* grad_acc, int32_t first)
+{
+    if (n_ranks < 1 || n_padded <= 0 || n_padded % n_ranks != 0 || !grads || !grad_acc)
+        return OR_EINVAL;
+    int64_t S = n_padded / n_ranks;
+    float inv_n = (float)(1.0 / (double)n_ranks);
+    for (int64_t i = 0; i < n_padded; ++i) {
+        int64_t k = i / S, j = i - k * S;
+        float a = first ? 0.0f : grad_acc[k][j];
+        grad_acc[k][j] = a + or_reduce_mean(grads, n_ranks, i, inv_n);
+    }
+    return OR_OK;
+}
+
+int or_zero2_step_accumulated(int32_t n_ranks, int64_t n_padded, const uint16_t* const* grads,
+                              const float* const* grad_acc, int32_t micro_batches,
+                              float* const* master, float* const* m, float* const* v,
+                              uint16_t* params_bf16, const or_hparams_t* hp)
+{
+    if (n_ranks < 1 || n_padded <= 0 || n_padded % n_ranks != 0 || !grads ||
+        (micro_batches > 1 && !grad_acc) || micro_batches < 1 || !master || !m || !v ||
+        !params_bf16 || bad_hp(hp))
+        return OR_EINVAL;
+    int64_t S = n_padded / n_ranks;
+    or_scalars_t s;
+    or_scalars(hp, n_ranks, &s);
+    float inv_m = (float)(1.0 / (double)micro_batches);
+    for (int64_t i = 0; i < n_padded; ++i) {
+        int64_t k = i / S, j = i - k * S;
+        float a = micro_batches > 1 ? grad_acc[k][j] : 0.0f;
+        float g = (a + or_reduce_mean(grads, n_ranks, i, s.inv_n)) * inv_m;
+        or_adamw(g, &master[k][j], &m[k][j], &v[k][j], &s);
+        params_bf16[i] = or_bf16_rne(master[k][j]);
+    }
+    return OR_OK;
+}
+
+/* Elements sent per rank per optimizer step with m micro-batches ([DZF]
+ * "Gradient accumulation" table; "How FSDP implements ZeRO-3", step 6, for
+ * reshard_after_forward = 0: the backward all-gather disappears): DDP 2P,
+ * ZeRO-1 2P, ZeRO-2 mP + P, ZeRO-3 3mP (2mP without resharding). */
+double or_comm_volume(int32_t stage, int32_t micro_batches, int32_t reshard_after_forward,
+                      double n_params)
+{
+    double m = (double)micro_batches, P = n_params;
+    switch (stage) {
+    case 0:
+    case 1: return 2.0 * P;
+    case 2: return m * P + P;
+    case 3: return (reshard_after_forward ? 3.0 : 2.0) * m * P;
+    default: return -1.0;
+    }
+}
+
+/* ======================================================================
  * Accounting.  [DZF] Theorem (ZeRO memory and communication), table and
  * proof steps 1-7; [DDF] "Memory accounting" (state_bytes raises on
  * params <= 0 or ranks < 1).  Bytes per parameter: bf16 weight 2, bf16

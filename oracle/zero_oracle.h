@@ -120,6 +120,16 @@ int or_zero3_reduce_scatter_unit_coef(const or_unit_t* unit, int32_t n_ranks,
                                       float* const* v, uint16_t* const* shard_bf16,
                                       const or_hparams_t* hp, float coef);
 
+/* ------------------------------------------------ ZeRO-2 gradient accumulation */
+int or_zero2_accumulate(int32_t n_ranks, int64_t n_padded, const uint16_t* const* grads,
+                        float* const* grad_acc, int32_t first);
+int or_zero2_step_accumulated(int32_t n_ranks, int64_t n_padded, const uint16_t* const* grads,
+                              const float* const* grad_acc, int32_t micro_batches,
+                              float* const* master, float* const* m, float* const* v,
+                              uint16_t* params_bf16, const or_hparams_t* hp);
+double or_comm_volume(int32_t stage, int32_t micro_batches, int32_t reshard_after_forward,
+                      double n_params);
+
 /* ------------------------------------------------------------- accounting */
 int or_state_bytes(int64_t n_params, int32_t n_ranks, int32_t stage, int32_t K,
                    or_bytes_t* out);

@@ -42,6 +42,12 @@ MUTANTS = [
      "double c = max_norm / norm;"),
     ("clip_coef_unused", "zero_oracle.c", "float g = or_reduce_mean(grads, n_ranks, i, s.inv_n) * coef;",
      "float g = or_reduce_mean(grads, n_ranks, i, s.inv_n);"),
+    ("accumulator_restarts", "zero_oracle.c", "float a = first ? 0.0f : grad_acc[k][j];",
+     "float a = 0.0f;"),
+    ("accumulation_not_averaged", "zero_oracle.c",
+     "float g = (a + or_reduce_mean(grads, n_ranks, i, s.inv_n)) * inv_m;",
+     "float g = (a + or_reduce_mean(grads, n_ranks, i, s.inv_n));"),
+    ("zero2_accum_volume_mP", "zero_oracle.c", "case 2: return m * P + P;", "case 2: return m * P;"),
     ("generator_lane_dropped", "gen_oracle.c", "(int32_t)(h >> 48) - 131070", "(int32_t)(h >> 48) * 0 - 131070"),
 ]
 

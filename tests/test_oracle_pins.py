@@ -476,6 +476,8 @@ def test_accounting_matches_pages(orc, kind, args, approx, cite):
         got = budget / orc.state_bytes(1, N, stage, K)["state_bytes"]
     elif kind == "sent":
         got = orc.state_bytes(int(args[0]), int(args[1]), int(args[2]))["comm_sent_elems"]
+    elif kind == "volume":
+        got = orc.comm_volume(int(args[0]), int(args[1]), int(args[2]), 1.0)
     elif kind == "ring":
         payload, N, k, count = float(args[0]), int(args[1]), int(args[2]), int(args[3])
         got = count * orc.ring_sent_bytes(payload, N, k)
@@ -612,3 +614,74 @@ def test_zero3_unit_coef_equals_clipped_flat_step(orc):
         rows = [w3[k][u.shard_offset:u.shard_offset + u.shard_len] for k in range(N)]
         got.append(np.concatenate(rows)[:u.n_params])
     np.testing.assert_allclose(np.concatenate(got), flat(w1), rtol=1e-6, atol=1e-9)
+
+
+# ------------------------------------------------------------------ accumulation
+def _acc_run(orc, N, P, micro, seed, T, same=False):
+    """T accumulated ZeRO-2 steps of `micro` micro-batches each; micro-batch mu of
+    step t draws its gradients at step id t*100 + mu (or t*100 when same)."""
+    (u,), _ = orc.layout([P], N)
+    w = orc.gen_master(seed, 0.02, [u], N)
+    m, v = np.zeros_like(w), np.zeros_like(w)
+    acc = np.zeros_like(w)
+    p = np.zeros(u.n_padded, np.uint16)
+    for t in range(1, T + 1):
+        for mu in range(micro):
+            g = orc.gen_grads_unit(seed, t * 100 + (0 if same else mu), 1e-3, 1, u, N)
+            if mu < micro - 1:
+                orc.zero2_accumulate(g, acc, first=mu == 0)
+            else:
+                orc.zero2_step_accumulated(g, acc if micro > 1 else None, micro, w, m, v, p,
+                                           orc.hparams(**HP, step=t))
+    return p, w, m, v
+
+
+@pytest.mark.parametrize("micro", [2, 4, 8])
+def test_accumulating_identical_micro_batches_is_the_plain_step(orc, micro):
+    """m equal micro-batch gradients x: the running fp32 sums x, 2x, 3x, 4x are exact up
+    to 4x (3x rounds, but 3x + x rounds back to 4x), and the 1/m scaling is exact, so
+    for m = 2 and 4 the step equals the plain one bit for bit; for m = 8 the sums 5x..7x
+    round and the step agrees within fp32 rounding."""
+    N, P, T, seed = 4, 3000, 4, 2
+    a = _acc_run(orc, N, P, micro, seed, T, same=True)
+    (u,), _ = orc.layout([P], N)
+    w = orc.gen_master(seed, 0.02, [u], N)
+    m, v = np.zeros_like(w), np.zeros_like(w)
+    p = np.zeros(u.n_padded, np.uint16)
+    for t in range(1, T + 1):
+        g = orc.gen_grads_unit(seed, t * 100, 1e-3, 1, u, N)
+        orc.zero12_step(2, g, w, m, v, p, orc.hparams(**HP, step=t))
+    if micro <= 4:
+        for x, y in zip(a, (p, w, m, v)):
+            np.testing.assert_array_equal(x.view(np.uint8), y.view(np.uint8))
+    else:
+        np.testing.assert_allclose(a[1], w, rtol=1e-6, atol=1e-9)
+        np.testing.assert_allclose(a[3], v, rtol=1e-5, atol=1e-20)
+
+
+def test_one_micro_batch_is_the_plain_step(orc):
+    a = _acc_run(orc, 8, 5000, 1, 3, 3)
+    (u,), _ = orc.layout([5000], 8)
+    w = orc.gen_master(3, 0.02, [u], 8)
+    m, v = np.zeros_like(w), np.zeros_like(w)
+    p = np.zeros(u.n_padded, np.uint16)
+    for t in range(1, 4):
+        orc.zero12_step(1, orc.gen_grads_unit(3, t * 100, 1e-3, 1, u, 8), w, m, v, p,
+                        orc.hparams(**HP, step=t))
+    for x, y in zip(a, (p, w, m, v)):
+        np.testing.assert_array_equal(x.view(np.uint8), y.view(np.uint8))
+
+
+def test_accumulated_gradient_is_the_large_batch_mean(orc):
+    """"The global batch grows by m": after one accumulated step the first moment is
+    (1 - b1) times the mean over all m*N micro-batch gradients, computed here
+    exactly in fp64 from the same bf16 inputs."""
+    N, P, micro, seed = 4, 2000, 3, 5
+    p, w, m, v = _acc_run(orc, N, P, micro, seed, 1)
+    (u,), _ = orc.layout([P], N)
+    allg = np.concatenate([orc.bf16_to_f32(orc.gen_grads_unit(seed, 100 + mu, 1e-3, 1, u, N))
+                           for mu in range(micro)]).astype(np.float64)
+    exact = allg.mean(axis=0)[:P]
+    scale = np.abs(allg).max(axis=0)[:P]
+    got = m.reshape(-1)[:P].astype(np.float64) / 0.1
+    assert np.all(np.abs(got - exact) <= (micro + N + 4) * 2.0**-24 * scale + 1e-30)
