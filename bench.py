@@ -276,6 +276,24 @@ def run_gpu(args):
     ms_c, _ = timed(torch, world, dev, stream, clipped_step, Kc)
     clip_bytes = (26 + 4 * N) * Pp
 
+    # ZeRO-2 with gradient accumulation over 4 micro-batches (the same gradients each
+    # micro-batch): 3 accumulate launches + the last micro-batch fused with the step
+    MICRO = 4
+    grad_acc = torch.empty_like(st.master)
+
+    def accumulated_step():
+        st.t += 1
+        for mu in range(MICRO - 1):
+            Z.zero2_accumulate(st.grads, grad_acc, first=mu == 0)
+        Z.zero2_step_accumulated(st.grads, grad_acc, MICRO, st.master, st.m, st.v, st.params,
+                                 Z.hparams(**HP, step=st.t))
+
+    for _ in range(min(W, 3)):
+        accumulated_step()
+    Ka = min(K, 100)
+    ms_a, _ = timed(torch, world, dev, stream, accumulated_step, Ka)
+    acc_bytes = (2 * N + 4) * Pp + (MICRO - 2) * (2 * N + 8) * Pp + (26 + 2 * N + 4) * Pp
+
     # end to end through the C ABI with host buffers: H2D gradients, step, D2H weights
     E = args.e2e_steps or min(K, 50)
     host_g = torch.empty((N, Pp), dtype=torch.int16, pin_memory=True)
@@ -334,6 +352,13 @@ def run_gpu(args):
             "hbm_gbs": clip_bytes * Kc / (ms_c * 1e-3) / 1e9, "bytes_per_step": clip_bytes,
             "note": "ZeRO-1 with global-norm clipping (max_norm 1.0): norm pass (2N B/param) + "
                     "coefficient + clipped fused step (26+2N B/param), 3 launches",
+        },
+        "accumulation": {
+            "micro_batches": MICRO, "ms_per_step": ms_a / Ka, "steps": Ka,
+            "hbm_gbs": acc_bytes * Ka / (ms_a * 1e-3) / 1e9, "bytes_per_step": acc_bytes,
+            "note": "ZeRO-2 with gradient accumulation: a reduce-scatter into the fp32 owner "
+                    "accumulator after each of the first m-1 micro-batches, the last one fused "
+                    "with AdamW",
         },
         "e2e": {
             "value": world * P * E / (ms_e2e * 1e-3), "unit": "params/s", "steps": E,

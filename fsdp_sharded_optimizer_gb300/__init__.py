@@ -19,7 +19,8 @@ _PUBLIC = ("ZERO_DEFAULT_ALIGN", "ZERO_EALIGN", "ZERO_ECUDA", "ZERO_EINVAL", "ZE
            "zero_state_bytes", "zero_step_stage12", "zero_stream_wait", "zero_unit_t",
            "zero3_plan", "zero3_step", "zero_op_t", "zero_regen_t", "zero_clip_scratch_bytes",
            "zero_grad_sqnorm", "zero_clip_coef", "zero_step_stage12_clip",
-           "zero3_reduce_scatter_unit_clip", "zero_clip_t", "clip_args")
+           "zero3_reduce_scatter_unit_clip", "zero_clip_t", "clip_args",
+           "zero2_accumulate", "zero2_step_accumulated", "zero_clip_coef_units_noalloc")
 
 __all__ = list(_PUBLIC)
 

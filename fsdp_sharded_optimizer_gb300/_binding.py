@@ -96,6 +96,8 @@ SIGNATURES = {
                                          _P]),
     "zero3_reduce_scatter_unit_clip": (C.c_int, [_P, _I32, _P, _P, _P, _P, _P, _P, _P, _P]),
     "zero_clip_coef_units_noalloc": (C.c_int, [_P, _I32, _I32, _P, _F64, _P, _P, _P]),
+    "zero2_accumulate": (C.c_int, [_I32, _I64, _P, _P, _I32, _P]),
+    "zero2_step_accumulated": (C.c_int, [_I32, _I64, _P, _P, _I32, _P, _P, _P, _P, _P, _P]),
     "zero3_plan": (C.c_int, [_I32, _I32, _I32, _P, _I32, _P]),
     "zero3_step": (C.c_int, [_P, _I32, _I32, _P, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                              _P]),
@@ -253,6 +255,28 @@ def zero3_reduce_scatter_unit_clip(unit, unit_grads, master, m, v, shard_bf16, h
     _check("zero3_reduce_scatter_unit_clip", lib.zero3_reduce_scatter_unit_clip(
         C.byref(unit), len(grows), g, w, mm, vv, s, C.byref(hp), _dev(norm_coef, 4, "norm_coef"),
         _stream(stream)))
+
+
+def zero2_accumulate(grads, grad_acc, first, stream=None):
+    """One earlier micro-batch of ZeRO-2 gradient accumulation: grad_acc
+    (N x S fp32, per owner) = (first ? 0 : grad_acc) + the micro-batch mean."""
+    g, grows = _rows(grads, 2, "grads")
+    a, _ = _rows(grad_acc, 4, "grad_acc")
+    _check("zero2_accumulate", lib.zero2_accumulate(len(grows), grows[0].numel(), g, a,
+                                                    1 if first else 0, _stream(stream)))
+
+
+def zero2_step_accumulated(grads, grad_acc, micro_batches, master, m, v, params_bf16, hp,
+                           stream=None):
+    """The last micro-batch fused with the ZeRO-2 step: g = (grad_acc + mean) / m."""
+    g, grows = _rows(grads, 2, "grads")
+    a, _ = _rows(grad_acc, 4, "grad_acc")
+    w, _ = _rows(master, 4, "master")
+    mm, _ = _rows(m, 4, "m")
+    vv, _ = _rows(v, 4, "v")
+    _check("zero2_step_accumulated", lib.zero2_step_accumulated(
+        len(grows), grows[0].numel(), g, a, int(micro_batches), w, mm, vv,
+        _dev(params_bf16, 2, "params_bf16"), C.byref(hp), _stream(stream)))
 
 
 ZERO_NOALLOC_MAX_UNITS = 1024

@@ -38,6 +38,7 @@ struct Tables {
     float4* m[ZERO_MAX_RANKS];
     float4* v[ZERO_MAX_RANKS];
     uint4* o[ZERO_MAX_RANKS];
+    float4* a[ZERO_MAX_RANKS]; // ZeRO-2 accumulation: rank k's fp32 gradient accumulator
 };
 
 // The vectors [q0, q1) this launch covers (a vector = 8 elements), the shard
@@ -47,6 +48,7 @@ struct Range {
     int64_t shard_vec;
     int64_t step_k, step_j;
     int32_t n_ranks;
+    float inv_m; // ZeRO-2 accumulation: 1/micro-batches
 };
 
 __device__ __forceinline__ void adamw(float g, float& w, float& m, float& v,
@@ -66,7 +68,9 @@ __device__ __forceinline__ void adamw(float g, float& w, float& m, float& v,
 
 // kClip: the mean gradient is multiplied by clip[1], the coefficient of the
 // global-norm clipping computed on the device by zero_clip_coef.
-template <bool kClip>
+// kAcc: the last micro-batch of ZeRO-2 gradient accumulation; the gradient is
+// (a[k] + this micro-batch's mean) * (1/m), a[k] holding the earlier ones.
+template <bool kClip, bool kAcc>
 __global__ void __launch_bounds__(kBlock, kMinBlocksPerSM)
 fused_step_kernel(const __grid_constant__ Tables T, const StepScalars s, const Range R,
                   const float* __restrict__ clip)
@@ -90,6 +94,12 @@ fused_step_kernel(const __grid_constant__ Tables T, const StepScalars s, const R
         // reduce-scatter: fp32 sum from +0 over ranks 0..N-1, in order
         float acc[8];
         dev::sum_ranks<kRankBatch>(T.g, N, q, acc);
+        float prior[8];
+        if (kAcc) {
+            const float4 a0 = dev::ld_stream(T.a[k] + 2 * j), a1 = dev::ld_stream(T.a[k] + 2 * j + 1);
+            prior[0] = a0.x; prior[1] = a0.y; prior[2] = a0.z; prior[3] = a0.w;
+            prior[4] = a1.x; prior[5] = a1.y; prior[6] = a1.z; prior[7] = a1.w;
+        }
 
         float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
         float m[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
@@ -97,6 +107,7 @@ fused_step_kernel(const __grid_constant__ Tables T, const StepScalars s, const R
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             float g = __fmul_rn(acc[e], s.inv_n);
+            if (kAcc) g = __fmul_rn(__fadd_rn(prior[e], g), R.inv_m);
             if (kClip) g = __fmul_rn(g, coef);
             adamw(g, w[e], m[e], v[e], s);
         }
@@ -121,23 +132,74 @@ fused_step_kernel(const __grid_constant__ Tables T, const StepScalars s, const R
     }
 }
 
+// ZeRO-2 accumulation of micro-batches 1..m-1: a[k] = (first ? +0 : a[k]) + mean.
+template <bool kFirst>
+__global__ void __launch_bounds__(kBlock, kMinBlocksPerSM)
+accumulate_kernel(const __grid_constant__ Tables T, const float inv_n, const Range R)
+{
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kBlock;
+    int64_t q = R.q0 + static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x;
+    if (q >= R.q1) return;
+    int64_t k = q / R.shard_vec;
+    int64_t j = q - k * R.shard_vec;
+    for (; q < R.q1; q += stride) {
+        float acc[8];
+        dev::sum_ranks<kRankBatch>(T.g, R.n_ranks, q, acc);
+        float4* ap = T.a[k] + 2 * j;
+        float prior[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (!kFirst) {
+            const float4 a0 = dev::ld_stream(ap), a1 = dev::ld_stream(ap + 1);
+            prior[0] = a0.x; prior[1] = a0.y; prior[2] = a0.z; prior[3] = a0.w;
+            prior[4] = a1.x; prior[5] = a1.y; prior[6] = a1.z; prior[7] = a1.w;
+        }
+        float out[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) out[e] = __fadd_rn(prior[e], __fmul_rn(acc[e], inv_n));
+        dev::st_stream(ap, make_float4(out[0], out[1], out[2], out[3]));
+        dev::st_stream(ap + 1, make_float4(out[4], out[5], out[6], out[7]));
+        k += R.step_k;
+        j += R.step_j;
+        if (j >= R.shard_vec) {
+            j -= R.shard_vec;
+            ++k;
+        }
+    }
+}
+
+Range make_range(const void* kernel, int64_t q0, int64_t q1, int64_t shard_vec, int32_t n_ranks,
+                 int* blocks_out)
+{
+    const int max_blocks = persistent_blocks(kernel, kBlock, 0);
+    const int64_t need = (q1 - q0 + kBlock - 1) / kBlock;
+    const int blocks = max_blocks <= 0 ? 0 : static_cast<int>(need < max_blocks ? need : max_blocks);
+    const int64_t stride = static_cast<int64_t>(blocks > 0 ? blocks : 1) * kBlock;
+    const StrideSplit sp = split_stride(stride, shard_vec);
+    *blocks_out = blocks;
+    return Range{q0, q1, shard_vec, sp.k, sp.j, n_ranks, 1.0f};
+}
+
 int launch(const Tables& T, const StepScalars& s, int64_t q0, int64_t q1, int64_t shard_vec,
-           int32_t n_ranks, const float* clip, cudaStream_t stream)
+           int32_t n_ranks, const float* clip, cudaStream_t stream, float inv_m = 0.0f)
 {
     if (q1 <= q0) return ZERO_OK;
-    const void* kernel = clip ? reinterpret_cast<const void*>(fused_step_kernel<true>)
-                              : reinterpret_cast<const void*>(fused_step_kernel<false>);
-    const int max_blocks = persistent_blocks(kernel, kBlock, 0);
-    if (max_blocks <= 0) return ZERO_ECUDA;
-    const int64_t need = (q1 - q0 + kBlock - 1) / kBlock;
-    const int blocks = static_cast<int>(need < max_blocks ? need : max_blocks);
-    const int64_t stride = static_cast<int64_t>(blocks) * kBlock;
-    const StrideSplit sp = split_stride(stride, shard_vec);
-    const Range R{q0, q1, shard_vec, sp.k, sp.j, n_ranks};
-    if (clip)
-        fused_step_kernel<true><<<blocks, kBlock, 0, stream>>>(T, s, R, clip);
+    const bool acc = inv_m != 0.0f;
+    const void* kernel =
+        clip ? (acc ? reinterpret_cast<const void*>(fused_step_kernel<true, true>)
+                    : reinterpret_cast<const void*>(fused_step_kernel<true, false>))
+             : (acc ? reinterpret_cast<const void*>(fused_step_kernel<false, true>)
+                    : reinterpret_cast<const void*>(fused_step_kernel<false, false>));
+    int blocks = 0;
+    Range R = make_range(kernel, q0, q1, shard_vec, n_ranks, &blocks);
+    if (blocks <= 0) return ZERO_ECUDA;
+    R.inv_m = acc ? inv_m : 1.0f;
+    if (clip && acc)
+        fused_step_kernel<true, true><<<blocks, kBlock, 0, stream>>>(T, s, R, clip);
+    else if (clip)
+        fused_step_kernel<true, false><<<blocks, kBlock, 0, stream>>>(T, s, R, clip);
+    else if (acc)
+        fused_step_kernel<false, true><<<blocks, kBlock, 0, stream>>>(T, s, R, nullptr);
     else
-        fused_step_kernel<false><<<blocks, kBlock, 0, stream>>>(T, s, R, nullptr);
+        fused_step_kernel<false, false><<<blocks, kBlock, 0, stream>>>(T, s, R, nullptr);
     return cuda_status(cudaGetLastError());
 }
 
@@ -264,4 +326,64 @@ extern "C" int zero3_reduce_scatter_unit_clip(const zero_unit_t* unit, int32_t n
     const int rc = check_clip(norm_coef);
     if (rc != ZERO_OK) return rc;
     return rs_unit(unit, n_ranks, unit_grads, master, m, v, shard_bf16, hp, norm_coef, stream);
+}
+
+extern "C" int zero2_accumulate(int32_t n_ranks, int64_t n_padded, const uint16_t* const* grads,
+                                float* const* grad_acc, int32_t first, cudaStream_t stream)
+{
+    if (n_ranks < 1 || n_ranks > ZERO_MAX_RANKS || n_padded <= 0 ||
+        n_padded % (8 * static_cast<int64_t>(n_ranks)) != 0)
+        return ZERO_EINVAL;
+    int rc;
+    if ((rc = check_table(grads, n_ranks)) != ZERO_OK) return rc;
+    if ((rc = check_table(grad_acc, n_ranks)) != ZERO_OK) return rc;
+    Tables T = {};
+    for (int32_t r = 0; r < n_ranks; ++r) {
+        T.g[r] = reinterpret_cast<const uint4*>(grads[r]);
+        T.a[r] = reinterpret_cast<float4*>(grad_acc[r]);
+    }
+    const int64_t S = n_padded / n_ranks;
+    const void* kernel = first ? reinterpret_cast<const void*>(accumulate_kernel<true>)
+                               : reinterpret_cast<const void*>(accumulate_kernel<false>);
+    int blocks = 0;
+    const Range R = make_range(kernel, 0, n_padded / 8, S / 8, n_ranks, &blocks);
+    if (blocks <= 0) return ZERO_ECUDA;
+    const float inv_n = static_cast<float>(1.0 / static_cast<double>(n_ranks));
+    if (first)
+        accumulate_kernel<true><<<blocks, kBlock, 0, stream>>>(T, inv_n, R);
+    else
+        accumulate_kernel<false><<<blocks, kBlock, 0, stream>>>(T, inv_n, R);
+    return cuda_status(cudaGetLastError());
+}
+
+extern "C" int zero2_step_accumulated(int32_t n_ranks, int64_t n_padded,
+                                      const uint16_t* const* grads, float* const* grad_acc,
+                                      int32_t micro_batches, float* const* master,
+                                      float* const* m, float* const* v, uint16_t* params_bf16,
+                                      const zero_hparams_t* hp, cudaStream_t stream)
+{
+    if (micro_batches < 1) return ZERO_EINVAL;
+    if (micro_batches == 1)  // nothing accumulated: the plain ZeRO-2 step
+        return step_stage12(2, n_ranks, n_padded, grads, master, m, v, params_bf16, hp, 0,
+                            nullptr, stream);
+    if (n_ranks < 1 || n_ranks > ZERO_MAX_RANKS || n_padded <= 0 ||
+        n_padded % (8 * static_cast<int64_t>(n_ranks)) != 0 || !valid_hparams(hp) || !params_bf16)
+        return ZERO_EINVAL;
+    int rc = check_state_tables(n_ranks, grads, master, m, v);
+    if (rc != ZERO_OK) return rc;
+    if ((rc = check_table(grad_acc, n_ranks)) != ZERO_OK) return rc;
+    if (!aligned16(params_bf16)) return ZERO_EALIGN;
+    const int64_t S = n_padded / n_ranks;
+    Tables T = {};
+    for (int32_t r = 0; r < n_ranks; ++r) {
+        T.g[r] = reinterpret_cast<const uint4*>(grads[r]);
+        T.w[r] = reinterpret_cast<float4*>(master[r]);
+        T.m[r] = reinterpret_cast<float4*>(m[r]);
+        T.v[r] = reinterpret_cast<float4*>(v[r]);
+        T.o[r] = reinterpret_cast<uint4*>(params_bf16 + r * S);
+        T.a[r] = reinterpret_cast<float4*>(grad_acc[r]);
+    }
+    const StepScalars s = make_scalars(hp, n_ranks);
+    const float inv_m = static_cast<float>(1.0 / static_cast<double>(micro_batches));
+    return launch(T, s, 0, n_padded / 8, S / 8, n_ranks, nullptr, stream, inv_m);
 }

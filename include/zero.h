@@ -177,6 +177,35 @@ int zero_state_bytes(int64_t n_params, int32_t n_ranks, int32_t stage, int32_t K
                      zero_bytes_t* out);
 
 /* ---------------------------------------------------------------------
+ * ZeRO-2 gradient accumulation.  [DZF] "Gradient accumulation": m
+ * micro-batches run one after the other and their gradients are added before
+ * one optimizer step; ZeRO-2 keeps no full gradient, so it reduce-scatters
+ * after every micro-batch (m*P + P elements per step).  Each owner k keeps an
+ * fp32 accumulator of its slice (S floats, caller memory).  Per element, with
+ * mean_mu the reduce-scatter mean of micro-batch mu:
+ *   acc = +0;  acc = acc + mean_mu  for mu = 1..m-1      (zero2_accumulate)
+ *   g = (acc + mean_m) * (float)(1/m), then AdamW and the bf16 write, as in
+ *   zero_step_stage12                               (zero2_step_accumulated)
+ * ------------------------------------------------------------------- */
+
+/* zero2_accumulate -- one earlier micro-batch: grad_acc[k] (n_ranks device
+ * pointers, S fp32 each) = (first ? +0 : grad_acc[k]) + the mean of this
+ * micro-batch's n_ranks bf16 gradients over rank k's slice.  Reads 2N bytes
+ * per parameter (+4 unless first), writes 4.  ZERO_EINVAL / ZERO_EALIGN /
+ * ZERO_ECUDA. */
+int zero2_accumulate(int32_t n_ranks, int64_t n_padded, const uint16_t* const* grads,
+                     float* const* grad_acc, int32_t first, cudaStream_t stream);
+
+/* zero2_step_accumulated -- the last micro-batch fused with the step: the
+ * fused kernel of zero_step_stage12 with g = (grad_acc + mean) * (1/m).
+ * micro_batches = m >= 1; with m = 1 it is zero_step_stage12 (stage 2) and
+ * grad_acc is not read.  Other arguments as zero_step_stage12. */
+int zero2_step_accumulated(int32_t n_ranks, int64_t n_padded, const uint16_t* const* grads,
+                           float* const* grad_acc, int32_t micro_batches, float* const* master,
+                           float* const* m, float* const* v, uint16_t* params_bf16,
+                           const zero_hparams_t* hp, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------
  * Global gradient-norm clipping across the shards.  [DZF] "7. Common
  * mistakes" (local gradient clipping: with sharded gradients the global norm
  * needs an all-reduce of the squared shard norms); the rule of the

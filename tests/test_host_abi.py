@@ -236,3 +236,21 @@ def test_clip_calls_reject_before_launch(B):
     (u,), _ = B.zero_layout([1000], 4)
     k = B.lib.zero3_reduce_scatter_unit_clip
     assert k(C.byref(u), 4, t, w, w, w, t, C.byref(hp), None, None) == B.ZERO_EINVAL
+
+
+@host_only
+def test_accumulation_calls_reject_before_launch(B):
+    t = _table(A16[:4])
+    hp = B.hparams()
+    p = C.c_void_p(0xB00000)
+    f = B.lib.zero2_accumulate
+    assert f(0, 1024, t, t, 1, None) == B.ZERO_EINVAL
+    assert f(4, 1000, t, t, 1, None) == B.ZERO_EINVAL      # not a multiple of 8 * N
+    assert f(4, 1024, t, None, 1, None) == B.ZERO_EINVAL
+    assert f(4, 1024, t, _table(A16[:3] + [A16[3] + 4]), 1, None) == B.ZERO_EALIGN
+    g = B.lib.zero2_step_accumulated
+    assert g(4, 1024, t, t, 0, t, t, t, p, C.byref(hp), None) == B.ZERO_EINVAL   # m = 0
+    assert g(4, 1024, t, None, 2, t, t, t, p, C.byref(hp), None) == B.ZERO_EINVAL
+    assert g(4, 1024, t, t, 2, t, t, t, None, C.byref(hp), None) == B.ZERO_EINVAL
+    assert g(4, 1024, t, t, 2, t, t, t, C.c_void_p(0xB00002), C.byref(hp), None) == B.ZERO_EALIGN
+    assert g(4, 1024, t, t, 1, t, t, t, p, C.byref(B.hparams(step=0)), None) == B.ZERO_EINVAL
