@@ -418,6 +418,19 @@ def run_gpu_zero3(args, torch, Z, world, rank, dev):
     clocks = ClockSampler(None)
     ms, _ = timed(torch, world, dev, stream, native_step, K)
     clk = clocks.stop()
+    # reshard_after_forward = False: one gather per unit, full weights kept (2 B/param)
+    kept = torch.empty(total, dtype=torch.int16, device=dev)
+
+    def kept_step():
+        t[0] += 1
+        Z.zero3_step(units, grads, master, m, v, shards, kept, None, Z.hparams(**HP, step=t[0]),
+                     reshard_after_forward=False, main_stream=stream, side_stream=side)
+
+    for _ in range(min(W, 2)):
+        kept_step()
+    Kk = max(1, min(K, 20))
+    ms_k, _ = timed(torch, world, dev, stream, kept_step, Kk)
+    del kept
     # per-kernel durations: the same order issued by the Python schedule with an
     # event pair around every call, on the stream each call runs on
     be = CudaBackend(N, shards, master, m, v, device=dev, time_calls=True)
@@ -462,6 +475,10 @@ def run_gpu_zero3(args, torch, Z, world, rank, dev):
         "gather": {"ms_per_step": ga_ms / Kt, "bytes_per_step": gather_bytes,
                    "gbs": gather_bytes * Kt / (ga_ms * 1e-3) / 1e9 if ga_ms > 0 else None,
                    "note": "2 gathers per unit per step on the side stream, overlapping the fused kernel"},
+        "no_reshard": {"ms_per_step": ms_k / Kk, "steps": Kk,
+                       "hbm_gbs": (fused_bytes + 4 * total) * Kk / (ms_k * 1e-3) / 1e9,
+                       "note": "reshard_after_forward=False: one gather per unit per step, every "
+                               "unit's full bf16 weights kept from forward to backward"},
         "with_regen": {"ms_per_step": ms_r / Kr, "regen_ms_per_step (difference)": regen_ms,
                        "note": "per-unit gradients regenerated from the seed in each backward "
                                "(harness work, not the method)"},

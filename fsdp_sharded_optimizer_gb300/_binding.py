@@ -98,9 +98,11 @@ SIGNATURES = {
     "zero_clip_coef_units_noalloc": (C.c_int, [_P, _I32, _I32, _P, _F64, _P, _P, _P]),
     "zero2_accumulate": (C.c_int, [_I32, _I64, _P, _P, _I32, _P]),
     "zero2_step_accumulated": (C.c_int, [_I32, _I64, _P, _P, _I32, _P, _P, _P, _P, _P, _P]),
-    "zero3_plan": (C.c_int, [_I32, _I32, _I32, _P, _I32, _P]),
-    "zero3_step": (C.c_int, [_P, _I32, _I32, _P, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
-                             _P]),
+    "zero3_plan": (C.c_int, [_I32, _I32, _I32, _I32, _P, _I32, _P]),
+    # units, n_units, n_ranks, grads, resident, master, m, v, shards, full_a, full_b, hp,
+    # regen, clip, reshard_after_forward, main stream, side stream
+    "zero3_step": (C.c_int, [_P, _I32, _I32, _P, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I32,
+                             _P, _P]),
     "zero_gen_grads_unit": (C.c_int, [_U64, _I64, _F64, _I32, _P, _I32, _P, _P]),
     "zero_gen_master": (C.c_int, [_U64, _F64, _P, _I32, _I32, _P, _P]),
     "zero_cast_bf16": (C.c_int, [_P, _P, _I64, _P]),
@@ -296,19 +298,20 @@ def zero_clip_coef_units_noalloc(units, grads, max_norm, norm_coef, unit_norms=N
         _stream(stream)))
 
 
-def zero3_plan(n_units, regen=False, clip=False):
+def zero3_plan(n_units, regen=False, clip=False, reshard_after_forward=True):
     """The operations of one ZeRO-3 step (host only): a list of
     (kind name, stream 0=main/1=side, unit, arg)."""
     cap = 17 * n_units + 3
     ops = (zero_op_t * cap)()
     n = C.c_int32()
-    _check("zero3_plan", lib.zero3_plan(n_units, 1 if regen else 0, 1 if clip else 0, ops, cap,
-                                        C.byref(n)))
+    _check("zero3_plan", lib.zero3_plan(n_units, 1 if regen else 0, 1 if clip else 0,
+                                        1 if reshard_after_forward else 0, ops, cap, C.byref(n)))
     return [(OP_NAMES[o.kind], o.stream, o.unit, o.arg) for o in ops[:n.value]]
 
 
 def zero3_step(units, grads, master, m, v, shard_bf16, full_a, full_b, hp, grads_resident=True,
-               regen=None, clip=None, main_stream=None, side_stream=None):
+               regen=None, clip=None, reshard_after_forward=True, main_stream=None,
+               side_stream=None):
     """One whole ZeRO-3 step issued by the native scheduler.  grads: per-rank
     gradients (all units concatenated when grads_resident, else one unit-sized
     buffer per rank refilled by `regen`, a zero_regen_t)."""
@@ -320,9 +323,10 @@ def zero3_step(units, grads, master, m, v, shard_bf16, full_a, full_b, hp, grads
     arr = (zero_unit_t * len(units))(*units)
     _check("zero3_step", lib.zero3_step(
         arr, len(units), len(rows), g, 1 if grads_resident else 0, w, mm, vv, s,
-        _dev(full_a, 2, "full_a"), _dev(full_b, 2, "full_b"), C.byref(hp),
+        _dev(full_a, 2, "full_a"), _dev(full_b, 2, "full_b") if full_b is not None else None,
+        C.byref(hp),
         C.byref(regen) if regen is not None else None, C.byref(clip) if clip is not None else None,
-        _stream(main_stream), _stream(side_stream)))
+        1 if reshard_after_forward else 0, _stream(main_stream), _stream(side_stream)))
 
 
 # ------------------------------------------------------------------ harness calls

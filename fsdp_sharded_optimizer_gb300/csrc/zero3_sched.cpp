@@ -22,6 +22,7 @@ namespace {
 constexpr int kEvents = 5; // start, gathered[2], released[2]
 constexpr int kMaxDevices = 64;
 constexpr int kEvStart = 0, kEvGathered = 1, kEvReleased = 3;
+constexpr int32_t kOwnRegion = 2; // GATHER/USE arg: the unit's region of the kept full buffer
 
 struct PlanBuilder {
     std::vector<zero_op_t> ops;
@@ -60,7 +61,33 @@ struct PlanBuilder {
         }
     }
 
-    void step(int32_t n_units, bool regen, bool clip)
+    // reshard_after_forward = false: the forward pass gathers every unit into
+    // its own region of one full buffer (arg kOwnRegion) and keeps it; the
+    // backward pass uses the kept weights with no second gather.
+    void forward_keep(int32_t n_units)
+    {
+        auto gather_own = [&](int32_t u, int32_t pos) {
+            add(ZERO_OP_GATHER, 1, u, kOwnRegion);
+            add(ZERO_OP_RECORD, 1, -1, kEvGathered + pos % 2);
+        };
+        gather_own(0, 0);
+        for (int32_t pos = 0; pos < n_units; ++pos) {
+            if (pos + 1 < n_units) gather_own(pos + 1, pos + 1); // prefetch
+            add(ZERO_OP_WAIT, 0, -1, kEvGathered + pos % 2);
+            add(ZERO_OP_USE, 0, pos, kOwnRegion);
+        }
+    }
+
+    void backward_kept(int32_t n_units, bool regen, bool clip)
+    {
+        for (int32_t u = n_units - 1; u >= 0; --u) {
+            add(ZERO_OP_USE, 0, u, kOwnRegion);
+            if (regen) add(ZERO_OP_REGEN, 0, u, 0);
+            add(ZERO_OP_REDUCE_SCATTER, 0, u, clip ? 1 : 0);
+        }
+    }
+
+    void step(int32_t n_units, bool regen, bool clip, bool reshard = true)
     {
         // the step's first gather must see everything the main stream did before
         add(ZERO_OP_RECORD, 0, -1, kEvStart);
@@ -75,8 +102,13 @@ struct PlanBuilder {
             }
             add(ZERO_OP_CLIP_COEF, 0, -1, 0);
         }
-        pass(n_units, false, regen, clip);
-        pass(n_units, true, regen, clip);
+        if (reshard) {
+            pass(n_units, false, regen, clip);
+            pass(n_units, true, regen, clip);
+        } else {
+            forward_keep(n_units);
+            backward_kept(n_units, regen, clip);
+        }
     }
 };
 
@@ -114,12 +146,13 @@ bool unit_consistent(const zero_unit_t& u, int32_t n_ranks)
 
 using namespace zero;
 
-extern "C" int zero3_plan(int32_t n_units, int32_t regen, int32_t clip, zero_op_t* ops,
-                          int32_t max_ops, int32_t* n_ops)
+extern "C" int zero3_plan(int32_t n_units, int32_t regen, int32_t clip,
+                          int32_t reshard_after_forward, zero_op_t* ops, int32_t max_ops,
+                          int32_t* n_ops)
 {
     if (n_units < 1 || !ops || !n_ops || max_ops < 0) return ZERO_EINVAL;
     PlanBuilder b;
-    b.step(n_units, regen != 0, clip != 0);
+    b.step(n_units, regen != 0, clip != 0, reshard_after_forward != 0);
     if (static_cast<int64_t>(b.ops.size()) > max_ops) return ZERO_EINVAL;
     for (size_t i = 0; i < b.ops.size(); ++i) ops[i] = b.ops[i];
     *n_ops = static_cast<int32_t>(b.ops.size());
@@ -131,11 +164,12 @@ extern "C" int zero3_step(const zero_unit_t* units, int32_t n_units, int32_t n_r
                           float* const* master, float* const* m, float* const* v,
                           uint16_t* const* shard_bf16, uint16_t* full_a, uint16_t* full_b,
                           const zero_hparams_t* hp, const zero_regen_t* regen,
-                          const zero_clip_t* clip, cudaStream_t main_stream,
-                          cudaStream_t side_stream)
+                          const zero_clip_t* clip, int32_t reshard_after_forward,
+                          cudaStream_t main_stream, cudaStream_t side_stream)
 {
+    const bool reshard = reshard_after_forward != 0;
     if (!units || n_units < 1 || n_ranks < 1 || n_ranks > ZERO_MAX_RANKS || !valid_hparams(hp) ||
-        !full_a || !full_b || full_a == full_b || main_stream == side_stream ||
+        !full_a || (reshard && (!full_b || full_a == full_b)) || main_stream == side_stream ||
         (!grads_resident && !regen))
         return ZERO_EINVAL;
     for (int32_t u = 0; u < n_units; ++u)
@@ -146,7 +180,7 @@ extern "C" int zero3_step(const zero_unit_t* units, int32_t n_units, int32_t n_r
     if ((rc = check_table(m, n_ranks)) != ZERO_OK) return rc;
     if ((rc = check_table(v, n_ranks)) != ZERO_OK) return rc;
     if ((rc = check_table(shard_bf16, n_ranks)) != ZERO_OK) return rc;
-    if (!aligned16(full_a) || !aligned16(full_b)) return ZERO_EALIGN;
+    if (!aligned16(full_a) || (reshard && !aligned16(full_b))) return ZERO_EALIGN;
     if (clip) {
         if (!clip->scratch || clip->scratch_bytes < kNormScratchBytes || !clip->norm_coef ||
             !(clip->max_norm > 0) || !std::isfinite(clip->max_norm))
@@ -157,7 +191,7 @@ extern "C" int zero3_step(const zero_unit_t* units, int32_t n_units, int32_t n_r
     cudaEvent_t* ev = nullptr;
     if ((rc = events_for_current_device(&ev)) != ZERO_OK) return rc;
     PlanBuilder plan;
-    plan.step(n_units, regen != nullptr, clip != nullptr);
+    plan.step(n_units, regen != nullptr, clip != nullptr, reshard);
 
     const uint16_t* unit_grads[ZERO_MAX_RANKS];
     uint16_t* unit_grads_w[ZERO_MAX_RANKS];
@@ -179,7 +213,9 @@ extern "C" int zero3_step(const zero_unit_t* units, int32_t n_units, int32_t n_r
             break;
         case ZERO_OP_GATHER:
             rc = zero3_gather_unit(&units[op.unit], n_ranks, shard_bf16,
-                                   op.arg == 0 ? full_a : full_b, s);
+                                   op.arg == kOwnRegion ? full_a + units[op.unit].offset
+                                                        : (op.arg == 0 ? full_a : full_b),
+                                   s);
             break;
         case ZERO_OP_REGEN:
             grads_of(op.unit);

@@ -325,6 +325,10 @@ typedef struct {
  * and one reduce-scatter per unit; at most two units gathered at a time.
  *   regen      non-zero: a REGEN op precedes each REDUCE_SCATTER (and each
  *              NORM)
+ *   reshard_after_forward  0: [DZF] "How FSDP implements ZeRO-3", step 6 --
+ *              the forward pass gathers every unit once into its own region
+ *              (GATHER/USE arg = 2) and the backward pass uses the kept
+ *              weights: one gather and one reduce-scatter per unit (2P)
  *   clip       non-zero: right after the start, NORM for every unit and one
  *              CLIP_COEF on the main stream, and REDUCE_SCATTER ops carry
  *              arg = 1 (scale by the coefficient)
@@ -332,8 +336,8 @@ typedef struct {
  *              (13*n_units + 2, plus n_units with regen, plus n_units + 1
  *              with clip, plus n_units with both, at most)
  * ZERO_EINVAL on n_units < 1, null pointers or max_ops too small. */
-int zero3_plan(int32_t n_units, int32_t regen, int32_t clip, zero_op_t* ops,
-               int32_t max_ops, int32_t* n_ops);
+int zero3_plan(int32_t n_units, int32_t regen, int32_t clip, int32_t reshard_after_forward,
+               zero_op_t* ops, int32_t max_ops, int32_t* n_ops);
 
 /* Harness regeneration of a unit's gradients inside zero3_step (the
  * stand-in for the backward compute that would produce them). */
@@ -362,7 +366,11 @@ typedef struct {
  *                    (requires regen, which fills it before each unit's
  *                    reduce-scatter)
  *   master, m, v, shard_bf16   as zero3_reduce_scatter_unit
- *   full_a, full_b   two device buffers of the largest unit's n_padded bf16
+ *   full_a, full_b   reshard_after_forward != 0: two device buffers of the
+ *                    largest unit's n_padded bf16 (the double buffer);
+ *                    == 0: full_a holds every unit's full weights (the total
+ *                    padded length, unit u at units[u].offset, kept from the
+ *                    forward to the backward pass), full_b is not used
  *   hp               the step's hyper-parameters (the same t for all units)
  *   clip             NULL, or global-norm clipping over all units (the norm
  *                    pre-pass reads every unit's gradients once more)
@@ -375,8 +383,8 @@ int zero3_step(const zero_unit_t* units, int32_t n_units, int32_t n_ranks,
                float* const* master, float* const* m, float* const* v,
                uint16_t* const* shard_bf16, uint16_t* full_a, uint16_t* full_b,
                const zero_hparams_t* hp, const zero_regen_t* regen,
-               const zero_clip_t* clip, cudaStream_t main_stream,
-               cudaStream_t side_stream);
+               const zero_clip_t* clip, int32_t reshard_after_forward,
+               cudaStream_t main_stream, cudaStream_t side_stream);
 
 /* ---------------------------------------------------------------------
  * Harness calls: seeded synthetic inputs and helpers.  They are not part

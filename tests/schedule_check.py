@@ -91,3 +91,35 @@ def check_zero3_trace(trace, n_units, n_steps):
     # at most two units gathered and not yet released at any time is implied by
     # the two buffers and the overwrite check above
     return True
+
+
+def check_zero3_kept_trace(trace, n_units, n_steps):
+    """The reshard_after_forward = False schedule ("How FSDP implements ZeRO-3",
+    step 6): one gather per unit per step into the unit's own region, kept from
+    the forward to the backward pass; the backward reuses it."""
+    U = n_units
+    pos, edges = happens_before_graph(trace)
+    order_of = {id(e): i for i, e in enumerate(trace)}
+    by_issue = lambda nodes: sorted(nodes, key=lambda n: order_of[id(pos[n])])
+    gathers = by_issue([n for n, e in pos.items() if e[0] == "gather"])
+    uses = by_issue([n for n, e in pos.items() if e[0] == "use"])
+    rss = by_issue([n for n, e in pos.items() if e[0] == "rs"])
+    assert len(gathers) == U * n_steps and len(uses) == 2 * U * n_steps
+    assert len(rss) == U * n_steps
+    assert all(n[0] == "side" for n in gathers) and all(n[0] == "main" for n in uses + rss)
+    assert [pos[n][2] for n in gathers] == list(range(U)) * n_steps
+    assert [pos[n][2] for n in uses] == (list(range(U)) + list(range(U - 1, -1, -1))) * n_steps
+    for s in range(n_steps):
+        g = gathers[s * U:(s + 1) * U]
+        us = uses[s * 2 * U:(s + 1) * 2 * U]
+        r = rss[s * U:(s + 1) * U]
+        for u in range(U):
+            fwd, bwd = us[u], us[2 * U - 1 - u]
+            assert hb(edges, g[u], fwd) and hb(edges, g[u], bwd)
+            rs = r[U - 1 - u]
+            assert pos[rs][2] == u and hb(edges, bwd, rs)
+            if u + 1 < U:  # forward prefetch: unit u+1's gather issued before unit u's use
+                assert order_of[id(pos[g[u + 1]])] < order_of[id(pos[fwd])]
+            if s + 1 < n_steps:  # the next step gathers only after this step updated the shard
+                assert hb(edges, rs, gathers[(s + 1) * U + u])
+    return True

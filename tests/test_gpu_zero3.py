@@ -268,3 +268,40 @@ def test_stream_wait_times_out_then_completes():
     assert e.value.code == B.ZERO_ETIMEOUT
     B.zero_stream_wait(timeout_ms=60_000)
     assert torch.cuda.current_stream().query()
+
+
+@pytest.mark.parametrize("regen", [False, True])
+def test_native_step_without_reshard_matches_ddp(orc, regen):
+    """reshard_after_forward = False: one gather per unit per step into the unit's
+    own region of a buffer holding every unit, kept for the backward pass.  The
+    result equals DDP bit for bit, and after each step the kept buffer holds the
+    weights the step started from."""
+    N, sizes, T, seed = 4, [70_000, 333, 200_000, 64, 90_001], 4, 5
+    units, total = B.zero_layout(sizes, N)
+    master, m, v, shards, grads, _, _ = _native_buffers(units, total, N, True, seed)
+    kept = H.Guarded(1, total, torch.int16)
+    side = torch.cuda.Stream()
+    ddp = [orc.sim_ddp(N, sum(sizes), seed, H.SIGMA_W, H.SIGMA_G, 1, orc.hparams(**H.HP, step=1), t)
+           for t in range(T + 1)]
+    for t in range(1, T + 1):
+        if regen:
+            B.zero3_step(units, grads.rows, master.rows, m.rows, v.rows, shards.rows, kept.rows[0],
+                         None, H.hp(t), grads_resident=True,
+                         regen=B.zero_regen_t(seed, H.SIGMA_G, 1), reshard_after_forward=False,
+                         side_stream=side)
+        else:
+            for u in units:
+                B.zero_gen_grads_unit(seed, t, H.SIGMA_G, 1, u,
+                                      [r[u.offset:u.offset + u.n_padded] for r in grads.rows])
+            B.zero3_step(units, grads.rows, master.rows, m.rows, v.rows, shards.rows, kept.rows[0],
+                         None, H.hp(t), reshard_after_forward=False, side_stream=side)
+        torch.cuda.synchronize()
+        k = kept.numpy()[0]
+        start = np.concatenate([k[u.offset:u.offset + u.n_params] for u in units])
+        np.testing.assert_array_equal(start, ddp[t - 1][0])
+    for b_ in (master, m, v, shards, grads, kept):
+        b_.check()
+    sh = shards.numpy()
+    got = [np.concatenate([sh[k_][u.shard_offset:u.shard_offset + u.shard_len]
+                           for k_ in range(N)])[:u.n_params] for u in units]
+    H.assert_bitwise(np.concatenate(got), ddp[T][0], "params")

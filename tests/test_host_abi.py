@@ -182,29 +182,31 @@ def test_zero3_step_rejects_before_launch(B):
     fa, fb = C.c_void_p(0x900000), C.c_void_p(0xA00000)
     s1, s2 = C.c_void_p(0x1), C.c_void_p(0x2)
     call = B.lib.zero3_step
-    ok_args = (arr, 2, 4, t, 1, t, t, t, t, fa, fb, C.byref(hp), None, None, s1, s2)
+    ok_args = (arr, 2, 4, t, 1, t, t, t, t, fa, fb, C.byref(hp), None, None, 1, s1, s2)
     bad = [
-        (arr, 0, 4, t, 1, t, t, t, t, fa, fb, C.byref(hp), None, None, s1, s2),   # no units
-        (arr, 2, 3, t, 1, t, t, t, t, fa, fb, C.byref(hp), None, None, s1, s2),   # layout for 4 ranks
-        (arr, 2, 4, t, 1, t, t, t, t, fa, fa, C.byref(hp), None, None, s1, s2),   # one full buffer
-        (arr, 2, 4, t, 1, t, t, t, t, fa, fb, C.byref(hp), None, None, s1, s1),   # one stream
-        (arr, 2, 4, t, 0, t, t, t, t, fa, fb, C.byref(hp), None, None, s1, s2),   # nothing fills grads
-        (arr, 2, 4, t, 1, t, t, t, None, fa, fb, C.byref(hp), None, None, s1, s2),
-        (None, 2, 4, t, 1, t, t, t, t, fa, fb, C.byref(hp), None, None, s1, s2),
+        (arr, 0, 4, t, 1, t, t, t, t, fa, fb, C.byref(hp), None, None, 1, s1, s2),   # no units
+        (arr, 2, 3, t, 1, t, t, t, t, fa, fb, C.byref(hp), None, None, 1, s1, s2),   # layout for 4 ranks
+        (arr, 2, 4, t, 1, t, t, t, t, fa, fa, C.byref(hp), None, None, 1, s1, s2),   # one full buffer
+        (arr, 2, 4, t, 1, t, t, t, t, fa, fb, C.byref(hp), None, None, 1, s1, s1),   # one stream
+        (arr, 2, 4, t, 0, t, t, t, t, fa, fb, C.byref(hp), None, None, 1, s1, s2),   # nothing fills grads
+        (arr, 2, 4, t, 1, t, t, t, None, fa, fb, C.byref(hp), None, None, 1, s1, s2),
+        (None, 2, 4, t, 1, t, t, t, t, fa, fb, C.byref(hp), None, None, 1, s1, s2),
     ]
     for args in bad:
         assert call(*args) == B.ZERO_EINVAL
-    mis = (arr, 2, 4, t, 1, t, t, t, t, C.c_void_p(0x900002), fb, C.byref(hp), None, None, s1, s2)
+    mis = (arr, 2, 4, t, 1, t, t, t, t, C.c_void_p(0x900002), fb, C.byref(hp), None, None, 1, s1, s2)
     assert call(*mis) == B.ZERO_EALIGN
-    assert len(ok_args) == 16
+    assert len(ok_args) == 17
+    no_b = (arr, 2, 4, t, 1, t, t, t, t, fa, None, C.byref(hp), None, None, 1, s1, s2)
+    assert call(*no_b) == B.ZERO_EINVAL   # the double buffer needs full_b
 
 
 def test_zero3_plan_rejects(B):
     ops = (B.zero_op_t * 10)()
     n = C.c_int32()
-    assert B.lib.zero3_plan(0, 0, 0, ops, 10, C.byref(n)) == B.ZERO_EINVAL
-    assert B.lib.zero3_plan(3, 0, 0, ops, 10, C.byref(n)) == B.ZERO_EINVAL   # too small
-    assert B.lib.zero3_plan(3, 0, 0, None, 10, C.byref(n)) == B.ZERO_EINVAL
+    assert B.lib.zero3_plan(0, 0, 0, 1, ops, 10, C.byref(n)) == B.ZERO_EINVAL
+    assert B.lib.zero3_plan(3, 0, 0, 1, ops, 10, C.byref(n)) == B.ZERO_EINVAL   # too small
+    assert B.lib.zero3_plan(3, 0, 0, 1, None, 10, C.byref(n)) == B.ZERO_EINVAL
 
 
 @host_only

@@ -9,7 +9,7 @@ import numpy as np
 import pytest
 
 from fsdp_sharded_optimizer_gb300.zero3 import Zero3Schedule
-from schedule_check import check_zero3_trace
+from schedule_check import check_zero3_kept_trace, check_zero3_trace
 
 HP = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
 
@@ -101,12 +101,12 @@ def test_prefetch_order_and_buffer_safety(orc):
     check_zero3_trace(be.trace, len(units), 2)
 
 
-def _native_trace(n_units, n_steps, regen=False, clip=False):
+def _native_trace(n_units, n_steps, regen=False, clip=False, reshard=True):
     from fsdp_sharded_optimizer_gb300 import _binding as B
     names = {0: "main", 1: "side"}
     trace = []
     for _ in range(n_steps):
-        for kind, stream, unit, arg in B.zero3_plan(n_units, regen, clip):
+        for kind, stream, unit, arg in B.zero3_plan(n_units, regen, clip, reshard):
             st = names[stream]
             if kind in ("record", "wait"):
                 trace.append((kind, st, "ev%d" % arg))
@@ -161,3 +161,22 @@ def test_native_plan_counts_and_regen():
         if o[0] == "regen":
             assert ops[i + 1][0] == "reduce_scatter" and ops[i + 1][2] == o[2]
             assert o[1] == 0
+
+
+
+@pytest.mark.parametrize("n_units,n_steps,regen,clip", [(1, 1, False, False), (2, 2, False, False),
+                                                        (7, 3, True, True), (33, 2, False, True)])
+def test_native_kept_plan_is_safe(n_units, n_steps, regen, clip):
+    check_zero3_kept_trace(_native_trace(n_units, n_steps, regen, clip, reshard=False), n_units,
+                           n_steps)
+
+
+def test_no_reshard_saves_one_gather_per_unit(orc):
+    """"With reshard_after_forward=False ... you would see one all-gather less"
+    ("Data parallelism, ZeRO and FSDP", "5. In code", third block): two units give
+    two all-gathers and two reduce-scatters, the 2P volume of the accounting."""
+    from fsdp_sharded_optimizer_gb300 import _binding as B
+    kinds = [o[0] for o in B.zero3_plan(2, False, False, False)]
+    assert kinds.count("gather") == 2 and kinds.count("reduce_scatter") == 2
+    assert orc.comm_volume(3, 1, False, 1.0) == 2.0
+    assert all(o[3] == 2 for o in B.zero3_plan(4, False, False, False) if o[0] in ("gather", "use"))
