@@ -86,6 +86,10 @@ def lib():
                                   i64, P, P, P, P, P]),
             "or_sample": (None, [i32, u64, f64, f64, i32, P, i32, P, i64, P, P, P, P]),
             "or_grad_sumsq": (f64, [i32, i64, P]),
+            "or_reduce_mean_f32": (f32, [P, i32, i64, f32]),
+            "or_zero12_step_f32grads": (i32, [i32, i32, i64, P, P, P, P, P, P, i64]),
+            "or_zero3_reduce_scatter_unit_f32grads": (i32, [P, i32, P, P, P, P, P, P]),
+            "or_gen_grads_unit_f32": (None, [u64, i64, f64, i32, P, i32, P]),
             "or_zero2_accumulate": (i32, [i32, i64, P, P, i32]),
             "or_zero2_step_accumulated": (i32, [i32, i64, P, P, i32, P, P, P, P, P]),
             "or_comm_volume": (f64, [i32, i32, i32, f64]),
@@ -218,6 +222,31 @@ def zero3_reduce_scatter_unit_coef(unit, unit_grads, master, m, v, shards, hp, c
     _check(lib().or_zero3_reduce_scatter_unit_coef(
         C.byref(unit), unit_grads.shape[0], _rows(unit_grads), _rows(master), _rows(m),
         _rows(v), _rows(shards), C.byref(hp), float(coef)), "or_zero3_reduce_scatter_unit_coef")
+
+
+# ------------------------------------------------------------- fp32 gradients
+def reduce_mean_f32(grad_rows, i, inv_n):
+    g = np.ascontiguousarray(grad_rows, dtype=np.float32)
+    return lib().or_reduce_mean_f32(_rows(g), g.shape[0], i, inv_n)
+
+
+def zero12_step_f32grads(stage, grads, master, m, v, params, hp, bucket_elems=0):
+    N, Pp = grads.shape
+    _check(lib().or_zero12_step_f32grads(stage, N, Pp, _rows(grads), _rows(master), _rows(m),
+                                         _rows(v), _ptr(params), C.byref(hp), bucket_elems),
+           "or_zero12_step_f32grads")
+
+
+def zero3_reduce_scatter_unit_f32grads(unit, unit_grads, master, m, v, shards, hp):
+    _check(lib().or_zero3_reduce_scatter_unit_f32grads(
+        C.byref(unit), unit_grads.shape[0], _rows(unit_grads), _rows(master), _rows(m), _rows(v),
+        _rows(shards), C.byref(hp)), "or_zero3_reduce_scatter_unit_f32grads")
+
+
+def gen_grads_unit_f32(seed, step, sigma, outliers, unit, n_ranks):
+    out = np.zeros((n_ranks, unit.n_padded), dtype=np.float32)
+    lib().or_gen_grads_unit_f32(seed, step, sigma, outliers, C.byref(unit), n_ranks, _rows(out))
+    return out
 
 
 # ------------------------------------------------------------- accumulation

@@ -115,3 +115,19 @@ void or_gen_grads_unit(uint64_t seed, int64_t step, double sigma, int32_t outlie
         }
     }
 }
+
+/* The same gradients kept in fp32 (not rounded to bf16): the inputs of the
+ * fp32-gradient reduce-scatter. */
+void or_gen_grads_unit_f32(uint64_t seed, int64_t step, double sigma, int32_t outliers,
+                           const or_unit_t* unit, int32_t n_ranks, float* const* unit_grads)
+{
+    float scale = or_gen_scale(sigma);
+    for (int32_t r = 0; r < n_ranks; ++r) {
+        uint64_t key = or_gen_key(seed, 1, (uint64_t)step, (uint64_t)r);
+        for (int64_t j = 0; j < unit->n_padded; ++j)
+            unit_grads[r][j] = j < unit->n_params
+                                   ? or_gen_value(key, (uint64_t)(unit->param_offset + j), scale,
+                                                  outliers)
+                                   : 0.0f;
+    }
+}

@@ -402,6 +402,67 @@ double or_comm_volume(int32_t stage, int32_t micro_batches, int32_t reshard_afte
 }
 
 /* ======================================================================
+ * fp32-gradient reduce-scatter.  [DZF] "Proposition (tokens that hide the
+ * all-reduce)" (fp32 gradient reduction doubles the bytes) and "6. Where it
+ * shows up" (Llama 3 reduce-scattered gradients in fp32): the N_d rank
+ * gradients arrive in fp32; the mean is the same fp32 sum from +0 in rank
+ * order times (float)(1/N), and the update is unchanged.
+ * ==================================================================== */
+float or_reduce_mean_f32(const float* const* grads, int32_t n_ranks, int64_t i, float inv_n)
+{
+    float g = 0.0f;
+    for (int32_t r = 0; r < n_ranks; ++r)
+        g = g + grads[r][i];
+    return g * inv_n;
+}
+
+int or_zero12_step_f32grads(int32_t stage, int32_t n_ranks, int64_t n_padded,
+                            const float* const* grads, float* const* master, float* const* m,
+                            float* const* v, uint16_t* params_bf16, const or_hparams_t* hp,
+                            int64_t bucket_elems)
+{
+    if ((stage != 1 && stage != 2) || n_ranks < 1 || n_padded <= 0 ||
+        n_padded % n_ranks != 0 || !grads || !master || !m || !v ||
+        !params_bf16 || bad_hp(hp) || bucket_elems < 0)
+        return OR_EINVAL;
+    int64_t S = n_padded / n_ranks;
+    or_scalars_t s;
+    or_scalars(hp, n_ranks, &s);
+    int64_t bucket = (stage == 2 && bucket_elems > 0) ? bucket_elems : n_padded;
+    for (int64_t b0 = 0; b0 < n_padded; b0 += bucket) {
+        int64_t b1 = b0 + bucket < n_padded ? b0 + bucket : n_padded;
+        for (int64_t i = b0; i < b1; ++i) {
+            int64_t k = i / S, j = i - k * S;
+            float g = or_reduce_mean_f32(grads, n_ranks, i, s.inv_n);
+            or_adamw(g, &master[k][j], &m[k][j], &v[k][j], &s);
+            params_bf16[i] = or_bf16_rne(master[k][j]);
+        }
+    }
+    return OR_OK;
+}
+
+int or_zero3_reduce_scatter_unit_f32grads(const or_unit_t* unit, int32_t n_ranks,
+                                          const float* const* unit_grads, float* const* master,
+                                          float* const* m, float* const* v,
+                                          uint16_t* const* shard_bf16, const or_hparams_t* hp)
+{
+    if (!unit || n_ranks < 1 || !unit_grads || !master || !m || !v ||
+        !shard_bf16 || bad_hp(hp) || unit->shard_len * n_ranks != unit->n_padded)
+        return OR_EINVAL;
+    or_scalars_t s;
+    or_scalars(hp, n_ranks, &s);
+    int64_t S = unit->shard_len;
+    for (int64_t i = 0; i < unit->n_padded; ++i) {
+        int64_t k = i / S;
+        int64_t j = unit->shard_offset + (i - k * S);
+        float g = or_reduce_mean_f32(unit_grads, n_ranks, i, s.inv_n);
+        or_adamw(g, &master[k][j], &m[k][j], &v[k][j], &s);
+        shard_bf16[k][j] = or_bf16_rne(master[k][j]);
+    }
+    return OR_OK;
+}
+
+/* ======================================================================
  * Accounting.  [DZF] Theorem (ZeRO memory and communication), table and
  * proof steps 1-7; [DDF] "Memory accounting" (state_bytes raises on
  * params <= 0 or ranks < 1).  Bytes per parameter: bf16 weight 2, bf16

@@ -130,6 +130,19 @@ int or_zero2_step_accumulated(int32_t n_ranks, int64_t n_padded, const uint16_t*
 double or_comm_volume(int32_t stage, int32_t micro_batches, int32_t reshard_after_forward,
                       double n_params);
 
+/* ------------------------------------------------ fp32-gradient reduce-scatter */
+float or_reduce_mean_f32(const float* const* grads, int32_t n_ranks, int64_t i, float inv_n);
+int or_zero12_step_f32grads(int32_t stage, int32_t n_ranks, int64_t n_padded,
+                            const float* const* grads, float* const* master, float* const* m,
+                            float* const* v, uint16_t* params_bf16, const or_hparams_t* hp,
+                            int64_t bucket_elems);
+int or_zero3_reduce_scatter_unit_f32grads(const or_unit_t* unit, int32_t n_ranks,
+                                          const float* const* unit_grads, float* const* master,
+                                          float* const* m, float* const* v,
+                                          uint16_t* const* shard_bf16, const or_hparams_t* hp);
+void or_gen_grads_unit_f32(uint64_t seed, int64_t step, double sigma, int32_t outliers,
+                           const or_unit_t* unit, int32_t n_ranks, float* const* unit_grads);
+
 /* ------------------------------------------------------------- accounting */
 int or_state_bytes(int64_t n_params, int32_t n_ranks, int32_t stage, int32_t K,
                    or_bytes_t* out);

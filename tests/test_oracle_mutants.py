@@ -48,6 +48,8 @@ MUTANTS = [
      "float g = (a + or_reduce_mean(grads, n_ranks, i, s.inv_n)) * inv_m;",
      "float g = (a + or_reduce_mean(grads, n_ranks, i, s.inv_n));"),
     ("zero2_accum_volume_mP", "zero_oracle.c", "case 2: return m * P + P;", "case 2: return m * P;"),
+    ("f32_mean_not_scaled", "zero_oracle.c",
+     "        g = g + grads[r][i];\n    return g * inv_n;", "        g = g + grads[r][i];\n    return g;"),
     ("generator_lane_dropped", "gen_oracle.c", "(int32_t)(h >> 48) - 131070", "(int32_t)(h >> 48) * 0 - 131070"),
 ]
 

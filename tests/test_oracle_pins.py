@@ -685,3 +685,62 @@ def test_accumulated_gradient_is_the_large_batch_mean(orc):
     scale = np.abs(allg).max(axis=0)[:P]
     got = m.reshape(-1)[:P].astype(np.float64) / 0.1
     assert np.all(np.abs(got - exact) <= (micro + N + 4) * 2.0**-24 * scale + 1e-30)
+
+
+# ------------------------------------------------------------------ fp32 gradients
+def test_fp32_grads_equal_bf16_path_on_bf16_values(orc):
+    """Gradients that are bf16 values, given in fp32: the fp32-gradient step is the
+    bf16-gradient step bit for bit (the reduction only sees the values)."""
+    N, P, T = 8, 5000, 5
+    (u,), _ = orc.layout([P], N)
+    a = [orc.gen_master(4, 0.02, [u], N)]
+    a += [np.zeros_like(a[0]), np.zeros_like(a[0]), np.zeros(u.n_padded, np.uint16)]
+    b = [x.copy() for x in a]
+    for t in range(1, T + 1):
+        g = orc.gen_grads_unit(4, t, 1e-3, 1, u, N)
+        orc.zero12_step(2, g, a[0], a[1], a[2], a[3], orc.hparams(**HP, step=t), 512)
+        orc.zero12_step_f32grads(2, np.ascontiguousarray(orc.bf16_to_f32(g)), b[0], b[1], b[2],
+                                 b[3], orc.hparams(**HP, step=t), 512)
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x.view(np.uint8), y.view(np.uint8))
+
+
+def test_fp32_grads_reduce_the_worked_example(orc):
+    g = _read_kv("worked_example.txt")
+    four = np.array(g["sample_grad"], np.float32).reshape(4, 1)
+    assert orc.reduce_mean_f32(four, 0, np.float32(0.25)) == g["full_batch_mean"][0]
+
+
+def test_fp32_mean_within_rounding_of_exact(orc):
+    N, P = 16, 4000
+    (u,), _ = orc.layout([P], N)
+    g = orc.gen_grads_unit_f32(9, 1, 1e-3, 1, u, N)
+    exact = g.astype(np.float64).mean(axis=0)
+    scale = np.abs(g).astype(np.float64).sum(axis=0) / N
+    got = np.array([orc.reduce_mean_f32(g, i, np.float32(1 / N)) for i in range(0, P, 7)])
+    idx = np.arange(0, P, 7)
+    assert np.all(np.abs(got - exact[idx]) <= (N + 1) * 2.0**-24 * scale[idx] + 1e-30)
+    # the fp32 inputs are not all bf16 values (the path differs from bf16 gradients)
+    assert np.any(orc.bf16_to_f32(orc.bf16_rne(g)) != g)
+
+
+def test_fp32_zero3_unit_equals_flat(orc):
+    N, sizes, T = 4, [1000, 3000], 3
+    units, _ = orc.layout(sizes, N)
+    (u1,), _ = orc.layout([sum(sizes)], N)
+    w3 = orc.gen_master(2, 0.02, units, N)
+    m3, v3 = np.zeros_like(w3), np.zeros_like(w3)
+    s3 = orc.bf16_rne(w3)
+    w1 = orc.gen_master(2, 0.02, [u1], N)
+    m1, v1 = np.zeros_like(w1), np.zeros_like(w1)
+    p1 = np.zeros(u1.n_padded, np.uint16)
+    for t in range(1, T + 1):
+        hp = orc.hparams(**HP, step=t)
+        for u in units:
+            orc.zero3_reduce_scatter_unit_f32grads(u, orc.gen_grads_unit_f32(2, t, 1e-3, 0, u, N),
+                                                   w3, m3, v3, s3, hp)
+        orc.zero12_step_f32grads(1, orc.gen_grads_unit_f32(2, t, 1e-3, 0, u1, N), w1, m1, v1, p1, hp)
+    got = [np.concatenate([w3[k][u.shard_offset:u.shard_offset + u.shard_len]
+                           for k in range(N)])[:u.n_params] for u in units]
+    np.testing.assert_array_equal(np.concatenate(got).view(np.uint32),
+                                  w1.reshape(-1)[:sum(sizes)].view(np.uint32))
