@@ -294,6 +294,22 @@ def run_gpu(args):
     ms_a, _ = timed(torch, world, dev, stream, accumulated_step, Ka)
     acc_bytes = (2 * N + 4) * Pp + (MICRO - 2) * (2 * N + 8) * Pp + (26 + 2 * N + 4) * Pp
 
+    # fp32 rank gradients (Llama 3's fp32 reduce-scatter): 26 + 4N bytes per parameter
+    grads32 = torch.empty((N, Pp), dtype=torch.float32, device=dev)
+    Z.zero_gen_grads_unit_f32(0, 1, SIGMA_G, 0, st.unit, grads32)
+
+    def f32_step():
+        st.t += 1
+        Z.zero_step_stage12_f32grads(1, grads32, st.master, st.m, st.v, st.params,
+                                     Z.hparams(**HP, step=st.t))
+
+    for _ in range(min(W, 3)):
+        f32_step()
+    Kf = min(K, 200)
+    ms_f, _ = timed(torch, world, dev, stream, f32_step, Kf)
+    f32_bytes = (26 + 4 * N) * Pp
+    del grads32
+
     # end to end through the C ABI with host buffers: H2D gradients, step, D2H weights
     E = args.e2e_steps or min(K, 50)
     host_g = torch.empty((N, Pp), dtype=torch.int16, pin_memory=True)
@@ -359,6 +375,11 @@ def run_gpu(args):
             "note": "ZeRO-2 with gradient accumulation: a reduce-scatter into the fp32 owner "
                     "accumulator after each of the first m-1 micro-batches, the last one fused "
                     "with AdamW",
+        },
+        "f32_grads": {
+            "ms_per_step": ms_f / Kf, "value": world * P * Kf / (ms_f * 1e-3), "steps": Kf,
+            "hbm_gbs": f32_bytes * Kf / (ms_f * 1e-3) / 1e9, "bytes_per_step": f32_bytes,
+            "note": "ZeRO-1 with fp32 rank gradients (26 + 4N B/param)",
         },
         "e2e": {
             "value": world * P * E / (ms_e2e * 1e-3), "unit": "params/s", "steps": E,

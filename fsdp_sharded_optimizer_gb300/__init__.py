@@ -20,7 +20,9 @@ _PUBLIC = ("ZERO_DEFAULT_ALIGN", "ZERO_EALIGN", "ZERO_ECUDA", "ZERO_EINVAL", "ZE
            "zero3_plan", "zero3_step", "zero_op_t", "zero_regen_t", "zero_clip_scratch_bytes",
            "zero_grad_sqnorm", "zero_clip_coef", "zero_step_stage12_clip",
            "zero3_reduce_scatter_unit_clip", "zero_clip_t", "clip_args",
-           "zero2_accumulate", "zero2_step_accumulated", "zero_clip_coef_units_noalloc")
+           "zero2_accumulate", "zero2_step_accumulated", "zero_clip_coef_units_noalloc",
+           "zero_step_stage12_f32grads", "zero3_reduce_scatter_unit_f32grads",
+           "zero_gen_grads_unit_f32")
 
 __all__ = list(_PUBLIC)
 

@@ -96,6 +96,10 @@ SIGNATURES = {
                                          _P]),
     "zero3_reduce_scatter_unit_clip": (C.c_int, [_P, _I32, _P, _P, _P, _P, _P, _P, _P, _P]),
     "zero_clip_coef_units_noalloc": (C.c_int, [_P, _I32, _I32, _P, _F64, _P, _P, _P]),
+    "zero_step_stage12_f32grads": (C.c_int, [_I32, _I32, _I64, _P, _P, _P, _P, _P, _P, _I64,
+                                             _P]),
+    "zero3_reduce_scatter_unit_f32grads": (C.c_int, [_P, _I32, _P, _P, _P, _P, _P, _P, _P]),
+    "zero_gen_grads_unit_f32": (C.c_int, [_U64, _I64, _F64, _I32, _P, _I32, _P, _P]),
     "zero2_accumulate": (C.c_int, [_I32, _I64, _P, _P, _I32, _P]),
     "zero2_step_accumulated": (C.c_int, [_I32, _I64, _P, _P, _I32, _P, _P, _P, _P, _P, _P]),
     "zero3_plan": (C.c_int, [_I32, _I32, _I32, _I32, _P, _I32, _P]),
@@ -256,6 +260,36 @@ def zero3_reduce_scatter_unit_clip(unit, unit_grads, master, m, v, shard_bf16, h
     s, _ = _rows(shard_bf16, 2, "shard_bf16")
     _check("zero3_reduce_scatter_unit_clip", lib.zero3_reduce_scatter_unit_clip(
         C.byref(unit), len(grows), g, w, mm, vv, s, C.byref(hp), _dev(norm_coef, 4, "norm_coef"),
+        _stream(stream)))
+
+
+def zero_step_stage12_f32grads(stage, grads, master, m, v, params_bf16, hp, bucket_elems=0,
+                               stream=None):
+    """The fused ZeRO-1/2 step with fp32 rank gradients (N x P' fp32)."""
+    g, grows = _rows(grads, 4, "grads")
+    w, _ = _rows(master, 4, "master")
+    mm, _ = _rows(m, 4, "m")
+    vv, _ = _rows(v, 4, "v")
+    _check("zero_step_stage12_f32grads", lib.zero_step_stage12_f32grads(
+        stage, len(grows), grows[0].numel(), g, w, mm, vv, _dev(params_bf16, 2, "params_bf16"),
+        C.byref(hp), int(bucket_elems), _stream(stream)))
+
+
+def zero3_reduce_scatter_unit_f32grads(unit, unit_grads, master, m, v, shard_bf16, hp,
+                                       stream=None):
+    g, grows = _rows(unit_grads, 4, "unit_grads")
+    w, _ = _rows(master, 4, "master")
+    mm, _ = _rows(m, 4, "m")
+    vv, _ = _rows(v, 4, "v")
+    s, _ = _rows(shard_bf16, 2, "shard_bf16")
+    _check("zero3_reduce_scatter_unit_f32grads", lib.zero3_reduce_scatter_unit_f32grads(
+        C.byref(unit), len(grows), g, w, mm, vv, s, C.byref(hp), _stream(stream)))
+
+
+def zero_gen_grads_unit_f32(seed, step, sigma, outliers, unit, unit_grads, stream=None):
+    g, rows = _rows(unit_grads, 4, "unit_grads")
+    _check("zero_gen_grads_unit_f32", lib.zero_gen_grads_unit_f32(
+        int(seed), int(step), float(sigma), int(outliers), C.byref(unit), len(rows), g,
         _stream(stream)))
 
 

@@ -70,7 +70,8 @@ __device__ __forceinline__ void adamw(float g, float& w, float& m, float& v,
 // global-norm clipping computed on the device by zero_clip_coef.
 // kAcc: the last micro-batch of ZeRO-2 gradient accumulation; the gradient is
 // (a[k] + this micro-batch's mean) * (1/m), a[k] holding the earlier ones.
-template <bool kClip, bool kAcc>
+// kF32: the rank gradients are fp32 (T.g holds float4 pointers).
+template <bool kClip, bool kAcc, bool kF32 = false>
 __global__ void __launch_bounds__(kBlock, kMinBlocksPerSM)
 fused_step_kernel(const __grid_constant__ Tables T, const StepScalars s, const Range R,
                   const float* __restrict__ clip)
@@ -93,7 +94,11 @@ fused_step_kernel(const __grid_constant__ Tables T, const StepScalars s, const R
 
         // reduce-scatter: fp32 sum from +0 over ranks 0..N-1, in order
         float acc[8];
-        dev::sum_ranks<kRankBatch>(T.g, N, q, acc);
+        if (kF32)
+            dev::sum_ranks_f32<kRankBatch / 2>(reinterpret_cast<const float4* const*>(T.g), N, q,
+                                               acc);
+        else
+            dev::sum_ranks<kRankBatch>(T.g, N, q, acc);
         float prior[8];
         if (kAcc) {
             const float4 a0 = dev::ld_stream(T.a[k] + 2 * j), a1 = dev::ld_stream(T.a[k] + 2 * j + 1);
@@ -179,9 +184,18 @@ Range make_range(const void* kernel, int64_t q0, int64_t q1, int64_t shard_vec, 
 }
 
 int launch(const Tables& T, const StepScalars& s, int64_t q0, int64_t q1, int64_t shard_vec,
-           int32_t n_ranks, const float* clip, cudaStream_t stream, float inv_m = 0.0f)
+           int32_t n_ranks, const float* clip, cudaStream_t stream, float inv_m = 0.0f,
+           bool f32 = false)
 {
     if (q1 <= q0) return ZERO_OK;
+    if (f32) { // fp32 gradients: no clipping or accumulation variant
+        int blocks = 0;
+        const Range R = make_range(reinterpret_cast<const void*>(fused_step_kernel<false, false, true>),
+                                   q0, q1, shard_vec, n_ranks, &blocks);
+        if (blocks <= 0) return ZERO_ECUDA;
+        fused_step_kernel<false, false, true><<<blocks, kBlock, 0, stream>>>(T, s, R, nullptr);
+        return cuda_status(cudaGetLastError());
+    }
     const bool acc = inv_m != 0.0f;
     const void* kernel =
         clip ? (acc ? reinterpret_cast<const void*>(fused_step_kernel<true, true>)
@@ -214,16 +228,16 @@ int check_state_tables(int32_t n, const uint16_t* const* grads, float* const* ma
 }
 
 // The two entry points with an optional device clip coefficient (nullptr = none).
-int step_stage12(int32_t stage, int32_t n_ranks, int64_t n_padded, const uint16_t* const* grads,
+int step_stage12(int32_t stage, int32_t n_ranks, int64_t n_padded, const void* const* grads,
                  float* const* master, float* const* m, float* const* v, uint16_t* params_bf16,
                  const zero_hparams_t* hp, int64_t bucket_elems, const float* clip,
-                 cudaStream_t stream)
+                 cudaStream_t stream, bool f32 = false)
 {
     if ((stage != 1 && stage != 2) || n_ranks < 1 || n_ranks > ZERO_MAX_RANKS ||
         n_padded <= 0 || n_padded % (8 * static_cast<int64_t>(n_ranks)) != 0 ||
         bucket_elems < 0 || bucket_elems % 8 != 0 || !valid_hparams(hp) || !params_bf16)
         return ZERO_EINVAL;
-    int rc = check_state_tables(n_ranks, grads, master, m, v);
+    int rc = check_state_tables(n_ranks, reinterpret_cast<const uint16_t* const*>(grads), master, m, v);
     if (rc != ZERO_OK) return rc;
     if (!aligned16(params_bf16)) return ZERO_EALIGN;
 
@@ -243,21 +257,22 @@ int step_stage12(int32_t stage, int32_t n_ranks, int64_t n_padded, const uint16_
     const int64_t bucket_vec = (stage == 2 && bucket_elems > 0) ? bucket_elems / 8 : nvec;
     for (int64_t q0 = 0; q0 < nvec; q0 += bucket_vec) {
         const int64_t q1 = q0 + bucket_vec < nvec ? q0 + bucket_vec : nvec;
-        if ((rc = launch(T, s, q0, q1, shard_vec, n_ranks, clip, stream)) != ZERO_OK) return rc;
+        if ((rc = launch(T, s, q0, q1, shard_vec, n_ranks, clip, stream, 0.0f, f32)) != ZERO_OK) return rc;
     }
     return ZERO_OK;
 }
 
-int rs_unit(const zero_unit_t* unit, int32_t n_ranks, const uint16_t* const* unit_grads,
+int rs_unit(const zero_unit_t* unit, int32_t n_ranks, const void* const* unit_grads,
             float* const* master, float* const* m, float* const* v, uint16_t* const* shard_bf16,
-            const zero_hparams_t* hp, const float* clip, cudaStream_t stream)
+            const zero_hparams_t* hp, const float* clip, cudaStream_t stream, bool f32 = false)
 {
     if (!unit || n_ranks < 1 || n_ranks > ZERO_MAX_RANKS || unit->n_padded <= 0 ||
         unit->shard_len <= 0 || unit->shard_len % 8 != 0 ||
         unit->shard_len * n_ranks != unit->n_padded || unit->shard_offset < 0 ||
         unit->shard_offset % 8 != 0 || !valid_hparams(hp))
         return ZERO_EINVAL;
-    int rc = check_state_tables(n_ranks, unit_grads, master, m, v);
+    int rc = check_state_tables(n_ranks, reinterpret_cast<const uint16_t* const*>(unit_grads), master, m,
+                                v);
     if (rc != ZERO_OK) return rc;
     if ((rc = check_table(shard_bf16, n_ranks)) != ZERO_OK) return rc;
 
@@ -271,7 +286,8 @@ int rs_unit(const zero_unit_t* unit, int32_t n_ranks, const uint16_t* const* uni
         T.o[r] = reinterpret_cast<uint4*>(shard_bf16[r] + off);
     }
     const StepScalars s = make_scalars(hp, n_ranks);
-    return launch(T, s, 0, unit->n_padded / 8, unit->shard_len / 8, n_ranks, clip, stream);
+    return launch(T, s, 0, unit->n_padded / 8, unit->shard_len / 8, n_ranks, clip, stream, 0.0f,
+                  f32);
 }
 
 int check_clip(const float* norm_coef)
@@ -291,8 +307,8 @@ extern "C" int zero_step_stage12(int32_t stage, int32_t n_ranks, int64_t n_padde
                                  const zero_hparams_t* hp, int64_t bucket_elems,
                                  cudaStream_t stream)
 {
-    return step_stage12(stage, n_ranks, n_padded, grads, master, m, v, params_bf16, hp,
-                        bucket_elems, nullptr, stream);
+    return step_stage12(stage, n_ranks, n_padded, reinterpret_cast<const void* const*>(grads),
+                        master, m, v, params_bf16, hp, bucket_elems, nullptr, stream);
 }
 
 extern "C" int zero_step_stage12_clip(int32_t stage, int32_t n_ranks, int64_t n_padded,
@@ -303,8 +319,8 @@ extern "C" int zero_step_stage12_clip(int32_t stage, int32_t n_ranks, int64_t n_
 {
     const int rc = check_clip(norm_coef);
     if (rc != ZERO_OK) return rc;
-    return step_stage12(stage, n_ranks, n_padded, grads, master, m, v, params_bf16, hp,
-                        bucket_elems, norm_coef, stream);
+    return step_stage12(stage, n_ranks, n_padded, reinterpret_cast<const void* const*>(grads),
+                        master, m, v, params_bf16, hp, bucket_elems, norm_coef, stream);
 }
 
 extern "C" int zero3_reduce_scatter_unit(const zero_unit_t* unit, int32_t n_ranks,
@@ -313,7 +329,8 @@ extern "C" int zero3_reduce_scatter_unit(const zero_unit_t* unit, int32_t n_rank
                                          float* const* v, uint16_t* const* shard_bf16,
                                          const zero_hparams_t* hp, cudaStream_t stream)
 {
-    return rs_unit(unit, n_ranks, unit_grads, master, m, v, shard_bf16, hp, nullptr, stream);
+    return rs_unit(unit, n_ranks, reinterpret_cast<const void* const*>(unit_grads), master, m, v,
+                   shard_bf16, hp, nullptr, stream);
 }
 
 extern "C" int zero3_reduce_scatter_unit_clip(const zero_unit_t* unit, int32_t n_ranks,
@@ -325,7 +342,8 @@ extern "C" int zero3_reduce_scatter_unit_clip(const zero_unit_t* unit, int32_t n
 {
     const int rc = check_clip(norm_coef);
     if (rc != ZERO_OK) return rc;
-    return rs_unit(unit, n_ranks, unit_grads, master, m, v, shard_bf16, hp, norm_coef, stream);
+    return rs_unit(unit, n_ranks, reinterpret_cast<const void* const*>(unit_grads), master, m, v,
+                   shard_bf16, hp, norm_coef, stream);
 }
 
 extern "C" int zero2_accumulate(int32_t n_ranks, int64_t n_padded, const uint16_t* const* grads,
@@ -364,8 +382,8 @@ extern "C" int zero2_step_accumulated(int32_t n_ranks, int64_t n_padded,
 {
     if (micro_batches < 1) return ZERO_EINVAL;
     if (micro_batches == 1)  // nothing accumulated: the plain ZeRO-2 step
-        return step_stage12(2, n_ranks, n_padded, grads, master, m, v, params_bf16, hp, 0,
-                            nullptr, stream);
+        return step_stage12(2, n_ranks, n_padded, reinterpret_cast<const void* const*>(grads),
+                            master, m, v, params_bf16, hp, 0, nullptr, stream);
     if (n_ranks < 1 || n_ranks > ZERO_MAX_RANKS || n_padded <= 0 ||
         n_padded % (8 * static_cast<int64_t>(n_ranks)) != 0 || !valid_hparams(hp) || !params_bf16)
         return ZERO_EINVAL;
@@ -386,4 +404,24 @@ extern "C" int zero2_step_accumulated(int32_t n_ranks, int64_t n_padded,
     const StepScalars s = make_scalars(hp, n_ranks);
     const float inv_m = static_cast<float>(1.0 / static_cast<double>(micro_batches));
     return launch(T, s, 0, n_padded / 8, S / 8, n_ranks, nullptr, stream, inv_m);
+}
+
+extern "C" int zero_step_stage12_f32grads(int32_t stage, int32_t n_ranks, int64_t n_padded,
+                                          const float* const* grads, float* const* master,
+                                          float* const* m, float* const* v,
+                                          uint16_t* params_bf16, const zero_hparams_t* hp,
+                                          int64_t bucket_elems, cudaStream_t stream)
+{
+    return step_stage12(stage, n_ranks, n_padded, reinterpret_cast<const void* const*>(grads),
+                        master, m, v, params_bf16, hp, bucket_elems, nullptr, stream, true);
+}
+
+extern "C" int zero3_reduce_scatter_unit_f32grads(const zero_unit_t* unit, int32_t n_ranks,
+                                                  const float* const* unit_grads,
+                                                  float* const* master, float* const* m,
+                                                  float* const* v, uint16_t* const* shard_bf16,
+                                                  const zero_hparams_t* hp, cudaStream_t stream)
+{
+    return rs_unit(unit, n_ranks, reinterpret_cast<const void* const*>(unit_grads), master, m, v,
+                   shard_bf16, hp, nullptr, stream, true);
 }

@@ -84,6 +84,33 @@ gen_grads_kernel(const __grid_constant__ GradArgs A, int64_t n_vec, int64_t n_pa
     }
 }
 
+struct GradArgsF32 {
+    float4* dst[ZERO_MAX_RANKS];
+    uint64_t key[ZERO_MAX_RANKS];
+};
+
+// The same draws kept in fp32 (no bf16 rounding): inputs of the fp32-gradient path.
+__global__ void __launch_bounds__(kBlock)
+gen_grads_f32_kernel(const __grid_constant__ GradArgsF32 A, int64_t n_vec, int64_t n_params,
+                     int64_t param_offset, float scale, int outliers)
+{
+    const int r = blockIdx.y;
+    const uint64_t key = A.key[r];
+    for (int64_t q = static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x; q < n_vec;
+         q += static_cast<int64_t>(gridDim.x) * kBlock) {
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int64_t j = q * 8 + e;
+            x[e] = j < n_params
+                       ? draw(key, static_cast<uint64_t>(param_offset + j), scale, outliers != 0)
+                       : 0.0f;
+        }
+        dev::st_stream(A.dst[r] + 2 * q, make_float4(x[0], x[1], x[2], x[3]));
+        dev::st_stream(A.dst[r] + 2 * q + 1, make_float4(x[4], x[5], x[6], x[7]));
+    }
+}
+
 struct MasterArgs {
     float4* dst[ZERO_MAX_RANKS]; // rank k's shard storage at this unit's offset
 };
@@ -198,5 +225,26 @@ extern "C" int zero_cast_bf16(const float* src, uint16_t* dst, int64_t n, cudaSt
     cast_bf16_kernel<<<grid_x(reinterpret_cast<const void*>(cast_bf16_kernel), n_vec, 1), kBlock, 0,
                        stream>>>(reinterpret_cast<const float4*>(src), reinterpret_cast<uint4*>(dst),
                                  n_vec);
+    return cuda_status(cudaGetLastError());
+}
+
+extern "C" int zero_gen_grads_unit_f32(uint64_t seed, int64_t step, double sigma, int32_t outliers,
+                                       const zero_unit_t* unit, int32_t n_ranks,
+                                       float* const* unit_grads, cudaStream_t stream)
+{
+    if (!unit_ok(unit, n_ranks) || step < 0 || !(sigma >= 0) || !std::isfinite(sigma))
+        return ZERO_EINVAL;
+    int rc = check_table(unit_grads, n_ranks);
+    if (rc != ZERO_OK) return rc;
+    GradArgsF32 A = {};
+    for (int32_t r = 0; r < n_ranks; ++r) {
+        A.dst[r] = reinterpret_cast<float4*>(unit_grads[r]);
+        A.key[r] = stream_key(seed, 1, static_cast<uint64_t>(step), static_cast<uint64_t>(r));
+    }
+    const int64_t n_vec = unit->n_padded / 8;
+    const dim3 grid(grid_x(reinterpret_cast<const void*>(gen_grads_f32_kernel), n_vec, n_ranks),
+                    static_cast<unsigned>(n_ranks));
+    gen_grads_f32_kernel<<<grid, kBlock, 0, stream>>>(A, n_vec, unit->n_params, unit->param_offset,
+                                                      value_scale(sigma), outliers);
     return cuda_status(cudaGetLastError());
 }

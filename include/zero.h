@@ -177,6 +177,25 @@ int zero_state_bytes(int64_t n_params, int32_t n_ranks, int32_t stage, int32_t K
                      zero_bytes_t* out);
 
 /* ---------------------------------------------------------------------
+ * fp32-gradient reduce-scatter.  [DZF] "Proposition (tokens that hide the
+ * all-reduce)" (fp32 gradient reduction doubles the bytes) and "6. Where it
+ * shows up" (Llama 3 reduce-scattered its gradients in fp32).  The rank
+ * gradients are fp32 (4 bytes each, 26 + 4N bytes per parameter per step);
+ * the mean is the same rank-order fp32 sum times (float)(1/N) and the
+ * update, the bf16 write and every other argument are those of the bf16
+ * calls.
+ * ------------------------------------------------------------------- */
+int zero_step_stage12_f32grads(int32_t stage, int32_t n_ranks, int64_t n_padded,
+                               const float* const* grads, float* const* master, float* const* m,
+                               float* const* v, uint16_t* params_bf16, const zero_hparams_t* hp,
+                               int64_t bucket_elems, cudaStream_t stream);
+int zero3_reduce_scatter_unit_f32grads(const zero_unit_t* unit, int32_t n_ranks,
+                                       const float* const* unit_grads, float* const* master,
+                                       float* const* m, float* const* v,
+                                       uint16_t* const* shard_bf16, const zero_hparams_t* hp,
+                                       cudaStream_t stream);
+
+/* ---------------------------------------------------------------------
  * ZeRO-2 gradient accumulation.  [DZF] "Gradient accumulation": m
  * micro-batches run one after the other and their gradients are added before
  * one optimizer step; ZeRO-2 keeps no full gradient, so it reduce-scatters
@@ -402,6 +421,13 @@ int zero3_step(const zero_unit_t* units, int32_t n_units, int32_t n_ranks,
 int zero_gen_grads_unit(uint64_t seed, int64_t step, double sigma, int32_t outliers,
                         const zero_unit_t* unit, int32_t n_ranks,
                         uint16_t* const* unit_grads, cudaStream_t stream);
+
+/* zero_gen_grads_unit_f32 -- the same draws as zero_gen_grads_unit kept in
+ * fp32 (no bf16 rounding): inputs of the fp32-gradient calls.
+ *   unit_grads  n_ranks device pointers, each unit->n_padded fp32 (written) */
+int zero_gen_grads_unit_f32(uint64_t seed, int64_t step, double sigma, int32_t outliers,
+                            const zero_unit_t* unit, int32_t n_ranks, float* const* unit_grads,
+                            cudaStream_t stream);
 
 /* zero_gen_master -- initial fp32 master weights of every unit, written into
  * each owner's shard storage: true parameter p draws from (seed, stream 0,

@@ -1,0 +1,77 @@
+"""GPU parity of the fp32-gradient reduce-scatter (Llama 3's fp32 gradient
+reduction) against the oracle: the fp32 generator, the fused ZeRO-1/2 step and
+the ZeRO-3 unit call, element by element and bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import gpu_harness as H
+from fsdp_sharded_optimizer_gb300 import _binding as B
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("stage,N,P,bucket", [(1, 2, 2**20, 0), (2, 8, 300_001, 104),
+                                              (2, 64, 2**16 + 37, 4096), (1, 3, 65, 0),
+                                              (2, 16, 1_000_003, 8 * 12345)])
+def test_f32_grads_zero12_matches_oracle(orc, stage, N, P, bucket):
+    T, seed = 6, 8
+    (u,), _ = B.zero_layout([P], N)
+    grads = H.Guarded(N, u.n_padded, torch.float32)
+    master = H.Guarded(N, u.shard_len, torch.float32)
+    m = H.Guarded(N, u.shard_len, torch.float32).zero_()
+    v = H.Guarded(N, u.shard_len, torch.float32).zero_()
+    params = H.Guarded(1, u.n_padded, torch.int16)
+    B.zero_gen_master(seed, H.SIGMA_W, [u], master.rows)
+    (ou,), _ = orc.layout([P], N)
+    rw = orc.gen_master(seed, H.SIGMA_W, [ou], N)
+    rm, rv = np.zeros_like(rw), np.zeros_like(rw)
+    rp = np.zeros(ou.n_padded, np.uint16)
+    for t in range(1, T + 1):
+        B.zero_gen_grads_unit_f32(seed, t, H.SIGMA_G, 1, u, grads.rows)
+        B.zero_step_stage12_f32grads(stage, grads.rows, master.rows, m.rows, v.rows,
+                                     params.rows[0], H.hp(t), bucket)
+        g = orc.gen_grads_unit_f32(seed, t, H.SIGMA_G, 1, ou, N)
+        if t == 1:
+            torch.cuda.synchronize()
+            H.assert_bitwise(grads.numpy(), g, "fp32 generator")
+        orc.zero12_step_f32grads(stage, g, rw, rm, rv, rp, orc.hparams(**H.HP, step=t), bucket)
+    torch.cuda.synchronize()
+    for b_ in (grads, master, m, v, params):
+        b_.check()
+    got = (params.numpy()[0], master.numpy(), m.numpy(), v.numpy())
+    H.assert_within_tolerance(got[1:], (rw, rm, rv), got[0], rp)
+    for name, g_, r_ in zip(("params", "master", "m", "v"), got, (rp, rw, rm, rv)):
+        H.assert_bitwise(g_, r_, name)
+
+
+def test_f32_grads_zero3_unit_matches_oracle(orc):
+    N, sizes, T, seed = 4, [1000, 64, 70_001, 8], 5, 1
+    units, total = B.zero_layout(sizes, N)
+    ounits, _ = orc.layout(sizes, N)
+    shard_total = total // N
+    master = H.Guarded(N, shard_total, torch.float32)
+    m = H.Guarded(N, shard_total, torch.float32).zero_()
+    v = H.Guarded(N, shard_total, torch.float32).zero_()
+    shards = H.Guarded(N, shard_total, torch.int16)
+    B.zero_gen_master(seed, H.SIGMA_W, units, master.rows)
+    for k in range(N):
+        B.zero_cast_bf16(master.rows[k], shards.rows[k])
+    grads = H.Guarded(N, max(u.n_padded for u in units), torch.float32)
+    rw = orc.gen_master(seed, H.SIGMA_W, ounits, N)
+    rm, rv = np.zeros_like(rw), np.zeros_like(rw)
+    rs = orc.bf16_rne(rw)
+    for t in range(1, T + 1):
+        for u, ou in zip(reversed(units), reversed(ounits)):
+            gv = [r[:u.n_padded] for r in grads.rows]
+            B.zero_gen_grads_unit_f32(seed, t, H.SIGMA_G, 1, u, gv)
+            B.zero3_reduce_scatter_unit_f32grads(u, gv, master.rows, m.rows, v.rows, shards.rows,
+                                                 H.hp(t))
+            g = orc.gen_grads_unit_f32(seed, t, H.SIGMA_G, 1, ou, N)
+            orc.zero3_reduce_scatter_unit_f32grads(ou, g, rw, rm, rv, rs, orc.hparams(**H.HP, step=t))
+    torch.cuda.synchronize()
+    for b_ in (master, m, v, shards, grads):
+        b_.check()
+    for name, g_, r_ in (("shards", shards.numpy(), rs), ("master", master.numpy(), rw),
+                         ("m", m.numpy(), rm), ("v", v.numpy(), rv)):
+        H.assert_bitwise(g_, r_, name)
