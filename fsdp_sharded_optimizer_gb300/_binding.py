@@ -7,7 +7,8 @@ in the library's CUDA kernels; there is no CPU or PyTorch fallback, and
 importing this module fails loudly if the library is missing.
 
 Per-rank buffers may be given as a list of tensors (one per rank) or as the
-rows of one 2-D tensor (row k = rank k).  bf16 buffers may be ``torch.bfloat16``
+rows of one 2-D tensor (row k = rank k).  Buffers may be CUDA memory or pinned
+host memory, which the kernels read and write in place (no staging copy).  bf16 buffers may be ``torch.bfloat16``
 or ``torch.int16``/``torch.uint16`` bit patterns.
 """
 import ctypes as C
@@ -140,12 +141,18 @@ def _check(fn, rc):
         raise ZeroError(fn, rc)
 
 
+def _addressable(t):
+    """CUDA memory, or pinned host memory: the GPU reads and writes pinned host
+    memory directly (unified addressing; over NVLink-C2C on Grace-Blackwell)."""
+    return t.is_cuda or (t.device.type == "cpu" and t.is_pinned())
+
+
 def _rows(x, dtype_bytes, what):
-    """A host table of device pointers from a list of tensors or a 2-D tensor."""
+    """A host table of device-addressable pointers from a list of tensors or a 2-D tensor."""
     rows = list(x) if isinstance(x, (list, tuple)) else [x[i] for i in range(x.shape[0])]
     for t in rows:
-        if not t.is_cuda:
-            raise ValueError("%s must live on a CUDA device" % what)
+        if not _addressable(t):
+            raise ValueError("%s must be CUDA memory or pinned host memory" % what)
         if t.element_size() != dtype_bytes:
             raise ValueError("%s: expected %d-byte elements, got %s" % (what, dtype_bytes, t.dtype))
         if not t.is_contiguous():
@@ -154,8 +161,9 @@ def _rows(x, dtype_bytes, what):
 
 
 def _dev(t, dtype_bytes, what):
-    if not t.is_cuda or t.element_size() != dtype_bytes or not t.is_contiguous():
-        raise ValueError("%s must be a contiguous CUDA tensor of %d-byte elements" % (what, dtype_bytes))
+    if not _addressable(t) or t.element_size() != dtype_bytes or not t.is_contiguous():
+        raise ValueError("%s must be a contiguous CUDA or pinned host tensor of %d-byte elements"
+                         % (what, dtype_bytes))
     return C.c_void_p(t.data_ptr())
 
 

@@ -31,7 +31,10 @@
  *    them into the kernel's parameters, so the tables may be freed as soon as
  *    the call returns.
  *  - bf16 values travel as uint16_t bit patterns.  Every device pointer must
- *    be 16-byte aligned (ZERO_EALIGN otherwise).
+ *    be 16-byte aligned (ZERO_EALIGN otherwise).  A "device pointer" may also
+ *    address pinned (page-locked) host memory: the kernels then read or write
+ *    it in place over the host link, with no staging copy (unified virtual
+ *    addressing; NVLink-C2C on Grace-Blackwell).
  *  - Arguments are checked on the host before anything is launched; a bad
  *    argument launches nothing.  ZERO_ECUDA reports a launch failure.
  *  - Stateless and re-entrant (zero3_step alone keeps a per-thread cache of

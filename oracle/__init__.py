@@ -86,6 +86,7 @@ def lib():
                                   i64, P, P, P, P, P]),
             "or_sample": (None, [i32, u64, f64, f64, i32, P, i32, P, i64, P, P, P, P]),
             "or_grad_sumsq": (f64, [i32, i64, P]),
+            "or_grad_nonfinite": (None, [i32, i64, P, P]),
             "or_reduce_mean_f32": (f32, [P, i32, i64, f32]),
             "or_zero12_step_f32grads": (i32, [i32, i32, i64, P, P, P, P, P, P, i64]),
             "or_zero3_reduce_scatter_unit_f32grads": (i32, [P, i32, P, P, P, P, P, P]),
@@ -191,6 +192,14 @@ def zero3_reduce_scatter_unit(unit, unit_grads, master, m, v, shards, hp):
     _check(lib().or_zero3_reduce_scatter_unit(
         C.byref(unit), unit_grads.shape[0], _rows(unit_grads), _rows(master), _rows(m),
         _rows(v), _rows(shards), C.byref(hp)), "or_zero3_reduce_scatter_unit")
+
+
+# ------------------------------------------------------------- finite check
+def grad_nonfinite(grads):
+    g = np.ascontiguousarray(grads, dtype=np.uint16)
+    out = np.zeros(g.shape[0], np.uint32)
+    lib().or_grad_nonfinite(g.shape[0], g.shape[1], _rows(g), _ptr(out))
+    return out
 
 
 # ------------------------------------------------------------- clipping

@@ -463,6 +463,26 @@ int or_zero3_reduce_scatter_unit_f32grads(const or_unit_t* unit, int32_t n_ranks
 }
 
 /* ======================================================================
+ * Pre-reduction finite check.  [DDF] "Failure investigation and recovery":
+ * record pre-reduction per-rank finite checks so that the reduction does not
+ * conceal where a NaN came from.  counts[r] = how many of rank r's bf16
+ * gradients are infinite or NaN (all exponent bits set).
+ * ==================================================================== */
+void or_grad_nonfinite(int32_t n_ranks, int64_t n, const uint16_t* const* grads,
+                       uint32_t* counts)
+{
+    for (int32_t r = 0; r < n_ranks; ++r) {
+        uint32_t c = 0;
+        for (int64_t i = 0; i < n; ++i) {
+            float x = or_bf16_to_f32(grads[r][i]);
+            if (isnan(x) || isinf(x))
+                c += 1;
+        }
+        counts[r] = c;
+    }
+}
+
+/* ======================================================================
  * Accounting.  [DZF] Theorem (ZeRO memory and communication), table and
  * proof steps 1-7; [DDF] "Memory accounting" (state_bytes raises on
  * params <= 0 or ranks < 1).  Bytes per parameter: bf16 weight 2, bf16

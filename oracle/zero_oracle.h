@@ -143,6 +143,10 @@ int or_zero3_reduce_scatter_unit_f32grads(const or_unit_t* unit, int32_t n_ranks
 void or_gen_grads_unit_f32(uint64_t seed, int64_t step, double sigma, int32_t outliers,
                            const or_unit_t* unit, int32_t n_ranks, float* const* unit_grads);
 
+/* ------------------------------------------ pre-reduction finite check */
+void or_grad_nonfinite(int32_t n_ranks, int64_t n, const uint16_t* const* grads,
+                       uint32_t* counts);
+
 /* ------------------------------------------------------------- accounting */
 int or_state_bytes(int64_t n_params, int32_t n_ranks, int32_t stage, int32_t K,
                    or_bytes_t* out);

@@ -246,3 +246,31 @@ def test_sweep(orc, N, P):
             H.assert_bitwise(g, r, name)
     del master, m, v, params
     H.free()
+
+
+def test_host_resident_gradients_and_weights_in_place(orc):
+    """Pinned host gradients read in place and bf16 weights written straight to
+    pinned host memory give the same bits as the device-buffer path."""
+    N, P, T = 8, 300_001, 3
+    ref = H.run_zero12(1, N, P, T, seed=4, outliers=1)
+    (u,), _ = B.zero_layout([P], N)
+    master = H.Guarded(N, u.shard_len, torch.float32)
+    m = H.Guarded(N, u.shard_len, torch.float32).zero_()
+    v = H.Guarded(N, u.shard_len, torch.float32).zero_()
+    B.zero_gen_master(4, H.SIGMA_W, [u], master.rows)
+    gd = torch.empty((N, u.n_padded), dtype=torch.int16, device="cuda")
+    gh = torch.empty((N, u.n_padded), dtype=torch.int16, pin_memory=True)
+    ph = torch.zeros(u.n_padded, dtype=torch.int16, pin_memory=True)
+    for t in range(1, T + 1):
+        B.zero_gen_grads_unit(4, t, H.SIGMA_G, 1, u, gd)
+        torch.cuda.synchronize()
+        gh.copy_(gd)
+        B.zero_step_stage12(1, gh, master.rows, m.rows, v.rows, ph, H.hp(t))
+        torch.cuda.synchronize()
+    for b_ in (master, m, v):
+        b_.check()
+    H.assert_bitwise(ph.numpy().view(np.uint16), ref[0], "params")
+    H.assert_bitwise(master.numpy(), ref[1], "master")
+    H.assert_bitwise(m.numpy(), ref[2], "m")
+    with pytest.raises(ValueError):
+        B.zero_step_stage12(1, gh.clone(), master.rows, m.rows, v.rows, ph, H.hp(1))  # pageable

@@ -744,3 +744,19 @@ def test_fp32_zero3_unit_equals_flat(orc):
                            for k in range(N)])[:u.n_params] for u in units]
     np.testing.assert_array_equal(np.concatenate(got).view(np.uint32),
                                   w1.reshape(-1)[:sum(sizes)].view(np.uint32))
+
+
+# ------------------------------------------------------------------ finite check
+def test_nonfinite_counts_classify_every_bf16_pattern(orc):
+    """Every bf16 bit pattern, classified against numpy's isfinite on its fp32 value;
+    per-rank counts of planted infinities and NaNs."""
+    allb = np.arange(2**16, dtype=np.uint16).reshape(1, -1)
+    want = int((~np.isfinite(orc.bf16_to_f32(allb))).sum())
+    assert orc.grad_nonfinite(allb)[0] == want == 2 * 127 + 2  # 254 NaNs + two infinities
+    rng = np.random.default_rng(0)
+    g = orc.bf16_rne((rng.normal(size=(4, 5000)) * 1e-3).astype(np.float32))
+    planted = [0, 3, 17, 1]
+    for r, n in enumerate(planted):
+        pos = rng.choice(5000, size=n, replace=False)
+        g[r, pos] = rng.choice(np.array([0x7F80, 0xFF80, 0x7FC0, 0xFFC1], np.uint16), size=n)
+    np.testing.assert_array_equal(orc.grad_nonfinite(g), planted)
