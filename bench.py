@@ -192,6 +192,8 @@ def barrier_sync(torch, world):
 
 
 def max_over_ranks(torch, world, x, dev):
+    """The slowest rank's time: every rank reports the same value (NCCL on GPUs,
+    gloo on CPU devices)."""
     if world == 1:
         return x
     t = torch.tensor([x], dtype=torch.float64, device=dev)

@@ -97,6 +97,7 @@ SIGNATURES = {
                                          _P]),
     "zero3_reduce_scatter_unit_clip": (C.c_int, [_P, _I32, _P, _P, _P, _P, _P, _P, _P, _P]),
     "zero_clip_coef_units_noalloc": (C.c_int, [_P, _I32, _I32, _P, _F64, _P, _P, _P]),
+    "zero_grad_nonfinite": (C.c_int, [_I32, _I64, _P, _P, _I32, _P]),
     "zero_step_stage12_f32grads": (C.c_int, [_I32, _I32, _I64, _P, _P, _P, _P, _P, _P, _I64,
                                              _P]),
     "zero3_reduce_scatter_unit_f32grads": (C.c_int, [_P, _I32, _P, _P, _P, _P, _P, _P, _P]),
@@ -321,6 +322,14 @@ def zero2_step_accumulated(grads, grad_acc, micro_batches, master, m, v, params_
     _check("zero2_step_accumulated", lib.zero2_step_accumulated(
         len(grows), grows[0].numel(), g, a, int(micro_batches), w, mm, vv,
         _dev(params_bf16, 2, "params_bf16"), C.byref(hp), _stream(stream)))
+
+
+def zero_grad_nonfinite(grads, counts, reset=True, stream=None):
+    """counts (device int32/uint32[N]) (+)= per-rank number of non-finite bf16 gradients."""
+    g, rows = _rows(grads, 2, "grads")
+    _check("zero_grad_nonfinite", lib.zero_grad_nonfinite(
+        len(rows), rows[0].numel(), g, _dev(counts, 4, "counts"), 1 if reset else 0,
+        _stream(stream)))
 
 
 ZERO_NOALLOC_MAX_UNITS = 1024

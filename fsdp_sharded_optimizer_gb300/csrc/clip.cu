@@ -85,6 +85,29 @@ clip_coef_kernel(const double* __restrict__ partials, int n, double max_norm,
     }
 }
 
+// y = rank; each warp counts the rank's non-finite bf16 values (all exponent
+// bits set) in its vectors and adds its count once.  Integer counts: the
+// result does not depend on the order of the additions.
+__global__ void __launch_bounds__(kNormThreads)
+grad_nonfinite_kernel(const __grid_constant__ GradTable T, int64_t n_vec,
+                      unsigned int* __restrict__ counts)
+{
+    const int r = blockIdx.y;
+    unsigned int c = 0;
+    for (int64_t q = static_cast<int64_t>(blockIdx.x) * kNormThreads + threadIdx.x; q < n_vec;
+         q += static_cast<int64_t>(gridDim.x) * kNormThreads) {
+        const uint4 x = dev::ld_stream(T.g[r] + q);
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            c += (w[i] & 0x7F80u) == 0x7F80u;
+            c += (w[i] & 0x7F800000u) == 0x7F800000u;
+        }
+    }
+    c = __reduce_add_sync(0xFFFFFFFFu, c);
+    if ((threadIdx.x & 31) == 0 && c) atomicAdd(&counts[r], c);
+}
+
 } // namespace
 
 int grad_sqnorm(int32_t n_ranks, int64_t n_elems, const uint16_t* const* grads, int32_t accumulate,
@@ -132,4 +155,27 @@ extern "C" int zero_clip_coef(const double* scratch, int64_t scratch_bytes, doub
                               float* norm_coef, cudaStream_t stream)
 {
     return clip_coef(scratch, scratch_bytes, max_norm, norm_coef, stream);
+}
+
+extern "C" int zero_grad_nonfinite(int32_t n_ranks, int64_t n_elems, const uint16_t* const* grads,
+                                   uint32_t* counts, int32_t reset, cudaStream_t stream)
+{
+    if (n_ranks < 1 || n_ranks > ZERO_MAX_RANKS || n_elems <= 0 || n_elems % 8 != 0 || !counts)
+        return ZERO_EINVAL;
+    int rc = check_table(grads, n_ranks);
+    if (rc != ZERO_OK) return rc;
+    if (!aligned16(counts)) return ZERO_EALIGN;
+    if (reset && (rc = cuda_status(cudaMemsetAsync(counts, 0, sizeof(uint32_t) * n_ranks,
+                                                   stream))) != ZERO_OK)
+        return rc;
+    GradTable T = {};
+    for (int32_t r = 0; r < n_ranks; ++r) T.g[r] = reinterpret_cast<const uint4*>(grads[r]);
+    const int64_t n_vec = n_elems / 8;
+    int64_t gx = (kNormBlocks + n_ranks - 1) / n_ranks;
+    const int64_t need = (n_vec + kNormThreads - 1) / kNormThreads;
+    if (gx > need) gx = need;
+    const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(n_ranks));
+    grad_nonfinite_kernel<<<grid, kNormThreads, 0, stream>>>(T, n_vec,
+                                                             reinterpret_cast<unsigned int*>(counts));
+    return cuda_status(cudaGetLastError());
 }

@@ -408,6 +408,18 @@ int zero3_step(const zero_unit_t* units, int32_t n_units, int32_t n_ranks,
                const zero_clip_t* clip, int32_t reshard_after_forward,
                cudaStream_t main_stream, cudaStream_t side_stream);
 
+/* zero_grad_nonfinite -- pre-reduction finite check ([DDF] "Failure
+ * investigation and recovery": record per-rank finite checks before the
+ * reduction, so that it does not conceal where a NaN came from).  Adds to
+ * counts[r] the number of rank r's bf16 gradients that are infinite or NaN.
+ *   n_elems  length of each rank's buffer (multiple of 8)
+ *   counts   device uint32[n_ranks], 16-byte aligned; reset != 0 zeroes it
+ *            first (on the stream), otherwise counts accumulate over calls
+ * Exact integer counts, independent of order.  Reads 2N bytes per
+ * parameter.  ZERO_EINVAL / ZERO_EALIGN / ZERO_ECUDA. */
+int zero_grad_nonfinite(int32_t n_ranks, int64_t n_elems, const uint16_t* const* grads,
+                        uint32_t* counts, int32_t reset, cudaStream_t stream);
+
 /* ---------------------------------------------------------------------
  * Harness calls: seeded synthetic inputs and helpers.  They are not part
  * of the method; the benchmark and the tests use them to fill device

@@ -1,0 +1,40 @@
+"""bench.py's multi-rank timing on the CPU: with two gloo ranks every rank gets
+the slowest rank's time (the contract times the job by its slowest GPU), and the
+default single-process path returns its own time unchanged."""
+import os
+import socket
+import tempfile
+
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+
+def _port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, outdir):
+    import bench
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    got = bench.max_over_ranks(torch, world, 10.0 * (rank + 1), torch.device("cpu"))
+    with open(os.path.join(outdir, "r%d" % rank), "w") as f:
+        f.write(repr(got))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_max_over_two_gloo_ranks():
+    with tempfile.TemporaryDirectory() as d:
+        mp.start_processes(_worker, args=(2, _port(), d), nprocs=2, join=True,
+                           start_method="spawn")
+        got = [float(open(os.path.join(d, "r%d" % r)).read()) for r in range(2)]
+    assert got == [20.0, 20.0]
+
+
+def test_single_rank_time_is_unchanged():
+    import bench
+    assert bench.max_over_ranks(torch, 1, 3.5, torch.device("cpu")) == 3.5

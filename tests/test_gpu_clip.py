@@ -194,3 +194,30 @@ def test_gpt2_shaped_norm_full_size(orc):
     assert float(nc[1]) == float(coef)
     del g
     H.free()
+
+
+def test_nonfinite_counts_match_oracle(orc):
+    """Per-rank pre-reduction finite check: planted infinities and NaNs counted per
+    rank exactly like the oracle, accumulated over two units."""
+    N, sizes = 8, [2**16 + 37, 300_001]
+    units, total = B.zero_layout(sizes, N)
+    g = torch.empty((N, total), dtype=torch.int16, device="cuda")
+    for u in units:
+        B.zero_gen_grads_unit(1, 1, H.SIGMA_G, 1, u, [g[r, u.offset:u.offset + u.n_padded]
+                                                     for r in range(N)])
+    torch.cuda.synchronize()
+    host = g.cpu().numpy().view(np.uint16)
+    rng = np.random.default_rng(3)
+    specials = np.array([0x7F80, 0xFF80, 0x7FC0, 0xFFC1, 0x7F81], np.uint16)
+    for r in range(N):
+        pos = rng.choice(total, size=int(rng.integers(0, 50)), replace=False)
+        host[r, pos] = rng.choice(specials, size=pos.size)
+    g.copy_(torch.from_numpy(host.view(np.int16)))
+    counts = torch.full((N,), 12345, dtype=torch.int32, device="cuda")
+    for i, u in enumerate(units):
+        B.zero_grad_nonfinite([g[r, u.offset:u.offset + u.n_padded] for r in range(N)], counts,
+                              reset=i == 0)
+    torch.cuda.synchronize()
+    ref = sum(orc.grad_nonfinite(np.ascontiguousarray(host[:, u.offset:u.offset + u.n_padded]))
+              for u in units)
+    np.testing.assert_array_equal(counts.cpu().numpy().astype(np.uint32), ref)

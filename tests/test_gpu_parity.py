@@ -274,3 +274,29 @@ def test_host_resident_gradients_and_weights_in_place(orc):
     H.assert_bitwise(m.numpy(), ref[2], "m")
     with pytest.raises(ValueError):
         B.zero_step_stage12(1, gh.clone(), master.rows, m.rows, v.rows, ph, H.hp(1))  # pageable
+
+
+def test_resume_from_host_checkpoint_is_bitwise():
+    """Checkpoint and resume: 5 steps, master/m/v and the step counter saved to host
+    memory and the device buffers freed, state restored into fresh buffers, 5 more
+    steps -- the same bits as 10 uninterrupted steps."""
+    N, P, T = 8, 300_001, 10
+    full = H.run_zero12(2, N, P, T, seed=9, outliers=1, bucket=8 * 1001)
+    first = H.run_zero12(2, N, P, 5, seed=9, outliers=1, bucket=8 * 1001)
+    saved = {"master": first[1].copy(), "m": first[2].copy(), "v": first[3].copy(), "step": 5}
+    del first
+    H.free()
+    (u,), _ = B.zero_layout([P], N)
+    grads = H.Guarded(N, u.n_padded, torch.int16)
+    st = {k: H.Guarded(N, u.shard_len, torch.float32) for k in ("master", "m", "v")}
+    for k, g in st.items():
+        g.full[:, H.CANARY:H.CANARY + u.shard_len].copy_(torch.from_numpy(saved[k]))
+    params = H.Guarded(1, u.n_padded, torch.int16)
+    for t in range(saved["step"] + 1, T + 1):
+        B.zero_gen_grads_unit(9, t, H.SIGMA_G, 1, u, grads.rows)
+        B.zero_step_stage12(2, grads.rows, st["master"].rows, st["m"].rows, st["v"].rows,
+                            params.rows[0], H.hp(t), 8 * 1001)
+    torch.cuda.synchronize()
+    for name, g, r in (("params", params.numpy()[0], full[0]), ("master", st["master"].numpy(), full[1]),
+                       ("m", st["m"].numpy(), full[2]), ("v", st["v"].numpy(), full[3])):
+        H.assert_bitwise(g, r, name)
