@@ -76,6 +76,15 @@ __global__ void __launch_bounds__(kBlock, kMinBlocksPerSM)
 fused_step_kernel(const __grid_constant__ Tables T, const StepScalars s, const Range R,
                   const float* __restrict__ clip)
 {
+    // Bucket chaining (programmatic dependent launch): the next bucket's grid
+    // may start as soon as every block of this one is running, so its blocks
+    // fill the SMs this grid's tail leaves idle.  Buckets touch disjoint
+    // elements; the wait at the end keeps "this grid completes after its
+    // predecessor" for everything later on the stream.  Threads without work
+    // leave at once; thread 0 of block 0 always has work (q0 < q1) and waits,
+    // which is enough to hold the grid's completion.  Both instructions do
+    // nothing for a launch without the attribute.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kBlock;
     int64_t q = R.q0 + static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x;
     if (q >= R.q1) return;
@@ -135,6 +144,7 @@ fused_step_kernel(const __grid_constant__ Tables T, const StepScalars s, const R
             ++k;
         }
     }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ZeRO-2 accumulation of micro-batches 1..m-1: a[k] = (first ? +0 : a[k]) + mean.
@@ -183,9 +193,29 @@ Range make_range(const void* kernel, int64_t q0, int64_t q1, int64_t shard_vec, 
     return Range{q0, q1, shard_vec, sp.k, sp.j, n_ranks, 1.0f};
 }
 
+// One fused-step launch.  chained: launched with programmatic stream
+// serialization, so it may begin while the previous kernel on the stream (the
+// previous bucket of the same step, which touches other elements) finishes.
+template <bool kClip, bool kAcc, bool kF32>
+cudaError_t launch_fused(int blocks, cudaStream_t stream, bool chained, const Tables& T,
+                         const StepScalars& s, const Range& R, const float* clip)
+{
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(kBlock);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = chained ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, fused_step_kernel<kClip, kAcc, kF32>, T, s, R, clip);
+}
+
 int launch(const Tables& T, const StepScalars& s, int64_t q0, int64_t q1, int64_t shard_vec,
            int32_t n_ranks, const float* clip, cudaStream_t stream, float inv_m = 0.0f,
-           bool f32 = false)
+           bool f32 = false, bool chained = false)
 {
     if (q1 <= q0) return ZERO_OK;
     if (f32) { // fp32 gradients: no clipping or accumulation variant
@@ -193,8 +223,7 @@ int launch(const Tables& T, const StepScalars& s, int64_t q0, int64_t q1, int64_
         const Range R = make_range(reinterpret_cast<const void*>(fused_step_kernel<false, false, true>),
                                    q0, q1, shard_vec, n_ranks, &blocks);
         if (blocks <= 0) return ZERO_ECUDA;
-        fused_step_kernel<false, false, true><<<blocks, kBlock, 0, stream>>>(T, s, R, nullptr);
-        return cuda_status(cudaGetLastError());
+        return cuda_status(launch_fused<false, false, true>(blocks, stream, chained, T, s, R, nullptr));
     }
     const bool acc = inv_m != 0.0f;
     const void* kernel =
@@ -206,15 +235,16 @@ int launch(const Tables& T, const StepScalars& s, int64_t q0, int64_t q1, int64_
     Range R = make_range(kernel, q0, q1, shard_vec, n_ranks, &blocks);
     if (blocks <= 0) return ZERO_ECUDA;
     R.inv_m = acc ? inv_m : 1.0f;
+    cudaError_t e;
     if (clip && acc)
-        fused_step_kernel<true, true><<<blocks, kBlock, 0, stream>>>(T, s, R, clip);
+        e = launch_fused<true, true, false>(blocks, stream, chained, T, s, R, clip);
     else if (clip)
-        fused_step_kernel<true, false><<<blocks, kBlock, 0, stream>>>(T, s, R, clip);
+        e = launch_fused<true, false, false>(blocks, stream, chained, T, s, R, clip);
     else if (acc)
-        fused_step_kernel<false, true><<<blocks, kBlock, 0, stream>>>(T, s, R, nullptr);
+        e = launch_fused<false, true, false>(blocks, stream, chained, T, s, R, nullptr);
     else
-        fused_step_kernel<false, false><<<blocks, kBlock, 0, stream>>>(T, s, R, nullptr);
-    return cuda_status(cudaGetLastError());
+        e = launch_fused<false, false, false>(blocks, stream, chained, T, s, R, nullptr);
+    return cuda_status(e);
 }
 
 int check_state_tables(int32_t n, const uint16_t* const* grads, float* const* master,
@@ -255,9 +285,11 @@ int step_stage12(int32_t stage, int32_t n_ranks, int64_t n_padded, const void* c
     // ZeRO-2 reduces the gradient bucket by bucket as it becomes ready; the
     // per-element arithmetic is the same, so stage 1 and 2 give equal bits.
     const int64_t bucket_vec = (stage == 2 && bucket_elems > 0) ? bucket_elems / 8 : nvec;
+    // Buckets after the first are chained to the one before (disjoint elements).
     for (int64_t q0 = 0; q0 < nvec; q0 += bucket_vec) {
         const int64_t q1 = q0 + bucket_vec < nvec ? q0 + bucket_vec : nvec;
-        if ((rc = launch(T, s, q0, q1, shard_vec, n_ranks, clip, stream, 0.0f, f32)) != ZERO_OK) return rc;
+        if ((rc = launch(T, s, q0, q1, shard_vec, n_ranks, clip, stream, 0.0f, f32, q0 > 0)) != ZERO_OK)
+            return rc;
     }
     return ZERO_OK;
 }

@@ -129,7 +129,11 @@ int zero_layout(const int64_t* unit_sizes, int32_t n_units, int32_t n_ranks,
  *                  weights every rank holds after the all-gather
  *   bucket_elems   stage 2: reduce-scatter+update bucket by bucket, one launch
  *                  per bucket of this many elements (multiple of 8; 0 = whole
- *                  buffer); ignored for stage 1
+ *                  buffer); ignored for stage 1.  Each bucket's launch after
+ *                  the first is a programmatic dependent launch on the one
+ *                  before it (the buckets touch disjoint elements), so it may
+ *                  start while that one drains; the call as a whole is still
+ *                  ordered on the stream like one kernel.
  * Buffers must not overlap.  ZERO_EINVAL / ZERO_EALIGN / ZERO_ECUDA. */
 int zero_step_stage12(int32_t stage, int32_t n_ranks, int64_t n_padded,
                       const uint16_t* const* grads, float* const* master,

@@ -87,6 +87,37 @@ def test_zero1_equals_zero2_bitwise():
     H.free()
 
 
+def test_chained_buckets_complete_in_stream_order():
+    """Stage-2 bucket launches after the first may start while the one before
+    drains (programmatic dependent launch); the call must still be ordered on
+    its stream like one kernel.  Copies queued on the same stream right after
+    each step, with no host synchronisation in between, hold every bucket's
+    result: bit for bit the one-launch ZeRO-1 result of that step."""
+    N, P, T, bucket = 8, 3_000_017, 2, 8 * 8192
+    refs = [H.run_zero12(1, N, P, t, seed=3, outliers=1)[:4] for t in range(1, T + 1)]
+    (u,), _ = B.zero_layout([P], N)
+    assert u.n_padded // bucket >= 40  # a long chain
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    snaps = []
+    with torch.cuda.stream(side):
+        grads = torch.empty((N, u.n_padded), dtype=torch.int16, device="cuda")
+        master = torch.empty((N, u.shard_len), dtype=torch.float32, device="cuda")
+        m, v = torch.zeros_like(master), torch.zeros_like(master)
+        params = torch.empty(u.n_padded, dtype=torch.int16, device="cuda")
+        B.zero_gen_master(3, H.SIGMA_W, [u], master)
+        for t in range(1, T + 1):
+            B.zero_gen_grads_unit(3, t, H.SIGMA_G, 1, u, grads)
+            B.zero_step_stage12(2, grads, master, m, v, params, H.hp(t), bucket)
+            snaps.append((params.clone(), master.clone(), m.clone(), v.clone()))
+    side.synchronize()
+    for t, (snap, ref) in enumerate(zip(snaps, refs), 1):
+        got = [snap[0].cpu().numpy().view(np.uint16)] + [x.cpu().numpy() for x in snap[1:]]
+        for x, y, n in zip(got, ref, ("params", "master", "m", "v")):
+            H.assert_bitwise(x, y, "step %d %s" % (t, n))
+    H.free()
+
+
 def test_special_values_follow_ieee(orc):
     """Crafted gradients with infinities, NaN, huge and subnormal values: the
     GPU and the oracle agree bit for bit except NaN payloads (any NaN matches
