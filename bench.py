@@ -418,7 +418,6 @@ def run_gpu_zero3(args, torch, Z, world, rank, dev):
     once and stay resident, so the timed step runs only the library's kernels;
     the per-unit regeneration from the seed (the harness's stand-in for the
     backward compute) is timed separately."""
-    from fsdp_sharded_optimizer_gb300.zero3 import CudaBackend, Zero3Schedule
 
     unit_sizes, N, desc = WORKLOADS[args.workload]
     K, W = args.steps, args.warmup
@@ -454,6 +453,20 @@ def run_gpu_zero3(args, torch, Z, world, rank, dev):
     clocks = ClockSampler(None)
     ms, _ = timed(torch, world, dev, stream, native_step, K)
     clk = clocks.stop()
+    # the same step captured once as a CUDA graph (zero3_graph) and replayed per step
+    cap = torch.cuda.Stream(device=dev)
+    cap.wait_stream(stream)
+    graph = Z.zero3_graph_create(units, grads, master, m, v, shards, full[0], full[1],
+                                 Z.hparams(**HP, step=1), cap, side)
+
+    def graph_step():
+        t[0] += 1
+        graph.launch(Z.hparams(**HP, step=t[0]), stream=stream)
+
+    for _ in range(min(W, 3)):
+        graph_step()
+    ms_g, _ = timed(torch, world, dev, stream, graph_step, K)
+    graph.close()
     # reshard_after_forward = False: one gather per unit, full weights kept (2 B/param)
     kept = torch.empty(total, dtype=torch.int16, device=dev)
 
@@ -467,19 +480,43 @@ def run_gpu_zero3(args, torch, Z, world, rank, dev):
     Kk = max(1, min(K, 20))
     ms_k, _ = timed(torch, world, dev, stream, kept_step, Kk)
     del kept
-    # per-kernel durations: the same order issued by the Python schedule with an
-    # event pair around every call, on the stream each call runs on
-    be = CudaBackend(N, shards, master, m, v, device=dev, time_calls=True)
-    sched = Zero3Schedule(units, be, full, grads, grad_view=unit_grads)
-    Kt = max(1, min(K, 5))
+    # the dominant kernel alone: every unit's fused reduce-scatter + AdamW launched
+    # back to back on the stream (no gathers beside it); its mean launch duration
+    # over these launches is the loop's time / launches.  The C calls' arguments
+    # are built once, so the loop issues one library call per unit and the host
+    # stays ahead of the GPU even for small units.
+    import ctypes
+    from fsdp_sharded_optimizer_gb300 import _binding as ZB
+    Kt = max(1, min(K, 50))
+    tabs = [ZB._rows(x, b, n)[0] for x, b, n in ((master, 4, "master"), (m, 4, "m"), (v, 4, "v"),
+                                                 (shards, 2, "shards"))]
+    unit_tabs = [ZB._rows(unit_grads(grads, u), 2, "grads")[0] for u in units]
+    full_ptr = [ctypes.c_void_p(f.data_ptr()) for f in full]
+    hp_c = Z.hparams(**HP, step=1)
+    s_c = ZB._stream(stream)
 
-    def timed_step():
+    def rs_only():
         t[0] += 1
-        sched.step(Z.hparams(**HP, step=t[0]), lambda ui, unit, gviews, s: None)
+        hp_c.step = t[0]
+        for u, g_tab in zip(units, unit_tabs):
+            rc = ZB.lib.zero3_reduce_scatter_unit(ctypes.byref(u), N, g_tab, tabs[0], tabs[1],
+                                                  tabs[2], tabs[3], ctypes.byref(hp_c), s_c)
+            if rc != Z.ZERO_OK:
+                raise Z.ZeroError("zero3_reduce_scatter_unit", rc)
 
-    timed(torch, world, dev, be.main, timed_step, Kt)
-    rs_ms = sum(a.elapsed_time(b) for kind, _, a, b in be.timings if kind == "reduce_scatter")
-    ga_ms = sum(a.elapsed_time(b) for kind, _, a, b in be.timings if kind == "gather")
+    rs_only()
+    rs_ms, _ = timed(torch, world, dev, stream, rs_only, Kt)
+
+    # the gathers alone: each unit's two gathers (forward, backward) back to back
+    def gathers_only():
+        for i, u in enumerate(units):
+            for f in (full_ptr[i % 2], full_ptr[(i + 1) % 2]):
+                rc = ZB.lib.zero3_gather_unit(ctypes.byref(u), N, tabs[3], f, s_c)
+                if rc != Z.ZERO_OK:
+                    raise Z.ZeroError("zero3_gather_unit", rc)
+
+    gathers_only()
+    ga_ms, _ = timed(torch, world, dev, stream, gathers_only, Kt)
     # the same step with each unit's gradients regenerated from the seed in its backward
     Kr = max(1, min(K, 5))
     ms_r, _ = timed(torch, world, dev, stream,
@@ -507,10 +544,19 @@ def run_gpu_zero3(args, torch, Z, world, rank, dev):
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": peak_kind, "frac_of_8tbs_nominal": achieved / 8000.0,
                      "bytes_per_step": fused_bytes, "kernel_ms_per_step": rs_ms / Kt,
+                     "launches_per_step": len(units),
+                     "launch_ms_from": "every unit's fused launch back to back on one stream, "
+                                       "no gathers beside it: loop time / launches",
                      "traffic": ncu_traffic(args.workload)},
         "gather": {"ms_per_step": ga_ms / Kt, "bytes_per_step": gather_bytes,
                    "gbs": gather_bytes * Kt / (ga_ms * 1e-3) / 1e9 if ga_ms > 0 else None,
-                   "note": "2 gathers per unit per step on the side stream, overlapping the fused kernel"},
+                   "note": "each unit's 2 gathers back to back on one stream (in the step they "
+                           "run on the side stream, beside the fused kernels)"},
+        "graph": {"ms_per_step": ms_g / K, "steps": K,
+                  "value": world * P * K / (ms_g * 1e-3),
+                  "hbm_gbs": (fused_bytes + gather_bytes) * K / (ms_g * 1e-3) / 1e9,
+                  "note": "zero3_graph: the same step captured once as a CUDA graph, replayed "
+                          "per step with that step's AdamW scalars"},
         "no_reshard": {"ms_per_step": ms_k / Kk, "steps": Kk,
                        "hbm_gbs": (fused_bytes + 4 * total) * Kk / (ms_k * 1e-3) / 1e9,
                        "note": "reshard_after_forward=False: one gather per unit per step, every "

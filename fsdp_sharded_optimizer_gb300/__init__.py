@@ -22,7 +22,8 @@ _PUBLIC = ("ZERO_DEFAULT_ALIGN", "ZERO_EALIGN", "ZERO_ECUDA", "ZERO_EINVAL", "ZE
            "zero3_reduce_scatter_unit_clip", "zero_clip_t", "clip_args",
            "zero2_accumulate", "zero2_step_accumulated", "zero_clip_coef_units_noalloc",
            "zero_step_stage12_f32grads", "zero3_reduce_scatter_unit_f32grads",
-           "zero_gen_grads_unit_f32", "zero_grad_nonfinite")
+           "zero_gen_grads_unit_f32", "zero_grad_nonfinite", "zero3_graph_create",
+           "zero3_graph_launch", "zero3_graph_destroy", "Zero3Graph")
 
 __all__ = list(_PUBLIC)
 

@@ -79,8 +79,10 @@ class zero_clip_t(C.Structure):
 def clip_args(max_norm, scratch, norm_coef):
     """A zero_clip_t for zero3_step from device tensors (scratch of
     zero_clip_scratch_bytes(), norm_coef of 2 floats)."""
-    return zero_clip_t(float(max_norm), scratch.data_ptr(), scratch.numel() * scratch.element_size(),
-                       norm_coef.data_ptr())
+    c = zero_clip_t(float(max_norm), scratch.data_ptr(), scratch.numel() * scratch.element_size(),
+                    norm_coef.data_ptr())
+    c.tensors = (scratch, norm_coef)  # kept alive with the struct (a graph holds their addresses)
+    return c
 
 # name -> (restype, argtypes); the same names as include/zero.h
 _P, _I32, _I64, _U64, _F64 = C.c_void_p, C.c_int32, C.c_int64, C.c_uint64, C.c_double
@@ -109,6 +111,12 @@ SIGNATURES = {
     # regen, clip, reshard_after_forward, main stream, side stream
     "zero3_step": (C.c_int, [_P, _I32, _I32, _P, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I32,
                              _P, _P]),
+    # units, n_units, n_ranks, grads, master, m, v, shards, full_a, full_b, hp, clip,
+    # reshard_after_forward, capture stream, side stream, out handle
+    "zero3_graph_create": (C.c_int, [_P, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I32,
+                                     _P, _P, _P]),
+    "zero3_graph_launch": (C.c_int, [_P, _P, _P]),
+    "zero3_graph_destroy": (C.c_int, [_P]),
     "zero_gen_grads_unit": (C.c_int, [_U64, _I64, _F64, _I32, _P, _I32, _P, _P]),
     "zero_gen_master": (C.c_int, [_U64, _F64, _P, _I32, _I32, _P, _P]),
     "zero_cast_bf16": (C.c_int, [_P, _P, _I64, _P]),
@@ -378,6 +386,55 @@ def zero3_step(units, grads, master, m, v, shard_bf16, full_a, full_b, hp, grads
         C.byref(hp),
         C.byref(regen) if regen is not None else None, C.byref(clip) if clip is not None else None,
         1 if reshard_after_forward else 0, _stream(main_stream), _stream(side_stream)))
+
+
+class Zero3Graph:
+    """A handle from zero3_graph_create.  It keeps the captured tensors alive
+    (the graph holds their addresses) until zero3_graph_destroy."""
+
+    def __init__(self, handle, keep):
+        self.handle, self._keep = handle, keep
+
+    def launch(self, hp, stream=None):
+        zero3_graph_launch(self, hp, stream)
+
+    def close(self):
+        zero3_graph_destroy(self)
+
+
+def zero3_graph_create(units, grads, master, m, v, shard_bf16, full_a, full_b, hp, capture_stream,
+                       side_stream, clip=None, reshard_after_forward=True):
+    """Capture one ZeRO-3 step (zero3_step's, gradients resident) as a CUDA
+    graph; capture_stream and side_stream are two distinct torch.cuda.Streams."""
+    if capture_stream is None or side_stream is None:
+        raise ValueError("zero3_graph_create needs two explicit streams (the default stream "
+                         "cannot be captured)")
+    g, rows = _rows(grads, 2, "grads")
+    w, _ = _rows(master, 4, "master")
+    mm, _ = _rows(m, 4, "m")
+    vv, _ = _rows(v, 4, "v")
+    s, _ = _rows(shard_bf16, 2, "shard_bf16")
+    arr = (zero_unit_t * len(units))(*units)
+    h = C.c_void_p()
+    _check("zero3_graph_create", lib.zero3_graph_create(
+        arr, len(units), len(rows), g, w, mm, vv, s, _dev(full_a, 2, "full_a"),
+        _dev(full_b, 2, "full_b") if full_b is not None else None, C.byref(hp),
+        C.byref(clip) if clip is not None else None, 1 if reshard_after_forward else 0,
+        _stream(capture_stream), _stream(side_stream), C.byref(h)))
+    return Zero3Graph(h, (grads, master, m, v, shard_bf16, full_a, full_b, clip))
+
+
+def zero3_graph_launch(graph, hp, stream=None):
+    if graph.handle is None:
+        raise ValueError("zero3_graph_launch: the graph was destroyed")
+    _check("zero3_graph_launch", lib.zero3_graph_launch(graph.handle, C.byref(hp), _stream(stream)))
+
+
+def zero3_graph_destroy(graph):
+    if graph.handle is not None:
+        h, graph.handle = graph.handle, None
+        _check("zero3_graph_destroy", lib.zero3_graph_destroy(h))
+        graph._keep = None
 
 
 # ------------------------------------------------------------------ harness calls

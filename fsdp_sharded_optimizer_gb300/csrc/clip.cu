@@ -138,6 +138,15 @@ int clip_coef(const double* scratch, int64_t scratch_bytes, double max_norm, flo
     return cuda_status(cudaGetLastError());
 }
 
+int preload_clip_kernels()
+{
+    cudaFuncAttributes a;
+    if (cudaFuncGetAttributes(&a, grad_sqnorm_kernel) != cudaSuccess ||
+        cudaFuncGetAttributes(&a, clip_coef_kernel) != cudaSuccess)
+        return ZERO_ECUDA;
+    return ZERO_OK;
+}
+
 } // namespace zero
 
 using namespace zero;

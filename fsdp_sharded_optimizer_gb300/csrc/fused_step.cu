@@ -15,6 +15,9 @@
 // consecutive elements (one 16-byte bf16 vector per rank, two 16-byte fp32
 // vectors per state array) and keeps all of a batch's loads in flight before
 // it sums.  No tensor cores: this is not a contraction.
+#include <new>
+#include <vector>
+
 #include "device.cuh"
 #include "zero_internal.h"
 
@@ -193,6 +196,56 @@ Range make_range(const void* kernel, int64_t q0, int64_t q1, int64_t shard_vec, 
     return Range{q0, q1, shard_vec, sp.k, sp.j, n_ranks, 1.0f};
 }
 
+// A fused-step launch recorded while a CUDA-graph capture is running: the
+// kernel node it added and a copy of its arguments.
+struct LoggedLaunch {
+    cudaGraphNode_t node;
+    const void* func;
+    unsigned blocks;
+    Tables T;
+    StepScalars s;
+    Range R;
+    const float* clip;
+};
+
+} // namespace
+
+// The fused-step launches of one capture (zero3_graph_create), in issue order.
+struct StepNodeList {
+    std::vector<LoggedLaunch> launches;
+    bool failed = false;
+};
+
+namespace {
+
+thread_local StepNodeList* t_capture_log = nullptr;
+
+// While a capture log is installed on this thread, a fused-step launch asks
+// the capture which node it just added (the stream's only dependency right
+// after a kernel launch) and keeps it with the arguments, so the graph's step
+// scalars can be rewritten before each replay.
+void log_capture(const void* func, int blocks, const Tables& T, const StepScalars& s,
+                 const Range& R, const float* clip, cudaStream_t stream)
+{
+    StepNodeList* log = t_capture_log;
+    if (!log) return;
+    cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+    const cudaGraphNode_t* deps = nullptr;
+    size_t n_deps = 0;
+    if (cudaStreamGetCaptureInfo(stream, &st, nullptr, nullptr, &deps, nullptr, &n_deps) !=
+            cudaSuccess ||
+        st != cudaStreamCaptureStatusActive || n_deps != 1) {
+        log->failed = true;
+        return;
+    }
+    try {
+        log->launches.push_back(
+            LoggedLaunch{deps[0], func, static_cast<unsigned>(blocks), T, s, R, clip});
+    } catch (...) {
+        log->failed = true;
+    }
+}
+
 // One fused-step launch.  chained: launched with programmatic stream
 // serialization, so it may begin while the previous kernel on the stream (the
 // previous bucket of the same step, which touches other elements) finishes.
@@ -210,7 +263,12 @@ cudaError_t launch_fused(int blocks, cudaStream_t stream, bool chained, const Ta
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = chained ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, fused_step_kernel<kClip, kAcc, kF32>, T, s, R, clip);
+    const cudaError_t e =
+        cudaLaunchKernelEx(&cfg, fused_step_kernel<kClip, kAcc, kF32>, T, s, R, clip);
+    if (e == cudaSuccess)
+        log_capture(reinterpret_cast<const void*>(fused_step_kernel<kClip, kAcc, kF32>), blocks, T,
+                    s, R, clip, stream);
+    return e;
 }
 
 int launch(const Tables& T, const StepScalars& s, int64_t q0, int64_t q1, int64_t shard_vec,
@@ -329,6 +387,55 @@ int check_clip(const float* norm_coef)
 }
 
 } // namespace
+
+StepNodeList* step_nodes_begin()
+{
+    StepNodeList* log = new (std::nothrow) StepNodeList;
+    t_capture_log = log;
+    return log;
+}
+
+void step_nodes_end() { t_capture_log = nullptr; }
+
+bool step_nodes_ok(const StepNodeList* log, size_t expected)
+{
+    return log && !log->failed && log->launches.size() == expected;
+}
+
+int step_nodes_set_scalars(StepNodeList* log, cudaGraphExec_t exec, const StepScalars& s)
+{
+    for (LoggedLaunch& x : log->launches) {
+        x.s = s;
+        void* args[4] = {&x.T, &x.s, &x.R, &x.clip};
+        cudaKernelNodeParams p = {};
+        p.func = const_cast<void*>(x.func);
+        p.gridDim = dim3(x.blocks);
+        p.blockDim = dim3(kBlock);
+        p.sharedMemBytes = 0;
+        p.kernelParams = args;
+        p.extra = nullptr;
+        const int rc = cuda_status(cudaGraphExecKernelNodeSetParams(exec, x.node, &p));
+        if (rc != ZERO_OK) return rc;
+    }
+    return ZERO_OK;
+}
+
+void step_nodes_free(StepNodeList* log) { delete log; }
+
+int preload_fused_kernels()
+{
+    const void* kernels[] = {
+        reinterpret_cast<const void*>(fused_step_kernel<false, false, false>),
+        reinterpret_cast<const void*>(fused_step_kernel<true, false, false>),
+        reinterpret_cast<const void*>(fused_step_kernel<false, true, false>),
+        reinterpret_cast<const void*>(fused_step_kernel<true, true, false>),
+        reinterpret_cast<const void*>(fused_step_kernel<false, false, true>),
+    };
+    for (const void* k : kernels)
+        if (persistent_blocks(k, kBlock, 0) <= 0) return ZERO_ECUDA;
+    return ZERO_OK;
+}
+
 } // namespace zero
 
 using namespace zero;

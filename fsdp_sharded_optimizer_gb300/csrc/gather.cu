@@ -47,6 +47,14 @@ gather_kernel(const __grid_constant__ Sources S, uint4* __restrict__ dst, int64_
 }
 
 } // namespace
+
+int preload_gather_kernel()
+{
+    return persistent_blocks(reinterpret_cast<const void*>(gather_kernel), kBlock, 0) > 0
+               ? ZERO_OK
+               : ZERO_ECUDA;
+}
+
 } // namespace zero
 
 using namespace zero;

@@ -1,0 +1,118 @@
+// graph.cpp -- zero3_graph: one ZeRO-3 step of fixed buffers captured once as
+// a CUDA graph (zero3_graph_create) and replayed once per step
+// (zero3_graph_launch).
+//
+// The step is the one zero3_step issues: the forward gathers, the backward
+// gathers and per-unit reduce-scatter + AdamW ("Data parallelism, ZeRO and
+// FSDP", "How FSDP implements ZeRO-3", steps 2-5), side-stream prefetch and
+// two full-unit buffers.  Stream capture turns its event records and waits
+// into graph edges, so a replay hands the GPU the whole dependency structure
+// at once instead of one launch and one event at a time.  That matters for
+// models of many small units, whose fused launches last tens of microseconds.
+//
+// What changes from step to step is the step number t (the bias corrections)
+// and, with a schedule, lr / betas / eps / weight decay: the fp32 AdamW
+// scalars, which the fused kernel takes by value.  The capture records every
+// fused-step node it creates, and zero3_graph_launch rewrites those nodes'
+// scalars in the instantiated graph before each replay.  The gathers and the
+// clipping kernels take nothing that changes.
+#include <new>
+
+#include "zero_internal.h"
+
+struct zero3_graph {
+    int device;
+    int32_t n_ranks;
+    cudaGraph_t graph;
+    cudaGraphExec_t exec;
+    zero::StepNodeList* nodes;
+};
+
+using namespace zero;
+
+extern "C" int zero3_graph_create(const zero_unit_t* units, int32_t n_units, int32_t n_ranks,
+                                  const uint16_t* const* grads, float* const* master,
+                                  float* const* m, float* const* v,
+                                  uint16_t* const* shard_bf16, uint16_t* full_a,
+                                  uint16_t* full_b, const zero_hparams_t* hp,
+                                  const zero_clip_t* clip, int32_t reshard_after_forward,
+                                  cudaStream_t capture_stream, cudaStream_t side_stream,
+                                  zero3_graph_t** out)
+{
+    if (!out) return ZERO_EINVAL;
+    *out = nullptr;
+    // The legacy default stream cannot be captured.
+    if (!units || n_units < 1 || n_ranks < 1 || n_ranks > ZERO_MAX_RANKS || !valid_hparams(hp) ||
+        !capture_stream || capture_stream == cudaStreamLegacy || capture_stream == side_stream)
+        return ZERO_EINVAL;
+    cudaStreamCaptureStatus status = cudaStreamCaptureStatusNone;
+    int rc = cuda_status(cudaStreamIsCapturing(capture_stream, &status));
+    if (rc != ZERO_OK) return rc;
+    if (status != cudaStreamCaptureStatusNone) return ZERO_EINVAL; // no nested capture
+    int dev = 0;
+    if ((rc = cuda_status(cudaGetDevice(&dev))) != ZERO_OK) return rc;
+    if ((rc = preload_fused_kernels()) != ZERO_OK || (rc = preload_gather_kernel()) != ZERO_OK ||
+        (clip && (rc = preload_clip_kernels()) != ZERO_OK) || (rc = preload_step_events()) != ZERO_OK)
+        return rc;
+
+    StepNodeList* nodes = step_nodes_begin();
+    if (!nodes) return ZERO_ECUDA;
+    cudaError_t e = cudaStreamBeginCapture(capture_stream, cudaStreamCaptureModeThreadLocal);
+    if (e != cudaSuccess) {
+        step_nodes_end();
+        step_nodes_free(nodes);
+        return cuda_status(e);
+    }
+    // zero3_step checks every argument before it issues anything; a rejected
+    // call leaves an empty capture behind, which is discarded below.
+    rc = zero3_step(units, n_units, n_ranks, grads, 1, master, m, v, shard_bf16, full_a, full_b,
+                    hp, nullptr, clip, reshard_after_forward, capture_stream, side_stream);
+    cudaGraph_t graph = nullptr;
+    e = cudaStreamEndCapture(capture_stream, &graph);
+    step_nodes_end();
+    if (rc == ZERO_OK && e != cudaSuccess) rc = cuda_status(e);
+    // one fused reduce-scatter + AdamW launch per unit
+    if (rc == ZERO_OK && !step_nodes_ok(nodes, static_cast<size_t>(n_units))) rc = ZERO_ECUDA;
+    cudaGraphExec_t exec = nullptr;
+    if (rc == ZERO_OK) rc = cuda_status(cudaGraphInstantiate(&exec, graph, 0));
+    zero3_graph_t* g = nullptr;
+    if (rc == ZERO_OK) {
+        g = new (std::nothrow) zero3_graph_t{dev, n_ranks, graph, exec, nodes};
+        if (!g) rc = ZERO_ECUDA;
+    }
+    if (rc != ZERO_OK) {
+        if (exec) cudaGraphExecDestroy(exec);
+        if (graph) cudaGraphDestroy(graph);
+        step_nodes_free(nodes);
+        return rc;
+    }
+    *out = g;
+    return ZERO_OK;
+}
+
+extern "C" int zero3_graph_launch(zero3_graph_t* graph, const zero_hparams_t* hp,
+                                  cudaStream_t stream)
+{
+    if (!graph || !valid_hparams(hp)) return ZERO_EINVAL;
+    int dev = 0;
+    int rc = cuda_status(cudaGetDevice(&dev));
+    if (rc != ZERO_OK) return rc;
+    if (dev != graph->device) return ZERO_EINVAL;
+    // Only later launches see the new scalars; a replay already queued keeps
+    // the ones it was launched with.
+    if ((rc = step_nodes_set_scalars(graph->nodes, graph->exec, make_scalars(hp, graph->n_ranks))) !=
+        ZERO_OK)
+        return rc;
+    return cuda_status(cudaGraphLaunch(graph->exec, stream));
+}
+
+extern "C" int zero3_graph_destroy(zero3_graph_t* graph)
+{
+    if (!graph) return ZERO_OK;
+    int rc = cuda_status(cudaGraphExecDestroy(graph->exec));
+    const int rc2 = cuda_status(cudaGraphDestroy(graph->graph));
+    if (rc == ZERO_OK) rc = rc2;
+    step_nodes_free(graph->nodes);
+    delete graph;
+    return rc;
+}

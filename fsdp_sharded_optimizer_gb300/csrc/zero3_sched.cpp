@@ -142,6 +142,13 @@ bool unit_consistent(const zero_unit_t& u, int32_t n_ranks)
 }
 
 } // namespace
+
+int preload_step_events()
+{
+    cudaEvent_t* ev = nullptr;
+    return events_for_current_device(&ev);
+}
+
 } // namespace zero
 
 using namespace zero;

@@ -62,4 +62,24 @@ int grad_sqnorm(int32_t n_ranks, int64_t n_elems, const uint16_t* const* grads, 
 int clip_coef(const double* scratch, int64_t scratch_bytes, double max_norm, float* norm_coef,
               cudaStream_t stream);
 
+// CUDA-graph support (zero3_graph).  Between step_nodes_begin and
+// step_nodes_end, every fused-step launch made on this thread into a stream
+// that is being captured records its graph node and a copy of its arguments
+// in the returned list; step_nodes_set_scalars later rewrites the AdamW
+// scalars of all of them in an instantiated graph.  step_nodes_ok: no
+// recording failed and exactly `expected` launches were recorded.
+struct StepNodeList;
+StepNodeList* step_nodes_begin(); // nullptr when out of host memory
+void step_nodes_end();
+bool step_nodes_ok(const StepNodeList* log, size_t expected);
+int step_nodes_set_scalars(StepNodeList* log, cudaGraphExec_t exec, const StepScalars& s);
+void step_nodes_free(StepNodeList* log);
+
+// Load the kernels a ZeRO-3 step launches and cache their launch geometry,
+// so that nothing is loaded or queried for the first time inside a capture.
+int preload_fused_kernels();
+int preload_gather_kernel();
+int preload_clip_kernels();
+int preload_step_events(); // zero3_step's per-thread events
+
 } // namespace zero

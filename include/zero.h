@@ -412,6 +412,50 @@ int zero3_step(const zero_unit_t* units, int32_t n_units, int32_t n_ranks,
                const zero_clip_t* clip, int32_t reshard_after_forward,
                cudaStream_t main_stream, cudaStream_t side_stream);
 
+/* zero3_graph -- the zero3_step of one fixed set of buffers captured once as a
+ * CUDA graph and replayed once per step.  The operations, their order and
+ * their results are zero3_step's; a replay gives the GPU the step's whole
+ * dependency structure at once (event records and waits become graph edges).
+ * That saves the launch and event latency between the kernels of models with
+ * many small units.  The pages have no counterpart: it is how this library
+ * issues [DZF] "How FSDP implements ZeRO-3", steps 2-5, on one GPU.
+ *
+ * zero3_graph_create -- captures one step.
+ *   units .. full_b, clip, reshard_after_forward   as zero3_step, with the
+ *                    gradients resident (grads_resident = 1; no regeneration)
+ *   hp               any valid hyper-parameters (checked; the step's own come
+ *                    with each launch)
+ *   capture_stream   a stream created by the caller (not the legacy default
+ *                    stream, and not being captured already); the step is
+ *                    captured from it
+ *   side_stream      a second stream, != capture_stream, idle during the call
+ *   out              receives the graph handle
+ * The call captures and instantiates; it runs no kernel and changes no
+ * buffer.  The buffers must stay allocated, at the same addresses, until
+ * zero3_graph_destroy.  This call and the graph, unlike the others, hold
+ * host memory and the driver's resources for the graph.  Arguments
+ * zero3_step would reject give its code, and nothing is created.
+ * ZERO_EINVAL / ZERO_EALIGN / ZERO_ECUDA (a capture or instantiation error).
+ *
+ * zero3_graph_launch -- queues one step on `stream` (any stream of the device
+ * the graph was created on; ZERO_EINVAL on another device or invalid hp).
+ * The AdamW scalars of every unit's fused kernel are set from *hp before the
+ * replay, so t, lr, betas, eps and weight decay may change from launch to
+ * launch; a replay already queued keeps the scalars it was launched with.
+ * Launches of one graph must be made from one host thread at a time.
+ *
+ * zero3_graph_destroy -- releases the graph (NULL: no-op).  Call it after
+ * the last launch has completed. */
+typedef struct zero3_graph zero3_graph_t;
+int zero3_graph_create(const zero_unit_t* units, int32_t n_units, int32_t n_ranks,
+                       const uint16_t* const* grads, float* const* master, float* const* m,
+                       float* const* v, uint16_t* const* shard_bf16, uint16_t* full_a,
+                       uint16_t* full_b, const zero_hparams_t* hp, const zero_clip_t* clip,
+                       int32_t reshard_after_forward, cudaStream_t capture_stream,
+                       cudaStream_t side_stream, zero3_graph_t** out);
+int zero3_graph_launch(zero3_graph_t* graph, const zero_hparams_t* hp, cudaStream_t stream);
+int zero3_graph_destroy(zero3_graph_t* graph);
+
 /* zero_grad_nonfinite -- pre-reduction finite check ([DDF] "Failure
  * investigation and recovery": record per-rank finite checks before the
  * reduction, so that it does not conceal where a NaN came from).  Adds to

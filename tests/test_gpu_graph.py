@@ -1,0 +1,158 @@
+"""zero3_graph: the ZeRO-3 step captured once as a CUDA graph and replayed per
+step, through the C ABI.
+
+Checked: the replayed steps equal DDP bit for bit (the oracle's all-reduce
+simulation), with and without resharding after the forward pass; they equal
+the streamed zero3_step bit for bit when t, lr, betas, eps and weight decay
+change every step and global-norm clipping is on; creating the graph runs
+nothing; bad arguments are rejected and leave the capture stream usable.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gpu_harness as H
+from fsdp_sharded_optimizer_gb300 import _binding as B
+
+pytestmark = pytest.mark.gpu
+
+SIZES = [70_000, 333, 200_000, 64, 90_001]
+
+
+def _state(units, total, N, seed, kept=False):
+    shard_total = total // N
+    master = H.Guarded(N, shard_total, torch.float32)
+    m = H.Guarded(N, shard_total, torch.float32).zero_()
+    v = H.Guarded(N, shard_total, torch.float32).zero_()
+    shards = H.Guarded(N, shard_total, torch.int16)
+    B.zero_gen_master(seed, H.SIGMA_W, units, master.rows)
+    for k in range(N):
+        B.zero_cast_bf16(master.rows[k], shards.rows[k])
+    grads = H.Guarded(N, total, torch.int16)
+    max_unit = max(u.n_padded for u in units)
+    if kept:
+        fa, fb = H.Guarded(1, total, torch.int16), None
+    else:
+        fa, fb = H.Guarded(1, max_unit, torch.int16), H.Guarded(1, max_unit, torch.int16)
+    return master, m, v, shards, grads, fa, fb
+
+
+def _fill_grads(units, grads, seed, t, stream=None):
+    for u in units:
+        B.zero_gen_grads_unit(seed, t, H.SIGMA_G, 1, u,
+                              [r[u.offset:u.offset + u.n_padded] for r in grads.rows], stream=stream)
+
+
+def _params(units, shards, N):
+    sh = shards.numpy()
+    return np.concatenate([np.concatenate([sh[k][u.shard_offset:u.shard_offset + u.shard_len]
+                                           for k in range(N)])[:u.n_params] for u in units])
+
+
+@pytest.mark.parametrize("reshard", [True, False])
+def test_graph_replays_equal_ddp(orc, reshard):
+    N, T, seed = 4, 4, 7
+    units, total = B.zero_layout(SIZES, N)
+    master, m, v, shards, grads, fa, fb = _state(units, total, N, seed, kept=not reshard)
+    cap, side = torch.cuda.Stream(), torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    g = B.zero3_graph_create(units, grads.rows, master.rows, m.rows, v.rows, shards.rows,
+                             fa.rows[0], fb.rows[0] if fb else None, H.hp(1), cap, side,
+                             reshard_after_forward=reshard)
+    try:
+        for t in range(1, T + 1):
+            _fill_grads(units, grads, seed, t)
+            g.launch(H.hp(t))  # on the current stream, not the capture stream
+        torch.cuda.synchronize()
+    finally:
+        g.close()
+    for b in (master, m, v, shards, grads, fa) + ((fb,) if fb else ()):
+        b.check()
+    ddp = orc.sim_ddp(N, sum(SIZES), seed, H.SIGMA_W, H.SIGMA_G, 1, orc.hparams(**H.HP, step=1), T)
+    H.assert_bitwise(_params(units, shards, N), ddp[0], "params")
+    w, mm, vv = master.numpy(), m.numpy(), v.numpy()
+    for name, src, ref in (("master", w, ddp[1]), ("m", mm, ddp[2]), ("v", vv, ddp[3])):
+        got = np.concatenate([np.concatenate([src[k][u.shard_offset:u.shard_offset + u.shard_len]
+                                              for k in range(N)])[:u.n_params] for u in units])
+        H.assert_bitwise(got, ref, name)
+    H.free()
+
+
+def test_graph_follows_changing_hyperparameters_with_clipping():
+    """Every launch sets new AdamW scalars: the replays equal the streamed
+    zero3_step bit for bit while t, lr, betas, eps and weight decay change from
+    step to step, with global-norm clipping on (each side its own scratch)."""
+    N, T, seed = 8, 5, 11
+    units, total = B.zero_layout(SIZES, N)
+    a = _state(units, total, N, seed)
+    b = _state(units, total, N, seed)
+    clips = [B.clip_args(2e-3, torch.empty(B.zero_clip_scratch_bytes() // 8, dtype=torch.float64,
+                                           device="cuda"),
+                         torch.empty(4, dtype=torch.float32, device="cuda")[:2]) for _ in range(2)]
+    cap, side_a, side_b = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    g = B.zero3_graph_create(units, b[4].rows, b[0].rows, b[1].rows, b[2].rows, b[3].rows,
+                             b[5].rows[0], b[6].rows[0], H.hp(1), cap, side_b, clip=clips[1])
+
+    def hp(t):
+        return B.hparams(lr=1e-3 * (1 + 0.3 * t), beta1=0.9 - 0.02 * t, beta2=0.999 - 0.001 * t,
+                         eps=1e-8 * t, weight_decay=0.01 * (t % 3), step=t)
+
+    try:
+        for t in range(1, T + 1):
+            _fill_grads(units, a[4], seed, t)
+            _fill_grads(units, b[4], seed, t)
+            B.zero3_step(units, a[4].rows, a[0].rows, a[1].rows, a[2].rows, a[3].rows,
+                         a[5].rows[0], a[6].rows[0], hp(t), clip=clips[0], side_stream=side_a)
+            g.launch(hp(t))
+        torch.cuda.synchronize()
+    finally:
+        g.close()
+    for x, y, name in zip(a[:4], b[:4], ("master", "m", "v", "shards")):
+        x.check()
+        y.check()
+        H.assert_bitwise(y.numpy(), x.numpy(), name)
+    H.assert_bitwise(clips[1].tensors[1].cpu().numpy(), clips[0].tensors[1].cpu().numpy(),
+                     "norm and coefficient")
+    assert float(clips[0].tensors[1][1]) < 1  # the clipping was active
+    H.free()
+
+
+def test_graph_create_runs_nothing_and_rejects_bad_arguments():
+    N = 2
+    units, total = B.zero_layout([1000, 64], N)
+    master, m, v, shards, grads, fa, fb = _state(units, total, N, 3)
+    torch.cuda.synchronize()
+    before = [x.numpy().copy() for x in (master, m, v, shards)]
+    cap, side = torch.cuda.Stream(), torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    g = B.zero3_graph_create(units, grads.rows, master.rows, m.rows, v.rows, shards.rows,
+                             fa.rows[0], fb.rows[0], H.hp(1), cap, side)
+    torch.cuda.synchronize()
+    for x, y in zip((master, m, v, shards), before):
+        np.testing.assert_array_equal(x.numpy(), y)  # capture only: nothing ran
+    with pytest.raises(B.ZeroError):
+        g.launch(B.hparams(step=0))
+    g.close()
+    g.close()  # a second close is a no-op
+    with pytest.raises(ValueError):
+        g.launch(H.hp(1))
+    with pytest.raises(B.ZeroError):  # the legacy default stream cannot be captured
+        B.zero3_graph_create(units, grads.rows, master.rows, m.rows, v.rows, shards.rows,
+                             fa.rows[0], fb.rows[0], H.hp(1), torch.cuda.default_stream(), side)
+    with pytest.raises(B.ZeroError) as e:  # zero3_step's own check, inside the capture
+        B.zero3_graph_create(units, grads.rows, master.rows, m.rows, v.rows, shards.rows,
+                             fa.rows[0], fa.rows[0], H.hp(1), cap, side)
+    assert e.value.code == B.ZERO_EINVAL
+    with pytest.raises(B.ZeroError) as e:
+        B.zero3_graph_create(units, grads.rows, master.rows, m.rows, v.rows, shards.rows,
+                             fa.rows[0][1:], fb.rows[0], H.hp(1), cap, side)
+    assert e.value.code == B.ZERO_EALIGN
+    # the capture stream is not left capturing: an ordinary step runs on it
+    _fill_grads(units, grads, 3, 1)
+    cap.wait_stream(torch.cuda.current_stream())
+    B.zero3_step(units, grads.rows, master.rows, m.rows, v.rows, shards.rows, fa.rows[0],
+                 fb.rows[0], H.hp(1), main_stream=cap, side_stream=side)
+    cap.synchronize()
+    assert not np.array_equal(master.numpy(), before[0])
+    H.free()

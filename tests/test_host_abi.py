@@ -201,6 +201,37 @@ def test_zero3_step_rejects_before_launch(B):
     assert call(*no_b) == B.ZERO_EINVAL   # the double buffer needs full_b
 
 
+@host_only
+def test_zero3_graph_rejects_before_capture(B):
+    """Arguments zero3_graph_create can judge on the host are rejected before
+    any CUDA call; the handle stays NULL.  Launch and destroy take NULL."""
+    units, _ = B.zero_layout([1000, 64], 4)
+    arr = (B.zero_unit_t * 2)(*units)
+    hp, bad_hp = B.hparams(), B.hparams(step=0)
+    t = _table(A16[:4])
+    fa, fb = C.c_void_p(0x900000), C.c_void_p(0xA00000)
+    s1, s2 = C.c_void_p(0x1000), C.c_void_p(0x2000)
+    legacy = C.c_void_p(0x1)  # cudaStreamLegacy
+    h = C.c_void_p(0x1234)
+    call = B.lib.zero3_graph_create
+    bad = [
+        (arr, 0, 4, t, t, t, t, t, fa, fb, C.byref(hp), None, 1, s1, s2, C.byref(h)),      # no units
+        (None, 2, 4, t, t, t, t, t, fa, fb, C.byref(hp), None, 1, s1, s2, C.byref(h)),
+        (arr, 2, 0, t, t, t, t, t, fa, fb, C.byref(hp), None, 1, s1, s2, C.byref(h)),      # no ranks
+        (arr, 2, 4, t, t, t, t, t, fa, fb, C.byref(bad_hp), None, 1, s1, s2, C.byref(h)),  # step 0
+        (arr, 2, 4, t, t, t, t, t, fa, fb, C.byref(hp), None, 1, None, s2, C.byref(h)),    # default stream
+        (arr, 2, 4, t, t, t, t, t, fa, fb, C.byref(hp), None, 1, legacy, s2, C.byref(h)),
+        (arr, 2, 4, t, t, t, t, t, fa, fb, C.byref(hp), None, 1, s1, s1, C.byref(h)),      # one stream
+    ]
+    for args in bad:
+        h.value = 0x1234
+        assert call(*args) == B.ZERO_EINVAL
+        assert h.value is None  # *out cleared
+    assert call(arr, 2, 4, t, t, t, t, t, fa, fb, C.byref(hp), None, 1, s1, s2, None) == B.ZERO_EINVAL
+    assert B.lib.zero3_graph_launch(None, C.byref(hp), s1) == B.ZERO_EINVAL
+    assert B.lib.zero3_graph_destroy(None) == B.ZERO_OK
+
+
 def test_zero3_plan_rejects(B):
     ops = (B.zero_op_t * 10)()
     n = C.c_int32()
