@@ -156,3 +156,45 @@ def test_graph_create_runs_nothing_and_rejects_bad_arguments():
     cap.synchronize()
     assert not np.array_equal(master.numpy(), before[0])
     H.free()
+
+
+def test_graph_at_gpt2_zero3_size_equals_streamed_step():
+    """The benchmark's GPT-2 ZeRO-3 workload (12 blocks of 7,087,872 parameters
+    and a root unit of 39,385,344, N_d = 8) in its launch configuration: three
+    graph replays equal three streamed zero3_step calls on every element."""
+    import bench
+    sizes, N, _ = bench.WORKLOADS["gpt2-small-zero3-n8"]
+    units, total = B.zero_layout(sizes, N)
+    shard_total = total // N
+    max_unit = max(u.n_padded for u in units)
+    grads = torch.empty((N, total), dtype=torch.int16, device="cuda")
+    for u in units:
+        B.zero_gen_grads_unit(9, 1, H.SIGMA_G, 1, u, [r[u.offset:u.offset + u.n_padded] for r in grads])
+
+    def state():
+        w = torch.empty((N, shard_total), dtype=torch.float32, device="cuda")
+        B.zero_gen_master(9, H.SIGMA_W, units, w)
+        sh = torch.empty((N, shard_total), dtype=torch.int16, device="cuda")
+        for k in range(N):
+            B.zero_cast_bf16(w[k], sh[k])
+        full = [torch.empty(max_unit, dtype=torch.int16, device="cuda") for _ in range(2)]
+        return [w, torch.zeros_like(w), torch.zeros_like(w), sh] + full
+
+    a, b = state(), state()
+    cap, side = torch.cuda.Stream(), torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    g = B.zero3_graph_create(units, grads, b[0], b[1], b[2], b[3], b[4], b[5], H.hp(1), cap, side)
+    try:
+        for t in range(1, 4):
+            B.zero3_step(units, grads, a[0], a[1], a[2], a[3], a[4], a[5], H.hp(t), side_stream=side)
+            g.launch(H.hp(t))
+        torch.cuda.synchronize()
+    finally:
+        g.close()
+    for x, y, name in zip(a[:4], b[:4], ("master", "m", "v", "shards")):
+        xi = x.view(torch.int32) if x.dtype == torch.float32 else x
+        yi = y.view(torch.int32) if y.dtype == torch.float32 else y
+        assert torch.equal(xi, yi), name
+    assert not torch.equal(a[0], state()[0])  # the steps did change the weights
+    del a, b, grads
+    H.free()
