@@ -69,6 +69,9 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=None,
                     help="steps of the end-to-end (host buffers) measurement; default min(K, 50)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="time only the ZeRO-1 step (skips the ZeRO-2, clipping, accumulation, "
+                         "fp32-gradient and end-to-end legs and their buffers)")
     return ap.parse_args()
 
 
@@ -97,9 +100,10 @@ def fused_source_sha():
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(workload):
-    """DRAM bytes per launch of the fused kernel from the committed ncu summary,
-    if it was taken on this kernel source and workload; else None."""
+def ncu_traffic(workload, launches_per_step=1):
+    """DRAM bytes per launch of the fused kernel from the committed ncu summary
+    (its DRAM bytes over one whole step, divided by the step's launches), if it
+    was taken on this kernel source and workload; else None."""
     path = os.path.join(ROOT, "profiles", "fused_step_traffic.txt")
     try:
         rows = [dict(kv.split("=", 1) for kv in line.split())
@@ -109,8 +113,14 @@ def ncu_traffic(workload):
     sha = fused_source_sha()
     for r in rows:
         if r.get("source_sha") == sha and r.get("workload") == workload:
-            return float(r["dram_bytes_per_launch"])
+            return float(r["dram_bytes_per_step"]) / launches_per_step
     return None
+
+
+def fused_launches(n_elems, Z):
+    """Launches the fused step uses for n_elems elements: chained chunks of
+    ZERO_CHUNK_ELEMS, the last one shorter (include/zero.h)."""
+    return -(-n_elems // Z.ZERO_CHUNK_ELEMS)
 
 
 class ClockSampler:
@@ -244,99 +254,141 @@ def run_gpu(args):
     except Exception:
         pass
     clocks = ClockSampler(uuid)
-    # headline: ZeRO-1, exactly one fused launch per step and nothing else on the
-    # stream, so the kernel's mean launch duration over the timed region is the
-    # region's time / K.  (An event pair around every launch would cost ~13 us a
-    # step: each kernel would wait for the previous timestamp instead of being
-    # launched behind the previous kernel.)
+    # headline: ZeRO-1, one pass of the fused kernel per step (its chained
+    # launches) and nothing else on the stream, so the kernel's mean launch
+    # duration over the timed region is the region's time / all its launches.
+    # (An event pair around every launch would cost ~13 us a step: each kernel
+    # would wait for the previous timestamp instead of being launched behind the
+    # previous kernel.)
     ms1, _ = timed(torch, world, dev, stream, lambda: st.step(1), K)
-    launch_ms = ms1 / K
+    n_launch = fused_launches(Pp, Z)  # chained chunks of the one pass
+    launch_ms = ms1 / K / n_launch
     clk = clocks.stop()
-    # ZeRO-2: 25 MiB buckets, one launch per bucket, identical results
-    ms2, _ = timed(torch, world, dev, stream, lambda: st.step(2, BUCKET_25MIB), K)
-    n_buckets = -(-Pp // BUCKET_25MIB)
 
-    # ZeRO-1 with global-norm clipping: norm pass + coefficient + clipped fused step
-    scratch = torch.empty(Z.zero_clip_scratch_bytes() // 8, dtype=torch.float64, device=dev)
-    norm_coef = torch.empty(4, dtype=torch.float32, device=dev)[:2]
+    def sub_legs():
+        """The other legs of the step, each timed on its own."""
+        # ZeRO-2: 25 MiB buckets, chained launches, identical results
+        ms2, _ = timed(torch, world, dev, stream, lambda: st.step(2, BUCKET_25MIB), K)
+        n_buckets = -(-Pp // BUCKET_25MIB)
 
-    def clipped_step():
-        st.t += 1
-        Z.zero_grad_sqnorm(st.grads, scratch)
-        Z.zero_clip_coef(scratch, 1.0, norm_coef)
-        Z.zero_step_stage12_clip(1, st.grads, st.master, st.m, st.v, st.params,
-                                 Z.hparams(**HP, step=st.t), norm_coef)
+        # ZeRO-1 with global-norm clipping: norm pass + coefficient + clipped fused step
+        scratch = torch.empty(Z.zero_clip_scratch_bytes() // 8, dtype=torch.float64, device=dev)
+        norm_coef = torch.empty(4, dtype=torch.float32, device=dev)[:2]
 
-    for _ in range(min(W, 3)):
-        clipped_step()
-    Kc = min(K, 200)
-    ms_c, _ = timed(torch, world, dev, stream, clipped_step, Kc)
-    clip_bytes = (26 + 4 * N) * Pp
+        def clipped_step():
+            st.t += 1
+            Z.zero_grad_sqnorm(st.grads, scratch)
+            Z.zero_clip_coef(scratch, 1.0, norm_coef)
+            Z.zero_step_stage12_clip(1, st.grads, st.master, st.m, st.v, st.params,
+                                     Z.hparams(**HP, step=st.t), norm_coef)
 
-    # ZeRO-2 with gradient accumulation over 4 micro-batches (the same gradients each
-    # micro-batch): 3 accumulate launches + the last micro-batch fused with the step
-    MICRO = 4
-    grad_acc = torch.empty_like(st.master)
+        for _ in range(min(W, 3)):
+            clipped_step()
+        Kc = min(K, 200)
+        ms_c, _ = timed(torch, world, dev, stream, clipped_step, Kc)
+        clip_bytes = (26 + 4 * N) * Pp
 
-    def accumulated_step():
-        st.t += 1
-        for mu in range(MICRO - 1):
-            Z.zero2_accumulate(st.grads, grad_acc, first=mu == 0)
-        Z.zero2_step_accumulated(st.grads, grad_acc, MICRO, st.master, st.m, st.v, st.params,
-                                 Z.hparams(**HP, step=st.t))
+        # ZeRO-2 with gradient accumulation over 4 micro-batches (the same gradients each
+        # micro-batch): 3 accumulate launches + the last micro-batch fused with the step
+        MICRO = 4
+        grad_acc = torch.empty_like(st.master)
 
-    for _ in range(min(W, 3)):
-        accumulated_step()
-    Ka = min(K, 100)
-    ms_a, _ = timed(torch, world, dev, stream, accumulated_step, Ka)
-    acc_bytes = (2 * N + 4) * Pp + (MICRO - 2) * (2 * N + 8) * Pp + (26 + 2 * N + 4) * Pp
-
-    # fp32 rank gradients (Llama 3's fp32 reduce-scatter): 26 + 4N bytes per parameter
-    grads32 = torch.empty((N, Pp), dtype=torch.float32, device=dev)
-    Z.zero_gen_grads_unit_f32(0, 1, SIGMA_G, 0, st.unit, grads32)
-
-    def f32_step():
-        st.t += 1
-        Z.zero_step_stage12_f32grads(1, grads32, st.master, st.m, st.v, st.params,
+        def accumulated_step():
+            st.t += 1
+            for mu in range(MICRO - 1):
+                Z.zero2_accumulate(st.grads, grad_acc, first=mu == 0)
+            Z.zero2_step_accumulated(st.grads, grad_acc, MICRO, st.master, st.m, st.v, st.params,
                                      Z.hparams(**HP, step=st.t))
 
-    for _ in range(min(W, 3)):
-        f32_step()
-    Kf = min(K, 200)
-    ms_f, _ = timed(torch, world, dev, stream, f32_step, Kf)
-    f32_bytes = (26 + 4 * N) * Pp
-    del grads32
+        for _ in range(min(W, 3)):
+            accumulated_step()
+        Ka = min(K, 100)
+        ms_a, _ = timed(torch, world, dev, stream, accumulated_step, Ka)
+        acc_bytes = (2 * N + 4) * Pp + (MICRO - 2) * (2 * N + 8) * Pp + (26 + 2 * N + 4) * Pp
 
-    # end to end through the C ABI with host buffers: H2D gradients, step, D2H weights
-    E = args.e2e_steps or min(K, 50)
-    host_g = torch.empty((N, Pp), dtype=torch.int16, pin_memory=True)
-    host_g.copy_(st.grads)
-    host_p = torch.empty(Pp, dtype=torch.int16, pin_memory=True)
+        # fp32 rank gradients (Llama 3's fp32 reduce-scatter): 26 + 4N bytes per parameter
+        grads32 = torch.empty((N, Pp), dtype=torch.float32, device=dev)
+        Z.zero_gen_grads_unit_f32(0, 1, SIGMA_G, 0, st.unit, grads32)
 
-    def e2e_step():
-        st.grads.copy_(host_g, non_blocking=True)
-        st.step(1)
-        host_p.copy_(st.params, non_blocking=True)
+        def f32_step():
+            st.t += 1
+            Z.zero_step_stage12_f32grads(1, grads32, st.master, st.m, st.v, st.params,
+                                         Z.hparams(**HP, step=st.t))
 
-    for _ in range(min(W, 3)):
-        e2e_step()
-    ms_copy, _ = timed(torch, world, dev, stream, e2e_step, E)
+        for _ in range(min(W, 3)):
+            f32_step()
+        Kf = min(K, 200)
+        ms_f, _ = timed(torch, world, dev, stream, f32_step, Kf)
+        f32_bytes = (26 + 4 * N) * Pp
+        del grads32
 
-    # the same call given the pinned host buffers themselves: the fused kernel reads
-    # every rank's gradient from host memory and writes the new bf16 weights to host
-    # memory in place (over NVLink-C2C), so the update hides under the host transfers
-    def e2e_inplace():
-        st.t += 1
-        Z.zero_step_stage12(1, host_g, st.master, st.m, st.v, host_p, Z.hparams(**HP, step=st.t))
+        # end to end through the C ABI with host buffers: H2D gradients, step, D2H weights
+        E = args.e2e_steps or min(K, 50)
+        host_g = torch.empty((N, Pp), dtype=torch.int16, pin_memory=True)
+        host_g.copy_(st.grads)
+        host_p = torch.empty(Pp, dtype=torch.int16, pin_memory=True)
 
-    for _ in range(min(W, 3)):
-        e2e_inplace()
-    ms_e2e, _ = timed(torch, world, dev, stream, e2e_inplace, E)
+        def e2e_step():
+            st.grads.copy_(host_g, non_blocking=True)
+            st.step(1)
+            host_p.copy_(st.params, non_blocking=True)
+
+        for _ in range(min(W, 3)):
+            e2e_step()
+        ms_copy, _ = timed(torch, world, dev, stream, e2e_step, E)
+
+        # the same call given the pinned host buffers themselves: the fused kernel reads
+        # every rank's gradient from host memory and writes the new bf16 weights to host
+        # memory in place (over NVLink-C2C), so the update hides under the host transfers
+        def e2e_inplace():
+            st.t += 1
+            Z.zero_step_stage12(1, host_g, st.master, st.m, st.v, host_p, Z.hparams(**HP, step=st.t))
+
+        for _ in range(min(W, 3)):
+            e2e_inplace()
+        ms_e2e, _ = timed(torch, world, dev, stream, e2e_inplace, E)
+
+        return {
+            "zero2": {
+                "ms_per_step": ms2 / K, "value": world * P * K / (ms2 * 1e-3),
+                "launches_per_step": n_buckets, "bucket_elems": BUCKET_25MIB,
+                "hbm_gbs": bytes_per_step * K / (ms2 * 1e-3) / 1e9,
+            },
+            "clip": {
+                "ms_per_step": ms_c / Kc, "value": world * P * Kc / (ms_c * 1e-3), "steps": Kc,
+                "hbm_gbs": clip_bytes * Kc / (ms_c * 1e-3) / 1e9, "bytes_per_step": clip_bytes,
+                "note": "ZeRO-1 with global-norm clipping (max_norm 1.0): norm pass (2N B/param) + "
+                        "coefficient + clipped fused step (26+2N B/param), 3 launches",
+            },
+            "accumulation": {
+                "micro_batches": MICRO, "ms_per_step": ms_a / Ka, "steps": Ka,
+                "hbm_gbs": acc_bytes * Ka / (ms_a * 1e-3) / 1e9, "bytes_per_step": acc_bytes,
+                "note": "ZeRO-2 with gradient accumulation: a reduce-scatter into the fp32 owner "
+                        "accumulator after each of the first m-1 micro-batches, the last one fused "
+                        "with AdamW",
+            },
+            "f32_grads": {
+                "ms_per_step": ms_f / Kf, "value": world * P * Kf / (ms_f * 1e-3), "steps": Kf,
+                "hbm_gbs": f32_bytes * Kf / (ms_f * 1e-3) / 1e9, "bytes_per_step": f32_bytes,
+                "note": "ZeRO-1 with fp32 rank gradients (26 + 4N B/param)",
+            },
+            "e2e": {
+                "value": world * P * E / (ms_e2e * 1e-3), "unit": "params/s", "steps": E,
+                "ms_per_step": ms_e2e / E,
+                "h2d_bytes_per_step": N * Pp * 2, "d2h_bytes_per_step": Pp * 2,
+                "path": "zero_step_stage12 on pinned host gradients and pinned host weights: the "
+                        "kernel reads and writes host memory in place",
+                "copy_engine": {"ms_per_step": ms_copy / E,
+                                "value": world * P * E / (ms_copy * 1e-3),
+                                "path": "cudaMemcpyAsync H2D of the gradients, the step on device "
+                                        "buffers, cudaMemcpyAsync D2H of the weights"},
+            },
+        }
 
     peak, peak_kind = measured_peak()
     per_step_ms = ms1 / K
-    achieved = bytes_per_step / (launch_ms * 1e-3) / 1e9
-    traffic = ncu_traffic(args.workload)
+    achieved = bytes_per_step / n_launch / (launch_ms * 1e-3) / 1e9
+    traffic = ncu_traffic(args.workload, n_launch)
     result = {
         "metric": METRIC,
         "value": world * P * K / (ms1 * 1e-3),
@@ -363,47 +415,17 @@ def run_gpu(args):
             "bound": "hbm", "kernel": "fused_step_kernel", "achieved": achieved, "peak": peak,
             "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind,
             "frac_of_8tbs_nominal": achieved / 8000.0,
-            "bytes_per_launch": bytes_per_step, "launch_ms": launch_ms,
-            "launch_ms_from": "timed region / K launches (one launch per step, back to back)",
+            "bytes_per_launch": bytes_per_step / n_launch, "launch_ms": launch_ms,
+            "launches_per_step": n_launch,
+            "launch_ms_from": "timed region / (K steps x launches per step): each step is one "
+                              "pass of the fused kernel in chained launches, back to back",
             "traffic": traffic,
         },
-        "zero2": {
-            "ms_per_step": ms2 / K, "value": world * P * K / (ms2 * 1e-3),
-            "launches_per_step": n_buckets, "bucket_elems": BUCKET_25MIB,
-            "hbm_gbs": bytes_per_step * K / (ms2 * 1e-3) / 1e9,
-        },
-        "clip": {
-            "ms_per_step": ms_c / Kc, "value": world * P * Kc / (ms_c * 1e-3), "steps": Kc,
-            "hbm_gbs": clip_bytes * Kc / (ms_c * 1e-3) / 1e9, "bytes_per_step": clip_bytes,
-            "note": "ZeRO-1 with global-norm clipping (max_norm 1.0): norm pass (2N B/param) + "
-                    "coefficient + clipped fused step (26+2N B/param), 3 launches",
-        },
-        "accumulation": {
-            "micro_batches": MICRO, "ms_per_step": ms_a / Ka, "steps": Ka,
-            "hbm_gbs": acc_bytes * Ka / (ms_a * 1e-3) / 1e9, "bytes_per_step": acc_bytes,
-            "note": "ZeRO-2 with gradient accumulation: a reduce-scatter into the fp32 owner "
-                    "accumulator after each of the first m-1 micro-batches, the last one fused "
-                    "with AdamW",
-        },
-        "f32_grads": {
-            "ms_per_step": ms_f / Kf, "value": world * P * Kf / (ms_f * 1e-3), "steps": Kf,
-            "hbm_gbs": f32_bytes * Kf / (ms_f * 1e-3) / 1e9, "bytes_per_step": f32_bytes,
-            "note": "ZeRO-1 with fp32 rank gradients (26 + 4N B/param)",
-        },
-        "e2e": {
-            "value": world * P * E / (ms_e2e * 1e-3), "unit": "params/s", "steps": E,
-            "ms_per_step": ms_e2e / E,
-            "h2d_bytes_per_step": N * Pp * 2, "d2h_bytes_per_step": Pp * 2,
-            "path": "zero_step_stage12 on pinned host gradients and pinned host weights: the "
-                    "kernel reads and writes host memory in place",
-            "copy_engine": {"ms_per_step": ms_copy / E,
-                            "value": world * P * E / (ms_copy * 1e-3),
-                            "path": "cudaMemcpyAsync H2D of the gradients, the step on device "
-                                    "buffers, cudaMemcpyAsync D2H of the weights"},
-        },
         "clocks": clk,
-        "gpu_launches": K,
+        "gpu_launches": K * n_launch,
     }
+    if not args.headline_only:
+        result.update(sub_legs())
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(args.workload, steps=20)
     if world > 1:
@@ -525,6 +547,7 @@ def run_gpu_zero3(args, torch, Z, world, rank, dev):
 
     peak, peak_kind = measured_peak()
     fused_bytes = (26 + 2 * N) * total
+    rs_launches = sum(fused_launches(u.n_padded, Z) for u in units)
     gather_bytes = 2 * 4 * total
     achieved = fused_bytes * Kt / (rs_ms * 1e-3) / 1e9
     return {
@@ -544,7 +567,7 @@ def run_gpu_zero3(args, torch, Z, world, rank, dev):
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": peak_kind, "frac_of_8tbs_nominal": achieved / 8000.0,
                      "bytes_per_step": fused_bytes, "kernel_ms_per_step": rs_ms / Kt,
-                     "launches_per_step": len(units),
+                     "launches_per_step": rs_launches,
                      "launch_ms_from": "every unit's fused launch back to back on one stream, "
                                        "no gathers beside it: loop time / launches",
                      "traffic": ncu_traffic(args.workload)},
@@ -565,7 +588,7 @@ def run_gpu_zero3(args, torch, Z, world, rank, dev):
                        "note": "per-unit gradients regenerated from the seed in each backward "
                                "(harness work, not the method)"},
         "clocks": clk,
-        "gpu_launches": K * len(units) * 3,
+        "gpu_launches": K * (2 * len(units) + rs_launches),
     } if rank == 0 else None
 
 

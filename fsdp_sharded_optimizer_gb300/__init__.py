@@ -12,7 +12,7 @@ The public calls carry the C ABI's names (include/zero.h) and live in
 before the library exists; using any of them without a built library raises
 ImportError (there is no fallback).
 """
-_PUBLIC = ("ZERO_DEFAULT_ALIGN", "ZERO_EALIGN", "ZERO_ECUDA", "ZERO_EINVAL", "ZERO_ETIMEOUT",
+_PUBLIC = ("ZERO_DEFAULT_ALIGN", "ZERO_CHUNK_ELEMS", "ZERO_EALIGN", "ZERO_ECUDA", "ZERO_EINVAL", "ZERO_ETIMEOUT",
            "ZERO_MAX_RANKS", "ZERO_OK", "LIB_PATH", "ZeroError", "hparams", "strerror",
            "zero3_gather_unit", "zero3_reduce_scatter_unit", "zero_bytes_t", "zero_cast_bf16",
            "zero_gen_grads_unit", "zero_gen_master", "zero_hparams_t", "zero_layout",

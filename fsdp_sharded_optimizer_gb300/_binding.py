@@ -22,6 +22,7 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libzero.so")
 ZERO_OK, ZERO_EINVAL, ZERO_EALIGN, ZERO_ECUDA, ZERO_ETIMEOUT = 0, -1, -2, -3, -4
 ZERO_MAX_RANKS = 64
 ZERO_DEFAULT_ALIGN = 64
+ZERO_CHUNK_ELEMS = 13107200  # fused-step launch granularity (include/zero.h)
 
 
 class ZeroError(RuntimeError):

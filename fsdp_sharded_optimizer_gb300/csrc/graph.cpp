@@ -71,8 +71,11 @@ extern "C" int zero3_graph_create(const zero_unit_t* units, int32_t n_units, int
     e = cudaStreamEndCapture(capture_stream, &graph);
     step_nodes_end();
     if (rc == ZERO_OK && e != cudaSuccess) rc = cuda_status(e);
-    // one fused reduce-scatter + AdamW launch per unit
-    if (rc == ZERO_OK && !step_nodes_ok(nodes, static_cast<size_t>(n_units))) rc = ZERO_ECUDA;
+    // each unit's fused reduce-scatter + AdamW, in its chained launches
+    int64_t expected = 0;
+    for (int32_t u = 0; u < n_units && rc == ZERO_OK; ++u)
+        expected += chunk_count(units[u].n_padded / 8);
+    if (rc == ZERO_OK && !step_nodes_ok(nodes, static_cast<size_t>(expected))) rc = ZERO_ECUDA;
     cudaGraphExec_t exec = nullptr;
     if (rc == ZERO_OK) rc = cuda_status(cudaGraphInstantiate(&exec, graph, 0));
     zero3_graph_t* g = nullptr;

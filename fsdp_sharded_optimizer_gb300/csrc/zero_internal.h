@@ -68,6 +68,11 @@ int clip_coef(const double* scratch, int64_t scratch_bytes, double max_norm, flo
 // in the returned list; step_nodes_set_scalars later rewrites the AdamW
 // scalars of all of them in an instantiated graph.  step_nodes_ok: no
 // recording failed and exactly `expected` launches were recorded.
+// Number of chained launches the fused step uses for n_vec vectors (a vector
+// = 8 elements): ceil(n_vec / (ZERO_CHUNK_ELEMS / 8)); all but the last cover
+// ZERO_CHUNK_ELEMS elements.
+int64_t chunk_count(int64_t n_vec);
+
 struct StepNodeList;
 StepNodeList* step_nodes_begin(); // nullptr when out of host memory
 void step_nodes_end();

@@ -64,6 +64,17 @@ extern "C" {
 #define ZERO_MAX_RANKS 64
 #define ZERO_DEFAULT_ALIGN 64 /* elements per shard granule */
 
+/* Launch granularity of the fused step.  A call (or a ZeRO-2 bucket) of n
+ * elements is covered by ceil(n / ZERO_CHUNK_ELEMS) launches, consecutive
+ * chunks of ZERO_CHUNK_ELEMS elements with a shorter last one, each after the
+ * first a programmatic dependent launch on the one before (the chunks touch
+ * disjoint elements).  A block that finishes its share of a chunk early hands
+ * its SM to the next chunk, which one persistent launch over the whole range
+ * cannot do.  The results do not depend on it.  The value is 25 MiB of bf16
+ * gradients, the DDP bucket default ([DZF] "How DDP overlaps the all-reduce
+ * with the backward pass", step 1). */
+#define ZERO_CHUNK_ELEMS 13107200
+
 /* AdamW hyper-parameters ([DZF] "5. In code": lr, b1, b2, eps, wd) and the
  * 1-based step counter t used by the bias correction 1 - b^t. */
 typedef struct {
@@ -127,13 +138,13 @@ int zero_layout(const int64_t* unit_sizes, int32_t n_units, int32_t n_ranks,
  *   master, m, v   n_ranks device pointers, each S fp32 (read and written)
  *   params_bf16    device pointer, n_padded bf16 (written): the replicated
  *                  weights every rank holds after the all-gather
- *   bucket_elems   stage 2: reduce-scatter+update bucket by bucket, one launch
- *                  per bucket of this many elements (multiple of 8; 0 = whole
- *                  buffer); ignored for stage 1.  Each bucket's launch after
- *                  the first is a programmatic dependent launch on the one
- *                  before it (the buckets touch disjoint elements), so it may
- *                  start while that one drains; the call as a whole is still
- *                  ordered on the stream like one kernel.
+ *   bucket_elems   stage 2: reduce-scatter+update bucket by bucket, in the
+ *                  launches of one bucket of this many elements after another
+ *                  (multiple of 8; 0 = whole buffer); ignored for stage 1.
+ *                  Every launch after the call's first is a programmatic
+ *                  dependent launch on the one before it (ZERO_CHUNK_ELEMS), so
+ *                  it may start while that one drains; the call as a whole is
+ *                  still ordered on the stream like one kernel.
  * Buffers must not overlap.  ZERO_EINVAL / ZERO_EALIGN / ZERO_ECUDA. */
 int zero_step_stage12(int32_t stage, int32_t n_ranks, int64_t n_padded,
                       const uint16_t* const* grads, float* const* master,

@@ -118,6 +118,36 @@ def test_graph_follows_changing_hyperparameters_with_clipping():
     H.free()
 
 
+def test_graph_with_units_of_several_chunks_equals_streamed_step():
+    """A unit longer than ZERO_CHUNK_ELEMS is reduce-scattered in chained
+    launches; the capture records each of them and every replay updates all."""
+    N, T, seed = 4, 3, 13
+    sizes = [2 * B.ZERO_CHUNK_ELEMS + 4096, 333, 3_000_000]
+    units, total = B.zero_layout(sizes, N)
+    assert -(-units[0].n_padded // B.ZERO_CHUNK_ELEMS) == 3
+    a = _state(units, total, N, seed)
+    b = _state(units, total, N, seed)
+    cap, side_a, side_b = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    g = B.zero3_graph_create(units, b[4].rows, b[0].rows, b[1].rows, b[2].rows, b[3].rows,
+                             b[5].rows[0], b[6].rows[0], H.hp(1), cap, side_b)
+    try:
+        for t in range(1, T + 1):
+            _fill_grads(units, a[4], seed, t)
+            _fill_grads(units, b[4], seed, t)
+            B.zero3_step(units, a[4].rows, a[0].rows, a[1].rows, a[2].rows, a[3].rows,
+                         a[5].rows[0], a[6].rows[0], H.hp(t), side_stream=side_a)
+            g.launch(H.hp(t))
+        torch.cuda.synchronize()
+    finally:
+        g.close()
+    for x, y, name in zip(a[:4], b[:4], ("master", "m", "v", "shards")):
+        x.check()
+        y.check()
+        H.assert_bitwise(y.numpy(), x.numpy(), name)
+    H.free()
+
+
 def test_graph_create_runs_nothing_and_rejects_bad_arguments():
     N = 2
     units, total = B.zero_layout([1000, 64], N)

@@ -87,6 +87,24 @@ def test_zero1_equals_zero2_bitwise():
     H.free()
 
 
+@pytest.mark.parametrize("stage,bucket", [(1, 0), (2, 3 * B.ZERO_CHUNK_ELEMS // 2)])
+def test_multi_chunk_step_matches_oracle_every_element(orc, stage, bucket):
+    """A call longer than ZERO_CHUNK_ELEMS runs as chained launches of that
+    many elements, the last one shorter: for ZeRO-1 two full chunks and a
+    1,024-element one; for ZeRO-2 a bucket of 1.5 chunks cut into a full and a
+    half chunk, then the shorter last bucket as one launch chained to the bucket
+    before.  Every element equals the oracle, bit for bit, over 3 steps."""
+    N, T = 8, 3
+    P = 2 * B.ZERO_CHUNK_ELEMS + 1000
+    (u,), _ = B.zero_layout([P], N)
+    assert -(-u.n_padded // B.ZERO_CHUNK_ELEMS) == 3
+    gp, gw, gm, gv, _ = H.run_zero12(stage, N, P, T, seed=4, outliers=1, bucket=bucket)
+    rp, rw, rm, rv = H.oracle_zero12(orc, stage, N, P, T, seed=4, outliers=1, bucket=bucket)
+    for name, g, r in (("params", gp, rp), ("master", gw, rw), ("m", gm, rm), ("v", gv, rv)):
+        H.assert_bitwise(g, r, name)
+    H.free()
+
+
 def test_chained_buckets_complete_in_stream_order():
     """Stage-2 bucket launches after the first may start while the one before
     drains (programmatic dependent launch); the call must still be ordered on

@@ -32,6 +32,15 @@ def test_header_declares_the_boundary():
         assert n in names
 
 
+def test_binding_constants_match_the_header(B):
+    text = open(os.path.join(ROOT, "include", "zero.h")).read()
+    defines = dict(re.findall(r"#define (ZERO_[A-Z_]+) \(?(-?\d+)\)?", text))
+    for name in ("ZERO_OK", "ZERO_EINVAL", "ZERO_EALIGN", "ZERO_ECUDA", "ZERO_ETIMEOUT",
+                 "ZERO_MAX_RANKS", "ZERO_DEFAULT_ALIGN", "ZERO_CHUNK_ELEMS"):
+        assert int(defines[name]) == getattr(B, name), name
+    assert B.ZERO_CHUNK_ELEMS % 8 == 0
+
+
 def test_library_exports_every_declared_symbol(B):
     lib = C.CDLL(B.LIB_PATH)
     missing = [n for n in _header_functions() if not hasattr(lib, n)]
