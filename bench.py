@@ -24,6 +24,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -93,10 +94,16 @@ def measured_peak():
 
 
 def fused_source_sha():
+    """sha256 (first 16 hex digits) of the fused kernel's sources with comments
+    and whitespace removed: an edit of the code, not of its comments, makes a
+    committed ncu record stale."""
     h = hashlib.sha256()
     for rel in FUSED_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

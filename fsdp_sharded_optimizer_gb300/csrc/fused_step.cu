@@ -14,7 +14,8 @@
 // grid-stride stream of 16-byte vector accesses: each thread handles 8
 // consecutive elements (one 16-byte bf16 vector per rank, two 16-byte fp32
 // vectors per state array) and keeps all of a batch's loads in flight before
-// it sums.  No tensor cores: this is not a contraction.
+// it sums.  A call is issued as chained launches over 25 MiB chunks (see
+// launch()).  No tensor cores: this is not a contraction.
 #include <new>
 #include <vector>
 
@@ -79,9 +80,9 @@ __global__ void __launch_bounds__(kBlock, kMinBlocksPerSM)
 fused_step_kernel(const __grid_constant__ Tables T, const StepScalars s, const Range R,
                   const float* __restrict__ clip)
 {
-    // Bucket chaining (programmatic dependent launch): the next bucket's grid
+    // Chained launches (programmatic dependent launch): the next chunk's grid
     // may start as soon as every block of this one is running, so its blocks
-    // fill the SMs this grid's tail leaves idle.  Buckets touch disjoint
+    // fill the SMs this grid's tail leaves idle.  Chunks touch disjoint
     // elements; the wait at the end keeps "this grid completes after its
     // predecessor" for everything later on the stream.  Threads without work
     // leave at once; thread 0 of block 0 always has work (q0 < q1) and waits,
@@ -257,7 +258,8 @@ void log_capture(const void* func, int blocks, const Tables& T, const StepScalar
 
 // One fused-step launch.  chained: launched with programmatic stream
 // serialization, so it may begin while the previous kernel on the stream (the
-// previous bucket of the same step, which touches other elements) finishes.
+// previous chunk or bucket of the same call, which touches other elements)
+// finishes.
 template <bool kClip, bool kAcc, bool kF32>
 cudaError_t launch_fused(int blocks, cudaStream_t stream, bool chained, const Tables& T,
                          const StepScalars& s, const Range& R, const float* clip)
