@@ -156,6 +156,8 @@ template <bool kFirst>
 __global__ void __launch_bounds__(kBlock, kMinBlocksPerSM)
 accumulate_kernel(const __grid_constant__ Tables T, const float inv_n, const Range R)
 {
+    // chained like fused_step_kernel (the same two instructions, the same reasons)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kBlock;
     int64_t q = R.q0 + static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x;
     if (q >= R.q1) return;
@@ -183,6 +185,7 @@ accumulate_kernel(const __grid_constant__ Tables T, const float inv_n, const Ran
             ++k;
         }
     }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 Range make_range(const void* kernel, int64_t q0, int64_t q1, int64_t shard_vec, int32_t n_ranks,
@@ -539,15 +542,28 @@ extern "C" int zero2_accumulate(int32_t n_ranks, int64_t n_padded, const uint16_
     const int64_t S = n_padded / n_ranks;
     const void* kernel = first ? reinterpret_cast<const void*>(accumulate_kernel<true>)
                                : reinterpret_cast<const void*>(accumulate_kernel<false>);
-    int blocks = 0;
-    const Range R = make_range(kernel, 0, n_padded / 8, S / 8, n_ranks, &blocks);
-    if (blocks <= 0) return ZERO_ECUDA;
     const float inv_n = static_cast<float>(1.0 / static_cast<double>(n_ranks));
-    if (first)
-        accumulate_kernel<true><<<blocks, kBlock, 0, stream>>>(T, inv_n, R);
-    else
-        accumulate_kernel<false><<<blocks, kBlock, 0, stream>>>(T, inv_n, R);
-    return cuda_status(cudaGetLastError());
+    // chained chunks of kChunkVec vectors, as the fused step's launch()
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    const int64_t nvec = n_padded / 8;
+    for (int64_t a = 0; a < nvec; a += kChunkVec) {
+        const int64_t b = nvec - a > kChunkVec ? a + kChunkVec : nvec;
+        int blocks = 0;
+        const Range R = make_range(kernel, a, b, S / 8, n_ranks, &blocks);
+        if (blocks <= 0) return ZERO_ECUDA;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+        cfg.blockDim = dim3(kBlock);
+        cfg.stream = stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = a > 0 ? 1 : 0;
+        const cudaError_t e = first ? cudaLaunchKernelEx(&cfg, accumulate_kernel<true>, T, inv_n, R)
+                                    : cudaLaunchKernelEx(&cfg, accumulate_kernel<false>, T, inv_n, R);
+        if (e != cudaSuccess) return cuda_status(e);
+    }
+    return ZERO_OK;
 }
 
 extern "C" int zero2_step_accumulated(int32_t n_ranks, int64_t n_padded,

@@ -12,10 +12,12 @@ from fsdp_sharded_optimizer_gb300 import _binding as B
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("N,P,micro", [(2, 2**20, 2), (8, 300_001, 3), (8, 2**16 + 37, 8),
-                                       (64, 70_000, 4), (3, 65, 5), (4, 5000, 1)])
-def test_accumulated_zero2_matches_oracle(orc, N, P, micro):
-    T, seed = 4, 7
+@pytest.mark.parametrize("N,P,micro,T", [(2, 2**20, 2, 4), (8, 300_001, 3, 4), (8, 2**16 + 37, 8, 4),
+                                         (64, 70_000, 4, 4), (3, 65, 5, 4), (4, 5000, 1, 4),
+                                         # three chained launches per call (ZERO_CHUNK_ELEMS)
+                                         (4, 2 * B.ZERO_CHUNK_ELEMS + 1000, 3, 2)])
+def test_accumulated_zero2_matches_oracle(orc, N, P, micro, T):
+    seed = 7
     (u,), _ = B.zero_layout([P], N)
     grads = H.Guarded(N, u.n_padded, torch.int16)
     acc = H.Guarded(N, u.shard_len, torch.float32)

@@ -80,7 +80,10 @@ def test_norm_is_deterministic_and_accumulates_over_units(orc):
 
 @pytest.mark.parametrize("stage,N,P,bucket,max_norm", [(1, 2, 2**20, 0, 1e-3), (2, 8, 300_001, 104, 2e-3),
                                                        (2, 64, 2**16 + 37, 4096, 1e-4),
-                                                       (1, 3, 65, 0, 1e-5)])
+                                                       (1, 3, 65, 0, 1e-5),
+                                                       # three chained launches
+                                                       (1, 4, 2 * B.ZERO_CHUNK_ELEMS + 1000, 0,
+                                                        1e-3)])
 def test_clipped_zero12_step_matches_oracle(orc, stage, N, P, bucket, max_norm):
     T, seed = 10, 6
     (u,), _ = B.zero_layout([P], N)

@@ -13,7 +13,9 @@ pytestmark = pytest.mark.gpu
 
 @pytest.mark.parametrize("stage,N,P,bucket", [(1, 2, 2**20, 0), (2, 8, 300_001, 104),
                                               (2, 64, 2**16 + 37, 4096), (1, 3, 65, 0),
-                                              (2, 16, 1_000_003, 8 * 12345)])
+                                              (2, 16, 1_000_003, 8 * 12345),
+                                              # three chained launches (ZERO_CHUNK_ELEMS)
+                                              (1, 4, 2 * B.ZERO_CHUNK_ELEMS + 1000, 0)])
 def test_f32_grads_zero12_matches_oracle(orc, stage, N, P, bucket):
     T, seed = 6, 8
     (u,), _ = B.zero_layout([P], N)
