@@ -5,8 +5,8 @@ Default workload: N_d = 8 emulated data-parallel ranks on one GPU, the flat
 buffer of GPT-2-small's tensor shapes (124,439,808 parameters padded to
 124,440,064), seeded synthetic bf16 gradients ~N(0, 1e-3) and fp32 master
 weights ~N(0, 0.02).  One step = one pass of the fused reduce-scatter + AdamW +
-bf16 all-gather over the whole buffer (ZeRO-1: one launch); the ZeRO-2 step
-(25 MiB buckets, one launch per bucket, the same bits) is timed beside it.
+bf16 all-gather over the whole buffer (ZeRO-1: chained launches of 25 MiB
+chunks); the ZeRO-2 step (25 MiB buckets, the same bits) is timed beside it.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
                     [--workload NAME]
