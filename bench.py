@@ -295,6 +295,24 @@ def run_gpu(args):
         ms_c, _ = timed(torch, world, dev, stream, clipped_step, Kc)
         clip_bytes = (26 + 4 * N) * Pp
 
+        # the same clipped step through the fp32 gradient shard: the norm pass also
+        # stores the mean gradient, and the update reads it instead of the N rank
+        # gradients (2N + 34 B/param instead of 4N + 26)
+        grad_shard = torch.empty_like(st.master)
+
+        def clipped_reduced_step():
+            st.t += 1
+            Z.zero_grad_reduce_sqnorm(st.grads, grad_shard, scratch)
+            Z.zero_clip_coef(scratch, 1.0, norm_coef)
+            Z.zero_step_stage12_reduced(1, grad_shard, st.master, st.m, st.v, st.params,
+                                        Z.hparams(**HP, step=st.t), norm_coef)
+
+        for _ in range(min(W, 3)):
+            clipped_reduced_step()
+        ms_cr, _ = timed(torch, world, dev, stream, clipped_reduced_step, Kc)
+        clip_red_bytes = (2 * N + 34) * Pp
+        del grad_shard
+
         # ZeRO-2 with gradient accumulation over 4 micro-batches (the same gradients each
         # micro-batch): 3 accumulate launches + the last micro-batch fused with the step
         MICRO = 4
@@ -360,6 +378,14 @@ def run_gpu(args):
                 "ms_per_step": ms2 / K, "value": world * P * K / (ms2 * 1e-3),
                 "launches_per_step": n_buckets, "bucket_elems": BUCKET_25MIB,
                 "hbm_gbs": bytes_per_step * K / (ms2 * 1e-3) / 1e9,
+            },
+            "clip_reduced": {
+                "ms_per_step": ms_cr / Kc, "value": world * P * Kc / (ms_cr * 1e-3), "steps": Kc,
+                "hbm_gbs": clip_red_bytes * Kc / (ms_cr * 1e-3) / 1e9,
+                "bytes_per_step": clip_red_bytes,
+                "note": "the clipped step through the fp32 gradient shard: norm pass that also "
+                        "stores the mean gradient (2N + 4 B/param) + coefficient + update from "
+                        "the shard (30 B/param); the same bits as `clip`",
             },
             "clip": {
                 "ms_per_step": ms_c / Kc, "value": world * P * Kc / (ms_c * 1e-3), "steps": Kc,

@@ -99,6 +99,9 @@ SIGNATURES = {
     "zero_step_stage12_clip": (C.c_int, [_I32, _I32, _I64, _P, _P, _P, _P, _P, _P, _I64, _P,
                                          _P]),
     "zero3_reduce_scatter_unit_clip": (C.c_int, [_P, _I32, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "zero_grad_reduce_sqnorm": (C.c_int, [_I32, _I64, _P, _P, _I32, _P, _I64, _P]),
+    "zero_step_stage12_reduced": (C.c_int, [_I32, _I32, _I64, _P, _P, _P, _P, _P, _P, _I64, _P,
+                                            _P]),
     "zero_clip_coef_units_noalloc": (C.c_int, [_P, _I32, _I32, _P, _F64, _P, _P, _P]),
     "zero_grad_nonfinite": (C.c_int, [_I32, _I64, _P, _P, _I32, _P]),
     "zero_step_stage12_f32grads": (C.c_int, [_I32, _I32, _I64, _P, _P, _P, _P, _P, _P, _I64,
@@ -267,6 +270,32 @@ def zero_step_stage12_clip(stage, grads, master, m, v, params_bf16, hp, norm_coe
     _check("zero_step_stage12_clip", lib.zero_step_stage12_clip(
         stage, len(grows), grows[0].numel(), g, w, mm, vv, _dev(params_bf16, 2, "params_bf16"),
         C.byref(hp), int(bucket_elems), _dev(norm_coef, 4, "norm_coef"), _stream(stream)))
+
+
+def zero_grad_reduce_sqnorm(grads, grad_shard, scratch, accumulate=False, stream=None):
+    """zero_grad_sqnorm that also stores the mean gradient to the owners' fp32
+    shards: grads (N x P' bf16), grad_shard (N x S fp32)."""
+    g, rows = _rows(grads, 2, "grads")
+    gs, srows = _rows(grad_shard, 4, "grad_shard")
+    if len(srows) != len(rows):
+        raise ValueError("grad_shard needs one row per rank")
+    _check("zero_grad_reduce_sqnorm", lib.zero_grad_reduce_sqnorm(
+        len(rows), rows[0].numel(), g, gs, 1 if accumulate else 0, C.c_void_p(scratch.data_ptr()),
+        scratch.numel() * scratch.element_size(), _stream(stream)))
+
+
+def zero_step_stage12_reduced(stage, grad_shard, master, m, v, params_bf16, hp, norm_coef=None,
+                              bucket_elems=0, stream=None):
+    """The ZeRO-1/2 step from the reduced fp32 gradient shards (N x S), clipped
+    by norm_coef (device float[2]) when given."""
+    gs, rows = _rows(grad_shard, 4, "grad_shard")
+    w, _ = _rows(master, 4, "master")
+    mm, _ = _rows(m, 4, "m")
+    vv, _ = _rows(v, 4, "v")
+    _check("zero_step_stage12_reduced", lib.zero_step_stage12_reduced(
+        stage, len(rows), params_bf16.numel(), gs, w, mm, vv, _dev(params_bf16, 2, "params_bf16"),
+        C.byref(hp), int(bucket_elems),
+        _dev(norm_coef, 4, "norm_coef") if norm_coef is not None else None, _stream(stream)))
 
 
 def zero3_reduce_scatter_unit_clip(unit, unit_grads, master, m, v, shard_bf16, hp, norm_coef,

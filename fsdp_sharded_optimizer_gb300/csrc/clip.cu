@@ -18,6 +18,13 @@
 // compensation; the block and final sums run in fp64.  The relative error of
 // the squared norm stays within about 6 fp32 roundings (< 4e-7), whatever the
 // length.
+//
+// zero_grad_reduce_sqnorm is the same pass that also keeps what it computes:
+// each element's mean gradient, stored to its owner's fp32 gradient shard
+// (the reduce-scatter's output, FSDP's fp32 gradient shard).  The clipped
+// update then reads 4 bytes per parameter of that shard instead of the 2N
+// bytes of rank gradients: 2N + 34 bytes per parameter for the clipped step
+// instead of 4N + 26.
 #include "device.cuh"
 #include "zero_internal.h"
 
@@ -85,6 +92,56 @@ clip_coef_kernel(const double* __restrict__ partials, int n, double max_norm,
     }
 }
 
+// The norm pass fused with the reduce-scatter's output.  The same grid, loop
+// order and arithmetic as grad_sqnorm_kernel, so the same partial sums and the
+// same norm, bit for bit; in addition each element's mean gradient
+// g = fp32 sum * (1/N) is stored to its owner's fp32 gradient shard, so the
+// clipped update reads 4 bytes of g instead of the N bf16 gradients again.
+// (owner, position) advance with the stride split into whole shards (step_k)
+// and a remainder (step_j), as in the fused step.
+struct ReduceTable {
+    const uint4* g[ZERO_MAX_RANKS];
+    float4* out[ZERO_MAX_RANKS];
+};
+
+__global__ void __launch_bounds__(kNormThreads)
+grad_reduce_sqnorm_kernel(const __grid_constant__ ReduceTable T, int n_ranks, int64_t n_vec,
+                          int64_t shard_vec, int64_t step_k, int64_t step_j, float inv_n,
+                          int accumulate, double* __restrict__ partials)
+{
+    float sum = 0.0f, comp = 0.0f; // Kahan: true sum ~ sum - comp
+    int64_t q = static_cast<int64_t>(blockIdx.x) * kNormThreads + threadIdx.x;
+    int64_t k = q / shard_vec;
+    int64_t j = q - k * shard_vec;
+    for (; q < n_vec; q += static_cast<int64_t>(gridDim.x) * kNormThreads) {
+        float acc[8];
+        dev::sum_ranks<8>(T.g, n_ranks, q, acc);
+        float g[8], sq[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            g[e] = __fmul_rn(acc[e], inv_n);
+            sq[e] = __fmul_rn(g[e], g[e]);
+        }
+        float4* o = T.out[k] + 2 * j;
+        dev::st_stream(o, make_float4(g[0], g[1], g[2], g[3]));
+        dev::st_stream(o + 1, make_float4(g[4], g[5], g[6], g[7]));
+        const float s8 = __fadd_rn(__fadd_rn(__fadd_rn(sq[0], sq[1]), __fadd_rn(sq[2], sq[3])),
+                                   __fadd_rn(__fadd_rn(sq[4], sq[5]), __fadd_rn(sq[6], sq[7])));
+        const float y = __fsub_rn(s8, comp);
+        const float t = __fadd_rn(sum, y);
+        comp = __fsub_rn(__fsub_rn(t, sum), y);
+        sum = t;
+        k += step_k;
+        j += step_j;
+        if (j >= shard_vec) {
+            j -= shard_vec;
+            ++k;
+        }
+    }
+    const double b = block_sum(static_cast<double>(sum) - static_cast<double>(comp));
+    if (threadIdx.x == 0) partials[blockIdx.x] = (accumulate ? partials[blockIdx.x] : 0.0) + b;
+}
+
 // y = rank; each warp counts the rank's non-finite bf16 values (all exponent
 // bits set) in its vectors and adds its count once.  Integer counts: the
 // result does not depend on the order of the additions.
@@ -127,6 +184,31 @@ int grad_sqnorm(int32_t n_ranks, int64_t n_elems, const uint16_t* const* grads, 
     return cuda_status(cudaGetLastError());
 }
 
+int grad_reduce_sqnorm(int32_t n_ranks, int64_t n_elems, const uint16_t* const* grads,
+                       float* const* grad_shard, int32_t accumulate, double* scratch,
+                       int64_t scratch_bytes, cudaStream_t stream)
+{
+    if (n_ranks < 1 || n_ranks > ZERO_MAX_RANKS || n_elems <= 0 ||
+        n_elems % (8 * static_cast<int64_t>(n_ranks)) != 0 || !scratch ||
+        scratch_bytes < kNormScratchBytes)
+        return ZERO_EINVAL;
+    int rc = check_table(grads, n_ranks);
+    if (rc != ZERO_OK) return rc;
+    if ((rc = check_table(grad_shard, n_ranks)) != ZERO_OK) return rc;
+    if (!aligned16(scratch)) return ZERO_EALIGN;
+    ReduceTable T = {};
+    for (int32_t r = 0; r < n_ranks; ++r) {
+        T.g[r] = reinterpret_cast<const uint4*>(grads[r]);
+        T.out[r] = reinterpret_cast<float4*>(grad_shard[r]);
+    }
+    const int64_t shard_vec = n_elems / n_ranks / 8;
+    const StrideSplit sp = split_stride(static_cast<int64_t>(kNormBlocks) * kNormThreads, shard_vec);
+    const float inv_n = static_cast<float>(1.0 / static_cast<double>(n_ranks));
+    grad_reduce_sqnorm_kernel<<<kNormBlocks, kNormThreads, 0, stream>>>(
+        T, n_ranks, n_elems / 8, shard_vec, sp.k, sp.j, inv_n, accumulate ? 1 : 0, scratch);
+    return cuda_status(cudaGetLastError());
+}
+
 int clip_coef(const double* scratch, int64_t scratch_bytes, double max_norm, float* norm_coef,
               cudaStream_t stream)
 {
@@ -158,6 +240,15 @@ extern "C" int zero_grad_sqnorm(int32_t n_ranks, int64_t n_elems, const uint16_t
                                 cudaStream_t stream)
 {
     return grad_sqnorm(n_ranks, n_elems, grads, accumulate, scratch, scratch_bytes, stream);
+}
+
+extern "C" int zero_grad_reduce_sqnorm(int32_t n_ranks, int64_t n_elems,
+                                       const uint16_t* const* grads, float* const* grad_shard,
+                                       int32_t accumulate, double* scratch, int64_t scratch_bytes,
+                                       cudaStream_t stream)
+{
+    return grad_reduce_sqnorm(n_ranks, n_elems, grads, grad_shard, accumulate, scratch,
+                              scratch_bytes, stream);
 }
 
 extern "C" int zero_clip_coef(const double* scratch, int64_t scratch_bytes, double max_norm,

@@ -75,7 +75,10 @@ __device__ __forceinline__ void adamw(float g, float& w, float& m, float& v,
 // kAcc: the last micro-batch of ZeRO-2 gradient accumulation; the gradient is
 // (a[k] + this micro-batch's mean) * (1/m), a[k] holding the earlier ones.
 // kF32: the rank gradients are fp32 (T.g holds float4 pointers).
-template <bool kClip, bool kAcc, bool kF32 = false>
+// kG32: the mean gradient is already reduced: read g from the owner's fp32
+// gradient shard T.a[k] (written by zero_grad_reduce_sqnorm) instead of the
+// N rank gradients.
+template <bool kClip, bool kAcc, bool kF32 = false, bool kG32 = false>
 __global__ void __launch_bounds__(kBlock, kMinBlocksPerSM)
 fused_step_kernel(const __grid_constant__ Tables T, const StepScalars s, const Range R,
                   const float* __restrict__ clip)
@@ -107,7 +110,11 @@ fused_step_kernel(const __grid_constant__ Tables T, const StepScalars s, const R
 
         // reduce-scatter: fp32 sum from +0 over ranks 0..N-1, in order
         float acc[8];
-        if (kF32)
+        if (kG32) {
+            const float4 g0 = dev::ld_stream(T.a[k] + 2 * j), g1 = dev::ld_stream(T.a[k] + 2 * j + 1);
+            acc[0] = g0.x; acc[1] = g0.y; acc[2] = g0.z; acc[3] = g0.w;
+            acc[4] = g1.x; acc[5] = g1.y; acc[6] = g1.z; acc[7] = g1.w;
+        } else if (kF32)
             dev::sum_ranks_f32<kRankBatch / 2>(reinterpret_cast<const float4* const*>(T.g), N, q,
                                                acc);
         else
@@ -124,7 +131,7 @@ fused_step_kernel(const __grid_constant__ Tables T, const StepScalars s, const R
         float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-            float g = __fmul_rn(acc[e], s.inv_n);
+            float g = kG32 ? acc[e] : __fmul_rn(acc[e], s.inv_n);
             if (kAcc) g = __fmul_rn(__fadd_rn(prior[e], g), R.inv_m);
             if (kClip) g = __fmul_rn(g, coef);
             adamw(g, w[e], m[e], v[e], s);
@@ -263,7 +270,7 @@ void log_capture(const void* func, int blocks, const Tables& T, const StepScalar
 // serialization, so it may begin while the previous kernel on the stream (the
 // previous chunk or bucket of the same call, which touches other elements)
 // finishes.
-template <bool kClip, bool kAcc, bool kF32>
+template <bool kClip, bool kAcc, bool kF32, bool kG32 = false>
 cudaError_t launch_fused(int blocks, cudaStream_t stream, bool chained, const Tables& T,
                          const StepScalars& s, const Range& R, const float* clip)
 {
@@ -278,18 +285,29 @@ cudaError_t launch_fused(int blocks, cudaStream_t stream, bool chained, const Ta
     cfg.attrs = attr;
     cfg.numAttrs = chained ? 1 : 0;
     const cudaError_t e =
-        cudaLaunchKernelEx(&cfg, fused_step_kernel<kClip, kAcc, kF32>, T, s, R, clip);
+        cudaLaunchKernelEx(&cfg, fused_step_kernel<kClip, kAcc, kF32, kG32>, T, s, R, clip);
     if (e == cudaSuccess)
-        log_capture(reinterpret_cast<const void*>(fused_step_kernel<kClip, kAcc, kF32>), blocks, T,
-                    s, R, clip, stream);
+        log_capture(reinterpret_cast<const void*>(fused_step_kernel<kClip, kAcc, kF32, kG32>),
+                    blocks, T, s, R, clip, stream);
     return e;
 }
 
 // One launch over the vectors [q0, q1).
 int launch_range(const Tables& T, const StepScalars& s, int64_t q0, int64_t q1, int64_t shard_vec,
                  int32_t n_ranks, const float* clip, cudaStream_t stream, float inv_m, bool f32,
-                 bool chained)
+                 bool chained, bool g32)
 {
+    if (g32) { // the reduced fp32 gradient shard, optionally clipped
+        const void* k = clip ? reinterpret_cast<const void*>(fused_step_kernel<true, false, false, true>)
+                             : reinterpret_cast<const void*>(fused_step_kernel<false, false, false, true>);
+        int blocks = 0;
+        const Range R = make_range(k, q0, q1, shard_vec, n_ranks, &blocks);
+        if (blocks <= 0) return ZERO_ECUDA;
+        return cuda_status(clip ? launch_fused<true, false, false, true>(blocks, stream, chained, T,
+                                                                         s, R, clip)
+                                : launch_fused<false, false, false, true>(blocks, stream, chained,
+                                                                          T, s, R, nullptr));
+    }
     if (f32) { // fp32 gradients: no clipping or accumulation variant
         int blocks = 0;
         const Range R = make_range(reinterpret_cast<const void*>(fused_step_kernel<false, false, true>),
@@ -334,12 +352,12 @@ int launch_range(const Tables& T, const StepScalars& s, int64_t q0, int64_t q1, 
 // same step).
 int launch(const Tables& T, const StepScalars& s, int64_t q0, int64_t q1, int64_t shard_vec,
            int32_t n_ranks, const float* clip, cudaStream_t stream, float inv_m = 0.0f,
-           bool f32 = false, bool chained = false)
+           bool f32 = false, bool chained = false, bool g32 = false)
 {
     for (int64_t a = q0; a < q1; a += kChunkVec) {
         const int64_t b = q1 - a > kChunkVec ? a + kChunkVec : q1;
         const int rc = launch_range(T, s, a, b, shard_vec, n_ranks, clip, stream, inv_m, f32,
-                                    chained || a > q0);
+                                    chained || a > q0, g32);
         if (rc != ZERO_OK) return rc;
     }
     return ZERO_OK;
@@ -359,8 +377,10 @@ int check_state_tables(int32_t n, const uint16_t* const* grads, float* const* ma
 int step_stage12(int32_t stage, int32_t n_ranks, int64_t n_padded, const void* const* grads,
                  float* const* master, float* const* m, float* const* v, uint16_t* params_bf16,
                  const zero_hparams_t* hp, int64_t bucket_elems, const float* clip,
-                 cudaStream_t stream, bool f32 = false)
+                 cudaStream_t stream, bool f32 = false, bool g32 = false)
 {
+    // g32: `grads` holds the n_ranks fp32 gradient shards (S each) of the
+    // reduced mean gradient instead of the rank gradients.
     if ((stage != 1 && stage != 2) || n_ranks < 1 || n_ranks > ZERO_MAX_RANKS ||
         n_padded <= 0 || n_padded % (8 * static_cast<int64_t>(n_ranks)) != 0 ||
         bucket_elems < 0 || bucket_elems % 8 != 0 || !valid_hparams(hp) || !params_bf16)
@@ -372,7 +392,10 @@ int step_stage12(int32_t stage, int32_t n_ranks, int64_t n_padded, const void* c
     const int64_t S = n_padded / n_ranks;
     Tables T = {};
     for (int32_t r = 0; r < n_ranks; ++r) {
-        T.g[r] = reinterpret_cast<const uint4*>(grads[r]);
+        if (g32)
+            T.a[r] = reinterpret_cast<float4*>(const_cast<void*>(grads[r]));
+        else
+            T.g[r] = reinterpret_cast<const uint4*>(grads[r]);
         T.w[r] = reinterpret_cast<float4*>(master[r]);
         T.m[r] = reinterpret_cast<float4*>(m[r]);
         T.v[r] = reinterpret_cast<float4*>(v[r]);
@@ -386,7 +409,8 @@ int step_stage12(int32_t stage, int32_t n_ranks, int64_t n_padded, const void* c
     // Buckets after the first are chained to the one before (disjoint elements).
     for (int64_t q0 = 0; q0 < nvec; q0 += bucket_vec) {
         const int64_t q1 = q0 + bucket_vec < nvec ? q0 + bucket_vec : nvec;
-        if ((rc = launch(T, s, q0, q1, shard_vec, n_ranks, clip, stream, 0.0f, f32, q0 > 0)) != ZERO_OK)
+        if ((rc = launch(T, s, q0, q1, shard_vec, n_ranks, clip, stream, 0.0f, f32, q0 > 0,
+                         g32)) != ZERO_OK)
             return rc;
     }
     return ZERO_OK;
@@ -470,6 +494,8 @@ int preload_fused_kernels()
         reinterpret_cast<const void*>(fused_step_kernel<false, true, false>),
         reinterpret_cast<const void*>(fused_step_kernel<true, true, false>),
         reinterpret_cast<const void*>(fused_step_kernel<false, false, true>),
+        reinterpret_cast<const void*>(fused_step_kernel<true, false, false, true>),
+        reinterpret_cast<const void*>(fused_step_kernel<false, false, false, true>),
     };
     for (const void* k : kernels)
         if (persistent_blocks(k, kBlock, 0) <= 0) return ZERO_ECUDA;
@@ -500,6 +526,21 @@ extern "C" int zero_step_stage12_clip(int32_t stage, int32_t n_ranks, int64_t n_
     if (rc != ZERO_OK) return rc;
     return step_stage12(stage, n_ranks, n_padded, reinterpret_cast<const void* const*>(grads),
                         master, m, v, params_bf16, hp, bucket_elems, norm_coef, stream);
+}
+
+extern "C" int zero_step_stage12_reduced(int32_t stage, int32_t n_ranks, int64_t n_padded,
+                                         const float* const* grad_shard, float* const* master,
+                                         float* const* m, float* const* v,
+                                         uint16_t* params_bf16, const zero_hparams_t* hp,
+                                         int64_t bucket_elems, const float* norm_coef,
+                                         cudaStream_t stream)
+{
+    if (norm_coef) {
+        const int rc = check_clip(norm_coef);
+        if (rc != ZERO_OK) return rc;
+    }
+    return step_stage12(stage, n_ranks, n_padded, reinterpret_cast<const void* const*>(grad_shard),
+                        master, m, v, params_bf16, hp, bucket_elems, norm_coef, stream, false, true);
 }
 
 extern "C" int zero3_reduce_scatter_unit(const zero_unit_t* unit, int32_t n_ranks,

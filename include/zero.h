@@ -295,6 +295,40 @@ int zero3_reduce_scatter_unit_clip(const zero_unit_t* unit, int32_t n_ranks,
                                    uint16_t* const* shard_bf16, const zero_hparams_t* hp,
                                    const float* norm_coef, cudaStream_t stream);
 
+/* The clipped ZeRO-1/2 step in two passes that keep the reduce-scatter's
+ * output, FSDP's fp32 gradient shard ([DZF] "How FSDP implements ZeRO-3",
+ * step 1: each rank keeps an fp32 shard of the gradient; [DZF] "7. Common
+ * mistakes": the global norm needs every shard before any update).
+ *
+ * zero_grad_reduce_sqnorm -- zero_grad_sqnorm that also stores each element's
+ * mean gradient g[i] = fp32 rank-order mean of grads[r][i] (the fused step's
+ * own g) to its owner's shard: grad_shard[k][i - k*S], k = i / S.  The
+ * partials equal zero_grad_sqnorm's bit for bit.
+ *   n_elems      multiple of 8*n_ranks; S = n_elems / n_ranks
+ *   grad_shard   n_ranks device pointers, each S fp32 (written)
+ *   other arguments as zero_grad_sqnorm
+ *
+ * zero_step_stage12_reduced -- zero_step_stage12 (or, with norm_coef, the
+ * clipped step) that reads g from grad_shard instead of reducing the rank
+ * gradients: the same bits as zero_step_stage12 / zero_step_stage12_clip on
+ * the gradients that filled the shard.
+ *   grad_shard   n_ranks device pointers, each S fp32 (read only)
+ *   norm_coef    NULL (no clipping) or the device float[2] of zero_clip_coef
+ *
+ * HBM bytes per parameter of a clipped step: 2N + 4 for the norm pass and
+ * 30 for the update = 2N + 34, against 4N + 26 for zero_grad_sqnorm +
+ * zero_step_stage12_clip (50 against 58 at N = 8).  The price is the fp32
+ * shard: 4 bytes per parameter of device memory.
+ * ZERO_EINVAL / ZERO_EALIGN / ZERO_ECUDA. */
+int zero_grad_reduce_sqnorm(int32_t n_ranks, int64_t n_elems, const uint16_t* const* grads,
+                            float* const* grad_shard, int32_t accumulate, double* scratch,
+                            int64_t scratch_bytes, cudaStream_t stream);
+int zero_step_stage12_reduced(int32_t stage, int32_t n_ranks, int64_t n_padded,
+                              const float* const* grad_shard, float* const* master,
+                              float* const* m, float* const* v, uint16_t* params_bf16,
+                              const zero_hparams_t* hp, int64_t bucket_elems,
+                              const float* norm_coef, cudaStream_t stream);
+
 /* zero_clip_coef_units_noalloc -- the same global-norm clip coefficient as
  * zero_grad_sqnorm over each unit followed by zero_clip_coef, for callers that
  * cannot allocate device memory (code running inside another framework whose

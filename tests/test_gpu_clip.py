@@ -224,3 +224,68 @@ def test_nonfinite_counts_match_oracle(orc):
     ref = sum(orc.grad_nonfinite(np.ascontiguousarray(host[:, u.offset:u.offset + u.n_padded]))
               for u in units)
     np.testing.assert_array_equal(counts.cpu().numpy().astype(np.uint32), ref)
+
+
+@pytest.mark.parametrize("stage,N,P,bucket,max_norm", [(1, 2, 2**20, 0, 1e-3), (2, 8, 300_001, 104, 2e-3),
+                                                       (1, 64, 2**16 + 37, 0, 1e-4),
+                                                       (1, 4, 2 * B.ZERO_CHUNK_ELEMS + 1000, 0, 1e-3),
+                                                       (1, 8, 300_001, 0, None)])
+def test_reduced_gradient_shard_path_equals_the_one_pass_path(orc, stage, N, P, bucket, max_norm):
+    """zero_grad_reduce_sqnorm + zero_step_stage12_reduced (the update reads the
+    fp32 gradient shard the norm pass wrote) gives the same bits as
+    zero_grad_sqnorm + zero_step_stage12_clip (the update reduces the rank
+    gradients again), clipped or not; the shard holds the oracle's rank-order
+    mean gradient."""
+    T, seed = 4, 12
+    (u,), _ = B.zero_layout([P], N)
+    S = u.shard_len
+
+    def state():
+        w = H.Guarded(N, S, torch.float32)
+        B.zero_gen_master(seed, H.SIGMA_W, [u], w.rows)
+        return (w, H.Guarded(N, S, torch.float32).zero_(), H.Guarded(N, S, torch.float32).zero_(),
+                H.Guarded(1, u.n_padded, torch.int16))
+
+    a, b = state(), state()
+    grads = H.Guarded(N, u.n_padded, torch.int16)
+    shard = H.Guarded(N, S, torch.float32)
+    sa, sb, na, nb = _scratch(), _scratch(), _norm_coef(), _norm_coef()
+    for t in range(1, T + 1):
+        B.zero_gen_grads_unit(seed, t, H.SIGMA_G, 1, u, grads.rows)
+        if max_norm is None:
+            B.zero_step_stage12(stage, grads.rows, a[0].rows, a[1].rows, a[2].rows, a[3].rows[0],
+                                H.hp(t), bucket)
+            B.zero_grad_reduce_sqnorm(grads.rows, shard.rows, sb)
+            B.zero_step_stage12_reduced(stage, shard.rows, b[0].rows, b[1].rows, b[2].rows,
+                                        b[3].rows[0], H.hp(t), None, bucket)
+        else:
+            B.zero_grad_sqnorm(grads.rows, sa)
+            B.zero_clip_coef(sa, max_norm, na)
+            B.zero_step_stage12_clip(stage, grads.rows, a[0].rows, a[1].rows, a[2].rows,
+                                     a[3].rows[0], H.hp(t), na, bucket)
+            B.zero_grad_reduce_sqnorm(grads.rows, shard.rows, sb)
+            B.zero_clip_coef(sb, max_norm, nb)
+            B.zero_step_stage12_reduced(stage, shard.rows, b[0].rows, b[1].rows, b[2].rows,
+                                        b[3].rows[0], H.hp(t), nb, bucket)
+    torch.cuda.synchronize()
+    for x in a + b + (grads, shard):
+        x.check()
+    for x, y, name in zip(a, b, ("master", "m", "v", "params")):
+        H.assert_bitwise(y.numpy(), x.numpy(), name)
+    H.assert_bitwise(sb.cpu().numpy(), (sa if max_norm is not None else sb).cpu().numpy(), "partials")
+    if max_norm is not None:
+        H.assert_bitwise(nb.cpu().numpy(), na.cpu().numpy(), "norm and coefficient")
+        assert float(na[1]) < 1  # clipping was active
+    # the shard holds the last step's mean gradient, owner by owner
+    (ou,), _ = orc.layout([P], N)
+    g_last = orc.gen_grads_unit(seed, T, H.SIGMA_G, 1, ou, N)
+    rng = np.random.default_rng(N)
+    idx = np.unique(np.concatenate([rng.integers(0, u.n_padded, 2000),
+                                    [0, S - 1, S, u.n_padded - 1, min(P, u.n_padded - 1)]]))
+    sh = shard.numpy()
+    inv_n = np.float32(1.0 / N)
+    for i in idx:
+        want = np.float32(orc.reduce_mean(g_last, int(i), inv_n))
+        got = sh[i // S][i % S]
+        assert got.view(np.uint32) == want.view(np.uint32), (int(i), got, want)
+    H.free()

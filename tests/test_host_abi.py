@@ -241,6 +241,26 @@ def test_zero3_graph_rejects_before_capture(B):
     assert B.lib.zero3_graph_destroy(None) == B.ZERO_OK
 
 
+@host_only
+def test_reduced_gradient_calls_reject_before_launch(B):
+    hp = B.hparams()
+    g, gs = _table(A16[:4]), _table(A16[4:8])
+    scratch, nbytes = C.c_void_p(0x900000), B.zero_clip_scratch_bytes()
+    call = B.lib.zero_grad_reduce_sqnorm
+    assert call(4, 1000, g, gs, 0, scratch, nbytes, None) == B.ZERO_EINVAL       # not a multiple of 8N
+    assert call(0, 1024, g, gs, 0, scratch, nbytes, None) == B.ZERO_EINVAL
+    assert call(4, 1024, g, None, 0, scratch, nbytes, None) == B.ZERO_EINVAL
+    assert call(4, 1024, g, gs, 0, scratch, nbytes - 8, None) == B.ZERO_EINVAL  # scratch too small
+    assert call(4, 1024, g, _table(A16[4:7] + [A16[7] + 4]), 0, scratch, nbytes, None) == B.ZERO_EALIGN
+    step = B.lib.zero_step_stage12_reduced
+    w, m, v = _table(A16[8:12]), _table(A16[12:16]), _table(A16[16:20])
+    p = C.c_void_p(0xA00000)
+    assert step(3, 4, 1024, gs, w, m, v, p, C.byref(hp), 0, None, None) == B.ZERO_EINVAL
+    assert step(1, 4, 1000, gs, w, m, v, p, C.byref(hp), 0, None, None) == B.ZERO_EINVAL
+    assert step(1, 4, 1024, None, w, m, v, p, C.byref(hp), 0, None, None) == B.ZERO_EINVAL
+    assert step(1, 4, 1024, gs, w, m, v, p, C.byref(hp), 0, C.c_void_p(0xB00004), None) == B.ZERO_EALIGN
+
+
 def test_zero3_plan_rejects(B):
     ops = (B.zero_op_t * 10)()
     n = C.c_int32()
