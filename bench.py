@@ -460,7 +460,7 @@ def run_gpu(args):
     if not args.headline_only:
         result.update(sub_legs())
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(args.workload, steps=20)
+        result["cpu_baseline"] = cpu_baseline(args.workload, steps=100)
     if world > 1:
         torch.distributed.destroy_process_group()
     return result if rank == 0 else None
