@@ -522,6 +522,29 @@ def run_gpu_zero3(args, torch, Z, world, rank, dev):
         graph_step()
     ms_g, _ = timed(torch, world, dev, stream, graph_step, K)
     graph.close()
+    # global-norm clipping over all units: the norm pre-pass and the clipped updates
+    # from the rank gradients (4N + 34 B/param with the gathers), and through the
+    # fp32 gradient shard the norm pass keeps (2N + 42 B/param)
+    scratch = torch.empty(Z.zero_clip_scratch_bytes() // 8, dtype=torch.float64, device=dev)
+    norm_coef = torch.empty(4, dtype=torch.float32, device=dev)[:2]
+    Kc = max(1, min(K, 50))
+
+    def clip_step(c):
+        t[0] += 1
+        Z.zero3_step(units, grads, master, m, v, shards, full[0], full[1],
+                     Z.hparams(**HP, step=t[0]), grads_resident=True, clip=c,
+                     main_stream=stream, side_stream=side)
+
+    clip_g = Z.clip_args(1.0, scratch, norm_coef)
+    for _ in range(min(W, 2)):
+        clip_step(clip_g)
+    ms_cg, _ = timed(torch, world, dev, stream, lambda: clip_step(clip_g), Kc)
+    grad_shard = torch.empty_like(master)
+    clip_s = Z.clip_args(1.0, scratch, norm_coef, grad_shard=grad_shard)
+    for _ in range(min(W, 2)):
+        clip_step(clip_s)
+    ms_cs, _ = timed(torch, world, dev, stream, lambda: clip_step(clip_s), Kc)
+    del clip_s, grad_shard
     # reshard_after_forward = False: one gather per unit, full weights kept (2 B/param)
     kept = torch.empty(total, dtype=torch.int16, device=dev)
 
@@ -613,6 +636,18 @@ def run_gpu_zero3(args, torch, Z, world, rank, dev):
                   "hbm_gbs": (fused_bytes + gather_bytes) * K / (ms_g * 1e-3) / 1e9,
                   "note": "zero3_graph: the same step captured once as a CUDA graph, replayed "
                           "per step with that step's AdamW scalars"},
+        "clip": {"ms_per_step": ms_cg / Kc, "steps": Kc,
+                 "value": world * P * Kc / (ms_cg * 1e-3),
+                 "hbm_gbs": (4 * N + 34) * total * Kc / (ms_cg * 1e-3) / 1e9,
+                 "bytes_per_step": (4 * N + 34) * total,
+                 "note": "global-norm clipping over all units (max_norm 1.0): norm pre-pass over "
+                         "the rank gradients, clipped updates reducing them again"},
+        "clip_shard": {"ms_per_step": ms_cs / Kc, "steps": Kc,
+                       "value": world * P * Kc / (ms_cs * 1e-3),
+                       "hbm_gbs": (2 * N + 42) * total * Kc / (ms_cs * 1e-3) / 1e9,
+                       "bytes_per_step": (2 * N + 42) * total,
+                       "note": "the same clipped step through the fp32 gradient shard the norm "
+                               "pass keeps; the same bits as `clip`"},
         "no_reshard": {"ms_per_step": ms_k / Kk, "steps": Kk,
                        "hbm_gbs": (fused_bytes + 4 * total) * Kk / (ms_k * 1e-3) / 1e9,
                        "note": "reshard_after_forward=False: one gather per unit per step, every "

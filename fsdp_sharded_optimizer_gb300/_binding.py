@@ -74,15 +74,20 @@ OP_NAMES = {1: "record", 2: "wait", 3: "gather", 4: "reduce_scatter", 5: "regen"
 
 class zero_clip_t(C.Structure):
     _fields_ = [("max_norm", C.c_double), ("scratch", C.c_void_p), ("scratch_bytes", C.c_int64),
-                ("norm_coef", C.c_void_p)]
+                ("norm_coef", C.c_void_p), ("grad_shard", C.c_void_p)]
 
 
-def clip_args(max_norm, scratch, norm_coef):
+def clip_args(max_norm, scratch, norm_coef, grad_shard=None):
     """A zero_clip_t for zero3_step from device tensors (scratch of
-    zero_clip_scratch_bytes(), norm_coef of 2 floats)."""
+    zero_clip_scratch_bytes(), norm_coef of 2 floats, and optionally the fp32
+    gradient shard storage, N x S_total, that the norm pass fills and the
+    updates read)."""
+    table = _rows(grad_shard, 4, "grad_shard")[0] if grad_shard is not None else None
     c = zero_clip_t(float(max_norm), scratch.data_ptr(), scratch.numel() * scratch.element_size(),
-                    norm_coef.data_ptr())
-    c.tensors = (scratch, norm_coef)  # kept alive with the struct (a graph holds their addresses)
+                    norm_coef.data_ptr(),
+                    C.cast(table, C.c_void_p).value if table is not None else None)
+    # kept alive with the struct (a graph holds these addresses)
+    c.tensors = (scratch, norm_coef, grad_shard, table)
     return c
 
 # name -> (restype, argtypes); the same names as include/zero.h
@@ -100,6 +105,7 @@ SIGNATURES = {
                                          _P]),
     "zero3_reduce_scatter_unit_clip": (C.c_int, [_P, _I32, _P, _P, _P, _P, _P, _P, _P, _P]),
     "zero_grad_reduce_sqnorm": (C.c_int, [_I32, _I64, _P, _P, _I32, _P, _I64, _P]),
+    "zero3_update_unit_reduced": (C.c_int, [_P, _I32, _P, _P, _P, _P, _P, _P, _P, _P]),
     "zero_step_stage12_reduced": (C.c_int, [_I32, _I32, _I64, _P, _P, _P, _P, _P, _P, _I64, _P,
                                             _P]),
     "zero_clip_coef_units_noalloc": (C.c_int, [_P, _I32, _I32, _P, _F64, _P, _P, _P]),
@@ -295,6 +301,20 @@ def zero_step_stage12_reduced(stage, grad_shard, master, m, v, params_bf16, hp, 
     _check("zero_step_stage12_reduced", lib.zero_step_stage12_reduced(
         stage, len(rows), params_bf16.numel(), gs, w, mm, vv, _dev(params_bf16, 2, "params_bf16"),
         C.byref(hp), int(bucket_elems),
+        _dev(norm_coef, 4, "norm_coef") if norm_coef is not None else None, _stream(stream)))
+
+
+def zero3_update_unit_reduced(unit, grad_shard, master, m, v, shard_bf16, hp, norm_coef=None,
+                              stream=None):
+    """One unit's ZeRO-3 update from the fp32 gradient shard storage (N x S_total),
+    clipped by norm_coef when given."""
+    gs, rows = _rows(grad_shard, 4, "grad_shard")
+    w, _ = _rows(master, 4, "master")
+    mm, _ = _rows(m, 4, "m")
+    vv, _ = _rows(v, 4, "v")
+    sh, _ = _rows(shard_bf16, 2, "shard_bf16")
+    _check("zero3_update_unit_reduced", lib.zero3_update_unit_reduced(
+        C.byref(unit), len(rows), gs, w, mm, vv, sh, C.byref(hp),
         _dev(norm_coef, 4, "norm_coef") if norm_coef is not None else None, _stream(stream)))
 
 

@@ -416,9 +416,13 @@ int step_stage12(int32_t stage, int32_t n_ranks, int64_t n_padded, const void* c
     return ZERO_OK;
 }
 
+// g32: unit_grads holds each rank's fp32 gradient-shard storage of all units
+// (laid out like master; this unit at shard_offset) instead of the unit's
+// rank gradients.
 int rs_unit(const zero_unit_t* unit, int32_t n_ranks, const void* const* unit_grads,
             float* const* master, float* const* m, float* const* v, uint16_t* const* shard_bf16,
-            const zero_hparams_t* hp, const float* clip, cudaStream_t stream, bool f32 = false)
+            const zero_hparams_t* hp, const float* clip, cudaStream_t stream, bool f32 = false,
+            bool g32 = false)
 {
     if (!unit || n_ranks < 1 || n_ranks > ZERO_MAX_RANKS || unit->n_padded <= 0 ||
         unit->shard_len <= 0 || unit->shard_len % 8 != 0 ||
@@ -433,7 +437,11 @@ int rs_unit(const zero_unit_t* unit, int32_t n_ranks, const void* const* unit_gr
     const int64_t off = unit->shard_offset;
     Tables T = {};
     for (int32_t r = 0; r < n_ranks; ++r) {
-        T.g[r] = reinterpret_cast<const uint4*>(unit_grads[r]);
+        if (g32)
+            T.a[r] = reinterpret_cast<float4*>(
+                const_cast<float*>(static_cast<const float*>(unit_grads[r])) + off);
+        else
+            T.g[r] = reinterpret_cast<const uint4*>(unit_grads[r]);
         T.w[r] = reinterpret_cast<float4*>(master[r] + off);
         T.m[r] = reinterpret_cast<float4*>(m[r] + off);
         T.v[r] = reinterpret_cast<float4*>(v[r] + off);
@@ -441,7 +449,7 @@ int rs_unit(const zero_unit_t* unit, int32_t n_ranks, const void* const* unit_gr
     }
     const StepScalars s = make_scalars(hp, n_ranks);
     return launch(T, s, 0, unit->n_padded / 8, unit->shard_len / 8, n_ranks, clip, stream, 0.0f,
-                  f32);
+                  f32, false, g32);
 }
 
 int check_clip(const float* norm_coef)
@@ -541,6 +549,20 @@ extern "C" int zero_step_stage12_reduced(int32_t stage, int32_t n_ranks, int64_t
     }
     return step_stage12(stage, n_ranks, n_padded, reinterpret_cast<const void* const*>(grad_shard),
                         master, m, v, params_bf16, hp, bucket_elems, norm_coef, stream, false, true);
+}
+
+extern "C" int zero3_update_unit_reduced(const zero_unit_t* unit, int32_t n_ranks,
+                                         const float* const* grad_shard, float* const* master,
+                                         float* const* m, float* const* v,
+                                         uint16_t* const* shard_bf16, const zero_hparams_t* hp,
+                                         const float* norm_coef, cudaStream_t stream)
+{
+    if (norm_coef) {
+        const int rc = check_clip(norm_coef);
+        if (rc != ZERO_OK) return rc;
+    }
+    return rs_unit(unit, n_ranks, reinterpret_cast<const void* const*>(grad_shard), master, m, v,
+                   shard_bf16, hp, norm_coef, stream, false, true);
 }
 
 extern "C" int zero3_reduce_scatter_unit(const zero_unit_t* unit, int32_t n_ranks,

@@ -193,6 +193,8 @@ extern "C" int zero3_step(const zero_unit_t* units, int32_t n_units, int32_t n_r
             !(clip->max_norm > 0) || !std::isfinite(clip->max_norm))
             return ZERO_EINVAL;
         if (!aligned16(clip->scratch) || !aligned16(clip->norm_coef)) return ZERO_EALIGN;
+        if (clip->grad_shard && (rc = check_table(clip->grad_shard, n_ranks)) != ZERO_OK)
+            return rc;
     }
 
     cudaEvent_t* ev = nullptr;
@@ -231,16 +233,28 @@ extern "C" int zero3_step(const zero_unit_t* units, int32_t n_units, int32_t n_r
             break;
         case ZERO_OP_REDUCE_SCATTER:
             grads_of(op.unit);
-            rc = op.arg ? zero3_reduce_scatter_unit_clip(&units[op.unit], n_ranks, unit_grads,
-                                                         master, m, v, shard_bf16, hp,
-                                                         clip->norm_coef, s)
-                        : zero3_reduce_scatter_unit(&units[op.unit], n_ranks, unit_grads, master,
-                                                    m, v, shard_bf16, hp, s);
+            if (op.arg && clip->grad_shard) // the mean the norm pass kept
+                rc = zero3_update_unit_reduced(&units[op.unit], n_ranks, clip->grad_shard, master,
+                                               m, v, shard_bf16, hp, clip->norm_coef, s);
+            else if (op.arg)
+                rc = zero3_reduce_scatter_unit_clip(&units[op.unit], n_ranks, unit_grads, master,
+                                                    m, v, shard_bf16, hp, clip->norm_coef, s);
+            else
+                rc = zero3_reduce_scatter_unit(&units[op.unit], n_ranks, unit_grads, master, m, v,
+                                               shard_bf16, hp, s);
             break;
         case ZERO_OP_NORM:
             grads_of(op.unit);
-            rc = grad_sqnorm(n_ranks, units[op.unit].n_padded, unit_grads, op.arg, clip->scratch,
-                             clip->scratch_bytes, s);
+            if (clip->grad_shard) {
+                float* unit_shard[ZERO_MAX_RANKS];
+                for (int32_t r = 0; r < n_ranks; ++r)
+                    unit_shard[r] = clip->grad_shard[r] + units[op.unit].shard_offset;
+                rc = grad_reduce_sqnorm(n_ranks, units[op.unit].n_padded, unit_grads, unit_shard,
+                                        op.arg, clip->scratch, clip->scratch_bytes, s);
+            } else {
+                rc = grad_sqnorm(n_ranks, units[op.unit].n_padded, unit_grads, op.arg,
+                                 clip->scratch, clip->scratch_bytes, s);
+            }
             break;
         case ZERO_OP_CLIP_COEF:
             rc = clip_coef(clip->scratch, clip->scratch_bytes, clip->max_norm, clip->norm_coef, s);

@@ -61,6 +61,9 @@ int grad_sqnorm(int32_t n_ranks, int64_t n_elems, const uint16_t* const* grads, 
                 double* scratch, int64_t scratch_bytes, cudaStream_t stream);
 int clip_coef(const double* scratch, int64_t scratch_bytes, double max_norm, float* norm_coef,
               cudaStream_t stream);
+int grad_reduce_sqnorm(int32_t n_ranks, int64_t n_elems, const uint16_t* const* grads,
+                       float* const* grad_shard, int32_t accumulate, double* scratch,
+                       int64_t scratch_bytes, cudaStream_t stream);
 
 // CUDA-graph support (zero3_graph).  Between step_nodes_begin and
 // step_nodes_end, every fused-step launch made on this thread into a stream

@@ -295,6 +295,22 @@ int zero3_reduce_scatter_unit_clip(const zero_unit_t* unit, int32_t n_ranks,
                                    uint16_t* const* shard_bf16, const zero_hparams_t* hp,
                                    const float* norm_coef, cudaStream_t stream);
 
+/* zero3_update_unit_reduced -- zero3_reduce_scatter_unit (or, with norm_coef,
+ * its clipped form) reading the unit's mean gradient from the fp32 gradient
+ * shard that zero_grad_reduce_sqnorm wrote, instead of reducing the rank
+ * gradients: the same bits.
+ *   grad_shard   n_ranks device pointers to each rank's fp32 gradient shard
+ *                storage of all units (laid out like master: this unit at
+ *                unit->shard_offset), read only
+ *   norm_coef    NULL or the device float[2] of zero_clip_coef
+ *   other arguments as zero3_reduce_scatter_unit
+ * 30 bytes per parameter.  ZERO_EINVAL / ZERO_EALIGN / ZERO_ECUDA. */
+int zero3_update_unit_reduced(const zero_unit_t* unit, int32_t n_ranks,
+                              const float* const* grad_shard, float* const* master,
+                              float* const* m, float* const* v, uint16_t* const* shard_bf16,
+                              const zero_hparams_t* hp, const float* norm_coef,
+                              cudaStream_t stream);
+
 /* The clipped ZeRO-1/2 step in two passes that keep the reduce-scatter's
  * output, FSDP's fp32 gradient shard ([DZF] "How FSDP implements ZeRO-3",
  * step 1: each rank keeps an fp32 shard of the gradient; [DZF] "7. Common
@@ -418,12 +434,19 @@ typedef struct {
     int32_t outliers;
 } zero_regen_t;
 
-/* Global-norm clipping inside zero3_step: the buffers of the clipping calls. */
+/* Global-norm clipping inside zero3_step: the buffers of the clipping calls.
+ * grad_shard: NULL, or n_ranks device pointers to each rank's fp32 gradient
+ * shard storage of all units (laid out like master, S_total fp32 each).
+ * With it the norm pre-pass is zero_grad_reduce_sqnorm, storing each unit's
+ * mean gradient there, and each unit's update is zero3_update_unit_reduced,
+ * reading it: 2N + 4 + 30 instead of 2N + 26 + 2N bytes per parameter of
+ * norm pass and update, the same bits. */
 typedef struct {
     double max_norm;
     double* scratch;       /* device, >= zero_clip_scratch_bytes() */
     int64_t scratch_bytes;
     float* norm_coef;      /* device float[2]: norm and coefficient of this step */
+    float* const* grad_shard; /* host table of n_ranks device pointers, or NULL */
 } zero_clip_t;
 
 /* zero3_step -- one whole ZeRO-3 step: executes zero3_plan's operations with
@@ -444,7 +467,9 @@ typedef struct {
  *                    forward to the backward pass), full_b is not used
  *   hp               the step's hyper-parameters (the same t for all units)
  *   clip             NULL, or global-norm clipping over all units (the norm
- *                    pre-pass reads every unit's gradients once more)
+ *                    pre-pass reads every unit's gradients once more; with
+ *                    clip->grad_shard it also keeps their mean, which the
+ *                    updates then read instead of the gradients)
  * The library keeps five timing-free CUDA events per host thread and device
  * (created on first use); no device memory is allocated.  Work is queued
  * asynchronously; on return main_stream carries the end of the step.

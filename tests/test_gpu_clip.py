@@ -289,3 +289,51 @@ def test_reduced_gradient_shard_path_equals_the_one_pass_path(orc, stage, N, P, 
         got = sh[i // S][i % S]
         assert got.view(np.uint32) == want.view(np.uint32), (int(i), got, want)
     H.free()
+
+
+@pytest.mark.parametrize("resident", [True, False])
+def test_clipped_zero3_step_through_the_gradient_shard_is_bitwise_the_same(resident):
+    """zero3_step with clip.grad_shard (the norm pass keeps each unit's mean
+    gradient in the fp32 shard and the updates read it) equals zero3_step
+    clipping from the rank gradients, bit for bit, with resident or
+    regenerated gradients and a unit of three chunks."""
+    N, T, seed, max_norm = 4, 3, 5, 1e-3
+    sizes = [70_000, 333, 2 * B.ZERO_CHUNK_ELEMS + 4096, 64, 90_001]
+    units, total = B.zero_layout(sizes, N)
+    shard_total = total // N
+    max_unit = max(u.n_padded for u in units)
+
+    def state():
+        w = H.Guarded(N, shard_total, torch.float32)
+        sh = H.Guarded(N, shard_total, torch.int16)
+        B.zero_gen_master(seed, H.SIGMA_W, units, w.rows)
+        for k in range(N):
+            B.zero_cast_bf16(w.rows[k], sh.rows[k])
+        return (w, H.Guarded(N, shard_total, torch.float32).zero_(),
+                H.Guarded(N, shard_total, torch.float32).zero_(), sh)
+
+    a, b = state(), state()
+    grads = H.Guarded(N, total if resident else max_unit, torch.int16)
+    fa, fb = H.Guarded(1, max_unit, torch.int16), H.Guarded(1, max_unit, torch.int16)
+    gshard = H.Guarded(N, shard_total, torch.float32)
+    ca = B.clip_args(max_norm, _scratch(), _norm_coef())
+    cb = B.clip_args(max_norm, _scratch(), _norm_coef(), grad_shard=gshard.rows)
+    side = torch.cuda.Stream()
+    regen = None if resident else B.zero_regen_t(seed, H.SIGMA_G, 1)
+    for t in range(1, T + 1):
+        if resident:
+            for u in units:
+                B.zero_gen_grads_unit(seed, t, H.SIGMA_G, 1, u,
+                                      [r[u.offset:u.offset + u.n_padded] for r in grads.rows])
+        for st, c in ((a, ca), (b, cb)):
+            B.zero3_step(units, grads.rows, st[0].rows, st[1].rows, st[2].rows, st[3].rows,
+                         fa.rows[0], fb.rows[0], H.hp(t), grads_resident=resident, regen=regen,
+                         clip=c, side_stream=side)
+    torch.cuda.synchronize()
+    for x in a + b + (grads, fa, fb, gshard):
+        x.check()
+    for x, y, name in zip(a, b, ("master", "m", "v", "shards")):
+        H.assert_bitwise(y.numpy(), x.numpy(), name)
+    H.assert_bitwise(cb.tensors[1].cpu().numpy(), ca.tensors[1].cpu().numpy(), "norm and coefficient")
+    assert float(ca.tensors[1][1]) < 1  # the clipping was active
+    H.free()

@@ -228,3 +228,36 @@ def test_graph_at_gpt2_zero3_size_equals_streamed_step():
     assert not torch.equal(a[0], state()[0])  # the steps did change the weights
     del a, b, grads
     H.free()
+
+
+def test_graph_of_the_clipped_step_through_the_gradient_shard():
+    """A graph captured from zero3_step clipping through the fp32 gradient shard
+    replays the streamed step (clipping from the rank gradients) bit for bit."""
+    N, T, seed = 8, 3, 17
+    units, total = B.zero_layout(SIZES, N)
+    a = _state(units, total, N, seed)
+    b = _state(units, total, N, seed)
+    gshard = H.Guarded(N, total // N, torch.float32)
+    mk = lambda shard: B.clip_args(
+        2e-3, torch.empty(B.zero_clip_scratch_bytes() // 8, dtype=torch.float64, device="cuda"),
+        torch.empty(4, dtype=torch.float32, device="cuda")[:2], grad_shard=shard)
+    ca, cb = mk(None), mk(gshard.rows)
+    cap, side_a, side_b = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    g = B.zero3_graph_create(units, b[4].rows, b[0].rows, b[1].rows, b[2].rows, b[3].rows,
+                             b[5].rows[0], b[6].rows[0], H.hp(1), cap, side_b, clip=cb)
+    try:
+        for t in range(1, T + 1):
+            _fill_grads(units, a[4], seed, t)
+            _fill_grads(units, b[4], seed, t)
+            B.zero3_step(units, a[4].rows, a[0].rows, a[1].rows, a[2].rows, a[3].rows,
+                         a[5].rows[0], a[6].rows[0], H.hp(t), clip=ca, side_stream=side_a)
+            g.launch(H.hp(t))
+        torch.cuda.synchronize()
+    finally:
+        g.close()
+    for x, y, name in zip(a[:4], b[:4], ("master", "m", "v", "shards")):
+        H.assert_bitwise(y.numpy(), x.numpy(), name)
+    assert float(ca.tensors[1][1]) < 1
+    gshard.check()
+    H.free()

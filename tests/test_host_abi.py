@@ -261,6 +261,22 @@ def test_reduced_gradient_calls_reject_before_launch(B):
     assert step(1, 4, 1024, gs, w, m, v, p, C.byref(hp), 0, C.c_void_p(0xB00004), None) == B.ZERO_EALIGN
 
 
+@host_only
+def test_zero3_step_checks_the_gradient_shard_table(B):
+    units, _ = B.zero_layout([1000, 64], 4)
+    arr = (B.zero_unit_t * 2)(*units)
+    hp = B.hparams()
+    t = _table(A16[:4])
+    fa, fb = C.c_void_p(0x900000), C.c_void_p(0xA00000)
+    s1, s2 = C.c_void_p(0x1000), C.c_void_p(0x2000)
+    nbytes = B.zero_clip_scratch_bytes()
+    for table, want in ((_table(A16[4:7] + [A16[7] + 4]), B.ZERO_EALIGN),
+                        (_table(A16[4:7] + [0]), B.ZERO_EINVAL)):
+        clip = B.zero_clip_t(1.0, 0xB00000, nbytes, 0xC00000, C.cast(table, C.c_void_p).value)
+        assert B.lib.zero3_step(arr, 2, 4, t, 1, t, t, t, t, fa, fb, C.byref(hp), None,
+                                C.byref(clip), 1, s1, s2) == want
+
+
 def test_zero3_plan_rejects(B):
     ops = (B.zero_op_t * 10)()
     n = C.c_int32()
