@@ -337,3 +337,56 @@ def test_clipped_zero3_step_through_the_gradient_shard_is_bitwise_the_same(resid
     H.assert_bitwise(cb.tensors[1].cpu().numpy(), ca.tensors[1].cpu().numpy(), "norm and coefficient")
     assert float(ca.tensors[1][1]) < 1  # the clipping was active
     H.free()
+
+
+@pytest.mark.parametrize("clipped", [False, True])
+def test_unit_update_from_the_gradient_shard_equals_the_unit_reduce_scatter(clipped):
+    """The public unit-level calls on their own: zero_grad_reduce_sqnorm on one
+    unit's gradients into that unit's region of the shard storage, then
+    zero3_update_unit_reduced, equal zero3_reduce_scatter_unit (or its clipped
+    form) bit for bit, unit by unit in reverse order."""
+    N, T, seed, max_norm = 8, 2, 21, 1e-3
+    sizes = [1000, 333_333, 64, 70_001]
+    units, total = B.zero_layout(sizes, N)
+    S = total // N
+
+    def state():
+        w = H.Guarded(N, S, torch.float32)
+        sh = H.Guarded(N, S, torch.int16)
+        B.zero_gen_master(seed, H.SIGMA_W, units, w.rows)
+        for k in range(N):
+            B.zero_cast_bf16(w.rows[k], sh.rows[k])
+        return (w, H.Guarded(N, S, torch.float32).zero_(), H.Guarded(N, S, torch.float32).zero_(), sh)
+
+    a, b = state(), state()
+    gshard = H.Guarded(N, S, torch.float32)
+    sa, sb, na, nb = _scratch(), _scratch(), _norm_coef(), _norm_coef()
+    grads = [H.Guarded(N, u.n_padded, torch.int16) for u in units]
+    for t in range(1, T + 1):
+        for u, g in zip(units, grads):
+            B.zero_gen_grads_unit(seed, t, H.SIGMA_G, 1, u, g.rows)
+        for i, (u, g) in enumerate(zip(units, grads)):
+            B.zero_grad_sqnorm(g.rows, sa, accumulate=i > 0)
+            B.zero_grad_reduce_sqnorm(g.rows, [r[u.shard_offset:u.shard_offset + u.shard_len]
+                                               for r in gshard.rows], sb, accumulate=i > 0)
+        if clipped:
+            B.zero_clip_coef(sa, max_norm, na)
+            B.zero_clip_coef(sb, max_norm, nb)
+        for u, g in zip(reversed(units), reversed(grads)):
+            if clipped:
+                B.zero3_reduce_scatter_unit_clip(u, g.rows, a[0].rows, a[1].rows, a[2].rows,
+                                                 a[3].rows, H.hp(t), na)
+            else:
+                B.zero3_reduce_scatter_unit(u, g.rows, a[0].rows, a[1].rows, a[2].rows, a[3].rows,
+                                            H.hp(t))
+            B.zero3_update_unit_reduced(u, gshard.rows, b[0].rows, b[1].rows, b[2].rows,
+                                        b[3].rows, H.hp(t), nb if clipped else None)
+    torch.cuda.synchronize()
+    for x in a + b + (gshard,) + tuple(grads):
+        x.check()
+    for x, y, name in zip(a, b, ("master", "m", "v", "shards")):
+        H.assert_bitwise(y.numpy(), x.numpy(), name)
+    H.assert_bitwise(sb.cpu().numpy(), sa.cpu().numpy(), "partials")
+    if clipped:
+        assert float(na[1]) < 1
+    H.free()
