@@ -6,9 +6,11 @@ Bound on the norm: the GPU sums squares pairwise in fp32 with Kahan
 compensation and in fp64 across threads and blocks (relative error of the
 squared norm < 4e-7, of the norm < 2e-7, plus one fp32 rounding of the
 stored norm); the oracle sums in fp64.  Both are checked within 1e-6
-relative.  The clipped updates differ from the oracle only through the
-coefficient (1 fp32 ulp at most) and are checked with the acceptance
-tolerance (1e-6 relative on master/m/v, 1 bf16 ulp on weights)."""
+relative.  The coefficient can therefore differ from the oracle's in its
+last bits, and where m cancels over steps even that difference exceeds a
+per-element relative tolerance.  So the clipped updates are checked bit for
+bit against the oracle's update given the coefficient the GPU computed, and
+the coefficient itself against the oracle's within 2e-6 relative."""
 import numpy as np
 import pytest
 import torch
@@ -96,7 +98,7 @@ def test_clipped_zero12_step_matches_oracle(orc, stage, N, P, bucket, max_norm):
     (ou,), _ = orc.layout([P], N)
     rw = orc.gen_master(seed, H.SIGMA_W, [ou], N)
     rm, rv = np.zeros_like(rw), np.zeros_like(rw)
-    rp = np.zeros(ou.n_padded, np.uint16)
+    rs = np.zeros_like(rw, dtype=np.uint16)  # rank k's bf16 shard = params[kS:(k+1)S]
     scratch, nc = _scratch(), _norm_coef()
     clipped = 0
     for t in range(1, T + 1):
@@ -106,17 +108,23 @@ def test_clipped_zero12_step_matches_oracle(orc, stage, N, P, bucket, max_norm):
         B.zero_step_stage12_clip(stage, grads.rows, master.rows, m.rows, v.rows, params.rows[0],
                                  H.hp(t), nc, bucket)
         g = orc.gen_grads_unit(seed, t, H.SIGMA_G, 1, ou, N)
-        norm, coef = orc.zero12_step_clip(stage, g, rw, rm, rv, rp, orc.hparams(**H.HP, step=t),
-                                          max_norm, bucket)
+        # the norm within its bound of the oracle's fp64 norm; the update bit for
+        # bit given the coefficient the GPU computed (the norm's last bits
+        # depend on the GPU's fixed-grid summation order, not the method)
         got = nc.cpu().numpy()
+        coef, norm = orc.clip_coef(orc.grad_sumsq(g), max_norm)
         assert abs(float(got[0]) - norm) <= 1e-6 * norm
+        assert abs(float(got[1]) - float(coef)) <= 2e-6 * float(coef)
+        orc.zero3_reduce_scatter_unit_coef(ou, g, rw, rm, rv, rs, orc.hparams(**H.HP, step=t),
+                                           got[1])
         clipped += coef < 1
     assert clipped == T  # every step actually clipped
     torch.cuda.synchronize()
     for b_ in (grads, master, m, v, params):
         b_.check()
-    H.assert_within_tolerance((master.numpy(), m.numpy(), v.numpy()), (rw, rm, rv),
-                              params.numpy()[0], rp)
+    for name, g_, r_ in (("master", master.numpy(), rw), ("m", m.numpy(), rm), ("v", v.numpy(), rv),
+                         ("params", params.numpy()[0], rs.reshape(-1))):
+        H.assert_bitwise(g_, r_, name)
     assert not params.numpy()[0][P:].any()
 
 
@@ -171,16 +179,18 @@ def test_clipped_zero3_native_step_matches_oracle(orc):
                      regen=B.zero_regen_t(seed, H.SIGMA_G, 1), clip=clip, side_stream=side)
         gs = [orc.gen_grads_unit(seed, t, H.SIGMA_G, 1, ou, N) for ou in ounits]
         coef, norm = orc.clip_coef(sum(orc.grad_sumsq(g) for g in gs), max_norm)
-        for ou, g in zip(reversed(ounits), reversed(gs)):
-            orc.zero3_reduce_scatter_unit_coef(ou, g, rw, rm, rv, rs, orc.hparams(**H.HP, step=t),
-                                               coef)
         got = nc.cpu().numpy()
         assert abs(float(got[0]) - norm) <= 1e-6 * norm and coef < 1
+        # the updates bit for bit given the GPU's coefficient
+        for ou, g in zip(reversed(ounits), reversed(gs)):
+            orc.zero3_reduce_scatter_unit_coef(ou, g, rw, rm, rv, rs, orc.hparams(**H.HP, step=t),
+                                               got[1])
     torch.cuda.synchronize()
     for b_ in (master, m, v, shards, grads, fa, fb):
         b_.check()
-    H.assert_within_tolerance((master.numpy(), m.numpy(), v.numpy()), (rw, rm, rv),
-                              shards.numpy(), rs)
+    for name, g_, r_ in (("master", master.numpy(), rw), ("m", m.numpy(), rm), ("v", v.numpy(), rv),
+                         ("shards", shards.numpy(), rs)):
+        H.assert_bitwise(g_, r_, name)
 
 
 def test_gpt2_shaped_norm_full_size(orc):
