@@ -31,7 +31,7 @@ CPU, against a recording or oracle backend in the tests.
 class CudaBackend:
     """The library's kernels on two torch CUDA streams (main + gather side stream)."""
 
-    def __init__(self, n_ranks, shards, master, m, v, device=None, time_calls=False):
+    def __init__(self, n_ranks, shards, master, m, v, device=None):
         import torch
 
         from . import _binding as B
@@ -42,20 +42,6 @@ class CudaBackend:
         dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
         self.main = torch.cuda.current_stream(dev)
         self.side = torch.cuda.Stream(device=dev)
-        # optional CUDA-event pairs around every call: (kind, unit index, start, end)
-        self.time_calls = time_calls
-        self.timings = []
-
-    def _timed(self, kind, ui, stream, fn):
-        if not self.time_calls:
-            fn()
-            return
-        a = self._torch.cuda.Event(enable_timing=True)
-        b = self._torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        fn()
-        b.record(stream)
-        self.timings.append((kind, ui, a, b))
 
     # stream/event primitives
     def event(self):
@@ -69,14 +55,11 @@ class CudaBackend:
 
     # the two collectives
     def gather(self, ui, unit, full, stream):
-        self._timed("gather", ui, stream,
-                    lambda: self._B.zero3_gather_unit(unit, self.shards, full, stream=stream))
+        self._B.zero3_gather_unit(unit, self.shards, full, stream=stream)
 
     def reduce_scatter(self, ui, unit, grads, hp, stream):
-        self._timed("reduce_scatter", ui, stream,
-                    lambda: self._B.zero3_reduce_scatter_unit(unit, grads, self.master, self.m,
-                                                              self.v, self.shards, hp,
-                                                              stream=stream))
+        self._B.zero3_reduce_scatter_unit(unit, grads, self.master, self.m, self.v, self.shards,
+                                          hp, stream=stream)
 
 
 class Zero3Schedule:
