@@ -121,6 +121,10 @@ SIGNATURES = {
     # regen, clip, reshard_after_forward, main stream, side stream
     "zero3_step": (C.c_int, [_P, _I32, _I32, _P, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I32,
                              _P, _P]),
+    # units, n_units, n_ranks, grads, master, m, v, shards, full_a, full_b, hp,
+    # reshard_after_forward, main stream, side stream
+    "zero3_step_f32grads": (C.c_int, [_P, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _I32, _P,
+                                      _P]),
     # units, n_units, n_ranks, grads, master, m, v, shards, full_a, full_b, hp, clip,
     # reshard_after_forward, capture stream, side stream, out handle
     "zero3_graph_create": (C.c_int, [_P, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I32,
@@ -435,6 +439,21 @@ def zero3_step(units, grads, master, m, v, shard_bf16, full_a, full_b, hp, grads
         _dev(full_a, 2, "full_a"), _dev(full_b, 2, "full_b") if full_b is not None else None,
         C.byref(hp),
         C.byref(regen) if regen is not None else None, C.byref(clip) if clip is not None else None,
+        1 if reshard_after_forward else 0, _stream(main_stream), _stream(side_stream)))
+
+
+def zero3_step_f32grads(units, grads, master, m, v, shard_bf16, full_a, full_b, hp,
+                        reshard_after_forward=True, main_stream=None, side_stream=None):
+    """zero3_step with fp32 rank gradients (every unit's, concatenated per rank)."""
+    g, rows = _rows(grads, 4, "grads")
+    w, _ = _rows(master, 4, "master")
+    mm, _ = _rows(m, 4, "m")
+    vv, _ = _rows(v, 4, "v")
+    s, _ = _rows(shard_bf16, 2, "shard_bf16")
+    arr = (zero_unit_t * len(units))(*units)
+    _check("zero3_step_f32grads", lib.zero3_step_f32grads(
+        arr, len(units), len(rows), g, w, mm, vv, s, _dev(full_a, 2, "full_a"),
+        _dev(full_b, 2, "full_b") if full_b is not None else None, C.byref(hp),
         1 if reshard_after_forward else 0, _stream(main_stream), _stream(side_stream)))
 
 

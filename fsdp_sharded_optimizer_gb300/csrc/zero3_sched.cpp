@@ -166,13 +166,15 @@ extern "C" int zero3_plan(int32_t n_units, int32_t regen, int32_t clip,
     return ZERO_OK;
 }
 
-extern "C" int zero3_step(const zero_unit_t* units, int32_t n_units, int32_t n_ranks,
-                          const uint16_t* const* grads, int32_t grads_resident,
-                          float* const* master, float* const* m, float* const* v,
-                          uint16_t* const* shard_bf16, uint16_t* full_a, uint16_t* full_b,
-                          const zero_hparams_t* hp, const zero_regen_t* regen,
-                          const zero_clip_t* clip, int32_t reshard_after_forward,
-                          cudaStream_t main_stream, cudaStream_t side_stream)
+namespace {
+
+// The step of zero3_step / zero3_step_f32grads.  f32: the rank gradients are
+// fp32 (grads holds float pointers; no regeneration, no clipping).
+int run_step(const zero_unit_t* units, int32_t n_units, int32_t n_ranks, const void* const* grads,
+             bool f32, int32_t grads_resident, float* const* master, float* const* m,
+             float* const* v, uint16_t* const* shard_bf16, uint16_t* full_a, uint16_t* full_b,
+             const zero_hparams_t* hp, const zero_regen_t* regen, const zero_clip_t* clip,
+             int32_t reshard_after_forward, cudaStream_t main_stream, cudaStream_t side_stream)
 {
     const bool reshard = reshard_after_forward != 0;
     if (!units || n_units < 1 || n_ranks < 1 || n_ranks > ZERO_MAX_RANKS || !valid_hparams(hp) ||
@@ -204,11 +206,16 @@ extern "C" int zero3_step(const zero_unit_t* units, int32_t n_units, int32_t n_r
 
     const uint16_t* unit_grads[ZERO_MAX_RANKS];
     uint16_t* unit_grads_w[ZERO_MAX_RANKS];
+    const float* unit_grads_f32[ZERO_MAX_RANKS];
     auto grads_of = [&](int32_t u) {
         const int64_t off = grads_resident ? units[u].offset : 0;
         for (int32_t r = 0; r < n_ranks; ++r) {
-            unit_grads[r] = grads[r] + off;
-            unit_grads_w[r] = const_cast<uint16_t*>(grads[r]) + off;
+            if (f32) {
+                unit_grads_f32[r] = static_cast<const float*>(grads[r]) + off;
+            } else {
+                unit_grads[r] = static_cast<const uint16_t*>(grads[r]) + off;
+                unit_grads_w[r] = const_cast<uint16_t*>(unit_grads[r]);
+            }
         }
     };
     for (const zero_op_t& op : plan.ops) {
@@ -233,7 +240,10 @@ extern "C" int zero3_step(const zero_unit_t* units, int32_t n_units, int32_t n_r
             break;
         case ZERO_OP_REDUCE_SCATTER:
             grads_of(op.unit);
-            if (op.arg && clip->grad_shard) // the mean the norm pass kept
+            if (f32)
+                rc = zero3_reduce_scatter_unit_f32grads(&units[op.unit], n_ranks, unit_grads_f32,
+                                                        master, m, v, shard_bf16, hp, s);
+            else if (op.arg && clip->grad_shard) // the mean the norm pass kept
                 rc = zero3_update_unit_reduced(&units[op.unit], n_ranks, clip->grad_shard, master,
                                                m, v, shard_bf16, hp, clip->norm_coef, s);
             else if (op.arg)
@@ -266,4 +276,31 @@ extern "C" int zero3_step(const zero_unit_t* units, int32_t n_units, int32_t n_r
         if (rc != ZERO_OK) return rc;
     }
     return ZERO_OK;
+}
+
+} // namespace
+
+extern "C" int zero3_step(const zero_unit_t* units, int32_t n_units, int32_t n_ranks,
+                          const uint16_t* const* grads, int32_t grads_resident,
+                          float* const* master, float* const* m, float* const* v,
+                          uint16_t* const* shard_bf16, uint16_t* full_a, uint16_t* full_b,
+                          const zero_hparams_t* hp, const zero_regen_t* regen,
+                          const zero_clip_t* clip, int32_t reshard_after_forward,
+                          cudaStream_t main_stream, cudaStream_t side_stream)
+{
+    return run_step(units, n_units, n_ranks, reinterpret_cast<const void* const*>(grads), false,
+                    grads_resident, master, m, v, shard_bf16, full_a, full_b, hp, regen, clip,
+                    reshard_after_forward, main_stream, side_stream);
+}
+
+extern "C" int zero3_step_f32grads(const zero_unit_t* units, int32_t n_units, int32_t n_ranks,
+                                   const float* const* grads, float* const* master,
+                                   float* const* m, float* const* v, uint16_t* const* shard_bf16,
+                                   uint16_t* full_a, uint16_t* full_b, const zero_hparams_t* hp,
+                                   int32_t reshard_after_forward, cudaStream_t main_stream,
+                                   cudaStream_t side_stream)
+{
+    return run_step(units, n_units, n_ranks, reinterpret_cast<const void* const*>(grads), true, 1,
+                    master, m, v, shard_bf16, full_a, full_b, hp, nullptr, nullptr,
+                    reshard_after_forward, main_stream, side_stream);
 }

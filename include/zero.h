@@ -482,6 +482,20 @@ int zero3_step(const zero_unit_t* units, int32_t n_units, int32_t n_ranks,
                const zero_clip_t* clip, int32_t reshard_after_forward,
                cudaStream_t main_stream, cudaStream_t side_stream);
 
+/* zero3_step_f32grads -- zero3_step with fp32 rank gradients ([DZF] "6. Where
+ * it shows up": Llama 3 reduce-scatters fp32 gradients): each unit's
+ * reduce-scatter is zero3_reduce_scatter_unit_f32grads.  grads holds n_ranks
+ * device pointers, each rank's fp32 gradients of every unit concatenated
+ * (unit u at units[u].offset); no regeneration, no clipping.  Other
+ * arguments as zero3_step.  26 + 4N bytes per parameter for the updates.
+ * ZERO_EINVAL / ZERO_EALIGN / ZERO_ECUDA. */
+int zero3_step_f32grads(const zero_unit_t* units, int32_t n_units, int32_t n_ranks,
+                        const float* const* grads, float* const* master, float* const* m,
+                        float* const* v, uint16_t* const* shard_bf16, uint16_t* full_a,
+                        uint16_t* full_b, const zero_hparams_t* hp,
+                        int32_t reshard_after_forward, cudaStream_t main_stream,
+                        cudaStream_t side_stream);
+
 /* zero3_graph -- the zero3_step of one fixed set of buffers captured once as a
  * CUDA graph and replayed once per step.  The operations, their order and
  * their results are zero3_step's; a replay gives the GPU the step's whole

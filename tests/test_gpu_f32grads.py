@@ -77,3 +77,47 @@ def test_f32_grads_zero3_unit_matches_oracle(orc):
     for name, g_, r_ in (("shards", shards.numpy(), rs), ("master", master.numpy(), rw),
                          ("m", m.numpy(), rm), ("v", v.numpy(), rv)):
         H.assert_bitwise(g_, r_, name)
+
+
+@pytest.mark.parametrize("reshard", [True, False])
+def test_native_zero3_step_with_f32_grads_matches_oracle(orc, reshard):
+    """zero3_step_f32grads (the native scheduler with fp32 rank gradients) equals
+    the oracle's fp32-gradient unit reduce-scatters, unit by unit in reverse
+    order, bit for bit over several steps."""
+    N, sizes, T, seed = 4, [70_000, 333, 200_000, 64, 90_001], 3, 6
+    units, total = B.zero_layout(sizes, N)
+    ounits, _ = orc.layout(sizes, N)
+    S = total // N
+    master = H.Guarded(N, S, torch.float32)
+    m = H.Guarded(N, S, torch.float32).zero_()
+    v = H.Guarded(N, S, torch.float32).zero_()
+    shards = H.Guarded(N, S, torch.int16)
+    B.zero_gen_master(seed, H.SIGMA_W, units, master.rows)
+    for k in range(N):
+        B.zero_cast_bf16(master.rows[k], shards.rows[k])
+    grads = H.Guarded(N, total, torch.float32)
+    max_unit = max(u.n_padded for u in units)
+    fa = H.Guarded(1, max_unit if reshard else total, torch.int16)
+    fb = H.Guarded(1, max_unit, torch.int16)
+    rw = orc.gen_master(seed, H.SIGMA_W, ounits, N)
+    rm, rv = np.zeros_like(rw), np.zeros_like(rw)
+    rs = orc.bf16_rne(rw)
+    side = torch.cuda.Stream()
+    for t in range(1, T + 1):
+        for u in units:
+            B.zero_gen_grads_unit_f32(seed, t, H.SIGMA_G, 1, u,
+                                      [r[u.offset:u.offset + u.n_padded] for r in grads.rows])
+        B.zero3_step_f32grads(units, grads.rows, master.rows, m.rows, v.rows, shards.rows,
+                              fa.rows[0], fb.rows[0] if reshard else None, H.hp(t),
+                              reshard_after_forward=reshard, side_stream=side)
+        for ou in reversed(ounits):
+            g = orc.gen_grads_unit_f32(seed, t, H.SIGMA_G, 1, ou, N)
+            orc.zero3_reduce_scatter_unit_f32grads(ou, g, rw, rm, rv, rs,
+                                                   orc.hparams(**H.HP, step=t))
+    torch.cuda.synchronize()
+    for b_ in (master, m, v, shards, grads, fa, fb):
+        b_.check()
+    for name, g_, r_ in (("master", master.numpy(), rw), ("m", m.numpy(), rm),
+                         ("v", v.numpy(), rv), ("shards", shards.numpy(), rs)):
+        H.assert_bitwise(g_, r_, name)
+    H.free()

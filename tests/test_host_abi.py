@@ -277,6 +277,23 @@ def test_zero3_step_checks_the_gradient_shard_table(B):
                                 C.byref(clip), 1, s1, s2) == want
 
 
+@host_only
+def test_zero3_step_f32grads_rejects_before_launch(B):
+    units, _ = B.zero_layout([1000, 64], 4)
+    arr = (B.zero_unit_t * 2)(*units)
+    hp = B.hparams()
+    t = _table(A16[:4])
+    fa, fb = C.c_void_p(0x900000), C.c_void_p(0xA00000)
+    s1, s2 = C.c_void_p(0x1000), C.c_void_p(0x2000)
+    call = B.lib.zero3_step_f32grads
+    assert call(arr, 0, 4, t, t, t, t, t, fa, fb, C.byref(hp), 1, s1, s2) == B.ZERO_EINVAL
+    assert call(arr, 2, 4, None, t, t, t, t, fa, fb, C.byref(hp), 1, s1, s2) == B.ZERO_EINVAL
+    assert call(arr, 2, 4, t, t, t, t, t, fa, fa, C.byref(hp), 1, s1, s2) == B.ZERO_EINVAL
+    assert call(arr, 2, 4, t, t, t, t, t, fa, fb, C.byref(hp), 1, s1, s1) == B.ZERO_EINVAL
+    odd = _table(A16[:3] + [A16[3] + 4])
+    assert call(arr, 2, 4, odd, t, t, t, t, fa, fb, C.byref(hp), 1, s1, s2) == B.ZERO_EALIGN
+
+
 def test_zero3_plan_rejects(B):
     ops = (B.zero_op_t * 10)()
     n = C.c_int32()
