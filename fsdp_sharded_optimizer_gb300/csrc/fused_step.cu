@@ -32,6 +32,15 @@ constexpr int kRankBatch = 8; // gradient loads issued together before summing
 // loads in flight to reach the HBM roofline (measured at N_d = 2..64 on GB300:
 // +12 % at N_d = 8 over two blocks per SM; four blocks per SM spill and lose).
 constexpr int kMinBlocksPerSM = 3;
+// Up to kSmallRanks ranks a thread has few gradient vectors to hold, and the
+// bytes in flight per thread fall (112 B at N_d = 1 against 224 B at 8): four
+// resident blocks per SM (a 64-register cap) and loads in batches of 4 ranks
+// win there (GB300, GPT-2 buffer: N_d = 1 5,719 -> 6,478 GB/s, N_d = 2
+// 5,876 -> 6,507, N_d = 4 6,260 -> 6,477; at N_d = 8 the three-block kernel
+// stays ahead, 6,912 against 6,768).
+constexpr int kSmallRanks = 4;
+constexpr int kMinBlocksPerSMSmall = 4;
+constexpr int kRankBatchSmall = 4;
 
 // Per-rank device pointers, passed by value in the kernel's parameter space
 // (5 x 64 x 8 B = 2.5 KB).  o[k] points at rank k's output slice: the
@@ -78,8 +87,9 @@ __device__ __forceinline__ void adamw(float g, float& w, float& m, float& v,
 // kG32: the mean gradient is already reduced: read g from the owner's fp32
 // gradient shard T.a[k] (written by zero_grad_reduce_sqnorm) instead of the
 // N rank gradients.
-template <bool kClip, bool kAcc, bool kF32 = false, bool kG32 = false>
-__global__ void __launch_bounds__(kBlock, kMinBlocksPerSM)
+// kSmall: the launch shape for up to kSmallRanks ranks (see kSmallRanks).
+template <bool kClip, bool kAcc, bool kF32 = false, bool kG32 = false, bool kSmall = false>
+__global__ void __launch_bounds__(kBlock, kSmall ? kMinBlocksPerSMSmall : kMinBlocksPerSM)
 fused_step_kernel(const __grid_constant__ Tables T, const StepScalars s, const Range R,
                   const float* __restrict__ clip)
 {
@@ -118,7 +128,7 @@ fused_step_kernel(const __grid_constant__ Tables T, const StepScalars s, const R
             dev::sum_ranks_f32<kRankBatch / 2>(reinterpret_cast<const float4* const*>(T.g), N, q,
                                                acc);
         else
-            dev::sum_ranks<kRankBatch>(T.g, N, q, acc);
+            dev::sum_ranks<kSmall ? kRankBatchSmall : kRankBatch>(T.g, N, q, acc);
         float prior[8];
         if (kAcc) {
             const float4 a0 = dev::ld_stream(T.a[k] + 2 * j), a1 = dev::ld_stream(T.a[k] + 2 * j + 1);
@@ -159,8 +169,9 @@ fused_step_kernel(const __grid_constant__ Tables T, const StepScalars s, const R
 }
 
 // ZeRO-2 accumulation of micro-batches 1..m-1: a[k] = (first ? +0 : a[k]) + mean.
-template <bool kFirst>
-__global__ void __launch_bounds__(kBlock, kMinBlocksPerSM)
+// kSmall: the launch shape for up to kSmallRanks ranks, as fused_step_kernel.
+template <bool kFirst, bool kSmall = false>
+__global__ void __launch_bounds__(kBlock, kSmall ? kMinBlocksPerSMSmall : kMinBlocksPerSM)
 accumulate_kernel(const __grid_constant__ Tables T, const float inv_n, const Range R)
 {
     // chained like fused_step_kernel (the same two instructions, the same reasons)
@@ -172,7 +183,7 @@ accumulate_kernel(const __grid_constant__ Tables T, const float inv_n, const Ran
     int64_t j = q - k * R.shard_vec;
     for (; q < R.q1; q += stride) {
         float acc[8];
-        dev::sum_ranks<kRankBatch>(T.g, R.n_ranks, q, acc);
+        dev::sum_ranks<kSmall ? kRankBatchSmall : kRankBatch>(T.g, R.n_ranks, q, acc);
         float4* ap = T.a[k] + 2 * j;
         float prior[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         if (!kFirst) {
@@ -270,7 +281,7 @@ void log_capture(const void* func, int blocks, const Tables& T, const StepScalar
 // serialization, so it may begin while the previous kernel on the stream (the
 // previous chunk or bucket of the same call, which touches other elements)
 // finishes.
-template <bool kClip, bool kAcc, bool kF32, bool kG32 = false>
+template <bool kClip, bool kAcc, bool kF32, bool kG32 = false, bool kSmall = false>
 cudaError_t launch_fused(int blocks, cudaStream_t stream, bool chained, const Tables& T,
                          const StepScalars& s, const Range& R, const float* clip)
 {
@@ -284,12 +295,43 @@ cudaError_t launch_fused(int blocks, cudaStream_t stream, bool chained, const Ta
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = chained ? 1 : 0;
-    const cudaError_t e =
-        cudaLaunchKernelEx(&cfg, fused_step_kernel<kClip, kAcc, kF32, kG32>, T, s, R, clip);
+    const cudaError_t e = cudaLaunchKernelEx(
+        &cfg, fused_step_kernel<kClip, kAcc, kF32, kG32, kSmall>, T, s, R, clip);
     if (e == cudaSuccess)
-        log_capture(reinterpret_cast<const void*>(fused_step_kernel<kClip, kAcc, kF32, kG32>),
-                    blocks, T, s, R, clip, stream);
+        log_capture(
+            reinterpret_cast<const void*>(fused_step_kernel<kClip, kAcc, kF32, kG32, kSmall>),
+            blocks, T, s, R, clip, stream);
     return e;
+}
+
+// One launch of a bf16-gradient variant (plain, clipped, accumulated) in the
+// launch shape kSmall selects.
+template <bool kSmall>
+int launch_bf16(const Tables& T, const StepScalars& s, int64_t q0, int64_t q1, int64_t shard_vec,
+                int32_t n_ranks, const float* clip, cudaStream_t stream, float inv_m, bool chained)
+{
+    const bool acc = inv_m != 0.0f;
+    const void* kernel =
+        clip ? (acc ? reinterpret_cast<const void*>(fused_step_kernel<true, true, false, false, kSmall>)
+                    : reinterpret_cast<const void*>(fused_step_kernel<true, false, false, false, kSmall>))
+             : (acc ? reinterpret_cast<const void*>(fused_step_kernel<false, true, false, false, kSmall>)
+                    : reinterpret_cast<const void*>(fused_step_kernel<false, false, false, false, kSmall>));
+    int blocks = 0;
+    Range R = make_range(kernel, q0, q1, shard_vec, n_ranks, &blocks);
+    if (blocks <= 0) return ZERO_ECUDA;
+    R.inv_m = acc ? inv_m : 1.0f;
+    cudaError_t e;
+    if (clip && acc)
+        e = launch_fused<true, true, false, false, kSmall>(blocks, stream, chained, T, s, R, clip);
+    else if (clip)
+        e = launch_fused<true, false, false, false, kSmall>(blocks, stream, chained, T, s, R, clip);
+    else if (acc)
+        e = launch_fused<false, true, false, false, kSmall>(blocks, stream, chained, T, s, R,
+                                                            nullptr);
+    else
+        e = launch_fused<false, false, false, false, kSmall>(blocks, stream, chained, T, s, R,
+                                                             nullptr);
+    return cuda_status(e);
 }
 
 // One launch over the vectors [q0, q1).
@@ -315,26 +357,9 @@ int launch_range(const Tables& T, const StepScalars& s, int64_t q0, int64_t q1, 
         if (blocks <= 0) return ZERO_ECUDA;
         return cuda_status(launch_fused<false, false, true>(blocks, stream, chained, T, s, R, nullptr));
     }
-    const bool acc = inv_m != 0.0f;
-    const void* kernel =
-        clip ? (acc ? reinterpret_cast<const void*>(fused_step_kernel<true, true>)
-                    : reinterpret_cast<const void*>(fused_step_kernel<true, false>))
-             : (acc ? reinterpret_cast<const void*>(fused_step_kernel<false, true>)
-                    : reinterpret_cast<const void*>(fused_step_kernel<false, false>));
-    int blocks = 0;
-    Range R = make_range(kernel, q0, q1, shard_vec, n_ranks, &blocks);
-    if (blocks <= 0) return ZERO_ECUDA;
-    R.inv_m = acc ? inv_m : 1.0f;
-    cudaError_t e;
-    if (clip && acc)
-        e = launch_fused<true, true, false>(blocks, stream, chained, T, s, R, clip);
-    else if (clip)
-        e = launch_fused<true, false, false>(blocks, stream, chained, T, s, R, clip);
-    else if (acc)
-        e = launch_fused<false, true, false>(blocks, stream, chained, T, s, R, nullptr);
-    else
-        e = launch_fused<false, false, false>(blocks, stream, chained, T, s, R, nullptr);
-    return cuda_status(e);
+    return n_ranks <= kSmallRanks
+               ? launch_bf16<true>(T, s, q0, q1, shard_vec, n_ranks, clip, stream, inv_m, chained)
+               : launch_bf16<false>(T, s, q0, q1, shard_vec, n_ranks, clip, stream, inv_m, chained);
 }
 
 // The fused step over the vectors [q0, q1), issued as chunk_count() chained
@@ -504,6 +529,10 @@ int preload_fused_kernels()
         reinterpret_cast<const void*>(fused_step_kernel<false, false, true>),
         reinterpret_cast<const void*>(fused_step_kernel<true, false, false, true>),
         reinterpret_cast<const void*>(fused_step_kernel<false, false, false, true>),
+        reinterpret_cast<const void*>(fused_step_kernel<false, false, false, false, true>),
+        reinterpret_cast<const void*>(fused_step_kernel<true, false, false, false, true>),
+        reinterpret_cast<const void*>(fused_step_kernel<false, true, false, false, true>),
+        reinterpret_cast<const void*>(fused_step_kernel<true, true, false, false, true>),
     };
     for (const void* k : kernels)
         if (persistent_blocks(k, kBlock, 0) <= 0) return ZERO_ECUDA;
@@ -603,8 +632,12 @@ extern "C" int zero2_accumulate(int32_t n_ranks, int64_t n_padded, const uint16_
         T.a[r] = reinterpret_cast<float4*>(grad_acc[r]);
     }
     const int64_t S = n_padded / n_ranks;
-    const void* kernel = first ? reinterpret_cast<const void*>(accumulate_kernel<true>)
-                               : reinterpret_cast<const void*>(accumulate_kernel<false>);
+    const bool small = n_ranks <= kSmallRanks;
+    const void* kernel =
+        small ? (first ? reinterpret_cast<const void*>(accumulate_kernel<true, true>)
+                       : reinterpret_cast<const void*>(accumulate_kernel<false, true>))
+              : (first ? reinterpret_cast<const void*>(accumulate_kernel<true, false>)
+                       : reinterpret_cast<const void*>(accumulate_kernel<false, false>));
     const float inv_n = static_cast<float>(1.0 / static_cast<double>(n_ranks));
     // chained chunks of kChunkVec vectors, as the fused step's launch()
     cudaLaunchAttribute attr[1];
@@ -622,8 +655,11 @@ extern "C" int zero2_accumulate(int32_t n_ranks, int64_t n_padded, const uint16_
         cfg.stream = stream;
         cfg.attrs = attr;
         cfg.numAttrs = a > 0 ? 1 : 0;
-        const cudaError_t e = first ? cudaLaunchKernelEx(&cfg, accumulate_kernel<true>, T, inv_n, R)
-                                    : cudaLaunchKernelEx(&cfg, accumulate_kernel<false>, T, inv_n, R);
+        const cudaError_t e =
+            small ? (first ? cudaLaunchKernelEx(&cfg, accumulate_kernel<true, true>, T, inv_n, R)
+                           : cudaLaunchKernelEx(&cfg, accumulate_kernel<false, true>, T, inv_n, R))
+                  : (first ? cudaLaunchKernelEx(&cfg, accumulate_kernel<true, false>, T, inv_n, R)
+                           : cudaLaunchKernelEx(&cfg, accumulate_kernel<false, false>, T, inv_n, R));
         if (e != cudaSuccess) return cuda_status(e);
     }
     return ZERO_OK;
