@@ -50,30 +50,153 @@ __device__ __forceinline__ double block_sum(double d)
     return total; // valid in thread 0
 }
 
+struct ReduceTable {
+    const uint4* g[ZERO_MAX_RANKS];
+    float4* out[ZERO_MAX_RANKS]; // the owners' fp32 gradient shards (kStore only)
+};
+
+// One vector's share of the squared norm: g = sum * (1/N) for its 8 elements,
+// their squares summed pairwise, the result added to the thread's Kahan sum.
+// Every path below calls it once per vector, in the vectors' order.
+__device__ __forceinline__ void add_squares(const float (&acc)[8], float inv_n, float (&g)[8],
+                                            float& sum, float& comp)
+{
+    float sq[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        g[e] = __fmul_rn(acc[e], inv_n);
+        sq[e] = __fmul_rn(g[e], g[e]);
+    }
+    const float s8 = __fadd_rn(__fadd_rn(__fadd_rn(sq[0], sq[1]), __fadd_rn(sq[2], sq[3])),
+                               __fadd_rn(__fadd_rn(sq[4], sq[5]), __fadd_rn(sq[6], sq[7])));
+    const float y = __fsub_rn(s8, comp);
+    const float t = __fadd_rn(sum, y);
+    comp = __fsub_rn(__fsub_rn(t, sum), y);
+    sum = t;
+}
+
+// The reduce-scatter's sum of one vector from loads already in registers:
+// fp32 from +0 over ranks 0..kN-1 in order, as dev::sum_ranks.
+template <int kN>
+__device__ __forceinline__ void sum_loaded(const uint4 (&G)[kN], float (&acc)[8])
+{
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+#pragma unroll
+    for (int r = 0; r < kN; ++r) {
+        acc[0] = __fadd_rn(acc[0], dev::bf16_lo(G[r].x));
+        acc[1] = __fadd_rn(acc[1], dev::bf16_hi(G[r].x));
+        acc[2] = __fadd_rn(acc[2], dev::bf16_lo(G[r].y));
+        acc[3] = __fadd_rn(acc[3], dev::bf16_hi(G[r].y));
+        acc[4] = __fadd_rn(acc[4], dev::bf16_lo(G[r].z));
+        acc[5] = __fadd_rn(acc[5], dev::bf16_hi(G[r].z));
+        acc[6] = __fadd_rn(acc[6], dev::bf16_lo(G[r].w));
+        acc[7] = __fadd_rn(acc[7], dev::bf16_hi(G[r].w));
+    }
+}
+
+// The norm pass.  Each thread takes the vectors q, q + stride, q + 2*stride,
+// ... (stride = the fixed grid's threads) and adds their squares in that
+// order; the block sums its threads in fp64.
+// kStore: also store each element's mean gradient to its owner's fp32 shard
+// (zero_grad_reduce_sqnorm); (owner, position) advance with the stride split
+// into whole shards (step_k) and a remainder (step_j), as in the fused step.
+// kN: the rank count (1, 2 or 4), known at compile time.  Then a loop trip
+// issues the loads of kU = 8/kN consecutive vectors of the thread before it
+// sums any, so a thread keeps 128 B in flight as at N_d = 8 (with 1 rank and
+// one vector a trip it would keep 16 B).  The sums are the same operations in
+// the same order as with kN = 0 (any count, one vector a trip): the bits do
+// not change.
+template <bool kStore, int kN>
 __global__ void __launch_bounds__(kNormThreads)
-grad_sqnorm_kernel(const __grid_constant__ GradTable T, int n_ranks, int64_t n_vec, float inv_n,
-                   int accumulate, double* __restrict__ partials)
+grad_sqnorm_kernel(const __grid_constant__ ReduceTable T, int n_ranks, int64_t n_vec,
+                   int64_t shard_vec, int64_t step_k, int64_t step_j, float inv_n, int accumulate,
+                   double* __restrict__ partials)
 {
     float sum = 0.0f, comp = 0.0f; // Kahan: true sum ~ sum - comp
-    for (int64_t q = static_cast<int64_t>(blockIdx.x) * kNormThreads + threadIdx.x; q < n_vec;
-         q += static_cast<int64_t>(gridDim.x) * kNormThreads) {
-        float acc[8];
-        dev::sum_ranks<8>(T.g, n_ranks, q, acc);
-        float sq[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const float g = __fmul_rn(acc[e], inv_n);
-            sq[e] = __fmul_rn(g, g);
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kNormThreads;
+    int64_t q = static_cast<int64_t>(blockIdx.x) * kNormThreads + threadIdx.x;
+    int64_t k = 0, j = 0;
+    if (kStore) {
+        k = q / shard_vec;
+        j = q - k * shard_vec;
+    }
+    auto finish = [&](const float (&acc)[8]) {
+        float g[8];
+        add_squares(acc, inv_n, g, sum, comp);
+        if (kStore) {
+            float4* o = T.out[k] + 2 * j;
+            dev::st_stream(o, make_float4(g[0], g[1], g[2], g[3]));
+            dev::st_stream(o + 1, make_float4(g[4], g[5], g[6], g[7]));
+            k += step_k;
+            j += step_j;
+            if (j >= shard_vec) {
+                j -= shard_vec;
+                ++k;
+            }
         }
-        const float s8 = __fadd_rn(__fadd_rn(__fadd_rn(sq[0], sq[1]), __fadd_rn(sq[2], sq[3])),
-                                   __fadd_rn(__fadd_rn(sq[4], sq[5]), __fadd_rn(sq[6], sq[7])));
-        const float y = __fsub_rn(s8, comp);
-        const float t = __fadd_rn(sum, y);
-        comp = __fsub_rn(__fsub_rn(t, sum), y);
-        sum = t;
+    };
+    if constexpr (kN == 0) {
+        for (; q < n_vec; q += stride) {
+            float acc[8];
+            dev::sum_ranks<8>(T.g, n_ranks, q, acc);
+            finish(acc);
+        }
+    } else {
+        constexpr int kU = 8 / kN;
+        for (; q < n_vec; q += kU * stride) {
+            uint4 G[kU][kN];
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int64_t qu = q + u * stride;
+                if (qu < n_vec) {
+#pragma unroll
+                    for (int r = 0; r < kN; ++r) G[u][r] = dev::ld_stream(T.g[r] + qu);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                if (q + u * stride < n_vec) {
+                    float acc[8];
+                    sum_loaded<kN>(G[u], acc);
+                    finish(acc);
+                }
+            }
+        }
     }
     const double b = block_sum(static_cast<double>(sum) - static_cast<double>(comp));
     if (threadIdx.x == 0) partials[blockIdx.x] = (accumulate ? partials[blockIdx.x] : 0.0) + b;
+}
+
+// The unrolled loop for 1, 2 or 4 ranks on the plain pass only.  Measured on
+// GB300 (GPT-2-sized buffer, GB/s, old -> unrolled): N_d = 1 3,177 -> 5,894,
+// N_d = 2 5,385 -> 6,675, N_d = 4 6,823 -> 6,945; N_d = 3 lost 3 % and the
+// pass that stores the shard lost 6-10 % at every N_d <= 4 (its stores come
+// in bursts after the loads), so those keep the one-vector loop.
+template <bool kStore>
+void launch_norm(const ReduceTable& T, int n_ranks, int64_t n_vec, int64_t shard_vec,
+                 int64_t step_k, int64_t step_j, float inv_n, int accumulate, double* partials,
+                 cudaStream_t stream)
+{
+    const int kn = kStore ? 0 : (n_ranks == 1 || n_ranks == 2 || n_ranks == 4 ? n_ranks : 0);
+    switch (kn) {
+    case 1:
+        grad_sqnorm_kernel<false, 1><<<kNormBlocks, kNormThreads, 0, stream>>>(
+            T, n_ranks, n_vec, shard_vec, step_k, step_j, inv_n, accumulate, partials);
+        break;
+    case 2:
+        grad_sqnorm_kernel<false, 2><<<kNormBlocks, kNormThreads, 0, stream>>>(
+            T, n_ranks, n_vec, shard_vec, step_k, step_j, inv_n, accumulate, partials);
+        break;
+    case 4:
+        grad_sqnorm_kernel<false, 4><<<kNormBlocks, kNormThreads, 0, stream>>>(
+            T, n_ranks, n_vec, shard_vec, step_k, step_j, inv_n, accumulate, partials);
+        break;
+    default:
+        grad_sqnorm_kernel<kStore, 0><<<kNormBlocks, kNormThreads, 0, stream>>>(
+            T, n_ranks, n_vec, shard_vec, step_k, step_j, inv_n, accumulate, partials);
+        break;
+    }
 }
 
 __global__ void __launch_bounds__(kNormThreads)
@@ -90,56 +213,6 @@ clip_coef_kernel(const double* __restrict__ partials, int n, double max_norm,
         norm_coef[0] = static_cast<float>(norm);
         norm_coef[1] = static_cast<float>(c);
     }
-}
-
-// The norm pass fused with the reduce-scatter's output.  The same grid, loop
-// order and arithmetic as grad_sqnorm_kernel, so the same partial sums and the
-// same norm, bit for bit; in addition each element's mean gradient
-// g = fp32 sum * (1/N) is stored to its owner's fp32 gradient shard, so the
-// clipped update reads 4 bytes of g instead of the N bf16 gradients again.
-// (owner, position) advance with the stride split into whole shards (step_k)
-// and a remainder (step_j), as in the fused step.
-struct ReduceTable {
-    const uint4* g[ZERO_MAX_RANKS];
-    float4* out[ZERO_MAX_RANKS];
-};
-
-__global__ void __launch_bounds__(kNormThreads)
-grad_reduce_sqnorm_kernel(const __grid_constant__ ReduceTable T, int n_ranks, int64_t n_vec,
-                          int64_t shard_vec, int64_t step_k, int64_t step_j, float inv_n,
-                          int accumulate, double* __restrict__ partials)
-{
-    float sum = 0.0f, comp = 0.0f; // Kahan: true sum ~ sum - comp
-    int64_t q = static_cast<int64_t>(blockIdx.x) * kNormThreads + threadIdx.x;
-    int64_t k = q / shard_vec;
-    int64_t j = q - k * shard_vec;
-    for (; q < n_vec; q += static_cast<int64_t>(gridDim.x) * kNormThreads) {
-        float acc[8];
-        dev::sum_ranks<8>(T.g, n_ranks, q, acc);
-        float g[8], sq[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            g[e] = __fmul_rn(acc[e], inv_n);
-            sq[e] = __fmul_rn(g[e], g[e]);
-        }
-        float4* o = T.out[k] + 2 * j;
-        dev::st_stream(o, make_float4(g[0], g[1], g[2], g[3]));
-        dev::st_stream(o + 1, make_float4(g[4], g[5], g[6], g[7]));
-        const float s8 = __fadd_rn(__fadd_rn(__fadd_rn(sq[0], sq[1]), __fadd_rn(sq[2], sq[3])),
-                                   __fadd_rn(__fadd_rn(sq[4], sq[5]), __fadd_rn(sq[6], sq[7])));
-        const float y = __fsub_rn(s8, comp);
-        const float t = __fadd_rn(sum, y);
-        comp = __fsub_rn(__fsub_rn(t, sum), y);
-        sum = t;
-        k += step_k;
-        j += step_j;
-        if (j >= shard_vec) {
-            j -= shard_vec;
-            ++k;
-        }
-    }
-    const double b = block_sum(static_cast<double>(sum) - static_cast<double>(comp));
-    if (threadIdx.x == 0) partials[blockIdx.x] = (accumulate ? partials[blockIdx.x] : 0.0) + b;
 }
 
 // y = rank; each warp counts the rank's non-finite bf16 values (all exponent
@@ -176,11 +249,11 @@ int grad_sqnorm(int32_t n_ranks, int64_t n_elems, const uint16_t* const* grads, 
     int rc = check_table(grads, n_ranks);
     if (rc != ZERO_OK) return rc;
     if (!aligned16(scratch)) return ZERO_EALIGN;
-    GradTable T = {};
+    ReduceTable T = {};
     for (int32_t r = 0; r < n_ranks; ++r) T.g[r] = reinterpret_cast<const uint4*>(grads[r]);
     const float inv_n = static_cast<float>(1.0 / static_cast<double>(n_ranks));
-    grad_sqnorm_kernel<<<kNormBlocks, kNormThreads, 0, stream>>>(T, n_ranks, n_elems / 8, inv_n,
-                                                                accumulate ? 1 : 0, scratch);
+    launch_norm<false>(T, n_ranks, n_elems / 8, 1, 0, 0, inv_n, accumulate ? 1 : 0, scratch,
+                       stream);
     return cuda_status(cudaGetLastError());
 }
 
@@ -204,8 +277,8 @@ int grad_reduce_sqnorm(int32_t n_ranks, int64_t n_elems, const uint16_t* const* 
     const int64_t shard_vec = n_elems / n_ranks / 8;
     const StrideSplit sp = split_stride(static_cast<int64_t>(kNormBlocks) * kNormThreads, shard_vec);
     const float inv_n = static_cast<float>(1.0 / static_cast<double>(n_ranks));
-    grad_reduce_sqnorm_kernel<<<kNormBlocks, kNormThreads, 0, stream>>>(
-        T, n_ranks, n_elems / 8, shard_vec, sp.k, sp.j, inv_n, accumulate ? 1 : 0, scratch);
+    launch_norm<true>(T, n_ranks, n_elems / 8, shard_vec, sp.k, sp.j, inv_n, accumulate ? 1 : 0,
+                      scratch, stream);
     return cuda_status(cudaGetLastError());
 }
 
@@ -223,9 +296,16 @@ int clip_coef(const double* scratch, int64_t scratch_bytes, double max_norm, flo
 int preload_clip_kernels()
 {
     cudaFuncAttributes a;
-    if (cudaFuncGetAttributes(&a, grad_sqnorm_kernel) != cudaSuccess ||
-        cudaFuncGetAttributes(&a, clip_coef_kernel) != cudaSuccess)
-        return ZERO_ECUDA;
+    const void* kernels[] = {
+        reinterpret_cast<const void*>(grad_sqnorm_kernel<false, 0>),
+        reinterpret_cast<const void*>(grad_sqnorm_kernel<false, 1>),
+        reinterpret_cast<const void*>(grad_sqnorm_kernel<false, 2>),
+        reinterpret_cast<const void*>(grad_sqnorm_kernel<false, 4>),
+        reinterpret_cast<const void*>(grad_sqnorm_kernel<true, 0>),
+        reinterpret_cast<const void*>(clip_coef_kernel),
+    };
+    for (const void* k : kernels)
+        if (cudaFuncGetAttributes(&a, k) != cudaSuccess) return ZERO_ECUDA;
     return ZERO_OK;
 }
 
