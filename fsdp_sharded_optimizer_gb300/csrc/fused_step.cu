@@ -125,8 +125,8 @@ fused_step_kernel(const __grid_constant__ Tables T, const StepScalars s, const R
             acc[0] = g0.x; acc[1] = g0.y; acc[2] = g0.z; acc[3] = g0.w;
             acc[4] = g1.x; acc[5] = g1.y; acc[6] = g1.z; acc[7] = g1.w;
         } else if (kF32)
-            dev::sum_ranks_f32<kRankBatch / 2>(reinterpret_cast<const float4* const*>(T.g), N, q,
-                                               acc);
+            dev::sum_ranks_f32<kSmall ? kRankBatchSmall / 2 : kRankBatch / 2>(
+                reinterpret_cast<const float4* const*>(T.g), N, q, acc);
         else
             dev::sum_ranks<kSmall ? kRankBatchSmall : kRankBatch>(T.g, N, q, acc);
         float prior[8];
@@ -351,11 +351,18 @@ int launch_range(const Tables& T, const StepScalars& s, int64_t q0, int64_t q1, 
                                                                           T, s, R, nullptr));
     }
     if (f32) { // fp32 gradients: no clipping or accumulation variant
+        const bool small = n_ranks <= kSmallRanks;
+        const void* k =
+            small ? reinterpret_cast<const void*>(fused_step_kernel<false, false, true, false, true>)
+                  : reinterpret_cast<const void*>(fused_step_kernel<false, false, true, false, false>);
         int blocks = 0;
-        const Range R = make_range(reinterpret_cast<const void*>(fused_step_kernel<false, false, true>),
-                                   q0, q1, shard_vec, n_ranks, &blocks);
+        const Range R = make_range(k, q0, q1, shard_vec, n_ranks, &blocks);
         if (blocks <= 0) return ZERO_ECUDA;
-        return cuda_status(launch_fused<false, false, true>(blocks, stream, chained, T, s, R, nullptr));
+        return cuda_status(
+            small ? launch_fused<false, false, true, false, true>(blocks, stream, chained, T, s, R,
+                                                                  nullptr)
+                  : launch_fused<false, false, true, false, false>(blocks, stream, chained, T, s,
+                                                                   R, nullptr));
     }
     return n_ranks <= kSmallRanks
                ? launch_bf16<true>(T, s, q0, q1, shard_vec, n_ranks, clip, stream, inv_m, chained)
@@ -533,6 +540,7 @@ int preload_fused_kernels()
         reinterpret_cast<const void*>(fused_step_kernel<true, false, false, false, true>),
         reinterpret_cast<const void*>(fused_step_kernel<false, true, false, false, true>),
         reinterpret_cast<const void*>(fused_step_kernel<true, true, false, false, true>),
+        reinterpret_cast<const void*>(fused_step_kernel<false, false, true, false, true>),
     };
     for (const void* k : kernels)
         if (persistent_blocks(k, kBlock, 0) <= 0) return ZERO_ECUDA;
