@@ -526,6 +526,11 @@ int step_nodes_set_scalars(StepNodeList* log, cudaGraphExec_t exec, const StepSc
 
 void step_nodes_free(StepNodeList* log) { delete log; }
 
+cudaGraphNode_t step_node_at(const StepNodeList* log, size_t i)
+{
+    return log && i < log->launches.size() ? log->launches[i].node : nullptr;
+}
+
 int preload_fused_kernels()
 {
     const void* kernels[] = {

@@ -17,6 +17,7 @@
 // scalars in the instantiated graph before each replay.  The gathers and the
 // clipping kernels take nothing that changes.
 #include <new>
+#include <vector>
 
 #include "zero_internal.h"
 
@@ -29,6 +30,69 @@ struct zero3_graph {
 };
 
 using namespace zero;
+
+namespace {
+
+// Turns the capture's direct edge from -> to (a kernel node to a kernel node,
+// default type) into a programmatic one: `to` may start as soon as every block
+// of `from` has triggered its dependents.  Nothing changes when the capture
+// made no such edge.
+int make_programmatic(cudaGraph_t graph, cudaGraphNode_t from, cudaGraphNode_t to)
+{
+    size_t n = 0;
+    int rc = cuda_status(cudaGraphNodeGetDependencies(to, nullptr, nullptr, &n));
+    if (rc != ZERO_OK || n == 0) return rc;
+    std::vector<cudaGraphNode_t> deps(n);
+    std::vector<cudaGraphEdgeData> edges(n);
+    if ((rc = cuda_status(cudaGraphNodeGetDependencies(to, deps.data(), edges.data(), &n))) !=
+        ZERO_OK)
+        return rc;
+    for (size_t i = 0; i < n; ++i) {
+        if (deps[i] != from || edges[i].type != cudaGraphDependencyTypeDefault ||
+            edges[i].from_port != cudaGraphKernelNodePortDefault)
+            continue;
+        if ((rc = cuda_status(cudaGraphRemoveDependencies(graph, &from, &to, &edges[i], 1))) !=
+            ZERO_OK)
+            return rc;
+        cudaGraphEdgeData e = {};
+        e.from_port = cudaGraphKernelNodePortProgrammatic;
+        e.type = cudaGraphDependencyTypeProgrammatic;
+        return cuda_status(cudaGraphAddDependencies(graph, &from, &to, &e, 1));
+    }
+    return ZERO_OK;
+}
+
+// The backward pass updates the units in reverse order, each unit's fused
+// launches following the previous unit's on the main stream.  Consecutive
+// units touch disjoint parameters, so the edge from one unit's last launch
+// to the next unit's first is made programmatic, like the edges between the
+// chunks of one unit: the next unit's blocks take over the SMs the previous
+// one's tail leaves idle.  The next unit's edge from its backward gather (the
+// gather reads the shard the update writes) stays a full dependency, and every
+// fused launch waits for its predecessors before it exits, so completion
+// stays ordered.  On GPT-2-sized units (7 M parameters) the launch tails are
+// a visible part of the step.
+int chain_units(cudaGraph_t graph, const StepNodeList* nodes, const zero_unit_t* units,
+                int32_t n_units)
+{
+    size_t idx = 0;
+    cudaGraphNode_t prev_last = nullptr;
+    for (int32_t pos = 0; pos < n_units; ++pos) {
+        const int32_t u = n_units - 1 - pos;
+        const int64_t c = chunk_count(units[u].n_padded / 8);
+        cudaGraphNode_t first = step_node_at(nodes, idx);
+        if (!first || c < 1) return ZERO_ECUDA;
+        if (prev_last) {
+            const int rc = make_programmatic(graph, prev_last, first);
+            if (rc != ZERO_OK) return rc;
+        }
+        idx += static_cast<size_t>(c);
+        prev_last = step_node_at(nodes, idx - 1);
+    }
+    return ZERO_OK;
+}
+
+} // namespace
 
 extern "C" int zero3_graph_create(const zero_unit_t* units, int32_t n_units, int32_t n_ranks,
                                   const uint16_t* const* grads, float* const* master,
@@ -76,6 +140,7 @@ extern "C" int zero3_graph_create(const zero_unit_t* units, int32_t n_units, int
     for (int32_t u = 0; u < n_units && rc == ZERO_OK; ++u)
         expected += chunk_count(units[u].n_padded / 8);
     if (rc == ZERO_OK && !step_nodes_ok(nodes, static_cast<size_t>(expected))) rc = ZERO_ECUDA;
+    if (rc == ZERO_OK) rc = chain_units(graph, nodes, units, n_units);
     cudaGraphExec_t exec = nullptr;
     if (rc == ZERO_OK) rc = cuda_status(cudaGraphInstantiate(&exec, graph, 0));
     zero3_graph_t* g = nullptr;

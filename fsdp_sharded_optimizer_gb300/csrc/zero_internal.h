@@ -82,6 +82,7 @@ void step_nodes_end();
 bool step_nodes_ok(const StepNodeList* log, size_t expected);
 int step_nodes_set_scalars(StepNodeList* log, cudaGraphExec_t exec, const StepScalars& s);
 void step_nodes_free(StepNodeList* log);
+cudaGraphNode_t step_node_at(const StepNodeList* log, size_t i); // nullptr past the end
 
 // Load the kernels a ZeRO-3 step launches and cache their launch geometry,
 // so that nothing is loaded or queried for the first time inside a capture.
