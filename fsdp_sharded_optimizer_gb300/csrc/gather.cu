@@ -32,6 +32,11 @@ struct Sources {
 __global__ void __launch_bounds__(kBlock)
 gather_kernel(const __grid_constant__ Sources S, uint4* __restrict__ dst, int64_t shard_vec)
 {
+    // In a graph, consecutive gathers may be joined by a programmatic edge
+    // (they write different buffers): this gather lets the next one start
+    // once all its blocks run, and completes only after its predecessor.  Both
+    // instructions do nothing otherwise.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int k = blockIdx.y;
     const uint4* __restrict__ src = S.src[k];
     uint4* __restrict__ out = dst + static_cast<int64_t>(k) * shard_vec;
@@ -50,9 +55,27 @@ gather_kernel(const __grid_constant__ Sources S, uint4* __restrict__ dst, int64_
             if (j < shard_vec) dev::st_stream(out + j, x[u]);
         }
     }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// The gathers launched on this thread while a capture log is installed
+// (zero3_graph_create), in issue order.
+thread_local std::vector<GatherNode>* t_gather_log = nullptr;
+thread_local bool t_gather_log_failed = false;
+
 } // namespace
+
+void gather_nodes_begin(std::vector<GatherNode>* log)
+{
+    t_gather_log = log;
+    t_gather_log_failed = false;
+}
+
+bool gather_nodes_end()
+{
+    t_gather_log = nullptr;
+    return !t_gather_log_failed;
+}
 
 int preload_gather_kernel()
 {
@@ -84,5 +107,25 @@ extern "C" int zero3_gather_unit(const zero_unit_t* unit, int32_t n_ranks,
     if (tiles > 0x7FFFFFFF) return ZERO_EINVAL; // grid.x limit (a shard of > 2^40 elements)
     const dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(n_ranks));
     gather_kernel<<<grid, kBlock, 0, stream>>>(S, reinterpret_cast<uint4*>(full_unit), shard_vec);
-    return cuda_status(cudaGetLastError());
+    rc = cuda_status(cudaGetLastError());
+    if (rc == ZERO_OK && t_gather_log) {
+        cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+        const cudaGraphNode_t* deps = nullptr;
+        const cudaGraphEdgeData* edges = nullptr;
+        size_t n_deps = 0;
+        if (cudaStreamGetCaptureInfo(stream, &st, nullptr, nullptr, &deps, &edges, &n_deps) !=
+                cudaSuccess ||
+            st != cudaStreamCaptureStatusActive || n_deps != 1) {
+            t_gather_log_failed = true;
+        } else {
+            try {
+                t_gather_log->push_back(GatherNode{
+                    deps[0], reinterpret_cast<uintptr_t>(full_unit),
+                    static_cast<uintptr_t>(unit->n_padded) * sizeof(uint16_t)});
+            } catch (...) {
+                t_gather_log_failed = true;
+            }
+        }
+    }
+    return rc;
 }

@@ -92,6 +92,27 @@ int chain_units(cudaGraph_t graph, const StepNodeList* nodes, const zero_unit_t*
     return ZERO_OK;
 }
 
+// The gathers run one after another on the side stream.  Two consecutive
+// gathers that write disjoint bytes (the two full-unit buffers alternate, and
+// without resharding each unit has its own region) only read the parameter
+// shards, so their stream-order edge is made programmatic too: the next
+// gather's blocks fill the SMs as the previous one drains.  Its edge from the
+// main stream's release of the buffer it overwrites stays a full dependency,
+// so a gather into a buffer still in use waits as before.  A pair that writes
+// the same bytes (the last forward and first backward gather of an odd number
+// of units, both into the first buffer) keeps its full edge.
+int chain_gathers(cudaGraph_t graph, const std::vector<GatherNode>& gathers)
+{
+    for (size_t i = 1; i < gathers.size(); ++i) {
+        const GatherNode& a = gathers[i - 1];
+        const GatherNode& b = gathers[i];
+        if (a.dst < b.dst + b.size && b.dst < a.dst + a.size) continue;
+        const int rc = make_programmatic(graph, a.node, b.node);
+        if (rc != ZERO_OK) return rc;
+    }
+    return ZERO_OK;
+}
+
 } // namespace
 
 extern "C" int zero3_graph_create(const zero_unit_t* units, int32_t n_units, int32_t n_ranks,
@@ -119,11 +140,19 @@ extern "C" int zero3_graph_create(const zero_unit_t* units, int32_t n_units, int
         (clip && (rc = preload_clip_kernels()) != ZERO_OK) || (rc = preload_step_events()) != ZERO_OK)
         return rc;
 
+    std::vector<GatherNode> gathers;
+    try {
+        gathers.reserve(2 * static_cast<size_t>(n_units));
+    } catch (...) {
+        return ZERO_ECUDA;
+    }
     StepNodeList* nodes = step_nodes_begin();
     if (!nodes) return ZERO_ECUDA;
+    gather_nodes_begin(&gathers);
     cudaError_t e = cudaStreamBeginCapture(capture_stream, cudaStreamCaptureModeThreadLocal);
     if (e != cudaSuccess) {
         step_nodes_end();
+        gather_nodes_end();
         step_nodes_free(nodes);
         return cuda_status(e);
     }
@@ -134,13 +163,20 @@ extern "C" int zero3_graph_create(const zero_unit_t* units, int32_t n_units, int
     cudaGraph_t graph = nullptr;
     e = cudaStreamEndCapture(capture_stream, &graph);
     step_nodes_end();
+    const bool gathers_logged = gather_nodes_end();
     if (rc == ZERO_OK && e != cudaSuccess) rc = cuda_status(e);
     // each unit's fused reduce-scatter + AdamW, in its chained launches
     int64_t expected = 0;
     for (int32_t u = 0; u < n_units && rc == ZERO_OK; ++u)
         expected += chunk_count(units[u].n_padded / 8);
     if (rc == ZERO_OK && !step_nodes_ok(nodes, static_cast<size_t>(expected))) rc = ZERO_ECUDA;
+    // a gather per unit in the forward pass, and again in the backward pass
+    // when the forward pass reshards
+    const size_t expected_gathers =
+        static_cast<size_t>(n_units) * (reshard_after_forward ? 2 : 1);
+    if (rc == ZERO_OK && (!gathers_logged || gathers.size() != expected_gathers)) rc = ZERO_ECUDA;
     if (rc == ZERO_OK) rc = chain_units(graph, nodes, units, n_units);
+    if (rc == ZERO_OK) rc = chain_gathers(graph, gathers);
     cudaGraphExec_t exec = nullptr;
     if (rc == ZERO_OK) rc = cuda_status(cudaGraphInstantiate(&exec, graph, 0));
     zero3_graph_t* g = nullptr;

@@ -4,6 +4,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <vector>
 
 #include <cuda_runtime.h>
 
@@ -83,6 +84,18 @@ bool step_nodes_ok(const StepNodeList* log, size_t expected);
 int step_nodes_set_scalars(StepNodeList* log, cudaGraphExec_t exec, const StepScalars& s);
 void step_nodes_free(StepNodeList* log);
 cudaGraphNode_t step_node_at(const StepNodeList* log, size_t i); // nullptr past the end
+
+// Between gather_nodes_begin and gather_nodes_end, every gather launched on
+// this thread into a stream being captured appends its graph node and the
+// byte range it writes to `log`.  gather_nodes_end: false when a record
+// failed (the log is then incomplete).
+struct GatherNode {
+    cudaGraphNode_t node;
+    uintptr_t dst;  // first byte written
+    uintptr_t size; // bytes written
+};
+void gather_nodes_begin(std::vector<GatherNode>* log);
+bool gather_nodes_end();
 
 // Load the kernels a ZeRO-3 step launches and cache their launch geometry,
 // so that nothing is loaded or queried for the first time inside a capture.

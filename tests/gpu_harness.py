@@ -132,3 +132,29 @@ def padding_is_zero(g, P, shard_len):
 def free():
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
+
+
+def assert_gathered(units, sizes, before, full_a, full_b=None):
+    """After a ZeRO-3 step the full-unit buffers hold what the step's last
+    gathers wrote, the bf16 weights each unit had before its update in that
+    step (`before`: every unit's parameters concatenated, as the oracle's DDP
+    simulation returns them after one step fewer).  With two buffers the
+    backward pass gathers unit n-1-p into buffer p % 2 at position p, so unit 0
+    and unit 1 are the last there; with one kept buffer every unit sits in its
+    own region.  A gather that read a shard after its update had begun, or a
+    gather racing another into the same buffer, shows up here."""
+    starts = np.cumsum([0] + [int(s) for s in sizes])
+
+    def want(i):
+        return before[starts[i]:starts[i] + int(sizes[i])]
+
+    if full_b is None:
+        a = full_a.numpy()[0]
+        for i, u in enumerate(units):
+            assert_bitwise(a[u.offset:u.offset + u.n_params], want(i), f"kept unit {i}")
+        return
+    bufs = (full_a.numpy()[0], full_b.numpy()[0])
+    n = len(units)
+    for i in range(min(n, 2)):
+        p = n - 1 - i
+        assert_bitwise(bufs[p % 2][:units[i].n_params], want(i), f"gathered unit {i}")

@@ -9,7 +9,8 @@ bit for bit given the GPU's clip coefficient, and that coefficient's norm to
 the oracle's fp64 norm within 1e-6: the norm's summation order is the GPU's
 own (fixed-grid partial sums), so its last bits are not the oracle's.  Each
 ZeRO-3 case draws unit sizes and runs the native scheduler with or without
-resharding after the forward pass.  The seeds are fixed, so a failure
+resharding after the forward pass, and checks the full-unit buffers hold the
+weights its last gathers had to read.  The seeds are fixed, so a failure
 repeats.
 """
 import numpy as np
@@ -144,4 +145,7 @@ def test_random_zero3_cases_match_ddp(orc, i):
         got = np.concatenate([np.concatenate([a[k][u.shard_offset:u.shard_offset + u.shard_len]
                                               for k in range(N)])[:u.n_params] for u in units])
         H.assert_bitwise(got, ref, name)
+    before = orc.sim_ddp(N, sum(sizes), seed, H.SIGMA_W, H.SIGMA_G, 1,
+                         orc.hparams(**H.HP, step=1), T - 1)[0]
+    H.assert_gathered(units, sizes, before, fa, fb if reshard else None)
     H.free()

@@ -2,7 +2,8 @@
 step, through the C ABI.
 
 Checked: the replayed steps equal DDP bit for bit (the oracle's all-reduce
-simulation), with and without resharding after the forward pass; they equal
+simulation), with and without resharding after the forward pass, and leave in
+the full-unit buffers the weights the last gathers had to read; they equal
 the streamed zero3_step bit for bit when t, lr, betas, eps and weight decay
 change every step and global-norm clipping is on; creating the graph runs
 nothing; bad arguments are rejected and leave the capture stream usable.
@@ -75,6 +76,11 @@ def test_graph_replays_equal_ddp(orc, reshard):
         got = np.concatenate([np.concatenate([src[k][u.shard_offset:u.shard_offset + u.shard_len]
                                               for k in range(N)])[:u.n_params] for u in units])
         H.assert_bitwise(got, ref, name)
+    # the last replay's gathers read the weights of step T-1, before any update
+    # of theirs, with gathers and updates joined by programmatic edges
+    before = orc.sim_ddp(N, sum(SIZES), seed, H.SIGMA_W, H.SIGMA_G, 1,
+                         orc.hparams(**H.HP, step=1), T - 1)[0]
+    H.assert_gathered(units, SIZES, before, fa, fb)
     H.free()
 
 

@@ -236,6 +236,9 @@ def test_native_zero3_step_matches_ddp(orc, resident):
             got[name].append(np.concatenate(rows)[:u.n_params])
     for (name, ref) in zip(("p", "w", "m", "v"), ddp):
         H.assert_bitwise(np.concatenate(got[name]), ref, name)
+    before = orc.sim_ddp(N, sum(sizes), seed, H.SIGMA_W, H.SIGMA_G, 1,
+                         orc.hparams(**H.HP, step=1), T - 1)[0]
+    H.assert_gathered(units, sizes, before, fa, fb)
 
 
 def test_native_zero3_step_rejects():
