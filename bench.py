@@ -584,6 +584,26 @@ def run_gpu_zero3(args, torch, Z, world, rank, dev):
     for _ in range(min(W, 2)):
         clip_step(clip_s)
     ms_cs, _ = timed(torch, world, dev, stream, lambda: clip_step(clip_s), Kc)
+
+    # both clipped steps again as CUDA graphs
+    def graph_ms(c):
+        cap.wait_stream(stream)
+        gc = Z.zero3_graph_create(units, grads, master, m, v, shards, full[0], full[1],
+                                  Z.hparams(**HP, step=1), cap, side, clip=c)
+
+        def g_step():
+            t[0] += 1
+            gc.launch(Z.hparams(**HP, step=t[0]), stream=stream)
+
+        try:
+            for _ in range(min(W, 2)):
+                g_step()
+            return timed(torch, world, dev, stream, g_step, Kc)[0]
+        finally:
+            torch.cuda.synchronize()
+            gc.close()
+
+    ms_gcg, ms_gcs = graph_ms(clip_g), graph_ms(clip_s)
     del clip_s, grad_shard
     # reshard_after_forward = False: one gather per unit, full weights kept (2 B/param)
     kept = torch.empty(total, dtype=torch.int16, device=dev)
@@ -688,6 +708,12 @@ def run_gpu_zero3(args, torch, Z, world, rank, dev):
                        "bytes_per_step": (2 * N + 42) * total,
                        "note": "the same clipped step through the fp32 gradient shard the norm "
                                "pass keeps; the same bits as `clip`"},
+        "graph_clip": {"ms_per_step": ms_gcg / Kc, "steps": Kc,
+                       "hbm_gbs": (4 * N + 34) * total * Kc / (ms_gcg * 1e-3) / 1e9,
+                       "note": "`clip` captured once as a CUDA graph (zero3_graph with a clip)"},
+        "graph_clip_shard": {"ms_per_step": ms_gcs / Kc, "steps": Kc,
+                             "hbm_gbs": (2 * N + 42) * total * Kc / (ms_gcs * 1e-3) / 1e9,
+                             "note": "`clip_shard` captured once as a CUDA graph"},
         "no_reshard": {"ms_per_step": ms_k / Kk, "steps": Kk,
                        "hbm_gbs": (fused_bytes + 4 * total) * Kk / (ms_k * 1e-3) / 1e9,
                        "note": "reshard_after_forward=False: one gather per unit per step, every "

@@ -113,6 +113,12 @@ grad_sqnorm_kernel(const __grid_constant__ ReduceTable T, int n_ranks, int64_t n
                    int64_t shard_vec, int64_t step_k, int64_t step_j, float inv_n, int accumulate,
                    double* __restrict__ partials)
 {
+    // A ZeRO-3 step's norm passes run one unit after another, each adding to
+    // the partials the one before left.  Launched chained, a pass reads and
+    // squares its own unit's gradients while the previous pass drains, and
+    // waits for that pass to complete only before it adds to the partials.
+    // Both instructions do nothing in a launch that is not chained.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     float sum = 0.0f, comp = 0.0f; // Kahan: true sum ~ sum - comp
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kNormThreads;
     int64_t q = static_cast<int64_t>(blockIdx.x) * kNormThreads + threadIdx.x;
@@ -165,6 +171,7 @@ grad_sqnorm_kernel(const __grid_constant__ ReduceTable T, int n_ranks, int64_t n
         }
     }
     const double b = block_sum(static_cast<double>(sum) - static_cast<double>(comp));
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (threadIdx.x == 0) partials[blockIdx.x] = (accumulate ? partials[blockIdx.x] : 0.0) + b;
 }
 
@@ -173,29 +180,32 @@ grad_sqnorm_kernel(const __grid_constant__ ReduceTable T, int n_ranks, int64_t n
 // N_d = 2 5,385 -> 6,675, N_d = 4 6,823 -> 6,945; N_d = 3 lost 3 % and the
 // pass that stores the shard lost 6-10 % at every N_d <= 4 (its stores come
 // in bursts after the loads), so those keep the one-vector loop.
+// chained: launched with programmatic stream serialization (the previous
+// kernel on the stream must be a norm pass over other gradients).
 template <bool kStore>
-void launch_norm(const ReduceTable& T, int n_ranks, int64_t n_vec, int64_t shard_vec,
-                 int64_t step_k, int64_t step_j, float inv_n, int accumulate, double* partials,
-                 cudaStream_t stream)
+cudaError_t launch_norm(const ReduceTable& T, int n_ranks, int64_t n_vec, int64_t shard_vec,
+                        int64_t step_k, int64_t step_j, float inv_n, int accumulate,
+                        double* partials, cudaStream_t stream, bool chained)
 {
     const int kn = kStore ? 0 : (n_ranks == 1 || n_ranks == 2 || n_ranks == 4 ? n_ranks : 0);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kNormBlocks);
+    cfg.blockDim = dim3(kNormThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = chained ? 1 : 0;
+    auto go = [&](auto kernel) {
+        return cudaLaunchKernelEx(&cfg, kernel, T, n_ranks, n_vec, shard_vec, step_k, step_j,
+                                  inv_n, accumulate, partials);
+    };
     switch (kn) {
-    case 1:
-        grad_sqnorm_kernel<false, 1><<<kNormBlocks, kNormThreads, 0, stream>>>(
-            T, n_ranks, n_vec, shard_vec, step_k, step_j, inv_n, accumulate, partials);
-        break;
-    case 2:
-        grad_sqnorm_kernel<false, 2><<<kNormBlocks, kNormThreads, 0, stream>>>(
-            T, n_ranks, n_vec, shard_vec, step_k, step_j, inv_n, accumulate, partials);
-        break;
-    case 4:
-        grad_sqnorm_kernel<false, 4><<<kNormBlocks, kNormThreads, 0, stream>>>(
-            T, n_ranks, n_vec, shard_vec, step_k, step_j, inv_n, accumulate, partials);
-        break;
-    default:
-        grad_sqnorm_kernel<kStore, 0><<<kNormBlocks, kNormThreads, 0, stream>>>(
-            T, n_ranks, n_vec, shard_vec, step_k, step_j, inv_n, accumulate, partials);
-        break;
+    case 1: return go(grad_sqnorm_kernel<false, 1>);
+    case 2: return go(grad_sqnorm_kernel<false, 2>);
+    case 4: return go(grad_sqnorm_kernel<false, 4>);
+    default: return go(grad_sqnorm_kernel<kStore, 0>);
     }
 }
 
@@ -241,7 +251,7 @@ grad_nonfinite_kernel(const __grid_constant__ GradTable T, int64_t n_vec,
 } // namespace
 
 int grad_sqnorm(int32_t n_ranks, int64_t n_elems, const uint16_t* const* grads, int32_t accumulate,
-                double* scratch, int64_t scratch_bytes, cudaStream_t stream)
+                double* scratch, int64_t scratch_bytes, cudaStream_t stream, bool chained)
 {
     if (n_ranks < 1 || n_ranks > ZERO_MAX_RANKS || n_elems <= 0 || n_elems % 8 != 0 || !scratch ||
         scratch_bytes < kNormScratchBytes)
@@ -252,14 +262,13 @@ int grad_sqnorm(int32_t n_ranks, int64_t n_elems, const uint16_t* const* grads, 
     ReduceTable T = {};
     for (int32_t r = 0; r < n_ranks; ++r) T.g[r] = reinterpret_cast<const uint4*>(grads[r]);
     const float inv_n = static_cast<float>(1.0 / static_cast<double>(n_ranks));
-    launch_norm<false>(T, n_ranks, n_elems / 8, 1, 0, 0, inv_n, accumulate ? 1 : 0, scratch,
-                       stream);
-    return cuda_status(cudaGetLastError());
+    return cuda_status(launch_norm<false>(T, n_ranks, n_elems / 8, 1, 0, 0, inv_n,
+                                          accumulate ? 1 : 0, scratch, stream, chained));
 }
 
 int grad_reduce_sqnorm(int32_t n_ranks, int64_t n_elems, const uint16_t* const* grads,
                        float* const* grad_shard, int32_t accumulate, double* scratch,
-                       int64_t scratch_bytes, cudaStream_t stream)
+                       int64_t scratch_bytes, cudaStream_t stream, bool chained)
 {
     if (n_ranks < 1 || n_ranks > ZERO_MAX_RANKS || n_elems <= 0 ||
         n_elems % (8 * static_cast<int64_t>(n_ranks)) != 0 || !scratch ||
@@ -277,9 +286,8 @@ int grad_reduce_sqnorm(int32_t n_ranks, int64_t n_elems, const uint16_t* const* 
     const int64_t shard_vec = n_elems / n_ranks / 8;
     const StrideSplit sp = split_stride(static_cast<int64_t>(kNormBlocks) * kNormThreads, shard_vec);
     const float inv_n = static_cast<float>(1.0 / static_cast<double>(n_ranks));
-    launch_norm<true>(T, n_ranks, n_elems / 8, shard_vec, sp.k, sp.j, inv_n, accumulate ? 1 : 0,
-                      scratch, stream);
-    return cuda_status(cudaGetLastError());
+    return cuda_status(launch_norm<true>(T, n_ranks, n_elems / 8, shard_vec, sp.k, sp.j, inv_n,
+                                         accumulate ? 1 : 0, scratch, stream, chained));
 }
 
 int clip_coef(const double* scratch, int64_t scratch_bytes, double max_norm, float* norm_coef,

@@ -218,8 +218,15 @@ int run_step(const zero_unit_t* units, int32_t n_units, int32_t n_ranks, const v
             }
         }
     };
+    // The norm passes of consecutive units are chained (programmatic
+    // dependent launch) when nothing else was issued on the main stream
+    // between them: each reads other gradients and waits for the one before
+    // it to complete only before it adds to the shared partials.
+    bool after_norm = false;
     for (const zero_op_t& op : plan.ops) {
         cudaStream_t s = op.stream == 0 ? main_stream : side_stream;
+        const bool chain_norm = after_norm;
+        if (op.stream == 0) after_norm = op.kind == ZERO_OP_NORM;
         switch (op.kind) {
         case ZERO_OP_RECORD:
             rc = cuda_status(cudaEventRecord(ev[op.arg], s));
@@ -260,10 +267,11 @@ int run_step(const zero_unit_t* units, int32_t n_units, int32_t n_ranks, const v
                 for (int32_t r = 0; r < n_ranks; ++r)
                     unit_shard[r] = clip->grad_shard[r] + units[op.unit].shard_offset;
                 rc = grad_reduce_sqnorm(n_ranks, units[op.unit].n_padded, unit_grads, unit_shard,
-                                        op.arg, clip->scratch, clip->scratch_bytes, s);
+                                        op.arg, clip->scratch, clip->scratch_bytes, s,
+                                        chain_norm);
             } else {
                 rc = grad_sqnorm(n_ranks, units[op.unit].n_padded, unit_grads, op.arg,
-                                 clip->scratch, clip->scratch_bytes, s);
+                                 clip->scratch, clip->scratch_bytes, s, chain_norm);
             }
             break;
         case ZERO_OP_CLIP_COEF:

@@ -58,13 +58,17 @@ int cuda_status(cudaError_t e);
 // partial sum each, so scratch holds kNormBlocks doubles (152 SMs x 8).
 constexpr int kNormBlocks = 1216;
 constexpr int64_t kNormScratchBytes = kNormBlocks * static_cast<int64_t>(sizeof(double));
+// chained: the previous kernel on `stream` is a norm pass over other
+// gradients; this one may start while it drains (programmatic dependent
+// launch) and adds to the partials only once it has completed.
 int grad_sqnorm(int32_t n_ranks, int64_t n_elems, const uint16_t* const* grads, int32_t accumulate,
-                double* scratch, int64_t scratch_bytes, cudaStream_t stream);
+                double* scratch, int64_t scratch_bytes, cudaStream_t stream,
+                bool chained = false);
 int clip_coef(const double* scratch, int64_t scratch_bytes, double max_norm, float* norm_coef,
               cudaStream_t stream);
 int grad_reduce_sqnorm(int32_t n_ranks, int64_t n_elems, const uint16_t* const* grads,
                        float* const* grad_shard, int32_t accumulate, double* scratch,
-                       int64_t scratch_bytes, cudaStream_t stream);
+                       int64_t scratch_bytes, cudaStream_t stream, bool chained = false);
 
 // CUDA-graph support (zero3_graph).  Between step_nodes_begin and
 // step_nodes_end, every fused-step launch made on this thread into a stream
