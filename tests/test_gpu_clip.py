@@ -400,3 +400,54 @@ def test_unit_update_from_the_gradient_shard_equals_the_unit_reduce_scatter(clip
     if clipped:
         assert float(na[1]) < 1
     H.free()
+
+
+@pytest.mark.parametrize("shard", [False, True])
+def test_chained_norm_passes_equal_the_unit_by_unit_calls(shard):
+    """zero3_step chains the norm passes of consecutive units: each pass reads
+    its own unit while the one before drains and waits for it only to add to
+    the shared partials.  Its partials, norm and coefficient (and the fp32
+    gradient shard, when it keeps one) equal those of the public norm calls
+    issued unit by unit without chaining, bit for bit, over 14 units of mixed
+    sizes with resident gradients."""
+    N, seed, max_norm = 8, 11, 1e-3
+    sizes = [7_000, 333, 250_000, 64, 90_001, 1_000_000, 5, 123_457, 8, 40_000, 300_000, 17,
+             2_000_000, 999]
+    units, total = B.zero_layout(sizes, N)
+    S = total // N
+    max_unit = max(u.n_padded for u in units)
+    grads = H.Guarded(N, total, torch.int16)
+    unit_rows = lambda u: [r[u.offset:u.offset + u.n_padded] for r in grads.rows]
+    for u in units:
+        B.zero_gen_grads_unit(seed, 1, H.SIGMA_G, 1, u, unit_rows(u))
+    master = H.Guarded(N, S, torch.float32)
+    m = H.Guarded(N, S, torch.float32).zero_()
+    v = H.Guarded(N, S, torch.float32).zero_()
+    shards = H.Guarded(N, S, torch.int16)
+    B.zero_gen_master(seed, H.SIGMA_W, units, master.rows)
+    for k in range(N):
+        B.zero_cast_bf16(master.rows[k], shards.rows[k])
+    fa, fb = H.Guarded(1, max_unit, torch.int16), H.Guarded(1, max_unit, torch.int16)
+    gs_a, gs_b = H.Guarded(N, S, torch.float32), H.Guarded(N, S, torch.float32)
+    sa, sb, na, nb = _scratch(), _scratch(), _norm_coef(), _norm_coef()
+    clip = B.clip_args(max_norm, sa, na, grad_shard=gs_a.rows if shard else None)
+    B.zero3_step(units, grads.rows, master.rows, m.rows, v.rows, shards.rows, fa.rows[0],
+                 fb.rows[0], H.hp(1), clip=clip, side_stream=torch.cuda.Stream())
+    for i, u in enumerate(units):
+        if shard:
+            B.zero_grad_reduce_sqnorm(
+                unit_rows(u), [r[u.shard_offset:u.shard_offset + u.shard_len] for r in gs_b.rows],
+                sb, accumulate=i > 0)
+        else:
+            B.zero_grad_sqnorm(unit_rows(u), sb, accumulate=i > 0)
+    B.zero_clip_coef(sb, max_norm, nb)
+    torch.cuda.synchronize()
+    for x in (grads, master, m, v, shards, fa, fb, gs_a, gs_b):
+        x.check()
+    H.assert_bitwise(sa.cpu().numpy().view(np.uint64), sb.cpu().numpy().view(np.uint64),
+                     "partials")
+    H.assert_bitwise(na.cpu().numpy(), nb.cpu().numpy(), "norm and coefficient")
+    assert float(na[1]) < 1  # the clipping was active
+    if shard:
+        H.assert_bitwise(gs_a.numpy(), gs_b.numpy(), "gradient shard")
+    H.free()
