@@ -36,6 +36,23 @@ __device__ __forceinline__ float4 ld_stream(const float4* p) { return __ldcs(p);
 __device__ __forceinline__ void st_stream(uint4* p, uint4 x) { __stcs(p, x); }
 __device__ __forceinline__ void st_stream(float4* p, float4 x) { __stcs(p, x); }
 
+// Streaming 32-byte (256-bit) load and store of 8 consecutive fp32 values, one
+// instruction each (sm_100 and later); p must be 32-byte aligned.
+__device__ __forceinline__ void ld8_stream(const float4* p, float (&x)[8])
+{
+    asm volatile("ld.global.cs.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=f"(x[0]), "=f"(x[1]), "=f"(x[2]), "=f"(x[3]), "=f"(x[4]), "=f"(x[5]),
+                   "=f"(x[6]), "=f"(x[7])
+                 : "l"(p));
+}
+__device__ __forceinline__ void st8_stream(float4* p, const float (&x)[8])
+{
+    asm volatile("st.global.cs.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p),
+                 "f"(x[0]), "f"(x[1]), "f"(x[2]), "f"(x[3]), "f"(x[4]), "f"(x[5]), "f"(x[6]),
+                 "f"(x[7])
+                 : "memory");
+}
+
 // The reduce-scatter's sum for 8 consecutive elements of vector q: fp32 from
 // +0 over ranks 0..n_ranks-1 in order.  All loads of a batch of `kBatch`
 // ranks are issued before any of them is summed.

@@ -451,3 +451,42 @@ def test_chained_norm_passes_equal_the_unit_by_unit_calls(shard):
     if shard:
         H.assert_bitwise(gs_a.numpy(), gs_b.numpy(), "gradient shard")
     H.free()
+
+
+@pytest.mark.parametrize("clipped", [False, True])
+def test_shard_update_at_16_byte_alignment_equals_the_32_byte_path(clipped):
+    """The update from the fp32 gradient shard moves 32 bytes per access when
+    every fp32 pointer is 32-byte aligned, and falls back to 16-byte accesses
+    otherwise (the ABI asks only 16).  State and shard rows 16 bytes off a
+    32-byte boundary (every other rank) give the same bits as aligned ones."""
+    N, P, T, seed, max_norm = 4, 300_001, 3, 17, 1e-3
+    (u,), _ = B.zero_layout([P], N)
+    S = u.shard_len
+    grads = H.Guarded(N, u.n_padded, torch.int16)
+
+    def state(off):
+        # rows of S fp32 starting `off` floats into rows of S + off
+        rows = []
+        for _ in range(4):  # master, m, v, gradient shard
+            t = torch.zeros((N, S + off), dtype=torch.float32, device="cuda")
+            rows.append([t[r, off:] for r in range(N)])
+        B.zero_gen_master(seed, H.SIGMA_W, [u], rows[0])
+        return rows, torch.empty(u.n_padded, dtype=torch.int16, device="cuda")
+
+    (a, pa), (b, pb) = state(0), state(4)
+    assert all(r.data_ptr() % 32 == 0 for x in a for r in x)
+    assert any(r.data_ptr() % 32 == 16 for x in b for r in x)
+    sc, nc = _scratch(), _norm_coef()
+    for t in range(1, T + 1):
+        B.zero_gen_grads_unit(seed, t, H.SIGMA_G, 1, u, grads.rows)
+        for st, params in ((a, pa), (b, pb)):
+            B.zero_grad_reduce_sqnorm(grads.rows, st[3], sc)
+            B.zero_clip_coef(sc, max_norm, nc)
+            B.zero_step_stage12_reduced(1, st[3], st[0], st[1], st[2], params, H.hp(t),
+                                        nc if clipped else None)
+    torch.cuda.synchronize()
+    grads.check()
+    for x, y, name in zip(a, b, ("master", "m", "v", "gradient shard")):
+        H.assert_bitwise(torch.stack(y).cpu().numpy(), torch.stack(x).cpu().numpy(), name)
+    H.assert_bitwise(pb.cpu().numpy().view(np.uint16), pa.cpu().numpy().view(np.uint16), "params")
+    H.free()
