@@ -548,7 +548,7 @@ int step_stage12(int32_t stage, int32_t n_ranks, int64_t n_padded, const void* c
 int rs_unit(const zero_unit_t* unit, int32_t n_ranks, const void* const* unit_grads,
             float* const* master, float* const* m, float* const* v, uint16_t* const* shard_bf16,
             const zero_hparams_t* hp, const float* clip, cudaStream_t stream, bool f32 = false,
-            bool g32 = false)
+            bool g32 = false, bool chain_first = false)
 {
     if (!unit || n_ranks < 1 || n_ranks > ZERO_MAX_RANKS || unit->n_padded <= 0 ||
         unit->shard_len <= 0 || unit->shard_len % 8 != 0 ||
@@ -575,7 +575,7 @@ int rs_unit(const zero_unit_t* unit, int32_t n_ranks, const void* const* unit_gr
     }
     const StepScalars s = make_scalars(hp, n_ranks);
     return launch(T, s, 0, unit->n_padded / 8, unit->shard_len / 8, n_ranks, clip, stream, 0.0f,
-                  f32, false, g32);
+                  f32, chain_first, g32);
 }
 
 int check_clip(const float* norm_coef)
@@ -585,6 +585,19 @@ int check_clip(const float* norm_coef)
 }
 
 } // namespace
+
+int unit_update(const zero_unit_t* unit, int32_t n_ranks, const void* const* grads,
+                float* const* master, float* const* m, float* const* v,
+                uint16_t* const* shard_bf16, const zero_hparams_t* hp, const float* clip,
+                cudaStream_t stream, bool f32, bool g32, bool chain_first)
+{
+    if (clip) {
+        const int rc = check_clip(clip);
+        if (rc != ZERO_OK) return rc;
+    }
+    return rs_unit(unit, n_ranks, grads, master, m, v, shard_bf16, hp, clip, stream, f32, g32,
+                   chain_first);
+}
 
 StepNodeList* step_nodes_begin()
 {

@@ -223,10 +223,22 @@ int run_step(const zero_unit_t* units, int32_t n_units, int32_t n_ranks, const v
     // between them: each reads other gradients and waits for the one before
     // it to complete only before it adds to the shared partials.
     bool after_norm = false;
+    // Likewise consecutive unit updates with nothing between them on the main
+    // stream (the backward pass without resharding: no gather, no event).
+    // Where an event record or wait separates them (the resharding backward
+    // pass) they are not chained: measured on GB300, chaining across the
+    // events gained nothing.  While the stream is being captured, the graph
+    // builder joins the units itself.
+    bool after_update = false;
+    cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+    if ((rc = cuda_status(cudaStreamIsCapturing(main_stream, &capture))) != ZERO_OK) return rc;
     for (const zero_op_t& op : plan.ops) {
         cudaStream_t s = op.stream == 0 ? main_stream : side_stream;
         const bool chain_norm = after_norm;
+        const bool chain_update = after_update && capture == cudaStreamCaptureStatusNone;
         if (op.stream == 0) after_norm = op.kind == ZERO_OP_NORM;
+        if (op.stream == 0 && op.kind != ZERO_OP_USE) // USE issues nothing
+            after_update = op.kind == ZERO_OP_REDUCE_SCATTER;
         switch (op.kind) {
         case ZERO_OP_RECORD:
             rc = cuda_status(cudaEventRecord(ev[op.arg], s));
@@ -248,17 +260,19 @@ int run_step(const zero_unit_t* units, int32_t n_units, int32_t n_ranks, const v
         case ZERO_OP_REDUCE_SCATTER:
             grads_of(op.unit);
             if (f32)
-                rc = zero3_reduce_scatter_unit_f32grads(&units[op.unit], n_ranks, unit_grads_f32,
-                                                        master, m, v, shard_bf16, hp, s);
+                rc = unit_update(&units[op.unit], n_ranks,
+                                 reinterpret_cast<const void* const*>(unit_grads_f32), master, m,
+                                 v, shard_bf16, hp, nullptr, s, true, false, chain_update);
             else if (op.arg && clip->grad_shard) // the mean the norm pass kept
-                rc = zero3_update_unit_reduced(&units[op.unit], n_ranks, clip->grad_shard, master,
-                                               m, v, shard_bf16, hp, clip->norm_coef, s);
-            else if (op.arg)
-                rc = zero3_reduce_scatter_unit_clip(&units[op.unit], n_ranks, unit_grads, master,
-                                                    m, v, shard_bf16, hp, clip->norm_coef, s);
+                rc = unit_update(&units[op.unit], n_ranks,
+                                 reinterpret_cast<const void* const*>(clip->grad_shard), master,
+                                 m, v, shard_bf16, hp, clip->norm_coef, s, false, true,
+                                 chain_update);
             else
-                rc = zero3_reduce_scatter_unit(&units[op.unit], n_ranks, unit_grads, master, m, v,
-                                               shard_bf16, hp, s);
+                rc = unit_update(&units[op.unit], n_ranks,
+                                 reinterpret_cast<const void* const*>(unit_grads), master, m, v,
+                                 shard_bf16, hp, op.arg ? clip->norm_coef : nullptr, s, false,
+                                 false, chain_update);
             break;
         case ZERO_OP_NORM:
             grads_of(op.unit);

@@ -70,6 +70,19 @@ int grad_reduce_sqnorm(int32_t n_ranks, int64_t n_elems, const uint16_t* const* 
                        float* const* grad_shard, int32_t accumulate, double* scratch,
                        int64_t scratch_bytes, cudaStream_t stream, bool chained = false);
 
+// One unit's fused reduce-scatter + AdamW + bf16 shard write, as
+// zero3_reduce_scatter_unit and its variants issue it: g from the rank
+// gradients (bf16, or fp32 with f32) or, with g32, from the fp32 gradient
+// shard storage (grads then holds its per-rank base pointers); clip = the
+// device coefficient or nullptr.  chain_first: the last thing issued on
+// `stream` was another unit's update and nothing else has been issued on it
+// since (no event record or wait); the first chunk is then chained to it
+// (programmatic dependent launch; the units touch disjoint elements).
+int unit_update(const zero_unit_t* unit, int32_t n_ranks, const void* const* grads,
+                float* const* master, float* const* m, float* const* v,
+                uint16_t* const* shard_bf16, const zero_hparams_t* hp, const float* clip,
+                cudaStream_t stream, bool f32, bool g32, bool chain_first);
+
 // CUDA-graph support (zero3_graph).  Between step_nodes_begin and
 // step_nodes_end, every fused-step launch made on this thread into a stream
 // that is being captured records its graph node and a copy of its arguments
