@@ -472,7 +472,12 @@ typedef struct {
  *                    updates then read instead of the gradients)
  * The library keeps five timing-free CUDA events per host thread and device
  * (created on first use); no device memory is allocated.  Work is queued
- * asynchronously; on return main_stream carries the end of the step.
+ * asynchronously; on return main_stream carries the end of the step.  Kernels
+ * that follow one another on the main stream with nothing else between them
+ * are chained with programmatic dependent launch (each may start while the
+ * one before drains, and completes after it): the units' norm passes, and,
+ * unless main_stream is being captured, the unit updates of the backward pass
+ * without resharding (zero3_graph_create joins those in the graph itself).
  * ZERO_EINVAL / ZERO_EALIGN / ZERO_ECUDA. */
 int zero3_step(const zero_unit_t* units, int32_t n_units, int32_t n_ranks,
                const uint16_t* const* grads, int32_t grads_resident,
