@@ -88,7 +88,8 @@ __device__ __forceinline__ void adamw(float g, float& w, float& m, float& v,
 // kF32: the rank gradients are fp32 (T.g holds float4 pointers).
 // kG32: the mean gradient is already reduced: read g from the owner's fp32
 // gradient shard T.a[k] (written by zero_grad_reduce_sqnorm) instead of the
-// N rank gradients.
+// N rank gradients.  Used when a pointer is only 16-byte aligned;
+// fused_step_wide_kernel does the same with 32-byte accesses otherwise.
 // kSmall: the launch shape for up to kSmallRanks ranks (see kSmallRanks).
 template <bool kClip, bool kAcc, bool kF32 = false, bool kG32 = false, bool kSmall = false>
 __global__ void __launch_bounds__(kBlock, kSmall ? kMinBlocksPerSMSmall : kMinBlocksPerSM)

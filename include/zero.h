@@ -304,7 +304,10 @@ int zero3_reduce_scatter_unit_clip(const zero_unit_t* unit, int32_t n_ranks,
  *                unit->shard_offset), read only
  *   norm_coef    NULL or the device float[2] of zero_clip_coef
  *   other arguments as zero3_reduce_scatter_unit
- * 30 bytes per parameter.  ZERO_EINVAL / ZERO_EALIGN / ZERO_ECUDA. */
+ * 30 bytes per parameter.  When every fp32 pointer (master, m, v and
+ * grad_shard, at this unit's offset) is 32-byte aligned the kernel moves 32
+ * bytes per access, else 16; the bits are the same.
+ * ZERO_EINVAL / ZERO_EALIGN / ZERO_ECUDA. */
 int zero3_update_unit_reduced(const zero_unit_t* unit, int32_t n_ranks,
                               const float* const* grad_shard, float* const* master,
                               float* const* m, float* const* v, uint16_t* const* shard_bf16,
@@ -334,7 +337,9 @@ int zero3_update_unit_reduced(const zero_unit_t* unit, int32_t n_ranks,
  * HBM bytes per parameter of a clipped step: 2N + 4 for the norm pass and
  * 30 for the update = 2N + 34, against 4N + 26 for zero_grad_sqnorm +
  * zero_step_stage12_clip (50 against 58 at N = 8).  The price is the fp32
- * shard: 4 bytes per parameter of device memory.
+ * shard: 4 bytes per parameter of device memory.  The update moves 32 bytes
+ * per access when every fp32 pointer (master, m, v, grad_shard) is 32-byte
+ * aligned, else 16; the bits are the same.
  * ZERO_EINVAL / ZERO_EALIGN / ZERO_ECUDA. */
 int zero_grad_reduce_sqnorm(int32_t n_ranks, int64_t n_elems, const uint16_t* const* grads,
                             float* const* grad_shard, int32_t accumulate, double* scratch,
