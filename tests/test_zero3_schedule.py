@@ -180,3 +180,29 @@ def test_no_reshard_saves_one_gather_per_unit(orc):
     assert kinds.count("gather") == 2 and kinds.count("reduce_scatter") == 2
     assert orc.comm_volume(3, 1, False, 1.0) == 2.0
     assert all(o[3] == 2 for o in B.zero3_plan(4, False, False, False) if o[0] in ("gather", "use"))
+
+
+@pytest.mark.parametrize("regen,clip", [(False, False), (False, True), (True, False), (True, True)])
+def test_which_main_stream_launches_follow_one_another(regen, clip):
+    """zero3_step chains a norm pass to a norm pass issued right before it on
+    the main stream, and a unit update to an update right before it, where
+    nothing else was issued between them (USE issues nothing; an event record
+    or wait, a regeneration or a gather's release does).  The plan fixes
+    where that happens: the norm passes follow one another unless the
+    regeneration of the gradients each reads sits between; without
+    resharding the backward updates follow one another unless regenerations
+    separate them; with resharding an event record and wait always separate
+    two updates, so those stay unchained."""
+    from fsdp_sharded_optimizer_gb300 import _binding as B
+    n = 6
+    for reshard in (True, False):
+        main = [o for o in B.zero3_plan(n, regen, clip, reshard) if o[1] == 0 and o[0] != "use"]
+        pairs = list(zip(main, main[1:]))
+        rs_pairs = [(a, b) for a, b in pairs if a[0] == b[0] == "reduce_scatter"]
+        norm_pairs = [(a, b) for a, b in pairs if a[0] == b[0] == "norm"]
+        assert len(rs_pairs) == (n - 1 if not reshard and not regen else 0)
+        assert len(norm_pairs) == (n - 1 if clip and not regen else 0)
+        # chained neighbours always work on different units
+        assert all(a[2] != b[2] for a, b in rs_pairs + norm_pairs)
+        # a norm pass that adds to the partials (arg 1) is never the first of the step
+        assert all(b[3] == 1 for _, b in norm_pairs)
