@@ -43,6 +43,11 @@ constexpr int kMinBlocksPerSM = 3;
 constexpr int kSmallRanks = 4;
 constexpr int kMinBlocksPerSMSmall = 4;
 constexpr int kRankBatchSmall = 4;
+// From kManyRanks ranks on, the bf16-gradient steps take the same four-block
+// shape again: more threads, each with 4-rank load batches, beat fewer with
+// 8-rank ones once gradients are most of the bytes (GB300, GPT-2 buffer,
+// GB/s: N_d = 32 6,980 -> 7,012, N_d = 64 6,990 -> 7,098; N_d = 16 equal).
+constexpr int kManyRanks = 32;
 
 // Per-rank device pointers, passed by value in the kernel's parameter space
 // (5 x 64 x 8 B = 2.5 KB).  o[k] points at rank k's output slice: the
@@ -90,7 +95,8 @@ __device__ __forceinline__ void adamw(float g, float& w, float& m, float& v,
 // gradient shard T.a[k] (written by zero_grad_reduce_sqnorm) instead of the
 // N rank gradients.  Used when a pointer is only 16-byte aligned;
 // fused_step_wide_kernel does the same with 32-byte accesses otherwise.
-// kSmall: the launch shape for up to kSmallRanks ranks (see kSmallRanks).
+// kSmall: the four-block launch shape (up to kSmallRanks ranks, and for bf16
+// gradients from kManyRanks on).
 template <bool kClip, bool kAcc, bool kF32 = false, bool kG32 = false, bool kSmall = false>
 __global__ void __launch_bounds__(kBlock, kSmall ? kMinBlocksPerSMSmall : kMinBlocksPerSM)
 fused_step_kernel(const __grid_constant__ Tables T, const StepScalars s, const Range R,
@@ -459,7 +465,7 @@ int launch_range(const Tables& T, const StepScalars& s, int64_t q0, int64_t q1, 
                   : launch_fused<false, false, true, false, false>(blocks, stream, chained, T, s,
                                                                    R, nullptr));
     }
-    return n_ranks <= kSmallRanks
+    return n_ranks <= kSmallRanks || n_ranks >= kManyRanks
                ? launch_bf16<true>(T, s, q0, q1, shard_vec, n_ranks, clip, stream, inv_m, chained)
                : launch_bf16<false>(T, s, q0, q1, shard_vec, n_ranks, clip, stream, inv_m, chained);
 }
