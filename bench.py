@@ -9,7 +9,7 @@ bf16 all-gather over the whole buffer (ZeRO-1: chained launches of 25 MiB
 chunks); the ZeRO-2 step (25 MiB buckets, the same bits) is timed beside it.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
-                    [--workload NAME]
+                    [--workload NAME | --workload flat-<P>-n<N_d>] [--headline-only]
 
 Prints one JSON line.  `value` is parameters updated per second over all GPUs
 with inputs resident in HBM; `e2e` is the same metric through the C ABI with
@@ -56,6 +56,28 @@ WORKLOADS = {
                           "per block + root"),
 }
 DEFAULT_WORKLOAD = "gpt2-small-flat-n8"
+FLAT_WORKLOAD = re.compile(r"flat-(\d+)-n(\d+)$")  # any flat buffer: flat-<P>-n<N_d>
+
+
+def workload(name):
+    """(unit sizes, N_d, description) of a named workload, or of flat-<P>-n<N_d>
+    (one flat buffer of P parameters, e.g. the sweep's flat-1073741824-n64)."""
+    if name in WORKLOADS:
+        return WORKLOADS[name]
+    mt = FLAT_WORKLOAD.match(name)
+    if not mt or int(mt.group(1)) < 1 or not 1 <= int(mt.group(2)) <= 64:
+        raise ValueError("unknown workload %r: one of %s, or flat-<P>-n<N_d> (N_d <= 64)"
+                         % (name, ", ".join(sorted(WORKLOADS))))
+    P, N = int(mt.group(1)), int(mt.group(2))
+    return [P], N, "flat P=%d, N_d=%d" % (P, N)
+
+
+def _workload_arg(name):
+    try:
+        workload(name)
+    except ValueError as e:
+        raise argparse.ArgumentTypeError(str(e))
+    return name
 FUSED_SOURCES = ["fsdp_sharded_optimizer_gb300/csrc/fused_step.cu",
                  "fsdp_sharded_optimizer_gb300/csrc/device.cuh"]
 
@@ -66,7 +88,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--workload", type=_workload_arg, default=DEFAULT_WORKLOAD,
+                    help="one of %s, or flat-<P>-n<N_d>" % ", ".join(sorted(WORKLOADS)))
     ap.add_argument("--e2e-steps", type=int, default=None,
                     help="steps of the end-to-end (host buffers) measurement; default min(K, 50)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -107,7 +130,7 @@ def fused_source_sha():
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(workload, launches_per_step=1):
+def ncu_traffic(workload_name, launches_per_step=1):
     """DRAM bytes per launch of the fused kernel from the committed ncu summary
     (its DRAM bytes over one whole step, divided by the step's launches), if it
     was taken on this kernel source and workload; else None."""
@@ -119,7 +142,7 @@ def ncu_traffic(workload, launches_per_step=1):
         return None
     sha = fused_source_sha()
     for r in rows:
-        if r.get("source_sha") == sha and r.get("workload") == workload:
+        if r.get("source_sha") == sha and r.get("workload") == workload_name:
             return float(r["dram_bytes_per_step"]) / launches_per_step
     return None
 
@@ -264,7 +287,7 @@ def run_gpu(args):
         torch.distributed.init_process_group("nccl")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    units, N, desc = WORKLOADS[args.workload]
+    units, N, desc = workload(args.workload)
     if len(units) > 1:
         return run_gpu_zero3(args, torch, Z, world, rank, dev)
     K, W = args.steps, args.warmup
@@ -514,7 +537,7 @@ def run_gpu_zero3(args, torch, Z, world, rank, dev):
     the per-unit regeneration from the seed (the harness's stand-in for the
     backward compute) is timed separately."""
 
-    unit_sizes, N, desc = WORKLOADS[args.workload]
+    unit_sizes, N, desc = workload(args.workload)
     K, W = args.steps, args.warmup
     units, total = Z.zero_layout(unit_sizes, N)
     P = sum(unit_sizes)
@@ -727,7 +750,7 @@ def run_gpu_zero3(args, torch, Z, world, rank, dev):
 
 
 # ------------------------------------------------------------------ CPU oracle
-def cpu_baseline(workload, steps, sample_params=2**22):
+def cpu_baseline(workload_name, steps, sample_params=2**22):
     """The oracle as it stands, single-threaded, on the first `sample_params`
     parameters of the workload (same generator, same N_d), timed over `steps`
     fused steps after the inputs are generated."""
@@ -735,7 +758,7 @@ def cpu_baseline(workload, steps, sample_params=2**22):
 
     import oracle as orc
 
-    unit_sizes, N, _ = WORKLOADS[workload]
+    unit_sizes, N, _ = workload(workload_name)
     P = min(sample_params, sum(unit_sizes))
     (u,), _ = orc.layout([P], N)
     w = orc.gen_master(0, SIGMA_W, [u], N)
@@ -748,14 +771,14 @@ def cpu_baseline(workload, steps, sample_params=2**22):
     dt = time.perf_counter() - t0
     return {"value": P * steps / dt, "unit": "params/s", "cores": 1, "kind": "oracle",
             "sample": "first %d params of %s, N_d=%d, %d ZeRO-1 steps, inputs pre-generated"
-                      % (P, workload, N, steps), "seconds": dt}
+                      % (P, workload_name, N, steps), "seconds": dt}
 
 
 def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return None
-    _, N, _ = WORKLOADS[args.workload]
+    _, N, _ = workload(args.workload)
     per_step_params = 2**20
     cb_w = cpu_baseline(args.workload, steps=max(1, args.warmup), sample_params=per_step_params)
     cb = cpu_baseline(args.workload, steps=args.steps, sample_params=per_step_params)

@@ -38,3 +38,16 @@ def test_max_over_two_gloo_ranks():
 def test_single_rank_time_is_unchanged():
     import bench
     assert bench.max_over_ranks(torch, 1, 3.5, torch.device("cpu")) == 3.5
+
+
+def test_workload_names():
+    """Named workloads and the flat-<P>-n<N_d> form (the sweep's sizes)."""
+    import pytest
+
+    import bench
+    assert bench.workload("gpt2-small-flat-n8")[:2] == ([124_439_808], 8)
+    assert bench.workload("flat-1073741824-n64")[:2] == ([2**30], 64)
+    assert bench.workload("flat-65573-n2")[:2] == ([2**16 + 37], 2)
+    for bad in ("flat-0-n8", "flat-10-n0", "flat-10-n65", "flat-10", "gpt3"):
+        with pytest.raises(ValueError):
+            bench.workload(bad)
