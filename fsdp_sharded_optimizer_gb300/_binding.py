@@ -129,6 +129,10 @@ SIGNATURES = {
     # reshard_after_forward, capture stream, side stream, out handle
     "zero3_graph_create": (C.c_int, [_P, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I32,
                                      _P, _P, _P]),
+    # units, n_units, n_ranks, grads (fp32), master, m, v, shards, full_a, full_b, hp,
+    # reshard_after_forward, capture stream, side stream, out handle
+    "zero3_graph_create_f32grads": (C.c_int, [_P, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P,
+                                              _I32, _P, _P, _P]),
     "zero3_graph_launch": (C.c_int, [_P, _P, _P]),
     "zero3_graph_destroy": (C.c_int, [_P]),
     "zero_gen_grads_unit": (C.c_int, [_U64, _I64, _F64, _I32, _P, _I32, _P, _P]),
@@ -458,7 +462,7 @@ def zero3_step_f32grads(units, grads, master, m, v, shard_bf16, full_a, full_b, 
 
 
 class Zero3Graph:
-    """A handle from zero3_graph_create.  It keeps the captured tensors alive
+    """A handle from zero3_graph_create(_f32grads).  It keeps the captured tensors alive
     (the graph holds their addresses) until zero3_graph_destroy."""
 
     def __init__(self, handle, keep):
@@ -491,6 +495,28 @@ def zero3_graph_create(units, grads, master, m, v, shard_bf16, full_a, full_b, h
         C.byref(clip) if clip is not None else None, 1 if reshard_after_forward else 0,
         _stream(capture_stream), _stream(side_stream), C.byref(h)))
     return Zero3Graph(h, (grads, master, m, v, shard_bf16, full_a, full_b, clip))
+
+
+def zero3_graph_create_f32grads(units, grads, master, m, v, shard_bf16, full_a, full_b, hp,
+                                capture_stream, side_stream, reshard_after_forward=True):
+    """zero3_graph_create for fp32 rank gradients (zero3_step_f32grads's step,
+    gradients resident, no clipping)."""
+    if capture_stream is None or side_stream is None:
+        raise ValueError("zero3_graph_create_f32grads needs two explicit streams (the default "
+                         "stream cannot be captured)")
+    g, rows = _rows(grads, 4, "grads")
+    w, _ = _rows(master, 4, "master")
+    mm, _ = _rows(m, 4, "m")
+    vv, _ = _rows(v, 4, "v")
+    s, _ = _rows(shard_bf16, 2, "shard_bf16")
+    arr = (zero_unit_t * len(units))(*units)
+    h = C.c_void_p()
+    _check("zero3_graph_create_f32grads", lib.zero3_graph_create_f32grads(
+        arr, len(units), len(rows), g, w, mm, vv, s, _dev(full_a, 2, "full_a"),
+        _dev(full_b, 2, "full_b") if full_b is not None else None, C.byref(hp),
+        1 if reshard_after_forward else 0, _stream(capture_stream), _stream(side_stream),
+        C.byref(h)))
+    return Zero3Graph(h, (grads, master, m, v, shard_bf16, full_a, full_b))
 
 
 def zero3_graph_launch(graph, hp, stream=None):

@@ -2,7 +2,7 @@
 // a CUDA graph (zero3_graph_create) and replayed once per step
 // (zero3_graph_launch).
 //
-// The step is the one zero3_step issues: the forward gathers, the backward
+// The step is the one zero3_step (or zero3_step_f32grads) issues: the forward gathers, the backward
 // gathers and per-unit reduce-scatter + AdamW ("Data parallelism, ZeRO and
 // FSDP", "How FSDP implements ZeRO-3", steps 2-5), side-stream prefetch and
 // two full-unit buffers.  Stream capture turns its event records and waits
@@ -115,14 +115,15 @@ int chain_gathers(cudaGraph_t graph, const std::vector<GatherNode>& gathers)
 
 } // namespace
 
-extern "C" int zero3_graph_create(const zero_unit_t* units, int32_t n_units, int32_t n_ranks,
-                                  const uint16_t* const* grads, float* const* master,
-                                  float* const* m, float* const* v,
-                                  uint16_t* const* shard_bf16, uint16_t* full_a,
-                                  uint16_t* full_b, const zero_hparams_t* hp,
-                                  const zero_clip_t* clip, int32_t reshard_after_forward,
-                                  cudaStream_t capture_stream, cudaStream_t side_stream,
-                                  zero3_graph_t** out)
+namespace {
+
+// Captures the step that issue() queues on capture_stream (and side_stream),
+// joins its launches with programmatic edges and instantiates the graph.
+template <typename Issue>
+int create_graph(const zero_unit_t* units, int32_t n_units, int32_t n_ranks,
+                 const zero_hparams_t* hp, bool clip, int32_t reshard_after_forward,
+                 cudaStream_t capture_stream, cudaStream_t side_stream, zero3_graph_t** out,
+                 Issue issue)
 {
     if (!out) return ZERO_EINVAL;
     *out = nullptr;
@@ -156,10 +157,9 @@ extern "C" int zero3_graph_create(const zero_unit_t* units, int32_t n_units, int
         step_nodes_free(nodes);
         return cuda_status(e);
     }
-    // zero3_step checks every argument before it issues anything; a rejected
+    // The step checks every argument before it issues anything; a rejected
     // call leaves an empty capture behind, which is discarded below.
-    rc = zero3_step(units, n_units, n_ranks, grads, 1, master, m, v, shard_bf16, full_a, full_b,
-                    hp, nullptr, clip, reshard_after_forward, capture_stream, side_stream);
+    rc = issue();
     cudaGraph_t graph = nullptr;
     e = cudaStreamEndCapture(capture_stream, &graph);
     step_nodes_end();
@@ -192,6 +192,45 @@ extern "C" int zero3_graph_create(const zero_unit_t* units, int32_t n_units, int
     }
     *out = g;
     return ZERO_OK;
+}
+
+} // namespace
+
+extern "C" int zero3_graph_create(const zero_unit_t* units, int32_t n_units, int32_t n_ranks,
+                                  const uint16_t* const* grads, float* const* master,
+                                  float* const* m, float* const* v,
+                                  uint16_t* const* shard_bf16, uint16_t* full_a,
+                                  uint16_t* full_b, const zero_hparams_t* hp,
+                                  const zero_clip_t* clip, int32_t reshard_after_forward,
+                                  cudaStream_t capture_stream, cudaStream_t side_stream,
+                                  zero3_graph_t** out)
+{
+    return create_graph(units, n_units, n_ranks, hp, clip != nullptr, reshard_after_forward,
+                        capture_stream, side_stream, out, [&] {
+                            return zero3_step(units, n_units, n_ranks, grads, 1, master, m, v,
+                                              shard_bf16, full_a, full_b, hp, nullptr, clip,
+                                              reshard_after_forward, capture_stream,
+                                              side_stream);
+                        });
+}
+
+extern "C" int zero3_graph_create_f32grads(const zero_unit_t* units, int32_t n_units,
+                                           int32_t n_ranks, const float* const* grads,
+                                           float* const* master, float* const* m,
+                                           float* const* v, uint16_t* const* shard_bf16,
+                                           uint16_t* full_a, uint16_t* full_b,
+                                           const zero_hparams_t* hp,
+                                           int32_t reshard_after_forward,
+                                           cudaStream_t capture_stream, cudaStream_t side_stream,
+                                           zero3_graph_t** out)
+{
+    return create_graph(units, n_units, n_ranks, hp, false, reshard_after_forward,
+                        capture_stream, side_stream, out, [&] {
+                            return zero3_step_f32grads(units, n_units, n_ranks, grads, master, m,
+                                                       v, shard_bf16, full_a, full_b, hp,
+                                                       reshard_after_forward, capture_stream,
+                                                       side_stream);
+                        });
 }
 
 extern "C" int zero3_graph_launch(zero3_graph_t* graph, const zero_hparams_t* hp,

@@ -538,6 +538,10 @@ int zero3_step_f32grads(const zero_unit_t* units, int32_t n_units, int32_t n_ran
  * launch; a replay already queued keeps the scalars it was launched with.
  * Launches of one graph must be made from one host thread at a time.
  *
+ * zero3_graph_create_f32grads -- the same for zero3_step_f32grads: grads
+ * holds each rank's fp32 gradients of every unit (resident), there is no
+ * clipping; the other arguments, the graph and its launches as above.
+ *
  * zero3_graph_destroy -- releases the graph (NULL: no-op).  Call it after
  * the last launch has completed. */
 typedef struct zero3_graph zero3_graph_t;
@@ -547,6 +551,12 @@ int zero3_graph_create(const zero_unit_t* units, int32_t n_units, int32_t n_rank
                        uint16_t* full_b, const zero_hparams_t* hp, const zero_clip_t* clip,
                        int32_t reshard_after_forward, cudaStream_t capture_stream,
                        cudaStream_t side_stream, zero3_graph_t** out);
+int zero3_graph_create_f32grads(const zero_unit_t* units, int32_t n_units, int32_t n_ranks,
+                                const float* const* grads, float* const* master,
+                                float* const* m, float* const* v, uint16_t* const* shard_bf16,
+                                uint16_t* full_a, uint16_t* full_b, const zero_hparams_t* hp,
+                                int32_t reshard_after_forward, cudaStream_t capture_stream,
+                                cudaStream_t side_stream, zero3_graph_t** out);
 int zero3_graph_launch(zero3_graph_t* graph, const zero_hparams_t* hp, cudaStream_t stream);
 int zero3_graph_destroy(zero3_graph_t* graph);
 

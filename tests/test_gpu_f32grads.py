@@ -121,3 +121,64 @@ def test_native_zero3_step_with_f32_grads_matches_oracle(orc, reshard):
                          ("v", v.numpy(), rv), ("shards", shards.numpy(), rs)):
         H.assert_bitwise(g_, r_, name)
     H.free()
+
+
+@pytest.mark.parametrize("reshard", [True, False])
+def test_zero3_graph_with_f32_grads_matches_oracle(orc, reshard):
+    """zero3_graph_create_f32grads: the fp32-gradient ZeRO-3 step captured once
+    and replayed with new AdamW scalars each step (t, lr and weight decay
+    change) equals the oracle's fp32-gradient unit reduce-scatters bit for bit.
+    One unit spans two chained chunks, so a replay patches several nodes per
+    unit; the full-unit buffers end each step holding the weights the last
+    gathers had to read."""
+    N, T, seed = 4, 3, 9
+    sizes = [70_000, 333, B.ZERO_CHUNK_ELEMS + 4096, 64]
+    units, total = B.zero_layout(sizes, N)
+    ounits, _ = orc.layout(sizes, N)
+    S = total // N
+    master = H.Guarded(N, S, torch.float32)
+    m = H.Guarded(N, S, torch.float32).zero_()
+    v = H.Guarded(N, S, torch.float32).zero_()
+    shards = H.Guarded(N, S, torch.int16)
+    B.zero_gen_master(seed, H.SIGMA_W, units, master.rows)
+    for k in range(N):
+        B.zero_cast_bf16(master.rows[k], shards.rows[k])
+    grads = H.Guarded(N, total, torch.float32)
+    max_unit = max(u.n_padded for u in units)
+    fa = H.Guarded(1, max_unit if reshard else total, torch.int16)
+    fb = H.Guarded(1, max_unit, torch.int16)
+    rw = orc.gen_master(seed, H.SIGMA_W, ounits, N)
+    rm, rv = np.zeros_like(rw), np.zeros_like(rw)
+    rs = orc.bf16_rne(rw)
+    hp_of = lambda t: dict(H.HP, lr=1e-3 * (1 + t) / 4, weight_decay=0.01 * t)
+    cap, side = torch.cuda.Stream(), torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    g = B.zero3_graph_create_f32grads(units, grads.rows, master.rows, m.rows, v.rows,
+                                      shards.rows, fa.rows[0], fb.rows[0] if reshard else None,
+                                      B.hparams(**hp_of(1), step=1), cap, side,
+                                      reshard_after_forward=reshard)
+    before = None
+    try:
+        for t in range(1, T + 1):
+            for u in units:
+                B.zero_gen_grads_unit_f32(seed, t, H.SIGMA_G, 1, u,
+                                          [r[u.offset:u.offset + u.n_padded] for r in grads.rows])
+            g.launch(B.hparams(**hp_of(t), step=t))
+            before = rs.copy()
+            for ou in reversed(ounits):
+                gr = orc.gen_grads_unit_f32(seed, t, H.SIGMA_G, 1, ou, N)
+                orc.zero3_reduce_scatter_unit_f32grads(ou, gr, rw, rm, rv, rs,
+                                                       orc.hparams(**hp_of(t), step=t))
+        torch.cuda.synchronize()
+    finally:
+        g.close()
+    for b_ in (master, m, v, shards, grads, fa, fb):
+        b_.check()
+    for name, g_, r_ in (("master", master.numpy(), rw), ("m", m.numpy(), rm),
+                         ("v", v.numpy(), rv), ("shards", shards.numpy(), rs)):
+        H.assert_bitwise(g_, r_, name)
+    # the weights every unit had before the last step, as the oracle's shards held them
+    flat = np.concatenate([np.concatenate([before[k][u.shard_offset:u.shard_offset + u.shard_len]
+                                           for k in range(N)])[:u.n_params] for u in ounits])
+    H.assert_gathered(units, sizes, flat, fa, fb if reshard else None)
+    H.free()

@@ -212,8 +212,9 @@ def test_zero3_step_rejects_before_launch(B):
 
 @host_only
 def test_zero3_graph_rejects_before_capture(B):
-    """Arguments zero3_graph_create can judge on the host are rejected before
-    any CUDA call; the handle stays NULL.  Launch and destroy take NULL."""
+    """Arguments zero3_graph_create (and its fp32-gradient form) can judge on
+    the host are rejected before any CUDA call; the handle stays NULL.  Launch
+    and destroy take NULL."""
     units, _ = B.zero_layout([1000, 64], 4)
     arr = (B.zero_unit_t * 2)(*units)
     hp, bad_hp = B.hparams(), B.hparams(step=0)
@@ -237,6 +238,13 @@ def test_zero3_graph_rejects_before_capture(B):
         assert call(*args) == B.ZERO_EINVAL
         assert h.value is None  # *out cleared
     assert call(arr, 2, 4, t, t, t, t, t, fa, fb, C.byref(hp), None, 1, s1, s2, None) == B.ZERO_EINVAL
+    # the fp32-gradient form: the same argument, minus clip
+    call = B.lib.zero3_graph_create_f32grads
+    for args in bad:
+        h.value = 0x1234
+        assert call(*(args[:11] + args[12:])) == B.ZERO_EINVAL
+        assert h.value is None
+    assert call(arr, 2, 4, t, t, t, t, t, fa, fb, C.byref(hp), 1, s1, s2, None) == B.ZERO_EINVAL
     assert B.lib.zero3_graph_launch(None, C.byref(hp), s1) == B.ZERO_EINVAL
     assert B.lib.zero3_graph_destroy(None) == B.ZERO_OK
 
