@@ -116,6 +116,11 @@ SIGNATURES = {
     "zero_gen_grads_unit_f32": (C.c_int, [_U64, _I64, _F64, _I32, _P, _I32, _P, _P]),
     "zero2_accumulate": (C.c_int, [_I32, _I64, _P, _P, _I32, _P]),
     "zero2_step_accumulated": (C.c_int, [_I32, _I64, _P, _P, _I32, _P, _P, _P, _P, _P, _P]),
+    # unit, n_ranks, unit grads, grad_acc storage, first, stream
+    "zero3_accumulate_unit": (C.c_int, [_P, _I32, _P, _P, _I32, _P]),
+    # unit, n_ranks, unit grads, grad_acc storage, micro_batches, master, m, v, shards, hp, stream
+    "zero3_reduce_scatter_unit_accumulated": (C.c_int, [_P, _I32, _P, _P, _I32, _P, _P, _P, _P,
+                                                        _P, _P]),
     "zero3_plan": (C.c_int, [_I32, _I32, _I32, _I32, _P, _I32, _P]),
     # units, n_units, n_ranks, grads, resident, master, m, v, shards, full_a, full_b, hp,
     # regen, clip, reshard_after_forward, main stream, side stream
@@ -388,6 +393,29 @@ def zero2_step_accumulated(grads, grad_acc, micro_batches, master, m, v, params_
     _check("zero2_step_accumulated", lib.zero2_step_accumulated(
         len(grows), grows[0].numel(), g, a, int(micro_batches), w, mm, vv,
         _dev(params_bf16, 2, "params_bf16"), C.byref(hp), _stream(stream)))
+
+
+def zero3_accumulate_unit(unit, unit_grads, grad_acc, first, stream=None):
+    """One earlier micro-batch of a ZeRO-3 unit: grad_acc (N x S_total fp32,
+    laid out like master) at the unit's offset = (first ? 0 : it) + the mean."""
+    g, grows = _rows(unit_grads, 2, "unit_grads")
+    a, _ = _rows(grad_acc, 4, "grad_acc")
+    _check("zero3_accumulate_unit", lib.zero3_accumulate_unit(
+        C.byref(unit), len(grows), g, a, 1 if first else 0, _stream(stream)))
+
+
+def zero3_reduce_scatter_unit_accumulated(unit, unit_grads, grad_acc, micro_batches, master, m, v,
+                                          shard_bf16, hp, stream=None):
+    """The unit's last micro-batch fused with its update: g = (grad_acc + mean) / m."""
+    g, grows = _rows(unit_grads, 2, "unit_grads")
+    a, _ = _rows(grad_acc, 4, "grad_acc")
+    w, _ = _rows(master, 4, "master")
+    mm, _ = _rows(m, 4, "m")
+    vv, _ = _rows(v, 4, "v")
+    s, _ = _rows(shard_bf16, 2, "shard_bf16")
+    _check("zero3_reduce_scatter_unit_accumulated", lib.zero3_reduce_scatter_unit_accumulated(
+        C.byref(unit), len(grows), g, a, int(micro_batches), w, mm, vv, s, C.byref(hp),
+        _stream(stream)))
 
 
 def zero_grad_nonfinite(grads, counts, reset=True, stream=None):

@@ -552,16 +552,21 @@ int step_stage12(int32_t stage, int32_t n_ranks, int64_t n_padded, const void* c
 // g32: unit_grads holds each rank's fp32 gradient-shard storage of all units
 // (laid out like master; this unit at shard_offset) instead of the unit's
 // rank gradients.
+// A unit layout a ZeRO-3 call can use with n_ranks ranks.
+bool unit_valid(const zero_unit_t* unit, int32_t n_ranks)
+{
+    return unit && n_ranks >= 1 && n_ranks <= ZERO_MAX_RANKS && unit->n_padded > 0 &&
+           unit->shard_len > 0 && unit->shard_len % 8 == 0 &&
+           unit->shard_len * n_ranks == unit->n_padded && unit->shard_offset >= 0 &&
+           unit->shard_offset % 8 == 0;
+}
+
 int rs_unit(const zero_unit_t* unit, int32_t n_ranks, const void* const* unit_grads,
             float* const* master, float* const* m, float* const* v, uint16_t* const* shard_bf16,
             const zero_hparams_t* hp, const float* clip, cudaStream_t stream, bool f32 = false,
             bool g32 = false, bool chain_first = false)
 {
-    if (!unit || n_ranks < 1 || n_ranks > ZERO_MAX_RANKS || unit->n_padded <= 0 ||
-        unit->shard_len <= 0 || unit->shard_len % 8 != 0 ||
-        unit->shard_len * n_ranks != unit->n_padded || unit->shard_offset < 0 ||
-        unit->shard_offset % 8 != 0 || !valid_hparams(hp))
-        return ZERO_EINVAL;
+    if (!unit_valid(unit, n_ranks) || !valid_hparams(hp)) return ZERO_EINVAL;
     int rc = check_state_tables(n_ranks, reinterpret_cast<const uint16_t* const*>(unit_grads), master, m,
                                 v);
     if (rc != ZERO_OK) return rc;
@@ -824,6 +829,52 @@ extern "C" int zero2_step_accumulated(int32_t n_ranks, int64_t n_padded,
     const StepScalars s = make_scalars(hp, n_ranks);
     const float inv_m = static_cast<float>(1.0 / static_cast<double>(micro_batches));
     return launch(T, s, 0, n_padded / 8, S / 8, n_ranks, nullptr, stream, inv_m);
+}
+
+extern "C" int zero3_accumulate_unit(const zero_unit_t* unit, int32_t n_ranks,
+                                     const uint16_t* const* unit_grads, float* const* grad_acc,
+                                     int32_t first, cudaStream_t stream)
+{
+    if (!unit_valid(unit, n_ranks)) return ZERO_EINVAL;
+    const int rc = check_table(grad_acc, n_ranks);
+    if (rc != ZERO_OK) return rc;
+    float* acc[ZERO_MAX_RANKS];
+    for (int32_t r = 0; r < n_ranks; ++r) acc[r] = grad_acc[r] + unit->shard_offset;
+    return zero2_accumulate(n_ranks, unit->n_padded, unit_grads, acc, first, stream);
+}
+
+extern "C" int zero3_reduce_scatter_unit_accumulated(const zero_unit_t* unit, int32_t n_ranks,
+                                                     const uint16_t* const* unit_grads,
+                                                     float* const* grad_acc,
+                                                     int32_t micro_batches, float* const* master,
+                                                     float* const* m, float* const* v,
+                                                     uint16_t* const* shard_bf16,
+                                                     const zero_hparams_t* hp,
+                                                     cudaStream_t stream)
+{
+    if (micro_batches < 1) return ZERO_EINVAL;
+    if (micro_batches == 1) // nothing accumulated: the plain unit step
+        return zero3_reduce_scatter_unit(unit, n_ranks, unit_grads, master, m, v, shard_bf16, hp,
+                                         stream);
+    if (!unit_valid(unit, n_ranks) || !valid_hparams(hp)) return ZERO_EINVAL;
+    int rc = check_state_tables(n_ranks, unit_grads, master, m, v);
+    if (rc != ZERO_OK) return rc;
+    if ((rc = check_table(shard_bf16, n_ranks)) != ZERO_OK) return rc;
+    if ((rc = check_table(grad_acc, n_ranks)) != ZERO_OK) return rc;
+    const int64_t off = unit->shard_offset;
+    Tables T = {};
+    for (int32_t r = 0; r < n_ranks; ++r) {
+        T.g[r] = reinterpret_cast<const uint4*>(unit_grads[r]);
+        T.w[r] = reinterpret_cast<float4*>(master[r] + off);
+        T.m[r] = reinterpret_cast<float4*>(m[r] + off);
+        T.v[r] = reinterpret_cast<float4*>(v[r] + off);
+        T.o[r] = reinterpret_cast<uint4*>(shard_bf16[r] + off);
+        T.a[r] = reinterpret_cast<float4*>(grad_acc[r] + off);
+    }
+    const StepScalars s = make_scalars(hp, n_ranks);
+    const float inv_m = static_cast<float>(1.0 / static_cast<double>(micro_batches));
+    return launch(T, s, 0, unit->n_padded / 8, unit->shard_len / 8, n_ranks, nullptr, stream,
+                  inv_m);
 }
 
 extern "C" int zero_step_stage12_f32grads(int32_t stage, int32_t n_ranks, int64_t n_padded,

@@ -242,6 +242,37 @@ int zero2_step_accumulated(int32_t n_ranks, int64_t n_padded, const uint16_t* co
                            float* const* m, float* const* v, uint16_t* params_bf16,
                            const zero_hparams_t* hp, cudaStream_t stream);
 
+/* The same accumulation per ZeRO-3 unit (FSDP with m micro-batches: every
+ * micro-batch gathers and reduce-scatters each unit, the 3mP volume of [DZF]
+ * "Gradient accumulation"; the update runs once, with the last one).
+ *
+ * zero3_accumulate_unit -- zero2_accumulate over one unit.
+ *   unit         a unit of zero_layout
+ *   unit_grads   n_ranks device pointers, each the unit's n_padded bf16
+ *                gradients of this micro-batch (read only)
+ *   grad_acc     n_ranks device pointers to each rank's fp32 accumulator
+ *                storage of all units (laid out like master: this unit at
+ *                unit->shard_offset)
+ *   first        1 for the step's first micro-batch (the accumulator is not
+ *                read), else 0
+ *
+ * zero3_reduce_scatter_unit_accumulated -- the unit's last micro-batch fused
+ * with its update: zero3_reduce_scatter_unit with g = (grad_acc + mean) *
+ * (1/m), m = micro_batches >= 1 (m = 1: zero3_reduce_scatter_unit, grad_acc
+ * not read).  Other arguments as zero3_reduce_scatter_unit.  Each unit gives
+ * the bits zero2_accumulate / zero2_step_accumulated give on that unit as a
+ * flat buffer (rank k's shard = slice k of the replicated buffer).
+ * ZERO_EINVAL / ZERO_EALIGN / ZERO_ECUDA. */
+int zero3_accumulate_unit(const zero_unit_t* unit, int32_t n_ranks,
+                          const uint16_t* const* unit_grads, float* const* grad_acc,
+                          int32_t first, cudaStream_t stream);
+int zero3_reduce_scatter_unit_accumulated(const zero_unit_t* unit, int32_t n_ranks,
+                                          const uint16_t* const* unit_grads,
+                                          float* const* grad_acc, int32_t micro_batches,
+                                          float* const* master, float* const* m,
+                                          float* const* v, uint16_t* const* shard_bf16,
+                                          const zero_hparams_t* hp, cudaStream_t stream);
+
 /* ---------------------------------------------------------------------
  * Global gradient-norm clipping across the shards.  [DZF] "7. Common
  * mistakes" (local gradient clipping: with sharded gradients the global norm

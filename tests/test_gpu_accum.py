@@ -53,3 +53,65 @@ def test_accumulated_zero2_matches_oracle(orc, N, P, micro, T):
     if micro > 1:
         H.assert_bitwise(acc.numpy(), ra, "accumulator")
     assert not got[0][P:].any()
+
+
+@pytest.mark.parametrize("micro", [1, 3])
+def test_zero3_unit_accumulation_matches_oracle(orc, micro):
+    """FSDP with m micro-batches: every micro-batch runs each unit's
+    reduce-scatter (zero3_accumulate_unit for the first m - 1, in the backward
+    order), and the last one is fused with the unit's update
+    (zero3_reduce_scatter_unit_accumulated), writing the unit's bf16 shards.
+    Each unit equals the oracle's ZeRO-2 accumulation on that unit as a flat
+    buffer bit for bit: rank k's shard of the unit is slice k of the oracle's
+    replicated buffer.  One unit spans two chained chunks; a unit-sized
+    gradient buffer per rank is refilled for every unit."""
+    N, T, seed = 4, 3, 21
+    sizes = [70_000, 333, B.ZERO_CHUNK_ELEMS + 4096, 64]
+    units, total = B.zero_layout(sizes, N)
+    ounits, _ = orc.layout(sizes, N)
+    S = total // N
+    master = H.Guarded(N, S, torch.float32)
+    m = H.Guarded(N, S, torch.float32).zero_()
+    v = H.Guarded(N, S, torch.float32).zero_()
+    acc = H.Guarded(N, S, torch.float32)
+    shards = H.Guarded(N, S, torch.int16)
+    B.zero_gen_master(seed, H.SIGMA_W, units, master.rows)
+    for k in range(N):
+        B.zero_cast_bf16(master.rows[k], shards.rows[k])
+    max_unit = max(u.n_padded for u in units)
+    grads = H.Guarded(N, max_unit, torch.int16)
+    rw_all = orc.gen_master(seed, H.SIGMA_W, ounits, N)
+    ref = []
+    for ou in ounits:
+        cols = slice(ou.shard_offset, ou.shard_offset + ou.shard_len)
+        w = np.ascontiguousarray(rw_all[:, cols])
+        ref.append(dict(w=w, m=np.zeros_like(w), v=np.zeros_like(w), a=np.zeros_like(w),
+                        p=np.zeros(ou.n_padded, np.uint16)))
+    for t in range(1, T + 1):
+        for mu in range(micro):
+            sid = t * 100 + mu
+            for i in reversed(range(len(units))):
+                u, ou, r = units[i], ounits[i], ref[i]
+                rows = [x[:u.n_padded] for x in grads.rows]
+                B.zero_gen_grads_unit(seed, sid, H.SIGMA_G, 1, u, rows)
+                g = orc.gen_grads_unit(seed, sid, H.SIGMA_G, 1, ou, N)
+                if mu < micro - 1:
+                    B.zero3_accumulate_unit(u, rows, acc.rows, first=mu == 0)
+                    orc.zero2_accumulate(g, r["a"], first=mu == 0)
+                else:
+                    B.zero3_reduce_scatter_unit_accumulated(u, rows, acc.rows, micro, master.rows,
+                                                            m.rows, v.rows, shards.rows, H.hp(t))
+                    orc.zero2_step_accumulated(g, r["a"] if micro > 1 else None, micro, r["w"],
+                                               r["m"], r["v"], r["p"], orc.hparams(**H.HP, step=t))
+    torch.cuda.synchronize()
+    for b_ in (master, m, v, acc, shards, grads):
+        b_.check()
+    got = dict(w=master.numpy(), m=m.numpy(), v=v.numpy(), a=acc.numpy(), p=shards.numpy())
+    for i, ou in enumerate(ounits):
+        cols = slice(ou.shard_offset, ou.shard_offset + ou.shard_len)
+        names = ("w", "m", "v", "a") if micro > 1 else ("w", "m", "v")
+        for name in names:
+            H.assert_bitwise(got[name][:, cols], ref[i][name], "unit %d %s" % (i, name))
+        H.assert_bitwise(got["p"][:, cols], ref[i]["p"].reshape(N, ou.shard_len),
+                         "unit %d shards" % i)
+    H.free()

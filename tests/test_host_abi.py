@@ -173,6 +173,20 @@ def test_zero3_calls_reject_before_launch(B):
     hp0 = B.hparams(step=0)
     assert B.lib.zero3_reduce_scatter_unit(C.byref(u), 4, t, t, t, t, t, C.byref(hp0),
                                            None) == B.ZERO_EINVAL
+    # gradient accumulation per unit
+    acc = B.lib.zero3_accumulate_unit
+    assert acc(None, 4, t, t, 1, None) == B.ZERO_EINVAL
+    assert acc(C.byref(u), 3, t, t, 1, None) == B.ZERO_EINVAL      # layout mismatch
+    assert acc(C.byref(bad), 4, t, t, 1, None) == B.ZERO_EINVAL
+    assert acc(C.byref(u), 4, t, None, 1, None) == B.ZERO_EINVAL
+    assert acc(C.byref(u), 4, t, _table(A16[:3] + [A16[3] + 4]), 1, None) == B.ZERO_EALIGN
+    last = B.lib.zero3_reduce_scatter_unit_accumulated
+    assert last(C.byref(u), 4, t, t, 0, t, t, t, t, C.byref(hp), None) == B.ZERO_EINVAL  # m = 0
+    assert last(C.byref(u), 4, t, t, -2, t, t, t, t, C.byref(hp), None) == B.ZERO_EINVAL
+    assert last(C.byref(bad), 4, t, t, 3, t, t, t, t, C.byref(hp), None) == B.ZERO_EINVAL
+    assert last(C.byref(u), 4, t, t, 3, t, t, t, t, C.byref(hp0), None) == B.ZERO_EINVAL
+    assert last(C.byref(u), 4, t, None, 3, t, t, t, t, C.byref(hp), None) == B.ZERO_EINVAL
+    assert last(C.byref(u), 4, t, t, 3, t, t, t, None, C.byref(hp), None) == B.ZERO_EINVAL
 
 
 def test_strerror_names_codes(B):
