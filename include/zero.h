@@ -37,8 +37,10 @@
  *    addressing; NVLink-C2C on Grace-Blackwell).
  *  - Arguments are checked on the host before anything is launched; a bad
  *    argument launches nothing.  ZERO_ECUDA reports a launch failure.
- *  - Stateless and re-entrant (zero3_step alone keeps a per-thread cache of
- *    five CUDA events).  1 <= n_ranks <= ZERO_MAX_RANKS.
+ *  - Stateless and re-entrant, with three documented exceptions: zero3_step
+ *    keeps a per-thread cache of five CUDA events, zero_clip_coef_units_noalloc
+ *    works in a library-internal device array, and a zero3_graph_t holds the
+ *    graph it captured.  1 <= n_ranks <= ZERO_MAX_RANKS.
  *
  * Layout (zero_layout): a unit of P true parameters is padded to
  * P' = ceil(P / (n_ranks*align)) * n_ranks*align; S = P'/n_ranks; rank k owns
