@@ -72,6 +72,7 @@ def lib():
             "or_adamw_f64": (None, [f64, P, P, P, P]),
             "or_zero12_step": (i32, [i32, i32, i64, P, P, P, P, P, P, i64]),
             "or_zero3_gather_unit": (i32, [P, i32, P, P]),
+            "or_reshard_f32": (i32, [P, i32, P, P, i32, P]),
             "or_zero3_reduce_scatter_unit": (i32, [P, i32, P, P, P, P, P, P]),
             "or_state_bytes": (i32, [i64, i32, i32, i32, P]),
             "or_ring_sent_bytes": (f64, [f64, i32, i32]),
@@ -186,6 +187,12 @@ def zero12_step(stage, grads, master, m, v, params, hp, bucket_elems=0):
 def zero3_gather_unit(unit, shards, full):
     _check(lib().or_zero3_gather_unit(C.byref(unit), shards.shape[0], _rows(shards),
                                       _ptr(full)), "or_zero3_gather_unit")
+
+
+def reshard_f32(from_unit, src, to_unit, dst):
+    """src: (n_from, S_total_from) fp32, dst: (n_to, S_total_to) fp32, written."""
+    _check(lib().or_reshard_f32(C.byref(from_unit), src.shape[0], _rows(src), C.byref(to_unit),
+                                dst.shape[0], _rows(dst)), "or_reshard_f32")
 
 
 def zero3_reduce_scatter_unit(unit, unit_grads, master, m, v, shards, hp):

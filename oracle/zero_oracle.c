@@ -219,6 +219,28 @@ int or_zero3_gather_unit(const or_unit_t* unit, int32_t n_ranks,
     return OR_OK;
 }
 
+/* A restart on another N_d ([DZF] "6. Where it shows up", checkpoints: sharded
+ * optimizer state must be resharded).  Element i of the unit's flat order
+ * (i < n_params) sits at rank i / S_from, position i % S_from, and moves to
+ * rank i / S_to, position i % S_to; the new layout's padding is +0. */
+int or_reshard_f32(const or_unit_t* from, int32_t n_from, const float* const* src,
+                   const or_unit_t* to, int32_t n_to, float* const* dst)
+{
+    if (!from || !to || n_from < 1 || n_to < 1 || !src || !dst ||
+        from->n_params != to->n_params || from->shard_len * n_from != from->n_padded ||
+        to->shard_len * n_to != to->n_padded)
+        return OR_EINVAL;
+    for (int32_t k = 0; k < n_to; ++k)
+        for (int64_t j = 0; j < to->shard_len; ++j) {
+            const int64_t i = (int64_t)k * to->shard_len + j;
+            float x = 0.0f;
+            if (i < to->n_params)
+                x = src[i / from->shard_len][from->shard_offset + i % from->shard_len];
+            dst[k][to->shard_offset + j] = x;
+        }
+    return OR_OK;
+}
+
 /* ZeRO-3 unit reduce-scatter followed by the owner's AdamW ([DZF] "How FSDP
  * implements ZeRO-3", steps 3-4; Theorem proof step 7: no all-gather follows
  * the update).  Rank k keeps the new fp32 state and its new bf16 shard. */

@@ -106,6 +106,11 @@ int or_zero3_reduce_scatter_unit(const or_unit_t* unit, int32_t n_ranks,
                                  float* const* v, uint16_t* const* shard_bf16,
                                  const or_hparams_t* hp);
 
+/* Re-lays one unit's per-rank fp32 state from n_from to n_to ranks (a
+ * restart on another N_d, [DZF] "6. Where it shows up", checkpoints). */
+int or_reshard_f32(const or_unit_t* from, int32_t n_from, const float* const* src,
+                   const or_unit_t* to, int32_t n_to, float* const* dst);
+
 /* ------------------------------------------------ global grad-norm clipping */
 double or_grad_sumsq(int32_t n_ranks, int64_t n, const uint16_t* const* grads);
 float or_clip_coef(double sumsq, double max_norm, double* out_norm);

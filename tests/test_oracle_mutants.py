@@ -51,6 +51,11 @@ MUTANTS = [
     ("f32_mean_not_scaled", "zero_oracle.c",
      "        g = g + grads[r][i];\n    return g * inv_n;", "        g = g + grads[r][i];\n    return g;"),
     ("generator_lane_dropped", "gen_oracle.c", "(int32_t)(h >> 48) - 131070", "(int32_t)(h >> 48) * 0 - 131070"),
+    ("reshard_source_rank_from_new_layout", "zero_oracle.c",
+     "x = src[i / from->shard_len][from->shard_offset + i % from->shard_len];",
+     "x = src[i / to->shard_len % n_from][from->shard_offset + i % from->shard_len];"),
+    ("reshard_ignores_unit_offset", "zero_oracle.c", "dst[k][to->shard_offset + j] = x;",
+     "dst[k][j] = x;"),
 ]
 
 

@@ -760,3 +760,48 @@ def test_nonfinite_counts_classify_every_bf16_pattern(orc):
         pos = rng.choice(5000, size=n, replace=False)
         g[r, pos] = rng.choice(np.array([0x7F80, 0xFF80, 0x7FC0, 0xFFC1], np.uint16), size=n)
     np.testing.assert_array_equal(orc.grad_nonfinite(g), planted)
+
+
+# ------------------------------------------------------------- resharding
+RESHARD_CASES = [([1000], 4, 8), ([1000], 8, 4), ([5, 64, 1, 130, 63, 2**16 + 37], 3, 64),
+                 ([5, 64, 1, 130, 63, 2**16 + 37], 64, 1), ([70_000, 333], 1, 7),
+                 ([7, 9], 2, 2)]
+
+
+@pytest.mark.parametrize("sizes,n_from,n_to", RESHARD_CASES)
+def test_reshard_maps_generated_state_onto_the_new_layout(orc, sizes, n_from, n_to):
+    """The generator keys every value by the parameter's true index and leaves
+    padding at +0, so the master weights generated for one rank count,
+    resharded unit by unit, are exactly those generated for the other: any
+    wrong index, offset or padding fails this."""
+    seed = 31
+    u_from, _ = orc.layout(sizes, n_from)
+    u_to, _ = orc.layout(sizes, n_to)
+    src = orc.gen_master(seed, 0.02, u_from, n_from)
+    dst = np.full((n_to, sum(u.shard_len for u in u_to)), np.nan, np.float32)
+    for a, b in zip(u_from, u_to):
+        orc.reshard_f32(a, src, b, dst)
+    want = orc.gen_master(seed, 0.02, u_to, n_to)
+    assert np.array_equal(dst.view(np.uint32), want.view(np.uint32))
+
+
+@pytest.mark.parametrize("sizes,n_from,n_to", RESHARD_CASES)
+def test_reshard_round_trip_is_the_identity(orc, sizes, n_from, n_to):
+    rng = np.random.default_rng(5)
+    u_from, _ = orc.layout(sizes, n_from)
+    u_to, _ = orc.layout(sizes, n_to)
+    src = np.zeros((n_from, sum(u.shard_len for u in u_from)), np.float32)
+    # random values at true positions, +0 padding, as every state the steps leave
+    for u in u_from:
+        flat = np.zeros(u.n_padded, np.float32)
+        flat[:u.n_params] = rng.standard_normal(u.n_params)
+        for k in range(n_from):
+            src[k, u.shard_offset:u.shard_offset + u.shard_len] = \
+                flat[k * u.shard_len:(k + 1) * u.shard_len]
+    mid = np.empty((n_to, sum(u.shard_len for u in u_to)), np.float32)
+    back = np.empty_like(src)
+    for a, b in zip(u_from, u_to):
+        orc.reshard_f32(a, src, b, mid)
+    for a, b in zip(u_to, u_from):
+        orc.reshard_f32(a, mid, b, back)
+    assert np.array_equal(back.view(np.uint32), src.view(np.uint32))
