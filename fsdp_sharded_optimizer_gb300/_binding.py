@@ -116,6 +116,8 @@ SIGNATURES = {
     "zero_gen_grads_unit_f32": (C.c_int, [_U64, _I64, _F64, _I32, _P, _I32, _P, _P]),
     "zero2_accumulate": (C.c_int, [_I32, _I64, _P, _P, _I32, _P]),
     "zero2_step_accumulated": (C.c_int, [_I32, _I64, _P, _P, _I32, _P, _P, _P, _P, _P, _P]),
+    # from unit, n_from, src table, to unit, n_to, dst table, stream
+    "zero_reshard_f32": (C.c_int, [_P, _I32, _P, _P, _I32, _P, _P]),
     # unit, n_ranks, unit grads, grad_acc storage, first, stream
     "zero3_accumulate_unit": (C.c_int, [_P, _I32, _P, _P, _I32, _P]),
     # unit, n_ranks, unit grads, grad_acc storage, micro_batches, master, m, v, shards, hp, stream
@@ -393,6 +395,17 @@ def zero2_step_accumulated(grads, grad_acc, micro_batches, master, m, v, params_
     _check("zero2_step_accumulated", lib.zero2_step_accumulated(
         len(grows), grows[0].numel(), g, a, int(micro_batches), w, mm, vv,
         _dev(params_bf16, 2, "params_bf16"), C.byref(hp), _stream(stream)))
+
+
+def zero_reshard_f32(from_unit, src, to_unit, dst, stream=None):
+    """One unit's fp32 state (rows: ranks, laid out like master) re-laid from
+    len(src) to len(dst) ranks."""
+    a, _ = _rows(src, 4, "src")
+    b, _ = _rows(dst, 4, "dst")
+    n_from = len(src) if isinstance(src, (list, tuple)) else src.shape[0]
+    n_to = len(dst) if isinstance(dst, (list, tuple)) else dst.shape[0]
+    _check("zero_reshard_f32", lib.zero_reshard_f32(C.byref(from_unit), n_from, a,
+                                                    C.byref(to_unit), n_to, b, _stream(stream)))
 
 
 def zero3_accumulate_unit(unit, unit_grads, grad_acc, first, stream=None):

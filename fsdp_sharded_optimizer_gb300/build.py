@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_lib", "obj")
 LIB = os.path.join(PKG, "_lib", "libzero.so")
 
-CUDA_SOURCES = ["fused_step.cu", "gather.cu", "gen.cu", "clip.cu", "noalloc.cu"]
+CUDA_SOURCES = ["fused_step.cu", "gather.cu", "gen.cu", "clip.cu", "noalloc.cu", "reshard.cu"]
 HOST_SOURCES = ["host.cpp", "zero3_sched.cpp", "graph.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]

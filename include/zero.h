@@ -275,6 +275,25 @@ int zero3_reduce_scatter_unit_accumulated(const zero_unit_t* unit, int32_t n_ran
                                           float* const* v, uint16_t* const* shard_bf16,
                                           const zero_hparams_t* hp, cudaStream_t stream);
 
+/* zero_reshard_f32 -- one unit's per-rank fp32 state (master, m or v; one
+ * call each) re-laid from n_from to n_to ranks, for a run restarted on
+ * another N_d ([DZF] "6. Where it shows up", checkpoints: sharded optimizer
+ * state needs resharding).  Element i of the unit's flat order (i <
+ * n_params) moves from rank i / S_from, position i % S_from, to rank
+ * i / S_to, position i % S_to; the new layout's padding is written +0.
+ *   from_unit, n_from   the unit's layout at the old rank count (zero_layout)
+ *   src          n_from device pointers to each old rank's fp32 storage
+ *                (this unit at from_unit->shard_offset), read only
+ *   to_unit, n_to       the same unit (same n_params) at the new rank count
+ *   dst          n_to device pointers (this unit at to_unit->shard_offset),
+ *                written; dst must not overlap src
+ * The bf16 shards of the new layout are the bf16 rounding of the new master
+ * (zero_cast_bf16).  8 bytes per parameter.
+ * ZERO_EINVAL / ZERO_EALIGN / ZERO_ECUDA. */
+int zero_reshard_f32(const zero_unit_t* from_unit, int32_t n_from, const float* const* src,
+                     const zero_unit_t* to_unit, int32_t n_to, float* const* dst,
+                     cudaStream_t stream);
+
 /* ---------------------------------------------------------------------
  * Global gradient-norm clipping across the shards.  [DZF] "7. Common
  * mistakes" (local gradient clipping: with sharded gradients the global norm

@@ -189,6 +189,25 @@ def test_zero3_calls_reject_before_launch(B):
     assert last(C.byref(u), 4, t, t, 3, t, t, t, None, C.byref(hp), None) == B.ZERO_EINVAL
 
 
+@host_only
+def test_reshard_rejects_before_launch(B):
+    (a,), _ = B.zero_layout([1000], 4)
+    (b,), _ = B.zero_layout([1000], 8)
+    (c,), _ = B.zero_layout([1001], 8)
+    t4, t8 = _table(A16[:4]), _table(A16[4:12])
+    call = B.lib.zero_reshard_f32
+    assert call(None, 4, t4, C.byref(b), 8, t8, None) == B.ZERO_EINVAL
+    assert call(C.byref(a), 8, t4, C.byref(b), 8, t8, None) == B.ZERO_EINVAL    # layout of 4 ranks
+    assert call(C.byref(a), 4, t4, C.byref(b), 4, t8, None) == B.ZERO_EINVAL
+    assert call(C.byref(a), 4, t4, C.byref(c), 8, t8, None) == B.ZERO_EINVAL    # other n_params
+    assert call(C.byref(a), 4, None, C.byref(b), 8, t8, None) == B.ZERO_EINVAL
+    assert call(C.byref(a), 4, t4, C.byref(b), 8, None, None) == B.ZERO_EINVAL
+    assert call(C.byref(a), 4, t4, C.byref(b), 8, _table(A16[4:11] + [A16[11] + 4]),
+                None) == B.ZERO_EALIGN
+    assert call(C.byref(a), 0, t4, C.byref(b), 8, t8, None) == B.ZERO_EINVAL
+    assert call(C.byref(a), 4, t4, C.byref(b), 65, t8, None) == B.ZERO_EINVAL
+
+
 def test_strerror_names_codes(B):
     assert B.strerror(B.ZERO_OK) == "ok"
     assert "align" in B.strerror(B.ZERO_EALIGN)
