@@ -628,6 +628,26 @@ def run_gpu_zero3(args, torch, Z, world, rank, dev):
 
     ms_gcg, ms_gcs = graph_ms(clip_g), graph_ms(clip_s)
     del clip_s, grad_shard
+    # gradient accumulation over 4 micro-batches (zero3_step_microbatch): both
+    # gathers in every micro-batch, the units accumulating into an fp32
+    # accumulator, the last micro-batch fused with the update (the resident
+    # gradients stand for every micro-batch's)
+    micro = 4
+    acc_buf = torch.empty_like(master)
+
+    def accum_step():
+        t[0] += 1
+        for mb in range(micro):
+            Z.zero3_step_microbatch(units, grads, acc_buf, mb, micro, master, m, v, shards,
+                                    full[0], full[1], Z.hparams(**HP, step=t[0]),
+                                    main_stream=stream, side_stream=side)
+
+    for _ in range(min(W, 2)):
+        accum_step()
+    Ka = max(1, min(K, 20))
+    ms_a, _ = timed(torch, world, dev, stream, accum_step, Ka)
+    accum_bytes = (8 * micro + (2 * N + 4) + (micro - 2) * (2 * N + 8) + (26 + 2 * N + 4)) * total
+    del acc_buf
     # reshard_after_forward = False: one gather per unit, full weights kept (2 B/param)
     kept = torch.empty(total, dtype=torch.int16, device=dev)
 
@@ -737,6 +757,12 @@ def run_gpu_zero3(args, torch, Z, world, rank, dev):
         "graph_clip_shard": {"ms_per_step": ms_gcs / Kc, "steps": Kc,
                              "hbm_gbs": (2 * N + 42) * total * Kc / (ms_gcs * 1e-3) / 1e9,
                              "note": "`clip_shard` captured once as a CUDA graph"},
+        "accumulation": {"micro_batches": micro, "ms_per_step": ms_a / Ka, "steps": Ka,
+                         "hbm_gbs": accum_bytes * Ka / (ms_a * 1e-3) / 1e9,
+                         "bytes_per_step": accum_bytes,
+                         "note": "zero3_step_microbatch x 4: gathers in every micro-batch, "
+                                 "per-unit accumulation into fp32, the last micro-batch fused "
+                                 "with the update (8m + 2N + 4 + (m-2)(2N + 8) + 2N + 30 B/param)"},
         "no_reshard": {"ms_per_step": ms_k / Kk, "steps": Kk,
                        "hbm_gbs": (fused_bytes + 4 * total) * Kk / (ms_k * 1e-3) / 1e9,
                        "note": "reshard_after_forward=False: one gather per unit per step, every "

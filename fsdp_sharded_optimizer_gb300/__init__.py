@@ -26,7 +26,8 @@ _PUBLIC = ("ZERO_DEFAULT_ALIGN", "ZERO_CHUNK_ELEMS", "ZERO_EALIGN", "ZERO_ECUDA"
            "zero3_graph_create_f32grads", "zero3_graph_launch", "zero3_graph_destroy",
            "Zero3Graph", "zero_grad_reduce_sqnorm", "zero_step_stage12_reduced",
            "zero3_update_unit_reduced", "zero3_step_f32grads", "zero3_accumulate_unit",
-           "zero3_reduce_scatter_unit_accumulated", "zero_reshard_f32")
+           "zero3_reduce_scatter_unit_accumulated", "zero_reshard_f32", "zero3_plan_microbatch",
+           "zero3_step_microbatch")
 
 __all__ = list(_PUBLIC)
 

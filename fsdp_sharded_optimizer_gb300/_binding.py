@@ -69,7 +69,7 @@ class zero_regen_t(C.Structure):
 ZERO_OP_RECORD, ZERO_OP_WAIT, ZERO_OP_GATHER = 1, 2, 3
 ZERO_OP_REDUCE_SCATTER, ZERO_OP_REGEN, ZERO_OP_USE = 4, 5, 6
 OP_NAMES = {1: "record", 2: "wait", 3: "gather", 4: "reduce_scatter", 5: "regen", 6: "use",
-            7: "norm", 8: "clip_coef"}
+            7: "norm", 8: "clip_coef", 9: "accumulate"}
 
 
 class zero_clip_t(C.Structure):
@@ -124,6 +124,11 @@ SIGNATURES = {
     "zero3_reduce_scatter_unit_accumulated": (C.c_int, [_P, _I32, _P, _P, _I32, _P, _P, _P, _P,
                                                         _P, _P]),
     "zero3_plan": (C.c_int, [_I32, _I32, _I32, _I32, _P, _I32, _P]),
+    "zero3_plan_microbatch": (C.c_int, [_I32, _I32, _I32, _I32, _P, _I32, _P]),
+    # units, n_units, n_ranks, grads, grad_acc, micro_batch, micro_batches, master, m, v,
+    # shards, full_a, full_b, hp, reshard_after_forward, main stream, side stream
+    "zero3_step_microbatch": (C.c_int, [_P, _I32, _I32, _P, _P, _I32, _I32, _P, _P, _P, _P, _P,
+                                        _P, _P, _I32, _P, _P]),
     # units, n_units, n_ranks, grads, resident, master, m, v, shards, full_a, full_b, hp,
     # regen, clip, reshard_after_forward, main stream, side stream
     "zero3_step": (C.c_int, [_P, _I32, _I32, _P, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I32,
@@ -465,6 +470,37 @@ def zero3_plan(n_units, regen=False, clip=False, reshard_after_forward=True):
     _check("zero3_plan", lib.zero3_plan(n_units, 1 if regen else 0, 1 if clip else 0,
                                         1 if reshard_after_forward else 0, ops, cap, C.byref(n)))
     return [(OP_NAMES[o.kind], o.stream, o.unit, o.arg) for o in ops[:n.value]]
+
+
+def zero3_plan_microbatch(n_units, micro_batch, micro_batches, reshard_after_forward=True):
+    """The operations of one micro-batch of a ZeRO-3 step with gradient
+    accumulation (host only), as zero3_plan's list."""
+    cap = 17 * n_units + 3
+    ops = (zero_op_t * cap)()
+    n = C.c_int32()
+    _check("zero3_plan_microbatch", lib.zero3_plan_microbatch(
+        n_units, 1 if reshard_after_forward else 0, int(micro_batch), int(micro_batches), ops, cap,
+        C.byref(n)))
+    return [(OP_NAMES[o.kind], o.stream, o.unit, o.arg) for o in ops[:n.value]]
+
+
+def zero3_step_microbatch(units, grads, grad_acc, micro_batch, micro_batches, master, m, v,
+                          shard_bf16, full_a, full_b, hp, reshard_after_forward=True,
+                          main_stream=None, side_stream=None):
+    """One micro-batch of a ZeRO-3 step with gradient accumulation (every
+    unit's gradients resident); the update happens in the last micro-batch."""
+    g, rows = _rows(grads, 2, "grads")
+    a = _rows(grad_acc, 4, "grad_acc")[0] if grad_acc is not None else None
+    w, _ = _rows(master, 4, "master")
+    mm, _ = _rows(m, 4, "m")
+    vv, _ = _rows(v, 4, "v")
+    s, _ = _rows(shard_bf16, 2, "shard_bf16")
+    arr = (zero_unit_t * len(units))(*units)
+    _check("zero3_step_microbatch", lib.zero3_step_microbatch(
+        arr, len(units), len(rows), g, a, int(micro_batch), int(micro_batches), w, mm, vv, s,
+        _dev(full_a, 2, "full_a"), _dev(full_b, 2, "full_b") if full_b is not None else None,
+        C.byref(hp), 1 if reshard_after_forward else 0, _stream(main_stream),
+        _stream(side_stream)))
 
 
 def zero3_step(units, grads, master, m, v, shard_bf16, full_a, full_b, hp, grads_resident=True,

@@ -24,9 +24,26 @@ constexpr int kMaxDevices = 64;
 constexpr int kEvStart = 0, kEvGathered = 1, kEvReleased = 3;
 constexpr int32_t kOwnRegion = 2; // GATHER/USE arg: the unit's region of the kept full buffer
 
+// What a backward pass does with a unit's gradients of this micro-batch.
+enum class Reduce {
+    kStep,       // reduce-scatter fused with the update (no accumulation)
+    kAccFirst,   // the step's first micro-batch: the accumulator starts at its mean
+    kAccLater,   // a later one, not the last: added to the accumulator
+    kAccLast,    // the last one: added and fused with the update
+};
+
 struct PlanBuilder {
     std::vector<zero_op_t> ops;
     bool released_recorded[2] = {false, false};
+    Reduce reduce_mode = Reduce::kStep;
+
+    void reduce(int32_t u, bool clip)
+    {
+        if (reduce_mode == Reduce::kAccFirst || reduce_mode == Reduce::kAccLater)
+            add(ZERO_OP_ACCUMULATE, 0, u, reduce_mode == Reduce::kAccFirst ? 1 : 0);
+        else
+            add(ZERO_OP_REDUCE_SCATTER, 0, u, reduce_mode == Reduce::kAccLast ? 2 : (clip ? 1 : 0));
+    }
 
     void add(int32_t kind, int32_t stream, int32_t unit, int32_t arg)
     {
@@ -54,7 +71,7 @@ struct PlanBuilder {
             add(ZERO_OP_USE, 0, u, slot);
             if (backward) {
                 if (regen) add(ZERO_OP_REGEN, 0, u, 0);
-                add(ZERO_OP_REDUCE_SCATTER, 0, u, clip ? 1 : 0);
+                reduce(u, clip);
             }
             add(ZERO_OP_RECORD, 0, -1, kEvReleased + slot);
             released_recorded[slot] = true;
@@ -83,7 +100,7 @@ struct PlanBuilder {
         for (int32_t u = n_units - 1; u >= 0; --u) {
             add(ZERO_OP_USE, 0, u, kOwnRegion);
             if (regen) add(ZERO_OP_REGEN, 0, u, 0);
-            add(ZERO_OP_REDUCE_SCATTER, 0, u, clip ? 1 : 0);
+            reduce(u, clip);
         }
     }
 
@@ -153,6 +170,44 @@ int preload_step_events()
 
 using namespace zero;
 
+namespace zero {
+namespace {
+
+// Gradient accumulation inside a ZeRO-3 step: the fp32 accumulator storage and
+// this call's place among the step's micro-batches.
+struct AccumArgs {
+    float* const* grad_acc;
+    int32_t micro_batch;   // 0 .. micro_batches - 1
+    int32_t micro_batches; // m >= 1
+};
+
+Reduce reduce_mode(const AccumArgs* acc)
+{
+    if (!acc || acc->micro_batches == 1) return Reduce::kStep;
+    if (acc->micro_batch == acc->micro_batches - 1) return Reduce::kAccLast;
+    return acc->micro_batch == 0 ? Reduce::kAccFirst : Reduce::kAccLater;
+}
+
+} // namespace
+} // namespace zero
+
+extern "C" int zero3_plan_microbatch(int32_t n_units, int32_t reshard_after_forward,
+                                     int32_t micro_batch, int32_t micro_batches,
+                                     zero_op_t* ops, int32_t max_ops, int32_t* n_ops)
+{
+    if (n_units < 1 || !ops || !n_ops || max_ops < 0 || micro_batches < 1 || micro_batch < 0 ||
+        micro_batch >= micro_batches)
+        return ZERO_EINVAL;
+    const AccumArgs acc{nullptr, micro_batch, micro_batches};
+    PlanBuilder b;
+    b.reduce_mode = reduce_mode(&acc);
+    b.step(n_units, false, false, reshard_after_forward != 0);
+    if (static_cast<int64_t>(b.ops.size()) > max_ops) return ZERO_EINVAL;
+    for (size_t i = 0; i < b.ops.size(); ++i) ops[i] = b.ops[i];
+    *n_ops = static_cast<int32_t>(b.ops.size());
+    return ZERO_OK;
+}
+
 extern "C" int zero3_plan(int32_t n_units, int32_t regen, int32_t clip,
                           int32_t reshard_after_forward, zero_op_t* ops, int32_t max_ops,
                           int32_t* n_ops)
@@ -174,7 +229,8 @@ int run_step(const zero_unit_t* units, int32_t n_units, int32_t n_ranks, const v
              bool f32, int32_t grads_resident, float* const* master, float* const* m,
              float* const* v, uint16_t* const* shard_bf16, uint16_t* full_a, uint16_t* full_b,
              const zero_hparams_t* hp, const zero_regen_t* regen, const zero_clip_t* clip,
-             int32_t reshard_after_forward, cudaStream_t main_stream, cudaStream_t side_stream)
+             int32_t reshard_after_forward, cudaStream_t main_stream, cudaStream_t side_stream,
+             const AccumArgs* acc = nullptr)
 {
     const bool reshard = reshard_after_forward != 0;
     if (!units || n_units < 1 || n_ranks < 1 || n_ranks > ZERO_MAX_RANKS || !valid_hparams(hp) ||
@@ -199,9 +255,19 @@ int run_step(const zero_unit_t* units, int32_t n_units, int32_t n_ranks, const v
             return rc;
     }
 
+    if (acc) {
+        // accumulation: bf16 rank gradients, no clipping
+        if (f32 || clip || acc->micro_batches < 1 || acc->micro_batch < 0 ||
+            acc->micro_batch >= acc->micro_batches)
+            return ZERO_EINVAL;
+        if (acc->micro_batches > 1 && (rc = check_table(acc->grad_acc, n_ranks)) != ZERO_OK)
+            return rc;
+    }
+
     cudaEvent_t* ev = nullptr;
     if ((rc = events_for_current_device(&ev)) != ZERO_OK) return rc;
     PlanBuilder plan;
+    plan.reduce_mode = reduce_mode(acc);
     plan.step(n_units, regen != nullptr, clip != nullptr, reshard);
 
     const uint16_t* unit_grads[ZERO_MAX_RANKS];
@@ -238,7 +304,7 @@ int run_step(const zero_unit_t* units, int32_t n_units, int32_t n_ranks, const v
         const bool chain_update = after_update && capture == cudaStreamCaptureStatusNone;
         if (op.stream == 0) after_norm = op.kind == ZERO_OP_NORM;
         if (op.stream == 0 && op.kind != ZERO_OP_USE) // USE issues nothing
-            after_update = op.kind == ZERO_OP_REDUCE_SCATTER;
+            after_update = op.kind == ZERO_OP_REDUCE_SCATTER && op.arg != 2;
         switch (op.kind) {
         case ZERO_OP_RECORD:
             rc = cuda_status(cudaEventRecord(ev[op.arg], s));
@@ -257,8 +323,19 @@ int run_step(const zero_unit_t* units, int32_t n_units, int32_t n_ranks, const v
             rc = zero_gen_grads_unit(regen->seed, hp->step, regen->sigma, regen->outliers,
                                      &units[op.unit], n_ranks, unit_grads_w, s);
             break;
+        case ZERO_OP_ACCUMULATE:
+            grads_of(op.unit);
+            rc = zero3_accumulate_unit(&units[op.unit], n_ranks, unit_grads, acc->grad_acc,
+                                       op.arg, s);
+            break;
         case ZERO_OP_REDUCE_SCATTER:
             grads_of(op.unit);
+            if (op.arg == 2) { // the last micro-batch, fused with the update
+                rc = zero3_reduce_scatter_unit_accumulated(&units[op.unit], n_ranks, unit_grads,
+                                                           acc->grad_acc, acc->micro_batches,
+                                                           master, m, v, shard_bf16, hp, s);
+                break;
+            }
             if (f32)
                 rc = unit_update(&units[op.unit], n_ranks,
                                  reinterpret_cast<const void* const*>(unit_grads_f32), master, m,
@@ -313,6 +390,21 @@ extern "C" int zero3_step(const zero_unit_t* units, int32_t n_units, int32_t n_r
     return run_step(units, n_units, n_ranks, reinterpret_cast<const void* const*>(grads), false,
                     grads_resident, master, m, v, shard_bf16, full_a, full_b, hp, regen, clip,
                     reshard_after_forward, main_stream, side_stream);
+}
+
+extern "C" int zero3_step_microbatch(const zero_unit_t* units, int32_t n_units, int32_t n_ranks,
+                                     const uint16_t* const* grads, float* const* grad_acc,
+                                     int32_t micro_batch, int32_t micro_batches,
+                                     float* const* master, float* const* m, float* const* v,
+                                     uint16_t* const* shard_bf16, uint16_t* full_a,
+                                     uint16_t* full_b, const zero_hparams_t* hp,
+                                     int32_t reshard_after_forward, cudaStream_t main_stream,
+                                     cudaStream_t side_stream)
+{
+    const AccumArgs acc{grad_acc, micro_batch, micro_batches};
+    return run_step(units, n_units, n_ranks, reinterpret_cast<const void* const*>(grads), false, 1,
+                    master, m, v, shard_bf16, full_a, full_b, hp, nullptr, nullptr,
+                    reshard_after_forward, main_stream, side_stream, &acc);
 }
 
 extern "C" int zero3_step_f32grads(const zero_unit_t* units, int32_t n_units, int32_t n_ranks,

@@ -458,6 +458,7 @@ typedef struct {
 #define ZERO_OP_USE 6
 #define ZERO_OP_NORM 7      /* unit's squared norm into the clip partials; arg = accumulate */
 #define ZERO_OP_CLIP_COEF 8 /* global norm and clip coefficient */
+#define ZERO_OP_ACCUMULATE 9 /* unit's micro-batch mean into the fp32 accumulator; arg = 1 first */
 
 /* zero3_plan -- host only.  The operations of one ZeRO-3 step over n_units
  * units, in issue order: record "start" on main and make side wait for it;
@@ -482,6 +483,19 @@ typedef struct {
  * ZERO_EINVAL on n_units < 1, null pointers or max_ops too small. */
 int zero3_plan(int32_t n_units, int32_t regen, int32_t clip, int32_t reshard_after_forward,
                zero_op_t* ops, int32_t max_ops, int32_t* n_ops);
+
+/* zero3_plan_microbatch -- host only.  The plan of one micro-batch of a
+ * ZeRO-3 step with gradient accumulation over micro_batches = m micro-batches
+ * ([DZF] "Gradient accumulation": ZeRO-3 gathers twice and reduce-scatters in
+ * every micro-batch, 3mP).  The plan of zero3_plan (no regeneration, no
+ * clipping), except for what each backward unit does with its gradients:
+ * ACCUMULATE (arg 1 for micro_batch 0) while micro_batch < m - 1, and in the
+ * last micro-batch REDUCE_SCATTER with arg 2: added to the accumulator and
+ * fused with the update.  m = 1 is zero3_plan's plan.
+ * ZERO_EINVAL as zero3_plan, and unless 0 <= micro_batch < micro_batches. */
+int zero3_plan_microbatch(int32_t n_units, int32_t reshard_after_forward, int32_t micro_batch,
+                          int32_t micro_batches, zero_op_t* ops, int32_t max_ops,
+                          int32_t* n_ops);
 
 /* Harness regeneration of a unit's gradients inside zero3_step (the
  * stand-in for the backward compute that would produce them). */
@@ -557,6 +571,25 @@ int zero3_step_f32grads(const zero_unit_t* units, int32_t n_units, int32_t n_ran
                         uint16_t* full_b, const zero_hparams_t* hp,
                         int32_t reshard_after_forward, cudaStream_t main_stream,
                         cudaStream_t side_stream);
+
+/* zero3_step_microbatch -- one micro-batch of a ZeRO-3 step with gradient
+ * accumulation: zero3_plan_microbatch's operations, issued like zero3_step's
+ * (every unit's bf16 gradients of this micro-batch resident; no regeneration,
+ * no clipping).  Call it for micro_batch = 0 .. m-1 in order, refilling the
+ * gradients between calls; the update happens in the last call, with
+ * g = (accumulator + mean) * (1/m) as zero3_reduce_scatter_unit_accumulated.
+ *   grad_acc     n_ranks device pointers to each rank's fp32 accumulator
+ *                storage of all units (laid out like master); not read when
+ *                micro_batches = 1
+ *   other arguments as zero3_step
+ * ZERO_EINVAL / ZERO_EALIGN / ZERO_ECUDA. */
+int zero3_step_microbatch(const zero_unit_t* units, int32_t n_units, int32_t n_ranks,
+                          const uint16_t* const* grads, float* const* grad_acc,
+                          int32_t micro_batch, int32_t micro_batches, float* const* master,
+                          float* const* m, float* const* v, uint16_t* const* shard_bf16,
+                          uint16_t* full_a, uint16_t* full_b, const zero_hparams_t* hp,
+                          int32_t reshard_after_forward, cudaStream_t main_stream,
+                          cudaStream_t side_stream);
 
 /* zero3_graph -- the zero3_step of one fixed set of buffers captured once as a
  * CUDA graph and replayed once per step.  The operations, their order and

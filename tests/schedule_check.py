@@ -64,8 +64,9 @@ def check_zero3_trace(trace, n_units, n_steps):
     # forward 0..U-1, backward U-1..0, every step
     assert [pos[n][2] for n in gathers] == (list(range(U)) + list(range(U - 1, -1, -1))) * n_steps
     assert [pos[n][2] for n in uses] == (list(range(U)) + list(range(U - 1, -1, -1))) * n_steps
-    # two full buffers, alternating
-    assert len({pos[n][3] for n in gathers}) == (2 if U > 1 or n_steps > 1 else 1)
+    # two full buffers, alternating (a single unit may always use the same one)
+    slots = {pos[n][3] for n in gathers}
+    assert len(slots) <= 2 and (len(slots) == 2 or U == 1)
     for g, u in zip(gathers, uses):
         assert pos[g][2] == pos[u][2] and pos[g][3] == pos[u][3]
         assert hb(edges, g, u), "unit %d used before it was gathered" % pos[u][2]

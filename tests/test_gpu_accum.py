@@ -115,3 +115,71 @@ def test_zero3_unit_accumulation_matches_oracle(orc, micro):
         H.assert_bitwise(got["p"][:, cols], ref[i]["p"].reshape(N, ou.shard_len),
                          "unit %d shards" % i)
     H.free()
+
+
+@pytest.mark.parametrize("micro,reshard", [(3, True), (2, False), (1, True)])
+def test_zero3_step_microbatches_match_oracle(orc, micro, reshard):
+    """zero3_step_microbatch: the whole ZeRO-3 step with m micro-batches (both
+    gathers in every micro-batch, the units accumulating, the last micro-batch
+    fused with the update), T steps.  Every unit equals the oracle's ZeRO-2
+    accumulation on that unit as a flat buffer, bit for bit, and the full-unit
+    buffers end holding the weights the last gathers had to read."""
+    N, T, seed = 4, 3, 23
+    sizes = [70_000, 333, 200_000, 64, 90_001]
+    units, total = B.zero_layout(sizes, N)
+    ounits, _ = orc.layout(sizes, N)
+    S = total // N
+    master = H.Guarded(N, S, torch.float32)
+    m = H.Guarded(N, S, torch.float32).zero_()
+    v = H.Guarded(N, S, torch.float32).zero_()
+    acc = H.Guarded(N, S, torch.float32)
+    shards = H.Guarded(N, S, torch.int16)
+    grads = H.Guarded(N, total, torch.int16)
+    B.zero_gen_master(seed, H.SIGMA_W, units, master.rows)
+    for k in range(N):
+        B.zero_cast_bf16(master.rows[k], shards.rows[k])
+    max_unit = max(u.n_padded for u in units)
+    fa = H.Guarded(1, max_unit if reshard else total, torch.int16)
+    fb = H.Guarded(1, max_unit, torch.int16)
+    side = torch.cuda.Stream()
+    rw_all = orc.gen_master(seed, H.SIGMA_W, ounits, N)
+    ref = []
+    for ou in ounits:
+        w = np.ascontiguousarray(rw_all[:, ou.shard_offset:ou.shard_offset + ou.shard_len])
+        ref.append(dict(w=w, m=np.zeros_like(w), v=np.zeros_like(w), a=np.zeros_like(w),
+                        p=np.zeros(ou.n_padded, np.uint16)))
+    before = None
+    for t in range(1, T + 1):
+        for mu in range(micro):
+            sid = t * 100 + mu
+            for u in units:
+                B.zero_gen_grads_unit(seed, sid, H.SIGMA_G, 1, u,
+                                      [r[u.offset:u.offset + u.n_padded] for r in grads.rows])
+            B.zero3_step_microbatch(units, grads.rows, acc.rows, mu, micro, master.rows, m.rows,
+                                    v.rows, shards.rows, fa.rows[0],
+                                    fb.rows[0] if reshard else None, H.hp(t),
+                                    reshard_after_forward=reshard, side_stream=side)
+            if mu == micro - 1:
+                before = [r["w"].copy() for r in ref]
+            for ou, r in zip(ounits, ref):
+                g = orc.gen_grads_unit(seed, sid, H.SIGMA_G, 1, ou, N)
+                if mu < micro - 1:
+                    orc.zero2_accumulate(g, r["a"], first=mu == 0)
+                else:
+                    orc.zero2_step_accumulated(g, r["a"] if micro > 1 else None, micro, r["w"],
+                                               r["m"], r["v"], r["p"], orc.hparams(**H.HP, step=t))
+    torch.cuda.synchronize()
+    for b_ in (master, m, v, acc, shards, grads, fa, fb):
+        b_.check()
+    got = dict(w=master.numpy(), m=m.numpy(), v=v.numpy(), a=acc.numpy(), p=shards.numpy())
+    for i, ou in enumerate(ounits):
+        cols = slice(ou.shard_offset, ou.shard_offset + ou.shard_len)
+        for name in (("w", "m", "v", "a") if micro > 1 else ("w", "m", "v")):
+            H.assert_bitwise(got[name][:, cols], ref[i][name], "unit %d %s" % (i, name))
+        H.assert_bitwise(got["p"][:, cols], ref[i]["p"].reshape(N, ou.shard_len),
+                         "unit %d shards" % i)
+    # the last micro-batch's gathers read the weights of the step before
+    flat = np.concatenate([orc.bf16_rne(w).reshape(-1)[:ou.n_params]
+                           for w, ou in zip(before, ounits)])
+    H.assert_gathered(units, sizes, flat, fa, fb if reshard else None)
+    H.free()

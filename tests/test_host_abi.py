@@ -241,6 +241,15 @@ def test_zero3_step_rejects_before_launch(B):
     assert len(ok_args) == 17
     no_b = (arr, 2, 4, t, 1, t, t, t, t, fa, None, C.byref(hp), None, None, 1, s1, s2)
     assert call(*no_b) == B.ZERO_EINVAL   # the double buffer needs full_b
+    # one micro-batch of an accumulated step: units, n, ranks, grads, acc, mb, m, w, m, v, shards,
+    # full_a, full_b, hp, reshard, main, side
+    mb = B.lib.zero3_step_microbatch
+    for micro_batch, micro, acc in ((3, 3, t), (-1, 3, t), (0, 0, t), (0, 3, None)):
+        assert mb(arr, 2, 4, t, acc, micro_batch, micro, t, t, t, t, fa, fb, C.byref(hp), 1, s1,
+                  s2) == B.ZERO_EINVAL
+    assert mb(arr, 2, 4, t, _table(A16[:3] + [A16[3] + 4]), 1, 3, t, t, t, t, fa, fb,
+              C.byref(hp), 1, s1, s2) == B.ZERO_EALIGN
+    assert mb(arr, 2, 4, t, t, 0, 2, t, t, t, t, fa, fb, C.byref(hp), 1, s1, s1) == B.ZERO_EINVAL
 
 
 @host_only

@@ -206,3 +206,44 @@ def test_which_main_stream_launches_follow_one_another(regen, clip):
         assert all(a[2] != b[2] for a, b in rs_pairs + norm_pairs)
         # a norm pass that adds to the partials (arg 1) is never the first of the step
         assert all(b[3] == 1 for _, b in norm_pairs)
+
+
+@pytest.mark.parametrize("n_units,micro,reshard", [(1, 2, True), (5, 3, True), (23, 4, True),
+                                                   (5, 3, False), (7, 1, True)])
+def test_microbatch_plans_are_safe_and_accumulate(n_units, micro, reshard):
+    """Each micro-batch of an accumulated step has zero3_plan's operations and
+    order, with the backward units accumulating (the first micro-batch
+    starting the accumulator) until the last, which reduce-scatters into the
+    update (arg 2).  The happens-before rules hold for every micro-batch."""
+    from fsdp_sharded_optimizer_gb300 import _binding as B
+    trace = []
+    for mb in range(micro):
+        ops = B.zero3_plan_microbatch(n_units, mb, micro, reshard)
+        plain = B.zero3_plan(n_units, False, False, reshard)
+        assert len(ops) == len(plain)
+        for o, p in zip(ops, plain):
+            if p[0] == "reduce_scatter":
+                if mb < micro - 1:
+                    assert o == ("accumulate", 0, p[2], 1 if mb == 0 else 0)
+                else:
+                    assert o == ("reduce_scatter", 0, p[2], 2 if micro > 1 else 0)
+            else:
+                assert o == p
+        for kind, stream, unit, arg in ops:
+            st = {0: "main", 1: "side"}[stream]
+            if kind in ("record", "wait"):
+                trace.append((kind, st, "ev%d" % arg))
+            elif kind in ("gather", "use"):
+                trace.append((kind, st, unit, arg))
+            elif kind in ("reduce_scatter", "accumulate"):  # both read the unit's gradients
+                trace.append(("rs", st, unit))
+            else:
+                trace.append((kind, st, unit))
+    if reshard:
+        check_zero3_trace(trace, n_units, micro)
+    else:
+        check_zero3_kept_trace(trace, n_units, micro)
+    with pytest.raises(B.ZeroError):
+        B.zero3_plan_microbatch(n_units, micro, micro, reshard)
+    with pytest.raises(B.ZeroError):
+        B.zero3_plan_microbatch(n_units, -1, micro, reshard)
