@@ -73,12 +73,34 @@ def _build_mutant(tmp, fname, old, new):
     return lib
 
 
+def _run_mutant(mutant):
+    """Builds one mutant and runs the pins against it: (pytest's exit code, the
+    end of its output), or (None, the error) if the mutant could not be built."""
+    name, fname, old, new = mutant
+    try:
+        with tempfile.TemporaryDirectory() as tmp:
+            lib = _build_mutant(tmp, fname, old, new)
+            env = dict(os.environ, ZERO_ORACLE_LIB=lib)
+            r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p",
+                                "no:cacheprovider",
+                                os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                               cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+            return r.returncode, r.stdout[-2000:]
+    except Exception as e:  # reported by the mutant's own test
+        return None, repr(e)
+
+
+@pytest.fixture(scope="module")
+def mutant_runs():
+    """Every mutant built and run against the pins, as many at a time as the
+    host has cores (each run is a separate process and library)."""
+    import concurrent.futures as cf
+    workers = max(1, min(len(MUTANTS), os.cpu_count() or 1))
+    with cf.ThreadPoolExecutor(workers) as ex:
+        return dict(zip([m[0] for m in MUTANTS], ex.map(_run_mutant, MUTANTS)))
+
+
 @pytest.mark.parametrize("name,fname,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
-def test_pins_catch_planted_mistake(name, fname, old, new):
-    with tempfile.TemporaryDirectory() as tmp:
-        lib = _build_mutant(tmp, fname, old, new)
-        env = dict(os.environ, ZERO_ORACLE_LIB=lib)
-        r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                            os.path.join(ROOT, "tests", "test_oracle_pins.py")],
-                           cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
-        assert r.returncode == 1, "mutant %s survived the pins:\n%s" % (name, r.stdout[-2000:])
+def test_pins_catch_planted_mistake(mutant_runs, name, fname, old, new):
+    code, out = mutant_runs[name]
+    assert code == 1, "mutant %s survived the pins (exit %s):\n%s" % (name, code, out)
