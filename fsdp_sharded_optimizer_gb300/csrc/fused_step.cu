@@ -43,10 +43,11 @@ constexpr int kMinBlocksPerSM = 3;
 constexpr int kSmallRanks = 4;
 constexpr int kMinBlocksPerSMSmall = 4;
 constexpr int kRankBatchSmall = 4;
-// From kManyRanks ranks on, the bf16-gradient steps take the same four-block
-// shape again: more threads, each with 4-rank load batches, beat fewer with
-// 8-rank ones once gradients are most of the bytes (GB300, GPT-2 buffer,
-// GB/s: N_d = 32 6,980 -> 7,012, N_d = 64 6,990 -> 7,098; N_d = 16 equal).
+// From kManyRanks ranks on, the bf16-gradient steps (and the ZeRO-2
+// accumulation) take the same four-block shape again: more threads, each
+// with 4-rank load batches, beat fewer with 8-rank ones once gradients are
+// most of the bytes (GB300, GPT-2 buffer, GB/s: N_d = 32 6,980 -> 7,012,
+// N_d = 64 6,990 -> 7,098; N_d = 16 equal).
 constexpr int kManyRanks = 32;
 
 // Per-rank device pointers, passed by value in the kernel's parameter space
@@ -766,7 +767,9 @@ extern "C" int zero2_accumulate(int32_t n_ranks, int64_t n_padded, const uint16_
         T.a[r] = reinterpret_cast<float4*>(grad_acc[r]);
     }
     const int64_t S = n_padded / n_ranks;
-    const bool small = n_ranks <= kSmallRanks;
+    // the fused step's launch shapes (GB300, GPT-2 buffer, a later micro-batch:
+    // N_d = 32 7,116 -> 7,216 GB/s, N_d = 64 7,135 -> 7,212 in the four-block one)
+    const bool small = n_ranks <= kSmallRanks || n_ranks >= kManyRanks;
     const void* kernel =
         small ? (first ? reinterpret_cast<const void*>(accumulate_kernel<true, true>)
                        : reinterpret_cast<const void*>(accumulate_kernel<false, true>))
