@@ -453,20 +453,29 @@ int launch_range(const Tables& T, const StepScalars& s, int64_t q0, int64_t q1, 
                                                                           T, s, R, nullptr));
     }
     if (f32) { // fp32 gradients: no clipping or accumulation variant
-        const bool small = n_ranks <= kSmallRanks;
-        const void* k =
-            small ? reinterpret_cast<const void*>(fused_step_kernel<false, false, true, false, true>)
-                  : reinterpret_cast<const void*>(fused_step_kernel<false, false, true, false, false>);
+        // The four-block shape at every rank count: with 32 B of gradient per
+        // rank and vector, more threads with 2-rank batches win throughout
+        // (GB300, GPT-2 buffer, GB/s: N_d = 8 6,860 -> 6,907, 16 6,867 ->
+        // 6,905, 32 6,887 -> 7,035, 64 6,887 -> 7,090; up to 4 it already was).
+        const void* k = reinterpret_cast<const void*>(fused_step_kernel<false, false, true, false, true>);
         int blocks = 0;
         const Range R = make_range(k, q0, q1, shard_vec, n_ranks, &blocks);
         if (blocks <= 0) return ZERO_ECUDA;
-        return cuda_status(
-            small ? launch_fused<false, false, true, false, true>(blocks, stream, chained, T, s, R,
-                                                                  nullptr)
-                  : launch_fused<false, false, true, false, false>(blocks, stream, chained, T, s,
-                                                                   R, nullptr));
+        return cuda_status(launch_fused<false, false, true, false, true>(blocks, stream, chained, T,
+                                                                         s, R, nullptr));
     }
-    return n_ranks <= kSmallRanks || n_ranks >= kManyRanks
+    // The plain and clipped steps take the four-block shape at every rank
+    // count; the last micro-batch of an accumulation (one more fp32 stream,
+    // 64 registers spill there) keeps three blocks between kSmallRanks and
+    // kManyRanks.  Measured on GB300, GPT-2 buffer, random gradients, ms:
+    // N_d = 8 plain 0.7482 -> 0.7403 and 0.7767 -> 0.7750 on two boxes,
+    // N_d = 12 0.9366 -> 0.9243, N_d = 16 1.0676 -> 1.0740; the accumulated
+    // step at N_d = 8 0.8527 -> 0.8814 in the four-block shape.  Elements
+    // whose gradient, m and v are all zero take a slower path through the
+    // IEEE division, which more resident warps hide better: all-zero
+    // gradients 1.098 -> 0.989 ms, half of them zero 0.921 -> 0.864.
+    const bool four = inv_m == 0.0f || n_ranks <= kSmallRanks || n_ranks >= kManyRanks;
+    return four
                ? launch_bf16<true>(T, s, q0, q1, shard_vec, n_ranks, clip, stream, inv_m, chained)
                : launch_bf16<false>(T, s, q0, q1, shard_vec, n_ranks, clip, stream, inv_m, chained);
 }
@@ -658,7 +667,6 @@ int preload_fused_kernels()
         reinterpret_cast<const void*>(fused_step_kernel<true, false, false>),
         reinterpret_cast<const void*>(fused_step_kernel<false, true, false>),
         reinterpret_cast<const void*>(fused_step_kernel<true, true, false>),
-        reinterpret_cast<const void*>(fused_step_kernel<false, false, true>),
         reinterpret_cast<const void*>(fused_step_kernel<true, false, false, true>),
         reinterpret_cast<const void*>(fused_step_kernel<false, false, false, true>),
         reinterpret_cast<const void*>(fused_step_kernel<false, false, false, false, true>),
