@@ -29,25 +29,27 @@ namespace {
 
 constexpr int kBlock = 256;
 constexpr int kRankBatch = 8; // gradient loads issued together before summing
-// Three resident blocks per SM (an 80-register cap) instead of the two that
-// the unconstrained 94-102 registers allow: 24 warps per SM keep enough 16-byte
-// loads in flight to reach the HBM roofline (measured at N_d = 2..64 on GB300:
-// +12 % at N_d = 8 over two blocks per SM; four blocks per SM spill and lose).
+// Two launch shapes.  The three-block one: three resident blocks per SM (an
+// 80-register cap) instead of the two that the unconstrained 94-102 registers
+// allow, with 8-rank load batches (+12 % at N_d = 8 over two blocks per SM on
+// one unchunked launch).  It now serves only the last micro-batch of an
+// accumulation between kSmallRanks and kManyRanks, which spills in the other.
 constexpr int kMinBlocksPerSM = 3;
-// Up to kSmallRanks ranks a thread has few gradient vectors to hold, and the
-// bytes in flight per thread fall (112 B at N_d = 1 against 224 B at 8): four
-// resident blocks per SM (a 64-register cap) and loads in batches of 4 ranks
-// win there (GB300, GPT-2 buffer: N_d = 1 5,719 -> 6,478 GB/s, N_d = 2
-// 5,876 -> 6,507, N_d = 4 6,260 -> 6,477; at N_d = 8 the three-block kernel
-// stays ahead, 6,912 against 6,768).
+// The four-block one: four resident blocks per SM (a 64-register cap) and
+// loads in batches of 4 ranks.  It first won up to kSmallRanks, where a
+// thread has few gradient vectors to hold and the bytes in flight per thread
+// fall (112 B at N_d = 1 against 224 B at 8; GB300, GPT-2 buffer: N_d = 1
+// 5,719 -> 6,478 GB/s, N_d = 2 5,876 -> 6,507, N_d = 4 6,260 -> 6,477), and
+// on chained chunks it also wins at N_d = 8 (0.748 -> 0.745 ms a step), so
+// the plain, clipped and fp32-gradient steps take it at every rank count.
 constexpr int kSmallRanks = 4;
 constexpr int kMinBlocksPerSMSmall = 4;
 constexpr int kRankBatchSmall = 4;
-// From kManyRanks ranks on, the bf16-gradient steps (and the ZeRO-2
-// accumulation) take the same four-block shape again: more threads, each
-// with 4-rank load batches, beat fewer with 8-rank ones once gradients are
-// most of the bytes (GB300, GPT-2 buffer, GB/s: N_d = 32 6,980 -> 7,012,
-// N_d = 64 6,990 -> 7,098; N_d = 16 equal).
+// From kManyRanks ranks on, the accumulation kernels take the four-block
+// shape as well: more threads, each with 4-rank load batches, beat fewer
+// with 8-rank ones once gradients are most of the bytes (GB300, GPT-2
+// buffer, the plain step in GB/s: N_d = 32 6,980 -> 7,012, N_d = 64 6,990 ->
+// 7,098; N_d = 16 equal).
 constexpr int kManyRanks = 32;
 
 // Per-rank device pointers, passed by value in the kernel's parameter space
