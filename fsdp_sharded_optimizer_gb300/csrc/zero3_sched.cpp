@@ -129,6 +129,30 @@ struct PlanBuilder {
     }
 };
 
+// Gradient accumulation inside a ZeRO-3 step: the fp32 accumulator storage and
+// this call's place among the step's micro-batches.
+struct AccumArgs {
+    float* const* grad_acc;
+    int32_t micro_batch;   // 0 .. micro_batches - 1
+    int32_t micro_batches; // m >= 1
+};
+
+Reduce reduce_mode(const AccumArgs* acc)
+{
+    if (!acc || acc->micro_batches == 1) return Reduce::kStep;
+    if (acc->micro_batch == acc->micro_batches - 1) return Reduce::kAccLast;
+    return acc->micro_batch == 0 ? Reduce::kAccFirst : Reduce::kAccLater;
+}
+
+// Copies a built plan to the caller's array.
+int copy_plan(const PlanBuilder& b, zero_op_t* ops, int32_t max_ops, int32_t* n_ops)
+{
+    if (static_cast<int64_t>(b.ops.size()) > max_ops) return ZERO_EINVAL;
+    for (size_t i = 0; i < b.ops.size(); ++i) ops[i] = b.ops[i];
+    *n_ops = static_cast<int32_t>(b.ops.size());
+    return ZERO_OK;
+}
+
 // Five timing-free events per host thread and device, created on first use.
 struct EventCache {
     int device = -1;
@@ -170,27 +194,6 @@ int preload_step_events()
 
 using namespace zero;
 
-namespace zero {
-namespace {
-
-// Gradient accumulation inside a ZeRO-3 step: the fp32 accumulator storage and
-// this call's place among the step's micro-batches.
-struct AccumArgs {
-    float* const* grad_acc;
-    int32_t micro_batch;   // 0 .. micro_batches - 1
-    int32_t micro_batches; // m >= 1
-};
-
-Reduce reduce_mode(const AccumArgs* acc)
-{
-    if (!acc || acc->micro_batches == 1) return Reduce::kStep;
-    if (acc->micro_batch == acc->micro_batches - 1) return Reduce::kAccLast;
-    return acc->micro_batch == 0 ? Reduce::kAccFirst : Reduce::kAccLater;
-}
-
-} // namespace
-} // namespace zero
-
 extern "C" int zero3_plan_microbatch(int32_t n_units, int32_t reshard_after_forward,
                                      int32_t micro_batch, int32_t micro_batches,
                                      zero_op_t* ops, int32_t max_ops, int32_t* n_ops)
@@ -202,10 +205,7 @@ extern "C" int zero3_plan_microbatch(int32_t n_units, int32_t reshard_after_forw
     PlanBuilder b;
     b.reduce_mode = reduce_mode(&acc);
     b.step(n_units, false, false, reshard_after_forward != 0);
-    if (static_cast<int64_t>(b.ops.size()) > max_ops) return ZERO_EINVAL;
-    for (size_t i = 0; i < b.ops.size(); ++i) ops[i] = b.ops[i];
-    *n_ops = static_cast<int32_t>(b.ops.size());
-    return ZERO_OK;
+    return copy_plan(b, ops, max_ops, n_ops);
 }
 
 extern "C" int zero3_plan(int32_t n_units, int32_t regen, int32_t clip,
@@ -215,10 +215,7 @@ extern "C" int zero3_plan(int32_t n_units, int32_t regen, int32_t clip,
     if (n_units < 1 || !ops || !n_ops || max_ops < 0) return ZERO_EINVAL;
     PlanBuilder b;
     b.step(n_units, regen != 0, clip != 0, reshard_after_forward != 0);
-    if (static_cast<int64_t>(b.ops.size()) > max_ops) return ZERO_EINVAL;
-    for (size_t i = 0; i < b.ops.size(); ++i) ops[i] = b.ops[i];
-    *n_ops = static_cast<int32_t>(b.ops.size());
-    return ZERO_OK;
+    return copy_plan(b, ops, max_ops, n_ops);
 }
 
 namespace {
