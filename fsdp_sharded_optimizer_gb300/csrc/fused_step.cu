@@ -80,10 +80,20 @@ __device__ __forceinline__ void adamw(float g, float& w, float& m, float& v,
     // The page's operand order; each operation is one rounded fp32 op.
     const float m1 = __fadd_rn(__fmul_rn(s.b1, m), __fmul_rn(s.omb1, g));
     const float v1 = __fadd_rn(__fmul_rn(s.b2, v), __fmul_rn(__fmul_rn(s.omb2, g), g));
-    const float mh = __fdiv_rn(m1, s.bc1);
-    const float vh = __fdiv_rn(v1, s.bc2);
-    const float upd = __fadd_rn(__fdiv_rn(mh, __fadd_rn(__fsqrt_rn(vh), s.eps)),
-                                __fmul_rn(s.wd, w));
+    // With m1 = v1 = 0 (a zero gradient on a zero state: padding, parameters
+    // that have not had a gradient yet) each quotient below is m1 itself:
+    // 0 / bc1, 0 / bc2 and 0 / (sqrt(0) + eps) are zeros of m1's sign, as
+    // bc1, bc2 and eps are finite and positive.  Skipping them keeps the bits
+    // and avoids the IEEE division's slow path for zero operands (GB300,
+    // GPT-2 buffer, N_d = 8: all-zero gradients 0.989 -> 0.752 ms, half of
+    // them zero 0.864 -> 0.749; random gradients 0.7420 -> 0.7444).
+    float q = m1;
+    if (m1 != 0.0f || v1 != 0.0f) {
+        const float mh = __fdiv_rn(m1, s.bc1);
+        const float vh = __fdiv_rn(v1, s.bc2);
+        q = __fdiv_rn(mh, __fadd_rn(__fsqrt_rn(vh), s.eps));
+    }
+    const float upd = __fadd_rn(q, __fmul_rn(s.wd, w));
     w = __fsub_rn(w, __fmul_rn(s.lr, upd));
     m = m1;
     v = v1;

@@ -169,6 +169,46 @@ def test_special_values_follow_ieee(orc):
     H.assert_bitwise(gpar.cpu().numpy().view(np.uint16), rp, "params")
 
 
+def test_zero_gradients_and_zero_state_match_oracle(orc):
+    """Elements whose gradient is zero on every rank while m and v are still
+    zero (padding, parameters that have not received a gradient yet), beside
+    elements that had gradients before and elements that get them later, with
+    signed zeros, a subnormal, infinities and NaN among the weights: bit for
+    bit the oracle's update (the kernel skips the quotients there, which are
+    the zero numerator itself)."""
+    N, Pp, T = 4, 1024, 4
+    S = Pp // N
+    rng = np.random.default_rng(8)
+    w0 = (rng.normal(size=(N, S)) * 0.02).astype(np.float32)
+    w0[0, :8] = [0.0, -0.0, 1e-42, -1e-42, np.inf, -np.inf, np.nan, 3e38]
+    w0[1, :4] = [-0.0, 0.0, -0.0, 0.0]
+    rw, rm, rv = w0.copy(), np.zeros_like(w0), np.zeros_like(w0)
+    rp = np.zeros(Pp, np.uint16)
+    gw = [torch.from_numpy(w0[r].copy()).cuda() for r in range(N)]
+    gm = [torch.zeros(S, device="cuda") for _ in range(N)]
+    gv = [torch.zeros(S, device="cuda") for _ in range(N)]
+    gpar = torch.zeros(Pp, dtype=torch.int16, device="cuda")
+    for t in range(1, T + 1):
+        g32 = (rng.normal(size=(N, Pp)) * 1e-3).astype(np.float32)
+        zero = np.zeros(Pp, bool)
+        zero[: Pp // 2] = t < 3          # zero for two steps, then gradients
+        zero[Pp // 2 + t * 64:] = True   # gradients for a while, then zero
+        zero[S - 8:S + 8] = True         # across an owner boundary, always zero
+        g32[:, zero] = 0.0
+        g32[1::2, zero] = -0.0           # the rank sum from +0 still gives +0
+        grads = orc.bf16_rne(g32)
+        gt = [torch.from_numpy(grads[r].view(np.int16).copy()).cuda() for r in range(N)]
+        orc.zero12_step(1, grads, rw, rm, rv, rp, orc.hparams(**H.HP, step=t))
+        B.zero_step_stage12(1, gt, gw, gm, gv, gpar, H.hp(t))
+    torch.cuda.synchronize()
+    for name, g, r in (("master", gw, rw), ("m", gm, rm), ("v", gv, rv)):
+        g = torch.stack(g).cpu().numpy()
+        both_nan = np.isnan(g) & np.isnan(r)
+        assert np.array_equal(np.isnan(g), np.isnan(r)), name
+        np.testing.assert_array_equal(g.view(np.uint32)[~both_nan], r.view(np.uint32)[~both_nan])
+    H.assert_bitwise(gpar.cpu().numpy().view(np.uint16), rp, "params")
+
+
 def test_invalid_calls_raise_without_launch():
     t = torch.zeros(1024, dtype=torch.int16, device="cuda")
     f = torch.zeros(512, device="cuda")
