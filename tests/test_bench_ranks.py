@@ -51,3 +51,27 @@ def test_workload_names():
     for bad in ("flat-0-n8", "flat-10-n0", "flat-10-n65", "flat-10", "gpt3"):
         with pytest.raises(ValueError):
             bench.workload(bad)
+
+
+def test_reference_arm_prints_the_contract_line():
+    """`bench.py --impl reference` (the oracle on the host cores) prints one
+    JSON line with the contract's keys, its own e2e and cpu_baseline, and
+    exits 0; it needs no GPU."""
+    import json
+    import subprocess
+    import sys
+
+    from conftest import ROOT
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "2",
+                        "--warmup", "1"], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "impl", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["steps"] == 2 and d["value"] > 0
+    assert d["e2e"]["value"] == d["value"] and d["e2e"]["h2d_bytes_per_step"] == 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
