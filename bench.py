@@ -94,8 +94,9 @@ def parse():
                     help="steps of the end-to-end (host buffers) measurement; default min(K, 50)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--headline-only", action="store_true",
-                    help="time only the ZeRO-1 step (skips the ZeRO-2, clipping, accumulation, "
-                         "fp32-gradient and end-to-end legs and their buffers)")
+                    help="time only the headline step (skips the ZeRO-2, clipping, accumulation, "
+                         "fp32-gradient and end-to-end legs, the ZeRO-3 Llama summaries, and the "
+                         "extra legs of a ZeRO-3 workload)")
     return ap.parse_args()
 
 
@@ -277,6 +278,48 @@ def timed(torch, world, dev, stream, fn, K):
     return max_over_ranks(torch, world, total, dev), None
 
 
+def host_link_rates(torch, dev, nbytes=2**30, reps=4):
+    """Pinned host <-> device copy rates by the copy engine, CUDA events around
+    `reps` copies of `nbytes` each: host to device alone, device to host alone,
+    and both at once on two streams (GB/s, best of two rounds)."""
+    hs = [torch.empty(nbytes, dtype=torch.uint8, pin_memory=True) for _ in range(2)]
+    ds = [torch.empty(nbytes, dtype=torch.uint8, device=dev) for _ in range(2)]
+    for h in hs:
+        h.fill_(1)
+    s1, s2 = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+
+    def time_on(streams_ops):
+        torch.cuda.synchronize()
+        ev = []
+        for st, op in streams_ops:
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(st):
+                a.record(st)
+                for _ in range(reps):
+                    op()
+                b.record(st)
+            ev.append((a, b))
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in ev]
+
+    h2d = lambda: ds[0].copy_(hs[0], non_blocking=True)
+    d2h = lambda: hs[1].copy_(ds[1], non_blocking=True)
+    best = {"h2d_gbs": 0.0, "d2h_gbs": 0.0, "both_gbs": 0.0}
+    for _ in range(2):
+        (t1,) = time_on([(s1, h2d)])
+        (t2,) = time_on([(s2, d2h)])
+        ta, tb = time_on([(s1, h2d), (s2, d2h)])
+        best["h2d_gbs"] = max(best["h2d_gbs"], reps * nbytes / (t1 * 1e-3) / 1e9)
+        best["d2h_gbs"] = max(best["d2h_gbs"], reps * nbytes / (t2 * 1e-3) / 1e9)
+        best["both_gbs"] = max(best["both_gbs"], 2 * reps * nbytes / (max(ta, tb) * 1e-3) / 1e9)
+    best["bytes_per_copy"] = nbytes
+    best["how"] = ("torch copy_ between pinned host and device memory, %d copies per direction, "
+                   "CUDA events, best of 2; both_gbs: the two directions at once on two streams"
+                   % reps)
+    del hs, ds
+    return best
+
+
 def run_gpu(args):
     import torch
 
@@ -435,6 +478,12 @@ def run_gpu(args):
         for _ in range(min(W, 3)):
             e2e_inplace()
         ms_e2e, _ = timed(torch, world, dev, stream, e2e_inplace, E)
+        del host_g, host_p
+        link = host_link_rates(torch, dev)
+        h2d_b, d2h_b = N * Pp * 2, Pp * 2
+        # with both directions moving at once (NVLink-C2C is full duplex), the
+        # step can take no less than its larger direction at that direction's rate
+        link_floor_ms = 1e3 * max(h2d_b / (link["h2d_gbs"] * 1e9), d2h_b / (link["d2h_gbs"] * 1e9))
 
         return {
             "zero2": {
@@ -474,6 +523,14 @@ def run_gpu(args):
                 "h2d_bytes_per_step": N * Pp * 2, "d2h_bytes_per_step": Pp * 2,
                 "path": "zero_step_stage12 on pinned host gradients and pinned host weights: the "
                         "kernel reads and writes host memory in place",
+                "link_gbs": (h2d_b + d2h_b) / (ms_e2e / E * 1e-3) / 1e9,
+                "link_peak": link,
+                "link_floor_ms": link_floor_ms,
+                "link_frac": link_floor_ms / (ms_e2e / E),
+                "link_note": "link_gbs = host bytes moved per step (gradients in, weights out) / "
+                             "step time; link_floor_ms = the larger direction's bytes at that "
+                             "direction's measured pinned-copy rate (link_peak); link_frac = "
+                             "floor / step time",
                 "copy_engine": {"ms_per_step": ms_copy / E,
                                 "value": world * P * E / (ms_copy * 1e-3),
                                 "path": "cudaMemcpyAsync H2D of the gradients, the step on device "
@@ -522,11 +579,277 @@ def run_gpu(args):
     }
     if not args.headline_only:
         result.update(sub_legs())
+    if not args.headline_only and args.workload == DEFAULT_WORKLOAD:
+        # the two ZeRO-3 configurations of the metric, measured briefly after the
+        # flat buffer's memory is released: Llama-1.1B (30 GB) and Llama-7B (203 GB)
+        del st
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        result["zero3_llama1b"] = zero3_summary(torch, Z, world, dev, "llama-1.1b-zero3-n8",
+                                                K=max(1, min(K, 10)), W=3)
+        result["zero3_llama7b"] = zero3_summary(torch, Z, world, dev, "llama-7b-zero3-n8",
+                                                K=max(1, min(K, 5)), W=3)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(args.workload, steps=100)
     if world > 1:
         torch.distributed.destroy_process_group()
     return result if rank == 0 else None
+
+
+class Zero3Bench:
+    """Device buffers and timed calls of one ZeRO-3 workload: per rank every
+    unit's gradients (resident, generated once), the fp32 master / m / v and
+    bf16 shard storage of every unit, two full-unit buffers."""
+
+    def __init__(self, torch, Z, unit_sizes, N, dev):
+        import ctypes
+        from fsdp_sharded_optimizer_gb300 import _binding as ZB
+
+        self.torch, self.Z, self.N, self.dev = torch, Z, N, dev
+        self.units, self.total = Z.zero_layout(unit_sizes, N)
+        self.P = sum(unit_sizes)
+        shard_total = self.total // N
+        max_unit = max(u.n_padded for u in self.units)
+        self.master = torch.empty((N, shard_total), dtype=torch.float32, device=dev)
+        self.m = torch.zeros_like(self.master)
+        self.v = torch.zeros_like(self.master)
+        self.shards = torch.empty((N, shard_total), dtype=torch.int16, device=dev)
+        self.grads = torch.empty((N, self.total), dtype=torch.int16, device=dev)
+        self.full = [torch.empty(max_unit, dtype=torch.int16, device=dev) for _ in range(2)]
+        Z.zero_gen_master(0, SIGMA_W, self.units, self.master)
+        for k in range(N):
+            Z.zero_cast_bf16(self.master[k], self.shards[k])
+        for u in self.units:
+            Z.zero_gen_grads_unit(0, 1, SIGMA_G, 0, u, self.unit_grads(u))
+        self.stream = torch.cuda.current_stream(dev)
+        self.side = torch.cuda.Stream(device=dev)
+        self.cap = torch.cuda.Stream(device=dev)
+        self.t = 0
+        self.fused_bytes = (26 + 2 * N) * self.total
+        self.gather_bytes = 2 * 4 * self.total
+        self.rs_launches = sum(fused_launches(u.n_padded, Z) for u in self.units)
+        # the C arguments of the kernel-alone loops, built once, so that the loop
+        # issues one library call per unit and the host stays ahead of the GPU
+        self._ZB, self._ct = ZB, ctypes
+        self._tabs = [ZB._rows(x, b, n)[0] for x, b, n in ((self.master, 4, "master"),
+                                                           (self.m, 4, "m"), (self.v, 4, "v"),
+                                                           (self.shards, 2, "shards"))]
+        self._unit_tabs = [ZB._rows(self.unit_grads(u), 2, "grads")[0] for u in self.units]
+        self._full_ptr = [ctypes.c_void_p(f.data_ptr()) for f in self.full]
+        self._hp_c = Z.hparams(**HP, step=1)
+        self._s_c = ZB._stream(self.stream)
+
+    def unit_grads(self, u):
+        return [self.grads[r][u.offset:u.offset + u.n_padded] for r in range(self.N)]
+
+    def hp(self):
+        self.t += 1
+        return self.Z.hparams(**HP, step=self.t)
+
+    def native_step(self, regen=None, clip=None, reshard=True, kept=None):
+        """The whole step issued by the library's C++ scheduler (zero3_step)."""
+        fa, fb = (kept, None) if kept is not None else (self.full[0], self.full[1])
+        self.Z.zero3_step(self.units, self.grads, self.master, self.m, self.v, self.shards, fa, fb,
+                          self.hp(), grads_resident=True, regen=regen, clip=clip,
+                          reshard_after_forward=reshard, main_stream=self.stream,
+                          side_stream=self.side)
+
+    def graph(self, clip=None):
+        """The same step captured once as a CUDA graph (zero3_graph)."""
+        self.cap.wait_stream(self.stream)
+        return self.Z.zero3_graph_create(self.units, self.grads, self.master, self.m, self.v,
+                                         self.shards, self.full[0], self.full[1],
+                                         self.Z.hparams(**HP, step=1), self.cap, self.side,
+                                         clip=clip)
+
+    def graph_step(self, g):
+        g.launch(self.hp(), stream=self.stream)
+
+    def rs_only(self):
+        """The dominant kernel alone: every unit's fused reduce-scatter + AdamW
+        launched back to back on the stream, no gathers beside it."""
+        ZB, ct, tabs = self._ZB, self._ct, self._tabs
+        self.t += 1
+        self._hp_c.step = self.t
+        for u, g_tab in zip(self.units, self._unit_tabs):
+            rc = ZB.lib.zero3_reduce_scatter_unit(ct.byref(u), self.N, g_tab, tabs[0], tabs[1],
+                                                  tabs[2], tabs[3], ct.byref(self._hp_c),
+                                                  self._s_c)
+            if rc != self.Z.ZERO_OK:
+                raise self.Z.ZeroError("zero3_reduce_scatter_unit", rc)
+
+    def gathers_only(self):
+        """Each unit's two gathers (forward, backward) back to back on one stream."""
+        ZB, ct = self._ZB, self._ct
+        for i, u in enumerate(self.units):
+            for f in (self._full_ptr[i % 2], self._full_ptr[(i + 1) % 2]):
+                rc = ZB.lib.zero3_gather_unit(ct.byref(u), self.N, self._tabs[3], f, self._s_c)
+                if rc != self.Z.ZERO_OK:
+                    raise self.Z.ZeroError("zero3_gather_unit", rc)
+
+
+def zero3_core(torch, world, dev, zb, K, W, Kt):
+    """The native step, the same step as a CUDA graph, and the fused kernel
+    alone (with the gathers alone), each timed on its own."""
+    for _ in range(W):
+        zb.native_step()
+    clocks = ClockSampler(None)
+    ms, _ = timed(torch, world, dev, zb.stream, zb.native_step, K)
+    clk = clocks.stop()
+    g = zb.graph()
+    try:
+        for _ in range(max(1, min(W, 3))):
+            zb.graph_step(g)
+        ms_g, _ = timed(torch, world, dev, zb.stream, lambda: zb.graph_step(g), K)
+    finally:
+        torch.cuda.synchronize()
+        g.close()
+    zb.rs_only()
+    rs_ms, _ = timed(torch, world, dev, zb.stream, zb.rs_only, Kt)
+    zb.gathers_only()
+    ga_ms, _ = timed(torch, world, dev, zb.stream, zb.gathers_only, Kt)
+    return ms, ms_g, rs_ms, ga_ms, clk
+
+
+def zero3_summary(torch, Z, world, dev, name, K=5, W=2):
+    """A short ZeRO-3 measurement of a named workload for the default run's
+    line: the step (native and as a CUDA graph), its GB/s over the fused and
+    gather bytes, and the fused kernel alone against the HBM roofline."""
+    unit_sizes, N, desc = workload(name)
+    zb = Zero3Bench(torch, Z, unit_sizes, N, dev)
+    try:
+        ms, ms_g, rs_ms, ga_ms, clk = zero3_core(torch, world, dev, zb, K, W, K)
+    finally:
+        torch.cuda.synchronize()
+    peak, peak_kind = measured_peak()
+    step_bytes = zb.fused_bytes + zb.gather_bytes
+    achieved = zb.fused_bytes * K / (rs_ms * 1e-3) / 1e9
+    out = {
+        "workload": name, "description": desc, "N_d": N, "params": zb.P, "n_padded": zb.total,
+        "units": len(zb.units), "steps": K, "warmup": W,
+        "ms_per_step": ms / K, "value": world * zb.P * K / (ms * 1e-3), "unit": "params/s",
+        "hbm_bytes_per_step": step_bytes,
+        "hbm_gbs": step_bytes * K / (ms * 1e-3) / 1e9,
+        "graph": {"ms_per_step": ms_g / K, "hbm_gbs": step_bytes * K / (ms_g * 1e-3) / 1e9},
+        "fused_kernel_alone": {
+            "kernel": "fused_step_kernel", "bytes_per_step": zb.fused_bytes,
+            "ms_per_step": rs_ms / K, "launches_per_step": zb.rs_launches,
+            "achieved_gbs": achieved, "peak": peak, "peak_kind": peak_kind,
+            "frac": achieved / peak, "frac_of_8tbs_nominal": achieved / 8000.0},
+        "gathers_alone": {"ms_per_step": ga_ms / K, "bytes_per_step": zb.gather_bytes,
+                          "gbs": zb.gather_bytes * K / (ga_ms * 1e-3) / 1e9},
+        "clocks": clk,
+        "gpu_launches": K * (2 * len(zb.units) + zb.rs_launches),
+        "bytes_note": "(26 + 2 N_d) B/param fused reduce-scatter + AdamW + 8 B/param for the "
+                      "two unit gathers, over P' = n_padded",
+    }
+    del zb
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
+def zero3_extra_legs(torch, Z, world, dev, zb, K, W):
+    """The other ZeRO-3 legs, each timed on its own: clipping (from the rank
+    gradients and through the fp32 gradient shard, natively and as graphs),
+    gradient accumulation, no resharding, and per-unit regeneration."""
+    N, total, P = zb.N, zb.total, zb.P
+    stream = zb.stream
+    # global-norm clipping over all units: the norm pre-pass and the clipped updates
+    # from the rank gradients (4N + 34 B/param with the gathers), and through the
+    # fp32 gradient shard the norm pass keeps (2N + 42 B/param)
+    scratch = torch.empty(Z.zero_clip_scratch_bytes() // 8, dtype=torch.float64, device=dev)
+    norm_coef = torch.empty(4, dtype=torch.float32, device=dev)[:2]
+    Kc = max(1, min(K, 50))
+    clip_g = Z.clip_args(1.0, scratch, norm_coef)
+    for _ in range(min(W, 2)):
+        zb.native_step(clip=clip_g)
+    ms_cg, _ = timed(torch, world, dev, stream, lambda: zb.native_step(clip=clip_g), Kc)
+    grad_shard = torch.empty_like(zb.master)
+    clip_s = Z.clip_args(1.0, scratch, norm_coef, grad_shard=grad_shard)
+    for _ in range(min(W, 2)):
+        zb.native_step(clip=clip_s)
+    ms_cs, _ = timed(torch, world, dev, stream, lambda: zb.native_step(clip=clip_s), Kc)
+
+    # both clipped steps again as CUDA graphs
+    def graph_ms(c):
+        gc = zb.graph(clip=c)
+        try:
+            for _ in range(min(W, 2)):
+                zb.graph_step(gc)
+            return timed(torch, world, dev, stream, lambda: zb.graph_step(gc), Kc)[0]
+        finally:
+            torch.cuda.synchronize()
+            gc.close()
+
+    ms_gcg, ms_gcs = graph_ms(clip_g), graph_ms(clip_s)
+    del clip_s, grad_shard
+    # gradient accumulation over 4 micro-batches (zero3_step_microbatch): both
+    # gathers in every micro-batch, the units accumulating into an fp32
+    # accumulator, the last micro-batch fused with the update (the resident
+    # gradients stand for every micro-batch's)
+    micro = 4
+    acc_buf = torch.empty_like(zb.master)
+
+    def accum_step():
+        hp = zb.hp()
+        for mb in range(micro):
+            Z.zero3_step_microbatch(zb.units, zb.grads, acc_buf, mb, micro, zb.master, zb.m, zb.v,
+                                    zb.shards, zb.full[0], zb.full[1], hp,
+                                    main_stream=stream, side_stream=zb.side)
+
+    for _ in range(min(W, 2)):
+        accum_step()
+    Ka = max(1, min(K, 20))
+    ms_a, _ = timed(torch, world, dev, stream, accum_step, Ka)
+    accum_bytes = (8 * micro + (2 * N + 4) + (micro - 2) * (2 * N + 8) + (26 + 2 * N + 4)) * total
+    del acc_buf
+    # reshard_after_forward = False: one gather per unit, full weights kept (2 B/param)
+    kept = torch.empty(total, dtype=torch.int16, device=dev)
+    for _ in range(min(W, 2)):
+        zb.native_step(reshard=False, kept=kept)
+    Kk = max(1, min(K, 20))
+    ms_k, _ = timed(torch, world, dev, stream, lambda: zb.native_step(reshard=False, kept=kept), Kk)
+    del kept
+    # the same step with each unit's gradients regenerated from the seed in its backward
+    Kr = max(1, min(K, 5))
+    ms_r, _ = timed(torch, world, dev, stream,
+                    lambda: zb.native_step(regen=Z.zero_regen_t(0, SIGMA_G, 0)), Kr)
+    ms_plain, _ = timed(torch, world, dev, stream, zb.native_step, Kr)
+    regen_ms = (ms_r - ms_plain) / Kr
+    return {
+        "clip": {"ms_per_step": ms_cg / Kc, "steps": Kc,
+                 "value": world * P * Kc / (ms_cg * 1e-3),
+                 "hbm_gbs": (4 * N + 34) * total * Kc / (ms_cg * 1e-3) / 1e9,
+                 "bytes_per_step": (4 * N + 34) * total,
+                 "note": "global-norm clipping over all units (max_norm 1.0): norm pre-pass over "
+                         "the rank gradients, clipped updates reducing them again"},
+        "clip_shard": {"ms_per_step": ms_cs / Kc, "steps": Kc,
+                       "value": world * P * Kc / (ms_cs * 1e-3),
+                       "hbm_gbs": (2 * N + 42) * total * Kc / (ms_cs * 1e-3) / 1e9,
+                       "bytes_per_step": (2 * N + 42) * total,
+                       "note": "the same clipped step through the fp32 gradient shard the norm "
+                               "pass keeps; the same bits as `clip`"},
+        "graph_clip": {"ms_per_step": ms_gcg / Kc, "steps": Kc,
+                       "hbm_gbs": (4 * N + 34) * total * Kc / (ms_gcg * 1e-3) / 1e9,
+                       "note": "`clip` captured once as a CUDA graph (zero3_graph with a clip)"},
+        "graph_clip_shard": {"ms_per_step": ms_gcs / Kc, "steps": Kc,
+                             "hbm_gbs": (2 * N + 42) * total * Kc / (ms_gcs * 1e-3) / 1e9,
+                             "note": "`clip_shard` captured once as a CUDA graph"},
+        "accumulation": {"micro_batches": micro, "ms_per_step": ms_a / Ka, "steps": Ka,
+                         "hbm_gbs": accum_bytes * Ka / (ms_a * 1e-3) / 1e9,
+                         "bytes_per_step": accum_bytes,
+                         "note": "zero3_step_microbatch x 4: gathers in every micro-batch, "
+                                 "per-unit accumulation into fp32, the last micro-batch fused "
+                                 "with the update (8m + 2N + 4 + (m-2)(2N + 8) + 2N + 30 B/param)"},
+        "no_reshard": {"ms_per_step": ms_k / Kk, "steps": Kk,
+                       "hbm_gbs": (zb.fused_bytes + 4 * total) * Kk / (ms_k * 1e-3) / 1e9,
+                       "note": "reshard_after_forward=False: one gather per unit per step, every "
+                               "unit's full bf16 weights kept from forward to backward"},
+        "with_regen": {"ms_per_step": ms_r / Kr, "regen_ms_per_step (difference)": regen_ms,
+                       "note": "per-unit gradients regenerated from the seed in each backward "
+                               "(harness work, not the method)"},
+    }
 
 
 def run_gpu_zero3(args, torch, Z, world, rank, dev):
@@ -539,177 +862,18 @@ def run_gpu_zero3(args, torch, Z, world, rank, dev):
 
     unit_sizes, N, desc = workload(args.workload)
     K, W = args.steps, args.warmup
-    units, total = Z.zero_layout(unit_sizes, N)
-    P = sum(unit_sizes)
-    shard_total = total // N
-    max_unit = max(u.n_padded for u in units)
-    master = torch.empty((N, shard_total), dtype=torch.float32, device=dev)
-    m = torch.zeros_like(master)
-    v = torch.zeros_like(master)
-    shards = torch.empty((N, shard_total), dtype=torch.int16, device=dev)
-    grads = torch.empty((N, total), dtype=torch.int16, device=dev)  # every unit's gradients
-    full = [torch.empty(max_unit, dtype=torch.int16, device=dev) for _ in range(2)]
-    Z.zero_gen_master(0, SIGMA_W, units, master)
-    for k in range(N):
-        Z.zero_cast_bf16(master[k], shards[k])
-    unit_grads = lambda bufs, u: [bufs[r][u.offset:u.offset + u.n_padded] for r in range(N)]
-    for u in units:
-        Z.zero_gen_grads_unit(0, 1, SIGMA_G, 0, u, unit_grads(grads, u))
-    stream = torch.cuda.current_stream(dev)
-    side = torch.cuda.Stream(device=dev)
-    t = [0]
-
-    def native_step(regen=None):
-        # the whole step issued by the library's C++ scheduler (zero3_step)
-        t[0] += 1
-        Z.zero3_step(units, grads, master, m, v, shards, full[0], full[1],
-                     Z.hparams(**HP, step=t[0]), grads_resident=True, regen=regen,
-                     main_stream=stream, side_stream=side)
-
-    for _ in range(W):
-        native_step()
-    clocks = ClockSampler(None)
-    ms, _ = timed(torch, world, dev, stream, native_step, K)
-    clk = clocks.stop()
-    # the same step captured once as a CUDA graph (zero3_graph) and replayed per step
-    cap = torch.cuda.Stream(device=dev)
-    cap.wait_stream(stream)
-    graph = Z.zero3_graph_create(units, grads, master, m, v, shards, full[0], full[1],
-                                 Z.hparams(**HP, step=1), cap, side)
-
-    def graph_step():
-        t[0] += 1
-        graph.launch(Z.hparams(**HP, step=t[0]), stream=stream)
-
-    for _ in range(min(W, 3)):
-        graph_step()
-    ms_g, _ = timed(torch, world, dev, stream, graph_step, K)
-    graph.close()
-    # global-norm clipping over all units: the norm pre-pass and the clipped updates
-    # from the rank gradients (4N + 34 B/param with the gathers), and through the
-    # fp32 gradient shard the norm pass keeps (2N + 42 B/param)
-    scratch = torch.empty(Z.zero_clip_scratch_bytes() // 8, dtype=torch.float64, device=dev)
-    norm_coef = torch.empty(4, dtype=torch.float32, device=dev)[:2]
-    Kc = max(1, min(K, 50))
-
-    def clip_step(c):
-        t[0] += 1
-        Z.zero3_step(units, grads, master, m, v, shards, full[0], full[1],
-                     Z.hparams(**HP, step=t[0]), grads_resident=True, clip=c,
-                     main_stream=stream, side_stream=side)
-
-    clip_g = Z.clip_args(1.0, scratch, norm_coef)
-    for _ in range(min(W, 2)):
-        clip_step(clip_g)
-    ms_cg, _ = timed(torch, world, dev, stream, lambda: clip_step(clip_g), Kc)
-    grad_shard = torch.empty_like(master)
-    clip_s = Z.clip_args(1.0, scratch, norm_coef, grad_shard=grad_shard)
-    for _ in range(min(W, 2)):
-        clip_step(clip_s)
-    ms_cs, _ = timed(torch, world, dev, stream, lambda: clip_step(clip_s), Kc)
-
-    # both clipped steps again as CUDA graphs
-    def graph_ms(c):
-        cap.wait_stream(stream)
-        gc = Z.zero3_graph_create(units, grads, master, m, v, shards, full[0], full[1],
-                                  Z.hparams(**HP, step=1), cap, side, clip=c)
-
-        def g_step():
-            t[0] += 1
-            gc.launch(Z.hparams(**HP, step=t[0]), stream=stream)
-
-        try:
-            for _ in range(min(W, 2)):
-                g_step()
-            return timed(torch, world, dev, stream, g_step, Kc)[0]
-        finally:
-            torch.cuda.synchronize()
-            gc.close()
-
-    ms_gcg, ms_gcs = graph_ms(clip_g), graph_ms(clip_s)
-    del clip_s, grad_shard
-    # gradient accumulation over 4 micro-batches (zero3_step_microbatch): both
-    # gathers in every micro-batch, the units accumulating into an fp32
-    # accumulator, the last micro-batch fused with the update (the resident
-    # gradients stand for every micro-batch's)
-    micro = 4
-    acc_buf = torch.empty_like(master)
-
-    def accum_step():
-        t[0] += 1
-        for mb in range(micro):
-            Z.zero3_step_microbatch(units, grads, acc_buf, mb, micro, master, m, v, shards,
-                                    full[0], full[1], Z.hparams(**HP, step=t[0]),
-                                    main_stream=stream, side_stream=side)
-
-    for _ in range(min(W, 2)):
-        accum_step()
-    Ka = max(1, min(K, 20))
-    ms_a, _ = timed(torch, world, dev, stream, accum_step, Ka)
-    accum_bytes = (8 * micro + (2 * N + 4) + (micro - 2) * (2 * N + 8) + (26 + 2 * N + 4)) * total
-    del acc_buf
-    # reshard_after_forward = False: one gather per unit, full weights kept (2 B/param)
-    kept = torch.empty(total, dtype=torch.int16, device=dev)
-
-    def kept_step():
-        t[0] += 1
-        Z.zero3_step(units, grads, master, m, v, shards, kept, None, Z.hparams(**HP, step=t[0]),
-                     reshard_after_forward=False, main_stream=stream, side_stream=side)
-
-    for _ in range(min(W, 2)):
-        kept_step()
-    Kk = max(1, min(K, 20))
-    ms_k, _ = timed(torch, world, dev, stream, kept_step, Kk)
-    del kept
-    # the dominant kernel alone: every unit's fused reduce-scatter + AdamW launched
-    # back to back on the stream (no gathers beside it); its mean launch duration
-    # over these launches is the loop's time / launches.  The C calls' arguments
-    # are built once, so the loop issues one library call per unit and the host
-    # stays ahead of the GPU even for small units.
-    import ctypes
-    from fsdp_sharded_optimizer_gb300 import _binding as ZB
+    zb = Zero3Bench(torch, Z, unit_sizes, N, dev)
+    units, total, P = zb.units, zb.total, zb.P
     Kt = max(1, min(K, 50))
-    tabs = [ZB._rows(x, b, n)[0] for x, b, n in ((master, 4, "master"), (m, 4, "m"), (v, 4, "v"),
-                                                 (shards, 2, "shards"))]
-    unit_tabs = [ZB._rows(unit_grads(grads, u), 2, "grads")[0] for u in units]
-    full_ptr = [ctypes.c_void_p(f.data_ptr()) for f in full]
-    hp_c = Z.hparams(**HP, step=1)
-    s_c = ZB._stream(stream)
-
-    def rs_only():
-        t[0] += 1
-        hp_c.step = t[0]
-        for u, g_tab in zip(units, unit_tabs):
-            rc = ZB.lib.zero3_reduce_scatter_unit(ctypes.byref(u), N, g_tab, tabs[0], tabs[1],
-                                                  tabs[2], tabs[3], ctypes.byref(hp_c), s_c)
-            if rc != Z.ZERO_OK:
-                raise Z.ZeroError("zero3_reduce_scatter_unit", rc)
-
-    rs_only()
-    rs_ms, _ = timed(torch, world, dev, stream, rs_only, Kt)
-
-    # the gathers alone: each unit's two gathers (forward, backward) back to back
-    def gathers_only():
-        for i, u in enumerate(units):
-            for f in (full_ptr[i % 2], full_ptr[(i + 1) % 2]):
-                rc = ZB.lib.zero3_gather_unit(ctypes.byref(u), N, tabs[3], f, s_c)
-                if rc != Z.ZERO_OK:
-                    raise Z.ZeroError("zero3_gather_unit", rc)
-
-    gathers_only()
-    ga_ms, _ = timed(torch, world, dev, stream, gathers_only, Kt)
-    # the same step with each unit's gradients regenerated from the seed in its backward
-    Kr = max(1, min(K, 5))
-    ms_r, _ = timed(torch, world, dev, stream,
-                    lambda: native_step(Z.zero_regen_t(0, SIGMA_G, 0)), Kr)
-    regen_ms = ms_r / Kr - ms / K
+    ms, ms_g, rs_ms, ga_ms, clk = zero3_core(torch, world, dev, zb, K, W, Kt)
+    extra = {} if args.headline_only else zero3_extra_legs(torch, Z, world, dev, zb, K, W)
 
     peak, peak_kind = measured_peak()
     fused_bytes = (26 + 2 * N) * total
     rs_launches = sum(fused_launches(u.n_padded, Z) for u in units)
     gather_bytes = 2 * 4 * total
     achieved = fused_bytes * Kt / (rs_ms * 1e-3) / 1e9
-    return {
+    result = {
         "metric": METRIC, "value": world * P * K / (ms * 1e-3), "unit": "params/s",
         "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": ms / K,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
@@ -739,40 +903,11 @@ def run_gpu_zero3(args, torch, Z, world, rank, dev):
                   "hbm_gbs": (fused_bytes + gather_bytes) * K / (ms_g * 1e-3) / 1e9,
                   "note": "zero3_graph: the same step captured once as a CUDA graph, replayed "
                           "per step with that step's AdamW scalars"},
-        "clip": {"ms_per_step": ms_cg / Kc, "steps": Kc,
-                 "value": world * P * Kc / (ms_cg * 1e-3),
-                 "hbm_gbs": (4 * N + 34) * total * Kc / (ms_cg * 1e-3) / 1e9,
-                 "bytes_per_step": (4 * N + 34) * total,
-                 "note": "global-norm clipping over all units (max_norm 1.0): norm pre-pass over "
-                         "the rank gradients, clipped updates reducing them again"},
-        "clip_shard": {"ms_per_step": ms_cs / Kc, "steps": Kc,
-                       "value": world * P * Kc / (ms_cs * 1e-3),
-                       "hbm_gbs": (2 * N + 42) * total * Kc / (ms_cs * 1e-3) / 1e9,
-                       "bytes_per_step": (2 * N + 42) * total,
-                       "note": "the same clipped step through the fp32 gradient shard the norm "
-                               "pass keeps; the same bits as `clip`"},
-        "graph_clip": {"ms_per_step": ms_gcg / Kc, "steps": Kc,
-                       "hbm_gbs": (4 * N + 34) * total * Kc / (ms_gcg * 1e-3) / 1e9,
-                       "note": "`clip` captured once as a CUDA graph (zero3_graph with a clip)"},
-        "graph_clip_shard": {"ms_per_step": ms_gcs / Kc, "steps": Kc,
-                             "hbm_gbs": (2 * N + 42) * total * Kc / (ms_gcs * 1e-3) / 1e9,
-                             "note": "`clip_shard` captured once as a CUDA graph"},
-        "accumulation": {"micro_batches": micro, "ms_per_step": ms_a / Ka, "steps": Ka,
-                         "hbm_gbs": accum_bytes * Ka / (ms_a * 1e-3) / 1e9,
-                         "bytes_per_step": accum_bytes,
-                         "note": "zero3_step_microbatch x 4: gathers in every micro-batch, "
-                                 "per-unit accumulation into fp32, the last micro-batch fused "
-                                 "with the update (8m + 2N + 4 + (m-2)(2N + 8) + 2N + 30 B/param)"},
-        "no_reshard": {"ms_per_step": ms_k / Kk, "steps": Kk,
-                       "hbm_gbs": (fused_bytes + 4 * total) * Kk / (ms_k * 1e-3) / 1e9,
-                       "note": "reshard_after_forward=False: one gather per unit per step, every "
-                               "unit's full bf16 weights kept from forward to backward"},
-        "with_regen": {"ms_per_step": ms_r / Kr, "regen_ms_per_step (difference)": regen_ms,
-                       "note": "per-unit gradients regenerated from the seed in each backward "
-                               "(harness work, not the method)"},
         "clocks": clk,
         "gpu_launches": K * (2 * len(units) + rs_launches),
-    } if rank == 0 else None
+    }
+    result.update(extra)
+    return result if rank == 0 else None
 
 
 # ------------------------------------------------------------------ CPU oracle

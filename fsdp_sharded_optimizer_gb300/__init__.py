@@ -5,7 +5,7 @@ GPU; one CUDA kernel reduce-scatters their bf16 gradients (fixed-order fp32
 mean), applies AdamW to each owner's fp32 shard and writes the new bf16
 weights (the all-gather).  ZeRO-3 adds the per-unit gather and the per-unit
 reduce-scatter, scheduled with next-unit prefetch on a side stream
-(``zero3.Zero3Schedule``).
+(``zero3_step``, natively or as a CUDA graph).
 
 The public calls carry the C ABI's names (include/zero.h) and live in
 ``_binding``.  They are loaded on first use, so that ``build`` can be imported

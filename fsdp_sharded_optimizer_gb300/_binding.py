@@ -452,7 +452,20 @@ def zero_clip_coef_units_noalloc(units, grads, max_norm, norm_coef, unit_norms=N
     unit concatenated in grads[r]) using the library's fixed internal scratch
     instead of caller memory: for callers that cannot allocate device memory.
     norm_coef (device float[2]) <- (norm, coef); unit_norms (optional device
-    float[len(units)]) <- each unit's norm.  At most ZERO_NOALLOC_MAX_UNITS units."""
+    float[len(units)]) <- each unit's norm.  At most ZERO_NOALLOC_MAX_UNITS units.
+    The C entry point has no lengths to check, so the sizes are checked here,
+    before anything is launched: every gradient row must cover every unit."""
+    n_rows = len(grads) if isinstance(grads, (list, tuple)) else grads.shape[0]
+    need = max((int(u.offset) + int(u.n_padded) for u in units), default=0)
+    for r in range(n_rows):
+        if grads[r].numel() < need:
+            raise ValueError("zero_clip_coef_units_noalloc: grads[%d] holds %d elements, the "
+                             "units need %d" % (r, grads[r].numel(), need))
+    if norm_coef.numel() < 2:
+        raise ValueError("zero_clip_coef_units_noalloc: norm_coef needs 2 floats")
+    if unit_norms is not None and unit_norms.numel() < len(units):
+        raise ValueError("zero_clip_coef_units_noalloc: unit_norms needs %d floats, has %d"
+                         % (len(units), unit_norms.numel()))
     g, rows = _rows(grads, 2, "grads")
     arr = (zero_unit_t * len(units))(*units)
     un = _dev(unit_norms, 4, "unit_norms") if unit_norms is not None else None

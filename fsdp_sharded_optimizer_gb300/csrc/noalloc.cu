@@ -31,7 +31,9 @@ constexpr int kMaxDevices = 64;
 static __device__ __align__(256) double g_noalloc_scratch[kNormBlocks + kMaxUnits];
 
 // Host code must not use g_noalloc_scratch's name as an address: look up its
-// device address once per device, with that device current.
+// device address once per device, with that device current, and keep it for
+// the process (a cudaDeviceReset, which rebuilds the context, is not followed;
+// the header says so).
 std::mutex g_addr_mu;
 double* g_addr[kMaxDevices] = {};
 

@@ -419,12 +419,17 @@ int zero_step_stage12_reduced(int32_t stage, int32_t n_ranks, int64_t n_padded,
  *   norm_coef       device float[2], 16-byte aligned: global norm, coefficient
  *   unit_norms      NULL or device float[n_units], 16-byte aligned: each
  *                   unit's gradient norm
- * The global norm sums the units' squared norms in a different association
- * than zero_clip_coef does, so the two agree within fp32 rounding, not bit for
- * bit.  The first call on a device looks up the array's device address with
- * that device current; make it before any stream capture.  All calls share the
- * array: calls whose GPU work overlaps (two streams, two threads) race; order
- * them on one stream. */
+ * Each unit's norm in unit_norms equals, bit for bit, norm_coef[0] of
+ * zero_grad_sqnorm over that unit alone followed by zero_clip_coef (the same
+ * block partials summed in the same order).  The global norm sums the units'
+ * squared norms in a different association than zero_clip_coef does over
+ * accumulated partials, so the two agree within fp32 rounding, not bit for bit.
+ * The first call on a device looks up the array's device address with that
+ * device current and keeps it for the process; make it before any stream
+ * capture.  cudaDeviceReset rebuilds the device's context and may move the
+ * array, so after a reset this entry point must not be called on that device
+ * again in the same process.  All calls share the array: calls whose GPU work
+ * overlaps (two streams, two threads) race; order them on one stream. */
 #define ZERO_NOALLOC_MAX_UNITS 1024
 int zero_clip_coef_units_noalloc(const zero_unit_t* units, int32_t n_units, int32_t n_ranks,
                                  const uint16_t* const* grads, double max_norm,

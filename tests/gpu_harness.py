@@ -129,6 +129,42 @@ def padding_is_zero(g, P, shard_len):
     return True
 
 
+def padding_is_zero_unit(g, u):
+    """True when unit u's padding [n_params, n_padded), which sits at the end of
+    the last ranks' shards of the unit in per-rank shard storage g, holds +0."""
+    bits = g.full.view(torch.int16 if g.dtype == torch.int16 else torch.int32)
+    for k in range(g.full.shape[0]):
+        lo = max(u.n_params - k * u.shard_len, 0)
+        if lo >= u.shard_len:
+            continue
+        a = CANARY + u.shard_offset + lo
+        if bool(bits[k, a:CANARY + u.shard_offset + u.shard_len].any()):
+            return False
+    return True
+
+
+def oracle_sample(orc, N, seed, T, idx, outliers=0, threads=None):
+    """orc.sample (the oracle's element-by-element run of T steps from step 1)
+    over the true parameter indices idx, split across host threads.  Each call
+    is independent and allocates its own buffers, and ctypes releases the GIL
+    around it, so the pieces run concurrently; the values are those of one call."""
+    from concurrent.futures import ThreadPoolExecutor
+    import os
+
+    idx = np.ascontiguousarray(np.asarray(idx, np.int64))
+    n = idx.size
+    threads = max(1, min(threads or os.cpu_count() or 1, 32, -(-n // 65536)))
+    cuts = np.linspace(0, n, threads + 1).astype(np.int64)
+    hp0 = orc.hparams(**HP, step=1)
+
+    def part(i):
+        return orc.sample(N, seed, SIGMA_W, SIGMA_G, outliers, hp0, T, idx[cuts[i]:cuts[i + 1]])
+
+    with ThreadPoolExecutor(threads) as ex:
+        parts = list(ex.map(part, range(threads)))
+    return tuple(np.concatenate([p[j] for p in parts]) for j in range(4))
+
+
 def free():
     torch.cuda.synchronize()
     torch.cuda.empty_cache()

@@ -1,21 +1,17 @@
 """GPU parity of the ZeRO-3 path: the unit gather, the per-unit reduce-scatter
-fused with AdamW, and the two-stream schedule with next-unit prefetch, against
-the oracle.  Full-size Llama-shaped workloads are compared on sampled
-parameters (plus every unit and shard boundary) computed one by one by the
-oracle."""
+fused with AdamW, and the two-stream schedule with next-unit prefetch (the
+native zero3_step, and the test-side Python model of the schedule for the race
+check), against the oracle.  The full-size Llama-shaped workloads, through the
+calls the benchmark times, are in test_gpu_zero3_timed.py."""
 import numpy as np
 import pytest
 import torch
 
 import gpu_harness as H
 from fsdp_sharded_optimizer_gb300 import _binding as B
-from fsdp_sharded_optimizer_gb300.zero3 import CudaBackend, Zero3Schedule
+from zero3_model import CudaBackend, Zero3Schedule
 
 pytestmark = pytest.mark.gpu
-
-LLAMA_1B = [44_044_288] * 22 + [131_074_048]
-LLAMA_7B = [202_383_360] * 32 + [262_148_096]
-
 
 @pytest.mark.parametrize("N,sizes", [(2, [1000, 64, 5]), (8, [2**16 + 37, 999_999]),
                                      (64, [70_000, 1]), (3, [12_345])])
@@ -146,56 +142,6 @@ def test_zero3_equals_zero1_on_the_same_parameters():
             for g3, g1 in ((master, w1), (m, m1), (v, v1)):
                 assert np.array_equal(g3.numpy()[k][src].view(np.uint32), flat(g1)[dst].view(np.uint32))
             assert np.array_equal(shards.numpy()[k][src], p1[dst])
-
-
-def _sampled_zero3_check(orc, sizes, N, T, n_random):
-    units, total = B.zero_layout(sizes, N)
-    sched, master, m, v, shards = _run_schedule(units, total, N, T)
-    assert sched.calls == {"allgather": 2 * len(units) * T, "reduce_scatter": len(units) * T}
-    P = sum(sizes)
-    rng = np.random.default_rng(1)
-    bounds = []
-    for u in units:
-        for k in range(N + 1):
-            for d in (-1, 0, 1):
-                bounds.append(u.param_offset + k * u.shard_len + d)
-    idx = np.unique(np.concatenate([rng.integers(0, P, size=n_random), np.array(bounds)]))
-    idx = idx[(idx >= 0) & (idx < P)]
-    # true parameter -> (owner rank, position in its shard storage)
-    starts = np.array([u.param_offset for u in units])
-    ui = np.searchsorted(starts, idx, side="right") - 1
-    local = idx - starts[ui]
-    S = np.array([units[i].shard_len for i in ui])
-    k = local // S
-    pos = np.array([units[i].shard_offset for i in ui]) + local - k * S
-    tk = torch.from_numpy(k).cuda()
-    tp = torch.from_numpy(pos + H.CANARY).cuda()
-    gp = shards.full[tk, tp].cpu().numpy().view(np.uint16)
-    gw, gm, gv = (a.full[tk, tp].cpu().numpy() for a in (master, m, v))
-    rp, rw, rm, rv = orc.sample(N, 0, H.SIGMA_W, H.SIGMA_G, 0, orc.hparams(**H.HP, step=1), T, idx)
-    H.assert_within_tolerance((gw, gm, gv), (rw, rm, rv), gp, rp)
-    for name, g, r in (("shards", gp, rp), ("master", gw, rw), ("m", gm, rm), ("v", gv, rv)):
-        H.assert_bitwise(g, r, name)
-    # the gather of the last unit returns exactly the owners' shards
-    u = units[-1]
-    full = torch.empty(u.n_padded, dtype=torch.int16, device="cuda")
-    B.zero3_gather_unit(u, shards.rows, full)
-    want = torch.cat([r[u.shard_offset:u.shard_offset + u.shard_len] for r in shards.rows])
-    assert torch.equal(full, want)
-    for b in (master, m, v, shards):
-        b.check()
-
-
-def test_llama_1b_shaped_zero3_full_size_sampled(orc):
-    _sampled_zero3_check(orc, LLAMA_1B, 8, 10, 1_000_000)
-    H.free()
-
-
-def test_llama_7b_shaped_zero3_full_size_sampled(orc):
-    """Llama-7B shapes, N_d = 8: 80.9 GB of fp32 master/m/v resident, per-unit
-    gradients regenerated from the seed in each unit's backward, 10 steps."""
-    _sampled_zero3_check(orc, LLAMA_7B, 8, 10, 1_000_000)
-    H.free()
 
 
 def _native_buffers(units, total, N, resident, seed=0):

@@ -399,3 +399,26 @@ def test_accumulation_calls_reject_before_launch(B):
     assert g(4, 1024, t, t, 2, t, t, t, None, C.byref(hp), None) == B.ZERO_EINVAL
     assert g(4, 1024, t, t, 2, t, t, t, C.c_void_p(0xB00002), C.byref(hp), None) == B.ZERO_EALIGN
     assert g(4, 1024, t, t, 1, t, t, t, p, C.byref(B.hparams(step=0)), None) == B.ZERO_EINVAL
+
+
+@host_only
+def test_noalloc_wrapper_checks_sizes_before_launch(B):
+    """The allocation-free entry point takes no lengths, so its Python wrapper
+    checks that every gradient row covers every unit and that the outputs are
+    large enough, before anything reaches the library (host tensors here: a
+    check that passed would fail later on the address test, never launch)."""
+    import torch
+
+    units, total = B.zero_layout([1000, 64, 333], 2)
+    rows = [torch.zeros(total, dtype=torch.int16) for _ in range(2)]
+    short = [rows[0], torch.zeros(total - 8, dtype=torch.int16)]
+    nc = torch.zeros(2, dtype=torch.float32)
+    with pytest.raises(ValueError, match="grads\\[1\\]"):
+        B.zero_clip_coef_units_noalloc(units, short, 1.0, nc)
+    with pytest.raises(ValueError, match="norm_coef"):
+        B.zero_clip_coef_units_noalloc(units, rows, 1.0, torch.zeros(1))
+    with pytest.raises(ValueError, match="unit_norms"):
+        B.zero_clip_coef_units_noalloc(units, rows, 1.0, nc, unit_norms=torch.zeros(2))
+    # sizes that fit get as far as the address check (host memory is refused there)
+    with pytest.raises(ValueError, match="CUDA memory or pinned host memory"):
+        B.zero_clip_coef_units_noalloc(units, rows, 1.0, nc, unit_norms=torch.zeros(3))

@@ -421,6 +421,22 @@ def test_sampled_elements_match_full_run(orc):
     np.testing.assert_array_equal(sv.view(np.uint32), v.reshape(-1)[idx].view(np.uint32))
 
 
+def test_threaded_sampling_equals_the_full_run(orc):
+    """The GPU tests split a large sample across host threads
+    (gpu_harness.oracle_sample); the pieces, put back together, are the full
+    run's values at every index, whatever the split."""
+    import gpu_harness as H
+
+    N, P, T, seed = 4, 200_000, 3, 9
+    params, master, m, v, u = _full_oracle_run(orc, 1, N, P, seed, T, outliers=1)
+    idx = np.arange(P, dtype=np.int64)[::-1].copy()
+    for threads in (1, 3, 7):
+        sp, sw, sm, sv = H.oracle_sample(orc, N, seed, T, idx, outliers=1, threads=threads)
+        np.testing.assert_array_equal(sp, params[idx])
+        for g, r in ((sw, master), (sm, m), (sv, v)):
+            np.testing.assert_array_equal(g.view(np.uint32), r.reshape(-1)[idx].view(np.uint32))
+
+
 def test_fp32_oracle_tracks_fp64_over_ten_steps(orc):
     N, P, T, seed = 4, 2000, 10, 12
     params, master, m, v, u = _full_oracle_run(orc, 1, N, P, seed, T)

@@ -8,7 +8,7 @@ and that the result equals DDP bit for bit."""
 import numpy as np
 import pytest
 
-from fsdp_sharded_optimizer_gb300.zero3 import Zero3Schedule
+from zero3_model import Zero3Schedule
 from schedule_check import check_zero3_kept_trace, check_zero3_trace
 
 HP = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)

@@ -4,15 +4,25 @@ It serves callers that cannot allocate device memory -- code running inside
 another framework whose memory pool owns the GPU, a monitoring thread that must
 not disturb the training loop's allocator, a runtime held to a fixed memory
 budget -- by keeping its scratch in a fixed array inside the library.  This
-test calls it through the C ABI and checks it against the entry points that
-take caller scratch (zero_grad_sqnorm over each unit, then zero_clip_coef),
-within the tolerance the clipping tests use (1e-6 relative), on two calls in a
-row with different gradients, so that the array's leftover contents from the
-first call cannot leak into the second.  The file is named to be collected
-last; it needs nothing from the other tests.
+test calls it through the C ABI on two calls in a row with different
+gradients, so that the array's leftover contents from the first call cannot
+leak into the second, and checks it
+
+* against the oracle: each unit's norm against the square root of the
+  oracle's fp64 sum of squares of that unit's averaged gradient, the global
+  norm against the root of the units' sums, and the coefficient against the
+  oracle's (torch's clip_grad_norm_ rule), within the 1e-6 relative bound the
+  clipping tests derive ("Data parallelism, ZeRO and FSDP", "7. Common
+  mistakes": the global norm is the all-reduce of the squared shard norms);
+* against the entry points that take caller scratch (zero_grad_sqnorm over
+  each unit, then zero_clip_coef): every per-unit norm bit for bit, the global
+  norm and coefficient within the same 1e-6.
+
+The file is named to be collected last; it needs nothing from the other tests.
 """
 import ctypes as C
 
+import numpy as np
 import pytest
 import torch
 
@@ -56,7 +66,17 @@ def _close(a, b):
     return bool(torch.all((a - b).abs() <= TOL * b.abs()))
 
 
-def test_noalloc_matches_scratch_entry_points_on_two_calls():
+def _oracle(orc, units, grads, max_norm):
+    """(norm, coef) and each unit's norm from the oracle's fp64 sums of squares."""
+    host = grads.cpu().numpy().view(np.uint16)
+    sums = [orc.grad_sumsq(np.ascontiguousarray(host[:, u.offset:u.offset + u.n_padded]))
+            for u in units]
+    coef, norm = orc.clip_coef(sum(sums), max_norm)
+    return (torch.tensor([norm, float(coef)], dtype=torch.float64),
+            torch.tensor([s ** 0.5 for s in sums], dtype=torch.float64))
+
+
+def test_noalloc_matches_oracle_and_scratch_entry_points_on_two_calls(orc):
     N = 8
     calls = [(11, [40_000, 1234, 77_777, 64, 2**16 + 37], 1e-3),
              (12, [900_001, 8, 333], 5.0)]
@@ -66,10 +86,13 @@ def test_noalloc_matches_scratch_entry_points_on_two_calls():
         unit_norms = torch.full((len(units),), float("nan"), device="cuda")
         B.zero_clip_coef_units_noalloc(units, grads, max_norm, norm_coef, unit_norms)
         torch.cuda.synchronize()
+        got, got_units = norm_coef.cpu().double(), unit_norms.cpu().double()
+        want, want_units = _oracle(orc, units, grads, max_norm)
+        assert _close(got, want), (got, want)
+        assert _close(got_units, want_units), (got_units, want_units)
         ref_total, ref_units = _reference(units, grads, max_norm)
-        got = norm_coef.cpu().double()
         assert _close(got, ref_total), (got, ref_total)
-        assert _close(unit_norms.cpu().double(), ref_units)
+        assert torch.equal(got_units, ref_units), (got_units, ref_units)
 
 
 def test_noalloc_rejects_more_units_than_its_array_holds():

@@ -1,7 +1,19 @@
-"""ZeRO-3 (FSDP) step schedule on one GPU: per-unit gathers with next-unit
-prefetch on a side stream, and per-unit reduce-scatter fused with AdamW.
+"""A Python model of the ZeRO-3 step schedule, for the tests: per-unit gathers
+with next-unit prefetch on a side stream, and per-unit reduce-scatter fused
+with AdamW.
 
-Method ("Data parallelism, ZeRO and FSDP", "How FSDP implements ZeRO-3"):
+TEST-SIDE CHECKER, NOT THE PRODUCT.  The library's schedule is the native one
+in csrc/zero3_sched.cpp (zero3_plan, zero3_step) and its CUDA-graph form
+(zero3_graph_create); the benchmark times those, and the tests compare them
+with the oracle.  This model issues the same order through a pluggable backend,
+so that a test can (a) run it on the CPU against a backend that executes the
+oracle's unit calls and records every stream operation, and (b) run it on the
+GPU with a consumer callback between a unit's gather and its release, which
+copies the gathered weights and poisons the buffer -- a race check the native
+scheduler, which runs no Python between its launches, cannot host.
+
+Method ("Data parallelism, ZeRO and FSDP", "How FSDP implements ZeRO-3",
+steps 2-5):
   2. forward of a unit: all-gather its bf16 parameters, run it, free them;
   3. backward in reverse unit order: all-gather again, compute the gradients,
      free the parameters, reduce-scatter the gradients;
@@ -20,11 +32,6 @@ the update into the unit's reduce-scatter gives the same bits as updating
 after the whole backward pass: unit u's shard is last read by unit u's own
 backward gather, which comes before its reduce-scatter, and the prefetch of
 unit u-1 reads a disjoint region.
-
-The schedule is host plumbing; every byte is moved by the library's kernels.
-A backend object supplies the two calls and the stream/event primitives, so
-the same schedule runs against the CUDA library (``CudaBackend``) or, on the
-CPU, against a recording or oracle backend in the tests.
 """
 
 
@@ -34,7 +41,7 @@ class CudaBackend:
     def __init__(self, n_ranks, shards, master, m, v, device=None):
         import torch
 
-        from . import _binding as B
+        from fsdp_sharded_optimizer_gb300 import _binding as B
 
         self._torch, self._B = torch, B
         self.n_ranks = n_ranks
