@@ -86,6 +86,7 @@ def lib():
             "or_sim_zero": (i32, [i32, i32, P, i32, i32, u64, f64, f64, i32, P, i32,
                                   i64, P, P, P, P, P]),
             "or_sample": (None, [i32, u64, f64, f64, i32, P, i32, P, i64, P, P, P, P]),
+            "or_sample_coef": (None, [i32, u64, f64, f64, i32, P, i32, P, P, i64, P, P, P, P]),
             "or_grad_sumsq": (f64, [i32, i64, P]),
             "or_grad_nonfinite": (None, [i32, i64, P, P]),
             "or_reduce_mean_f32": (f32, [P, i32, i64, f32]),
@@ -366,6 +367,20 @@ def sample(n_ranks, seed, sigma_w, sigma_g, outliers, hp0, n_steps, param_index)
            np.zeros(n, np.float32))
     lib().or_sample(n_ranks, seed, sigma_w, sigma_g, outliers, C.byref(hp0), n_steps,
                     _ptr(idx), n, *[_ptr(a) for a in out])
+    return out
+
+
+def sample_coef(n_ranks, seed, sigma_w, sigma_g, outliers, hp0, n_steps, coefs, param_index):
+    """sample() under global-norm clipping with the given per-step coefficients."""
+    idx = np.ascontiguousarray(np.asarray(param_index, dtype=np.int64))
+    c = np.ascontiguousarray(np.asarray(coefs, dtype=np.float32))
+    if c.size != n_steps:
+        raise ValueError("one coefficient per step")
+    n = idx.size
+    out = (np.zeros(n, np.uint16), np.zeros(n, np.float32), np.zeros(n, np.float32),
+           np.zeros(n, np.float32))
+    lib().or_sample_coef(n_ranks, seed, sigma_w, sigma_g, outliers, C.byref(hp0), n_steps,
+                         _ptr(c), _ptr(idx), n, *[_ptr(a) for a in out])
     return out
 
 

@@ -833,10 +833,37 @@ int or_sim_zero(int32_t stage, int32_t n_ranks, const int64_t* unit_sizes,
  * Sampled parity: the step is elementwise, so the final state of any true
  * parameter after n_steps can be computed alone from its generated inputs.
  * ==================================================================== */
+static void sample_steps(int32_t n_ranks, uint64_t seed, double sigma_w, double sigma_g,
+                         int32_t outliers, const or_hparams_t* hp0, int32_t n_steps,
+                         const float* coef, const int64_t* param_index, int64_t n_index,
+                         uint16_t* out_params, float* out_master, float* out_m, float* out_v);
+
 void or_sample(int32_t n_ranks, uint64_t seed, double sigma_w, double sigma_g,
                int32_t outliers, const or_hparams_t* hp0, int32_t n_steps,
                const int64_t* param_index, int64_t n_index, uint16_t* out_params,
                float* out_master, float* out_m, float* out_v)
+{
+    sample_steps(n_ranks, seed, sigma_w, sigma_g, outliers, hp0, n_steps, NULL, param_index,
+                 n_index, out_params, out_master, out_m, out_v);
+}
+
+/* The same with global-norm clipping: step t (0-based) multiplies the mean
+ * gradient by coef[t], as or_zero3_reduce_scatter_unit_coef does.  The
+ * coefficients are inputs (the norm of a whole model cannot be formed from a
+ * sample of its parameters). */
+void or_sample_coef(int32_t n_ranks, uint64_t seed, double sigma_w, double sigma_g,
+                    int32_t outliers, const or_hparams_t* hp0, int32_t n_steps,
+                    const float* coef, const int64_t* param_index, int64_t n_index,
+                    uint16_t* out_params, float* out_master, float* out_m, float* out_v)
+{
+    sample_steps(n_ranks, seed, sigma_w, sigma_g, outliers, hp0, n_steps, coef, param_index,
+                 n_index, out_params, out_master, out_m, out_v);
+}
+
+static void sample_steps(int32_t n_ranks, uint64_t seed, double sigma_w, double sigma_g,
+                         int32_t outliers, const or_hparams_t* hp0, int32_t n_steps,
+                         const float* coef, const int64_t* param_index, int64_t n_index,
+                         uint16_t* out_params, float* out_master, float* out_m, float* out_v)
 {
     uint64_t wkey = or_gen_key(seed, 0, 0, 0);
     float wscale = or_gen_scale(sigma_w);
@@ -861,6 +888,8 @@ void or_sample(int32_t n_ranks, uint64_t seed, double sigma_w, double sigma_g,
             for (int32_t r = 0; r < n_ranks; ++r)
                 g1[r] = or_bf16_rne(or_gen_value(keys[(size_t)t * n_ranks + r], p, gscale, outliers));
             float g = or_reduce_mean(gp, n_ranks, 0, sc[t].inv_n);
+            if (coef)
+                g = g * coef[t];
             or_adamw(g, &w, &m, &v, &sc[t]);
         }
         if (out_params) out_params[q] = or_bf16_rne(w);

@@ -185,6 +185,12 @@ void or_sample(int32_t n_ranks, uint64_t seed, double sigma_w, double sigma_g,
                int32_t outliers, const or_hparams_t* hp0, int32_t n_steps,
                const int64_t* param_index, int64_t n_index, uint16_t* out_params,
                float* out_master, float* out_m, float* out_v);
+/* The same under global-norm clipping: the mean gradient of step t (0-based,
+ * step hp0->step + t) is multiplied by coef[t] before AdamW. */
+void or_sample_coef(int32_t n_ranks, uint64_t seed, double sigma_w, double sigma_g,
+                    int32_t outliers, const or_hparams_t* hp0, int32_t n_steps,
+                    const float* coef, const int64_t* param_index, int64_t n_index,
+                    uint16_t* out_params, float* out_master, float* out_m, float* out_v);
 
 #ifdef __cplusplus
 }

@@ -56,6 +56,9 @@ MUTANTS = [
      "x = src[i / to->shard_len % n_from][from->shard_offset + i % from->shard_len];"),
     ("reshard_ignores_unit_offset", "zero_oracle.c", "dst[k][to->shard_offset + j] = x;",
      "dst[k][j] = x;"),
+    ("sampled_clip_first_coef_every_step", "zero_oracle.c", "g = g * coef[t];",
+     "g = g * coef[0];"),
+    ("sampled_clip_coef_ignored", "zero_oracle.c", "g = g * coef[t];", "g = g * 1.0f;"),
 ]
 
 

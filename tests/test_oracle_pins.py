@@ -421,6 +421,36 @@ def test_sampled_elements_match_full_run(orc):
     np.testing.assert_array_equal(sv.view(np.uint32), v.reshape(-1)[idx].view(np.uint32))
 
 
+def test_sampled_clipped_run_matches_the_unit_updates(orc):
+    """The sampled run under clipping (each step's mean gradient times that
+    step's coefficient, given) equals T clipped unit updates of the whole
+    buffer at every sampled index, and with every coefficient 1 equals the
+    unclipped sampled run."""
+    N, P, T, seed = 4, 3000, 5, 13
+    coefs = np.array([0.5, 1.0, 0.25, 0.8125, 0.0625], np.float32)
+    (u,), _ = orc.layout([P], N, 64)
+    master = orc.gen_master(seed, 0.02, [u], N)
+    m, v = np.zeros_like(master), np.zeros_like(master)
+    shards = orc.bf16_rne(master)
+    for t in range(1, T + 1):
+        g = orc.gen_grads_unit(seed, t, 1e-3, 1, u, N)
+        orc.zero3_reduce_scatter_unit_coef(u, g, master, m, v, shards, orc.hparams(**HP, step=t),
+                                           coefs[t - 1])
+    idx = np.array([0, 1, 7, 749, 750, 751, 1500, P - 1, 2222], np.int64)
+    sp, sw, sm, sv = orc.sample_coef(N, seed, 0.02, 1e-3, 1, orc.hparams(**HP, step=1), T, coefs, idx)
+    k, j = idx // u.shard_len, idx % u.shard_len
+    np.testing.assert_array_equal(sp, shards[k, j])
+    for got, ref in ((sw, master), (sm, m), (sv, v)):
+        np.testing.assert_array_equal(got.view(np.uint32), ref[k, j].view(np.uint32))
+    # a coefficient of 1 is no clipping
+    hp0 = orc.hparams(**HP, step=1)
+    ones = orc.sample_coef(N, seed, 0.02, 1e-3, 1, hp0, T, np.ones(T, np.float32), idx)
+    plain = orc.sample(N, seed, 0.02, 1e-3, 1, hp0, T, idx)
+    for a, b in zip(ones, plain):
+        np.testing.assert_array_equal(a.view(np.uint16 if a.dtype == np.uint16 else np.uint32),
+                                      b.view(np.uint16 if b.dtype == np.uint16 else np.uint32))
+
+
 def test_threaded_sampling_equals_the_full_run(orc):
     """The GPU tests split a large sample across host threads
     (gpu_harness.oracle_sample); the pieces, put back together, are the full
