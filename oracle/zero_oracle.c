@@ -835,15 +835,16 @@ int or_sim_zero(int32_t stage, int32_t n_ranks, const int64_t* unit_sizes,
  * ==================================================================== */
 static void sample_steps(int32_t n_ranks, uint64_t seed, double sigma_w, double sigma_g,
                          int32_t outliers, const or_hparams_t* hp0, int32_t n_steps,
-                         const float* coef, const int64_t* param_index, int64_t n_index,
-                         uint16_t* out_params, float* out_master, float* out_m, float* out_v);
+                         const float* coef, int32_t micro_batches, const int64_t* param_index,
+                         int64_t n_index, uint16_t* out_params, float* out_master, float* out_m,
+                         float* out_v);
 
 void or_sample(int32_t n_ranks, uint64_t seed, double sigma_w, double sigma_g,
                int32_t outliers, const or_hparams_t* hp0, int32_t n_steps,
                const int64_t* param_index, int64_t n_index, uint16_t* out_params,
                float* out_master, float* out_m, float* out_v)
 {
-    sample_steps(n_ranks, seed, sigma_w, sigma_g, outliers, hp0, n_steps, NULL, param_index,
+    sample_steps(n_ranks, seed, sigma_w, sigma_g, outliers, hp0, n_steps, NULL, 0, param_index,
                  n_index, out_params, out_master, out_m, out_v);
 }
 
@@ -856,15 +857,33 @@ void or_sample_coef(int32_t n_ranks, uint64_t seed, double sigma_w, double sigma
                     const float* coef, const int64_t* param_index, int64_t n_index,
                     uint16_t* out_params, float* out_master, float* out_m, float* out_v)
 {
-    sample_steps(n_ranks, seed, sigma_w, sigma_g, outliers, hp0, n_steps, coef, param_index,
+    sample_steps(n_ranks, seed, sigma_w, sigma_g, outliers, hp0, n_steps, coef, 0, param_index,
                  n_index, out_params, out_master, out_m, out_v);
+}
+
+/* The same with gradient accumulation over micro_batches identical
+ * micro-batches (each micro-batch's rank gradients are the step's generated
+ * ones): the owner accumulator starts at +0 and adds the mean after each of
+ * the first micro_batches - 1 micro-batches (or_zero2_accumulate), and the
+ * update takes g = (accumulator + mean) * (1/micro_batches)
+ * (or_zero2_step_accumulated; accumulator +0 for one micro-batch). */
+void or_sample_accum(int32_t n_ranks, uint64_t seed, double sigma_w, double sigma_g,
+                     int32_t outliers, const or_hparams_t* hp0, int32_t n_steps,
+                     int32_t micro_batches, const int64_t* param_index, int64_t n_index,
+                     uint16_t* out_params, float* out_master, float* out_m, float* out_v)
+{
+    sample_steps(n_ranks, seed, sigma_w, sigma_g, outliers, hp0, n_steps, NULL,
+                 micro_batches < 1 ? 1 : micro_batches, param_index, n_index, out_params,
+                 out_master, out_m, out_v);
 }
 
 static void sample_steps(int32_t n_ranks, uint64_t seed, double sigma_w, double sigma_g,
                          int32_t outliers, const or_hparams_t* hp0, int32_t n_steps,
-                         const float* coef, const int64_t* param_index, int64_t n_index,
-                         uint16_t* out_params, float* out_master, float* out_m, float* out_v)
+                         const float* coef, int32_t micro_batches, const int64_t* param_index,
+                         int64_t n_index, uint16_t* out_params, float* out_master, float* out_m,
+                         float* out_v)
 {
+    float inv_m = micro_batches > 0 ? (float)(1.0 / (double)micro_batches) : 1.0f;
     uint64_t wkey = or_gen_key(seed, 0, 0, 0);
     float wscale = or_gen_scale(sigma_w);
     float gscale = or_gen_scale(sigma_g);
@@ -890,6 +909,15 @@ static void sample_steps(int32_t n_ranks, uint64_t seed, double sigma_w, double 
             float g = or_reduce_mean(gp, n_ranks, 0, sc[t].inv_n);
             if (coef)
                 g = g * coef[t];
+            if (micro_batches > 0) {
+                float a = 0.0f;
+                if (micro_batches > 1) {
+                    a = 0.0f + g;
+                    for (int32_t mu = 1; mu < micro_batches - 1; ++mu)
+                        a = a + g;
+                }
+                g = (a + g) * inv_m;
+            }
             or_adamw(g, &w, &m, &v, &sc[t]);
         }
         if (out_params) out_params[q] = or_bf16_rne(w);

@@ -191,6 +191,13 @@ void or_sample_coef(int32_t n_ranks, uint64_t seed, double sigma_w, double sigma
                     int32_t outliers, const or_hparams_t* hp0, int32_t n_steps,
                     const float* coef, const int64_t* param_index, int64_t n_index,
                     uint16_t* out_params, float* out_master, float* out_m, float* out_v);
+/* The same with gradient accumulation over micro_batches identical
+ * micro-batches (or_zero2_accumulate for the first micro_batches - 1, then
+ * or_zero2_step_accumulated, every micro-batch carrying the step's gradients). */
+void or_sample_accum(int32_t n_ranks, uint64_t seed, double sigma_w, double sigma_g,
+                     int32_t outliers, const or_hparams_t* hp0, int32_t n_steps,
+                     int32_t micro_batches, const int64_t* param_index, int64_t n_index,
+                     uint16_t* out_params, float* out_master, float* out_m, float* out_v);
 
 #ifdef __cplusplus
 }

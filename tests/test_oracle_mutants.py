@@ -59,6 +59,10 @@ MUTANTS = [
     ("sampled_clip_first_coef_every_step", "zero_oracle.c", "g = g * coef[t];",
      "g = g * coef[0];"),
     ("sampled_clip_coef_ignored", "zero_oracle.c", "g = g * coef[t];", "g = g * 1.0f;"),
+    ("sampled_accum_one_short", "zero_oracle.c",
+     "for (int32_t mu = 1; mu < micro_batches - 1; ++mu)",
+     "for (int32_t mu = 2; mu < micro_batches - 1; ++mu)"),
+    ("sampled_accum_not_averaged", "zero_oracle.c", "g = (a + g) * inv_m;", "g = (a + g);"),
 ]
 
 

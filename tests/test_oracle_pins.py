@@ -451,6 +451,32 @@ def test_sampled_clipped_run_matches_the_unit_updates(orc):
                                       b.view(np.uint16 if b.dtype == np.uint16 else np.uint32))
 
 
+@pytest.mark.parametrize("micro", [1, 2, 3, 4, 5])
+def test_sampled_accumulated_run_matches_the_accumulation_steps(orc, micro):
+    """The sampled run with accumulation over identical micro-batches equals,
+    at every sampled index, T steps of the whole buffer through the
+    accumulation calls (micro - 1 accumulations, then the accumulated update)
+    fed the step's gradients in every micro-batch."""
+    N, P, T, seed = 4, 3000, 4, 17
+    (u,), _ = orc.layout([P], N, 64)
+    master = orc.gen_master(seed, 0.02, [u], N)
+    m, v = np.zeros_like(master), np.zeros_like(master)
+    acc = np.zeros_like(master)
+    params = np.zeros(u.n_padded, np.uint16)
+    for t in range(1, T + 1):
+        g = orc.gen_grads_unit(seed, t, 1e-3, 1, u, N)
+        for mu in range(micro - 1):
+            orc.zero2_accumulate(g, acc, mu == 0)
+        orc.zero2_step_accumulated(g, acc, micro, master, m, v, params, orc.hparams(**HP, step=t))
+    idx = np.array([0, 1, 7, 749, 750, 751, 1500, P - 1, 2222], np.int64)
+    sp, sw, sm, sv = orc.sample_accum(N, seed, 0.02, 1e-3, 1, orc.hparams(**HP, step=1), T, micro,
+                                      idx)
+    k, j = idx // u.shard_len, idx % u.shard_len
+    np.testing.assert_array_equal(sp, params[idx])
+    for got, ref in ((sw, master), (sm, m), (sv, v)):
+        np.testing.assert_array_equal(got.view(np.uint32), ref[k, j].view(np.uint32))
+
+
 def test_threaded_sampling_equals_the_full_run(orc):
     """The GPU tests split a large sample across host threads
     (gpu_harness.oracle_sample); the pieces, put back together, are the full
