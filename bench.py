@@ -735,7 +735,8 @@ def zero3_summary(torch, Z, world, dev, name, K=5, W=2):
             "kernel": "fused_step_kernel", "bytes_per_step": zb.fused_bytes,
             "ms_per_step": rs_ms / K, "launches_per_step": zb.rs_launches,
             "achieved_gbs": achieved, "peak": peak, "peak_kind": peak_kind,
-            "frac": achieved / peak, "frac_of_8tbs_nominal": achieved / 8000.0},
+            "frac": achieved / peak, "frac_of_8tbs_nominal": achieved / 8000.0,
+            "traffic_per_step": ncu_traffic(name)},
         "gathers_alone": {"ms_per_step": ga_ms / K, "bytes_per_step": zb.gather_bytes,
                           "gbs": zb.gather_bytes * K / (ga_ms * 1e-3) / 1e9},
         "clocks": clk,

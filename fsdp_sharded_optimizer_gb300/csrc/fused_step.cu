@@ -32,24 +32,27 @@ constexpr int kRankBatch = 8; // gradient loads issued together before summing
 // Two launch shapes.  The three-block one: three resident blocks per SM (an
 // 80-register cap) instead of the two that the unconstrained 94-102 registers
 // allow, with 8-rank load batches (+12 % at N_d = 8 over two blocks per SM on
-// one unchunked launch).  It now serves only the last micro-batch of an
-// accumulation between kSmallRanks and kManyRanks, which spills in the other.
+// one unchunked launch).  It now serves the update from the fp32 gradient
+// shard and the accumulation of micro-batches 1..m-1 between kSmallRanks and
+// kManyRanks.
 constexpr int kMinBlocksPerSM = 3;
 // The four-block one: four resident blocks per SM (a 64-register cap) and
 // loads in batches of 4 ranks.  It first won up to kSmallRanks, where a
 // thread has few gradient vectors to hold and the bytes in flight per thread
 // fall (112 B at N_d = 1 against 224 B at 8; GB300, GPT-2 buffer: N_d = 1
 // 5,719 -> 6,478 GB/s, N_d = 2 5,876 -> 6,507, N_d = 4 6,260 -> 6,477), and
-// on chained chunks it also wins at N_d = 8 (0.748 -> 0.745 ms a step), so
-// the plain, clipped and fp32-gradient steps take it at every rank count.
+// on chained chunks it also wins at N_d = 8 (0.748 -> 0.745 ms a step).
+// Since the kernel loads the gradients before the state (no register spill),
+// every variant of the step from bf16 rank gradients -- plain, clipped, the
+// last micro-batch of an accumulation -- and the fp32-gradient step take it
+// at every rank count.
 constexpr int kSmallRanks = 4;
 constexpr int kMinBlocksPerSMSmall = 4;
 constexpr int kRankBatchSmall = 4;
-// From kManyRanks ranks on, the accumulation kernels take the four-block
-// shape as well: more threads, each with 4-rank load batches, beat fewer
-// with 8-rank ones once gradients are most of the bytes (GB300, GPT-2
-// buffer, the plain step in GB/s: N_d = 32 6,980 -> 7,012, N_d = 64 6,990 ->
-// 7,098; N_d = 16 equal).
+// From kManyRanks ranks on, the accumulation of micro-batches 1..m-1 takes
+// the four-block shape as well: more threads, each with 4-rank load batches,
+// beat fewer with 8-rank ones once gradients are most of the bytes (GB300,
+// GPT-2 buffer, GB/s: N_d = 32 7,116 -> 7,216, N_d = 64 7,135 -> 7,212).
 constexpr int kManyRanks = 32;
 
 // Per-rank device pointers, passed by value in the kernel's parameter space
@@ -99,6 +102,16 @@ __device__ __forceinline__ void adamw(float g, float& w, float& m, float& v,
     v = v1;
 }
 
+// The clip coefficient clip[1], read in each loop trip where it is used (an
+// L1 hit) instead of being held in a register across the loop.  It was
+// written by an earlier kernel on the stream, so the read-only path is safe.
+__device__ __forceinline__ float ld_coef(const float* clip)
+{
+    float c;
+    asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(c) : "l"(clip + 1));
+    return c;
+}
+
 // kClip: the mean gradient is multiplied by clip[1], the coefficient of the
 // global-norm clipping computed on the device by zero_clip_coef.
 // kAcc: the last micro-batch of ZeRO-2 gradient accumulation; the gradient is
@@ -115,6 +128,7 @@ __global__ void __launch_bounds__(kBlock, kSmall ? kMinBlocksPerSMSmall : kMinBl
 fused_step_kernel(const __grid_constant__ Tables T, const StepScalars s, const Range R,
                   const float* __restrict__ clip)
 {
+    static_assert(!(kAcc && (kF32 || kG32)), "accumulation reads bf16 rank gradients");
     // Chained launches (programmatic dependent launch): the next chunk's grid
     // may start as soon as every block of this one is running, so its blocks
     // fill the SMs this grid's tail leaves idle.  Chunks touch disjoint
@@ -130,16 +144,19 @@ fused_step_kernel(const __grid_constant__ Tables T, const StepScalars s, const R
     int64_t k = q / R.shard_vec;     // owner
     int64_t j = q - k * R.shard_vec; // vector position inside the owner's shard
     const int N = R.n_ranks;
-    const float coef = kClip ? clip[1] : 1.0f;
 
     for (; q < R.q1; q += stride) {
-        float4* wp = T.w[k] + 2 * j;
-        float4* mp = T.m[k] + 2 * j;
-        float4* vp = T.v[k] + 2 * j;
-        const float4 w0 = dev::ld_stream(wp), w1 = dev::ld_stream(wp + 1);
-        const float4 m0 = dev::ld_stream(mp), m1 = dev::ld_stream(mp + 1);
-        const float4 v0 = dev::ld_stream(vp), v1 = dev::ld_stream(vp + 1);
-
+        // The gradient of the 8 elements is loaded, summed and scaled before
+        // the owner's state is loaded, so the 24 state values are not live
+        // while a rank batch is in flight.  Loading the state first needed
+        // more than the 64 registers of the four-block shape (16-32 B of
+        // spill a thread); this order spills nothing in any variant and is
+        // faster throughout (GB300, GPT-2 buffer, same data, ms a step: N_d = 8
+        // 0.7800 -> 0.7558, N_d = 1 0.531 -> 0.518, N_d = 64 2.846 -> 2.785;
+        // last micro-batch of an accumulation at N_d = 8 0.851 -> 0.806; fp32
+        // rank gradients at N_d = 8 1.070 -> 1.025).  The results are the same
+        // operations on the same values.
+        //
         // reduce-scatter: fp32 sum from +0 over ranks 0..N-1, in order
         float acc[8];
         if (kG32) {
@@ -151,23 +168,36 @@ fused_step_kernel(const __grid_constant__ Tables T, const StepScalars s, const R
                 reinterpret_cast<const float4* const*>(T.g), N, q, acc);
         else
             dev::sum_ranks<kSmall ? kRankBatchSmall : kRankBatch>(T.g, N, q, acc);
-        float prior[8];
+        // g = mean (the shard already holds it), then for the last micro-batch
+        // (earlier micro-batches + this mean) / m, then times the clip coefficient
         if (kAcc) {
             const float4 a0 = dev::ld_stream(T.a[k] + 2 * j), a1 = dev::ld_stream(T.a[k] + 2 * j + 1);
-            prior[0] = a0.x; prior[1] = a0.y; prior[2] = a0.z; prior[3] = a0.w;
-            prior[4] = a1.x; prior[5] = a1.y; prior[6] = a1.z; prior[7] = a1.w;
+            const float prior[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                acc[e] = __fmul_rn(__fadd_rn(prior[e], __fmul_rn(acc[e], s.inv_n)), R.inv_m);
+        } else if (!kG32) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = __fmul_rn(acc[e], s.inv_n);
+        }
+        if (kClip) {
+            const float coef = ld_coef(clip);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = __fmul_rn(acc[e], coef);
         }
 
+        // AdamW on the owner's fp32 state
+        float4* wp = T.w[k] + 2 * j;
+        float4* mp = T.m[k] + 2 * j;
+        float4* vp = T.v[k] + 2 * j;
+        const float4 w0 = dev::ld_stream(wp), w1 = dev::ld_stream(wp + 1);
+        const float4 m0 = dev::ld_stream(mp), m1 = dev::ld_stream(mp + 1);
+        const float4 v0 = dev::ld_stream(vp), v1 = dev::ld_stream(vp + 1);
         float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
         float m[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
         float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            float g = kG32 ? acc[e] : __fmul_rn(acc[e], s.inv_n);
-            if (kAcc) g = __fmul_rn(__fadd_rn(prior[e], g), R.inv_m);
-            if (kClip) g = __fmul_rn(g, coef);
-            adamw(g, w[e], m[e], v[e], s);
-        }
+        for (int e = 0; e < 8; ++e) adamw(acc[e], w[e], m[e], v[e], s);
 
         dev::st_stream(wp, make_float4(w[0], w[1], w[2], w[3]));
         dev::st_stream(wp + 1, make_float4(w[4], w[5], w[6], w[7]));
@@ -409,33 +439,30 @@ bool wide_aligned(const Tables& T, int32_t n)
     return (bits & 31u) == 0;
 }
 
-// One launch of a bf16-gradient variant (plain, clipped, accumulated) in the
-// launch shape kSmall selects.
-template <bool kSmall>
+// One launch of a bf16-gradient variant (plain, clipped, last micro-batch of an
+// accumulation), in the four-block shape.
 int launch_bf16(const Tables& T, const StepScalars& s, int64_t q0, int64_t q1, int64_t shard_vec,
                 int32_t n_ranks, const float* clip, cudaStream_t stream, float inv_m, bool chained)
 {
     const bool acc = inv_m != 0.0f;
     const void* kernel =
-        clip ? (acc ? reinterpret_cast<const void*>(fused_step_kernel<true, true, false, false, kSmall>)
-                    : reinterpret_cast<const void*>(fused_step_kernel<true, false, false, false, kSmall>))
-             : (acc ? reinterpret_cast<const void*>(fused_step_kernel<false, true, false, false, kSmall>)
-                    : reinterpret_cast<const void*>(fused_step_kernel<false, false, false, false, kSmall>));
+        clip ? (acc ? reinterpret_cast<const void*>(fused_step_kernel<true, true, false, false, true>)
+                    : reinterpret_cast<const void*>(fused_step_kernel<true, false, false, false, true>))
+             : (acc ? reinterpret_cast<const void*>(fused_step_kernel<false, true, false, false, true>)
+                    : reinterpret_cast<const void*>(fused_step_kernel<false, false, false, false, true>));
     int blocks = 0;
     Range R = make_range(kernel, q0, q1, shard_vec, n_ranks, &blocks);
     if (blocks <= 0) return ZERO_ECUDA;
     R.inv_m = acc ? inv_m : 1.0f;
     cudaError_t e;
     if (clip && acc)
-        e = launch_fused<true, true, false, false, kSmall>(blocks, stream, chained, T, s, R, clip);
+        e = launch_fused<true, true, false, false, true>(blocks, stream, chained, T, s, R, clip);
     else if (clip)
-        e = launch_fused<true, false, false, false, kSmall>(blocks, stream, chained, T, s, R, clip);
+        e = launch_fused<true, false, false, false, true>(blocks, stream, chained, T, s, R, clip);
     else if (acc)
-        e = launch_fused<false, true, false, false, kSmall>(blocks, stream, chained, T, s, R,
-                                                            nullptr);
+        e = launch_fused<false, true, false, false, true>(blocks, stream, chained, T, s, R, nullptr);
     else
-        e = launch_fused<false, false, false, false, kSmall>(blocks, stream, chained, T, s, R,
-                                                             nullptr);
+        e = launch_fused<false, false, false, false, true>(blocks, stream, chained, T, s, R, nullptr);
     return cuda_status(e);
 }
 
@@ -476,20 +503,17 @@ int launch_range(const Tables& T, const StepScalars& s, int64_t q0, int64_t q1, 
         return cuda_status(launch_fused<false, false, true, false, true>(blocks, stream, chained, T,
                                                                          s, R, nullptr));
     }
-    // The plain and clipped steps take the four-block shape at every rank
-    // count; the last micro-batch of an accumulation (one more fp32 stream,
-    // 64 registers spill there) keeps three blocks between kSmallRanks and
-    // kManyRanks.  Measured on GB300, GPT-2 buffer, random gradients, ms:
-    // N_d = 8 plain 0.7482 -> 0.7403 and 0.7767 -> 0.7750 on two boxes,
-    // N_d = 12 0.9366 -> 0.9243, N_d = 16 1.0676 -> 1.0740; the accumulated
-    // step at N_d = 8 0.8527 -> 0.8814 in the four-block shape.  Elements
-    // whose gradient, m and v are all zero take a slower path through the
-    // IEEE division, which more resident warps hide better: all-zero
-    // gradients 1.098 -> 0.989 ms, half of them zero 0.921 -> 0.864.
-    const bool four = inv_m == 0.0f || n_ranks <= kSmallRanks || n_ranks >= kManyRanks;
-    return four
-               ? launch_bf16<true>(T, s, q0, q1, shard_vec, n_ranks, clip, stream, inv_m, chained)
-               : launch_bf16<false>(T, s, q0, q1, shard_vec, n_ranks, clip, stream, inv_m, chained);
+    // The plain, clipped and accumulated steps: the four-block shape at every
+    // rank count.  Measured on GB300, GPT-2 buffer, random gradients, ms: the
+    // plain step at N_d = 8 0.7482 -> 0.7403 and 0.7767 -> 0.7750 on two
+    // boxes, N_d = 12 0.9366 -> 0.9243, N_d = 16 1.0676 -> 1.0740; the last
+    // micro-batch of an accumulation, once it no longer spilled, N_d = 5
+    // 0.7272 -> 0.7036, 8 0.8053 -> 0.8016, 12 0.9548 -> 0.9290, 16 1.0795 ->
+    // 1.0694, 24 1.3547 -> 1.3485.  Elements whose gradient, m and v are all
+    // zero take a slower path through the IEEE division, which more resident
+    // warps hide better: all-zero gradients 1.098 -> 0.989 ms, half of them
+    // zero 0.921 -> 0.864.
+    return launch_bf16(T, s, q0, q1, shard_vec, n_ranks, clip, stream, inv_m, chained);
 }
 
 // The fused step over the vectors [q0, q1), issued as chunk_count() chained
@@ -675,10 +699,6 @@ cudaGraphNode_t step_node_at(const StepNodeList* log, size_t i)
 int preload_fused_kernels()
 {
     const void* kernels[] = {
-        reinterpret_cast<const void*>(fused_step_kernel<false, false, false>),
-        reinterpret_cast<const void*>(fused_step_kernel<true, false, false>),
-        reinterpret_cast<const void*>(fused_step_kernel<false, true, false>),
-        reinterpret_cast<const void*>(fused_step_kernel<true, true, false>),
         reinterpret_cast<const void*>(fused_step_kernel<true, false, false, true>),
         reinterpret_cast<const void*>(fused_step_kernel<false, false, false, true>),
         reinterpret_cast<const void*>(fused_step_kernel<false, false, false, false, true>),

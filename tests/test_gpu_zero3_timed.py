@@ -13,7 +13,19 @@ calls and compare the result with the oracle:
 * the Llama-1.1B and Llama-7B shapes at full size (N_d = 8, 10 steps), on a
   million random parameters plus every unit, shard and chunk boundary: the
   native step with resident gradients, with each unit's gradients regenerated
-  from the seed in its backward, without resharding, and as a graph.
+  from the seed in its backward, without resharding, and as a graph;
+* with gradient accumulation over 4 micro-batches (zero3_step_microbatch, both
+  gathers in every micro-batch, the units accumulating into fp32 storage and
+  the last micro-batch fused with the update), each micro-batch carrying the
+  step's gradients as in the benchmark; the oracle runs the same accumulation
+  (orc.sample_accum);
+* with global-norm clipping (the norm pre-pass over every unit, then the
+  clipped updates, from the rank gradients or through the fp32 gradient shard
+  the norm pass keeps), natively and as a graph.  The coefficient of a whole
+  model's gradient cannot come from a sample, so the oracle takes the GPU's
+  per-step coefficient as an input (orc.sample_coef); the coefficient is
+  checked against the clip rule on the GPU's norm, and the norm against the
+  oracle's in test_gpu_clip.py.
 
 Method: "Data parallelism, ZeRO and FSDP", "How FSDP implements ZeRO-3",
 steps 2-5 (step 6 for reshard_after_forward=False).  ZeRO-3 reaches the DDP
@@ -36,7 +48,10 @@ CH = B.ZERO_CHUNK_ELEMS
 T = 10
 LLAMA = {"llama-1.1b": [44_044_288] * 22 + [131_074_048],
          "llama-7b": [202_383_360] * 32 + [262_148_096]}
-VARIANTS = ("native", "native-regen", "native-kept", "graph", "graph-kept")
+VARIANTS = ("native", "native-regen", "native-kept", "graph", "graph-kept", "native-micro4",
+            "native-clip", "native-clip-shard", "graph-clip", "graph-clip-shard")
+MICRO = 4  # micro-batches of the accumulated step (each carrying the step's gradients)
+MAX_NORM = 1.0  # below the averaged gradient's norm at these sizes: clipping is active
 
 
 class Job:
@@ -57,6 +72,10 @@ class Job:
         self.full_a = H.Guarded(1, self.max_unit, torch.int16)
         self.full_b = H.Guarded(1, self.max_unit, torch.int16)
         self.kept = None
+        self.grad_shard = None  # fp32 gradient shard storage, for one variant at a time
+        self.scratch = torch.empty(B.zero_clip_scratch_bytes() // 8, dtype=torch.float64,
+                                   device="cuda")
+        self.norm_coef = torch.empty(4, dtype=torch.float32, device="cuda")[:2]
 
     def reset(self):
         """Step-0 state: generated master, m = v = 0, shards = RNE(master)."""
@@ -72,28 +91,52 @@ class Job:
                                   [r[u.offset:u.offset + u.n_padded] for r in self.grads.rows])
 
     def run(self, variant, steps):
-        """`steps` ZeRO-3 steps from step 1 through the named call."""
+        """`steps` ZeRO-3 steps from step 1 through the named call.  Returns the
+        global-norm clip (norm, coefficient) of each step, read back after it,
+        for the clipped variants, else None."""
         self.reset()
         kept = variant.endswith("kept")
         if kept and self.kept is None:
             self.kept = H.Guarded(1, self.total, torch.int16)
         fa, fb = ((self.kept.rows[0], None) if kept
                   else (self.full_a.rows[0], self.full_b.rows[0]))
+        clip, clipped, acc = None, None, None
+        if "-clip" in variant:
+            shard = None
+            if variant.endswith("clip-shard"):
+                self.grad_shard = H.Guarded(self.N, self.total // self.N, torch.float32)
+                shard = self.grad_shard.rows
+            clip = B.clip_args(MAX_NORM, self.scratch, self.norm_coef, grad_shard=shard)
+            clipped = []
         main = torch.cuda.current_stream()
         side = torch.cuda.Stream()
         state = (self.master.rows, self.m.rows, self.v.rows, self.shards.rows)
+
+        def read_coef():
+            if clipped is not None:
+                torch.cuda.synchronize()
+                clipped.append(tuple(float(x) for x in self.norm_coef.cpu()))
+
         if variant.startswith("graph"):
             cap = torch.cuda.Stream()
             cap.wait_stream(main)
             graph = B.zero3_graph_create(self.units, self.grads.rows, *state, fa, fb, H.hp(1), cap,
-                                         side, reshard_after_forward=not kept)
+                                         side, clip=clip, reshard_after_forward=not kept)
             try:
                 for t in range(1, steps + 1):
                     self.fill_grads(t)
                     graph.launch(H.hp(t), stream=main)
+                    read_coef()
                 torch.cuda.synchronize()
             finally:
                 graph.close()
+        elif variant == "native-micro4":
+            acc = H.Guarded(self.N, self.total // self.N, torch.float32)
+            for t in range(1, steps + 1):
+                self.fill_grads(t)
+                for mb in range(MICRO):
+                    B.zero3_step_microbatch(self.units, self.grads.rows, acc.rows, mb, MICRO, *state,
+                                            fa, fb, H.hp(t), main_stream=main, side_stream=side)
         elif variant == "native-regen":
             unit_rows = [r[:self.max_unit] for r in self.grads.rows]
             regen = B.zero_regen_t(self.seed, H.SIGMA_G, self.outliers)
@@ -104,13 +147,16 @@ class Job:
             for t in range(1, steps + 1):
                 self.fill_grads(t)
                 B.zero3_step(self.units, self.grads.rows, *state, fa, fb, H.hp(t),
-                             grads_resident=True, reshard_after_forward=not kept,
+                             grads_resident=True, clip=clip, reshard_after_forward=not kept,
                              main_stream=main, side_stream=side)
+                read_coef()
         torch.cuda.synchronize()
         for b in (self.master, self.m, self.v, self.shards, self.grads, self.full_a, self.full_b,
-                  self.kept):
+                  self.kept, self.grad_shard, acc):
             if b is not None:
                 b.check()
+        self.grad_shard = None  # 27 GB at 7B: released for the next variant
+        return clipped
 
     # ---------------------------------------------------------------- reading
     def owner(self, idx):
@@ -177,6 +223,36 @@ def boundaries(units, N, P):
     return out[(out >= 0) & (out < P)]
 
 
+def check_clip(clipped, seen):
+    """The clipped variants: each step's coefficient is the clip rule applied to
+    the step's norm, clipping is active, and every clipped variant of a job
+    (from the rank gradients or through the fp32 gradient shard, natively or
+    as a graph: the same norm pass partials) sees the same coefficients bit
+    for bit.  The norm itself is compared with the oracle's fp64 norm in
+    test_gpu_clip.py; a whole model's norm is beyond a sampled oracle."""
+    for norm, coef in clipped:
+        assert 0.0 < coef < 1.0, (norm, coef)
+        want = MAX_NORM / (norm + 1e-6)
+        assert abs(coef - want) <= 2e-6 * want, (norm, coef)
+    if "coefs" in seen:
+        assert clipped == seen["coefs"], "clipped variants disagree on the coefficients"
+    seen["coefs"] = clipped
+
+
+def references(orc, N, seed, outliers, idx, variant, clipped, cache):
+    """The oracle's state after T and after T - 1 steps at idx (given the
+    GPU's per-step coefficients for a clipped run; with accumulation over
+    MICRO identical micro-batches for the accumulated one), computed once per
+    kind of run."""
+    micro = MICRO if "micro" in variant else 0
+    key = (micro, None if clipped is None else tuple(c for _, c in clipped))
+    if key not in cache:
+        coefs = None if key[1] is None else np.array(key[1], np.float32)
+        cache[key] = tuple(H.oracle_sample(orc, N, seed, n, idx, outliers=outliers, coefs=coefs,
+                                           micro=micro) for n in (T, T - 1))
+    return cache[key]
+
+
 def compare(job, variant, idx, ref_T, ref_before):
     got = job.state_at(idx)
     H.assert_within_tolerance(got[1:], ref_T[1:], got[0], ref_T[0])
@@ -194,23 +270,22 @@ MULTI_SIZES = [40_000, 3 * CH + 4321, 777]  # one launch, 3 full chunks + a ragg
 
 @pytest.fixture(scope="module")
 def multi(orc):
-    """The job and the oracle's run of every parameter (outliers on)."""
+    """The job, every parameter's index, and a cache of oracle references."""
     job = Job(MULTI_SIZES, MULTI_N, MULTI_SEED, outliers=1)
     assert -(-job.units[1].n_padded // CH) == 4
-    P = sum(MULTI_SIZES)
-    idx = np.arange(P, dtype=np.int64)
-    ref_T = H.oracle_sample(orc, MULTI_N, MULTI_SEED, T, idx, outliers=1)
-    ref_before = H.oracle_sample(orc, MULTI_N, MULTI_SEED, T - 1, idx, outliers=1)
-    yield job, idx, ref_T, ref_before
+    idx = np.arange(sum(MULTI_SIZES), dtype=np.int64)
+    yield job, idx, {}, {}
     del job
     H.free()
 
 
-@pytest.mark.parametrize("variant", ("native", "native-kept", "graph", "graph-kept",
-                                     "native-regen"))
-def test_multi_chunk_units_every_element(multi, variant):
-    job, idx, ref_T, ref_before = multi
-    job.run(variant, T)
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_multi_chunk_units_every_element(orc, multi, variant):
+    job, idx, cache, seen = multi
+    clipped = job.run(variant, T)
+    if clipped is not None:
+        check_clip(clipped, seen)
+    ref_T, ref_before = references(orc, MULTI_N, MULTI_SEED, 1, idx, variant, clipped, cache)
     compare(job, variant, idx, ref_T, ref_before)
     # the padding of every unit holds +0 in every state buffer and shard
     for u in job.units:
@@ -229,9 +304,10 @@ def _release():
     H.free()
 
 
-def llama(orc, name):
-    """The model's job and its oracle reference, built once; any other model's
-    buffers are released first, so that one model at a time holds the GPU."""
+def llama(name):
+    """The model's job, its sampled indices and its caches, built once; any
+    other model's buffers are released first, so that one model at a time
+    holds the GPU."""
     if name not in _jobs:
         _jobs.clear()
         H.free()
@@ -241,9 +317,7 @@ def llama(orc, name):
         rng = np.random.default_rng(1)
         idx = np.unique(np.concatenate([rng.integers(0, P, size=1_000_000),
                                         boundaries(job.units, 8, P)]))
-        ref_T = H.oracle_sample(orc, 8, 0, T, idx)
-        ref_before = H.oracle_sample(orc, 8, 0, T - 1, idx)
-        _jobs[name] = (job, idx, ref_T, ref_before)
+        _jobs[name] = (job, idx, {}, {})
     return _jobs[name]
 
 
@@ -251,8 +325,12 @@ def llama(orc, name):
 def test_llama_full_size_timed_path_sampled(orc, name, variant):
     """Llama shapes, N_d = 8, 10 steps.  At 7B the job holds 203 GB: every
     unit's gradients of all ranks (108 GB), the fp32 state (81 GB), the bf16
-    shards and two full-unit buffers, plus 13.5 GB of kept weights for the
-    variants without resharding."""
-    job, idx, ref_T, ref_before = llama(orc, name)
-    job.run(variant, T)
+    shards and two full-unit buffers; the variants without resharding add
+    13.5 GB of kept weights, and the accumulated variant and those through the
+    gradient shard 27 GB of fp32 storage each, released after the variant."""
+    job, idx, cache, seen = llama(name)
+    clipped = job.run(variant, T)
+    if clipped is not None:
+        check_clip(clipped, seen)
+    ref_T, ref_before = references(orc, 8, 0, 0, idx, variant, clipped, cache)
     compare(job, variant, idx, ref_T, ref_before)
