@@ -93,6 +93,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=None,
                     help="steps of the end-to-end (host buffers) measurement; default min(K, 50)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-zero3-summaries", action="store_true",
+                    help="skip the Llama-1.1B / Llama-7B ZeRO-3 summaries of the default run")
     ap.add_argument("--headline-only", action="store_true",
                     help="time only the headline step (skips the ZeRO-2, clipping, accumulation, "
                          "fp32-gradient and end-to-end legs, the ZeRO-3 Llama summaries, and the "
@@ -579,7 +581,7 @@ def run_gpu(args):
     }
     if not args.headline_only:
         result.update(sub_legs())
-    if not args.headline_only and args.workload == DEFAULT_WORKLOAD:
+    if not (args.headline_only or args.no_zero3_summaries) and args.workload == DEFAULT_WORKLOAD:
         # the two ZeRO-3 configurations of the metric, measured briefly after the
         # flat buffer's memory is released: Llama-1.1B (30 GB) and Llama-7B (203 GB)
         del st

@@ -28,32 +28,26 @@ namespace zero {
 namespace {
 
 constexpr int kBlock = 256;
-constexpr int kRankBatch = 8; // gradient loads issued together before summing
+constexpr int kRankBatch = 8; // gradient loads issued together before summing (three-block shape)
 // Two launch shapes.  The three-block one: three resident blocks per SM (an
 // 80-register cap) instead of the two that the unconstrained 94-102 registers
 // allow, with 8-rank load batches (+12 % at N_d = 8 over two blocks per SM on
-// one unchunked launch).  It now serves the update from the fp32 gradient
-// shard and the accumulation of micro-batches 1..m-1 between kSmallRanks and
-// kManyRanks.
+// one unchunked launch).  It now serves only the update from the fp32
+// gradient shard (fused_step_wide_kernel and its 16-byte fallback), which
+// reads no rank gradients.
 constexpr int kMinBlocksPerSM = 3;
 // The four-block one: four resident blocks per SM (a 64-register cap) and
-// loads in batches of 4 ranks.  It first won up to kSmallRanks, where a
-// thread has few gradient vectors to hold and the bytes in flight per thread
-// fall (112 B at N_d = 1 against 224 B at 8; GB300, GPT-2 buffer: N_d = 1
-// 5,719 -> 6,478 GB/s, N_d = 2 5,876 -> 6,507, N_d = 4 6,260 -> 6,477), and
-// on chained chunks it also wins at N_d = 8 (0.748 -> 0.745 ms a step).
-// Since the kernel loads the gradients before the state (no register spill),
-// every variant of the step from bf16 rank gradients -- plain, clipped, the
-// last micro-batch of an accumulation -- and the fp32-gradient step take it
-// at every rank count.
-constexpr int kSmallRanks = 4;
+// loads in batches of 4 ranks.  It first won up to 4 ranks, where a thread
+// has few gradient vectors to hold and the bytes in flight per thread fall
+// (112 B at N_d = 1 against 224 B at 8; GB300, GPT-2 buffer: N_d = 1 5,719 ->
+// 6,478 GB/s, N_d = 2 5,876 -> 6,507, N_d = 4 6,260 -> 6,477), and on chained
+// chunks it also wins at N_d = 8 (0.748 -> 0.745 ms a step).  Since the
+// kernel loads the gradients before the state (no register spill), every
+// kernel that reads rank gradients -- the plain, clipped and accumulated
+// steps, the fp32-gradient step and the accumulation of micro-batches
+// 1..m-1 -- takes it at every rank count.
 constexpr int kMinBlocksPerSMSmall = 4;
 constexpr int kRankBatchSmall = 4;
-// From kManyRanks ranks on, the accumulation of micro-batches 1..m-1 takes
-// the four-block shape as well: more threads, each with 4-rank load batches,
-// beat fewer with 8-rank ones once gradients are most of the bytes (GB300,
-// GPT-2 buffer, GB/s: N_d = 32 7,116 -> 7,216, N_d = 64 7,135 -> 7,212).
-constexpr int kManyRanks = 32;
 
 // Per-rank device pointers, passed by value in the kernel's parameter space
 // (5 x 64 x 8 B = 2.5 KB).  o[k] points at rank k's output slice: the
@@ -121,8 +115,9 @@ __device__ __forceinline__ float ld_coef(const float* clip)
 // gradient shard T.a[k] (written by zero_grad_reduce_sqnorm) instead of the
 // N rank gradients.  Used when a pointer is only 16-byte aligned;
 // fused_step_wide_kernel does the same with 32-byte accesses otherwise.
-// kSmall: the four-block launch shape (up to kSmallRanks ranks, and for bf16
-// gradients from kManyRanks on).
+// kSmall: the four-block launch shape (every step that reads rank gradients);
+// without it the three-block shape of the 16-byte update from the gradient
+// shard.
 template <bool kClip, bool kAcc, bool kF32 = false, bool kG32 = false, bool kSmall = false>
 __global__ void __launch_bounds__(kBlock, kSmall ? kMinBlocksPerSMSmall : kMinBlocksPerSM)
 fused_step_kernel(const __grid_constant__ Tables T, const StepScalars s, const Range R,
@@ -270,10 +265,10 @@ fused_step_wide_kernel(const __grid_constant__ Tables T, const StepScalars s, co
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
-// ZeRO-2 accumulation of micro-batches 1..m-1: a[k] = (first ? +0 : a[k]) + mean.
-// kSmall: the launch shape for up to kSmallRanks ranks, as fused_step_kernel.
-template <bool kFirst, bool kSmall = false>
-__global__ void __launch_bounds__(kBlock, kSmall ? kMinBlocksPerSMSmall : kMinBlocksPerSM)
+// ZeRO-2 accumulation of micro-batches 1..m-1: a[k] = (first ? +0 : a[k]) + mean,
+// in the fused step's four-block launch shape.
+template <bool kFirst>
+__global__ void __launch_bounds__(kBlock, kMinBlocksPerSMSmall)
 accumulate_kernel(const __grid_constant__ Tables T, const float inv_n, const Range R)
 {
     // chained like fused_step_kernel (the same two instructions, the same reasons)
@@ -285,7 +280,7 @@ accumulate_kernel(const __grid_constant__ Tables T, const float inv_n, const Ran
     int64_t j = q - k * R.shard_vec;
     for (; q < R.q1; q += stride) {
         float acc[8];
-        dev::sum_ranks<kSmall ? kRankBatchSmall : kRankBatch>(T.g, R.n_ranks, q, acc);
+        dev::sum_ranks<kRankBatchSmall>(T.g, R.n_ranks, q, acc);
         float4* ap = T.a[k] + 2 * j;
         float prior[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         if (!kFirst) {
@@ -807,14 +802,12 @@ extern "C" int zero2_accumulate(int32_t n_ranks, int64_t n_padded, const uint16_
         T.a[r] = reinterpret_cast<float4*>(grad_acc[r]);
     }
     const int64_t S = n_padded / n_ranks;
-    // the fused step's launch shapes (GB300, GPT-2 buffer, a later micro-batch:
-    // N_d = 32 7,116 -> 7,216 GB/s, N_d = 64 7,135 -> 7,212 in the four-block one)
-    const bool small = n_ranks <= kSmallRanks || n_ranks >= kManyRanks;
-    const void* kernel =
-        small ? (first ? reinterpret_cast<const void*>(accumulate_kernel<true, true>)
-                       : reinterpret_cast<const void*>(accumulate_kernel<false, true>))
-              : (first ? reinterpret_cast<const void*>(accumulate_kernel<true, false>)
-                       : reinterpret_cast<const void*>(accumulate_kernel<false, false>));
+    // The four-block launch shape at every rank count (GB300, GPT-2 buffer, a
+    // later micro-batch, ms: N_d = 5 0.335 -> 0.320, 8 0.425 -> 0.413, 12 0.573
+    // -> 0.554, 16 0.701 -> 0.688, 24 0.981 -> 0.965 against the three-block
+    // one; N_d = 32 7,116 -> 7,216 GB/s, 64 7,135 -> 7,212).
+    const void* kernel = first ? reinterpret_cast<const void*>(accumulate_kernel<true>)
+                               : reinterpret_cast<const void*>(accumulate_kernel<false>);
     const float inv_n = static_cast<float>(1.0 / static_cast<double>(n_ranks));
     // chained chunks of kChunkVec vectors, as the fused step's launch()
     cudaLaunchAttribute attr[1];
@@ -832,11 +825,8 @@ extern "C" int zero2_accumulate(int32_t n_ranks, int64_t n_padded, const uint16_
         cfg.stream = stream;
         cfg.attrs = attr;
         cfg.numAttrs = a > 0 ? 1 : 0;
-        const cudaError_t e =
-            small ? (first ? cudaLaunchKernelEx(&cfg, accumulate_kernel<true, true>, T, inv_n, R)
-                           : cudaLaunchKernelEx(&cfg, accumulate_kernel<false, true>, T, inv_n, R))
-                  : (first ? cudaLaunchKernelEx(&cfg, accumulate_kernel<true, false>, T, inv_n, R)
-                           : cudaLaunchKernelEx(&cfg, accumulate_kernel<false, false>, T, inv_n, R));
+        const cudaError_t e = first ? cudaLaunchKernelEx(&cfg, accumulate_kernel<true>, T, inv_n, R)
+                                    : cudaLaunchKernelEx(&cfg, accumulate_kernel<false>, T, inv_n, R);
         if (e != cudaSuccess) return cuda_status(e);
     }
     return ZERO_OK;

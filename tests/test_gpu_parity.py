@@ -294,7 +294,8 @@ SWEEP_N = [2, 4, 8, 16, 64]
 def test_sweep(orc, N, P):
     """Padding-exercising sweep with 1 % x100 outliers, 5 steps (ZeRO-2, 25 MiB
     buckets): every element against the oracle when that takes the oracle a
-    few seconds, otherwise sampled elements plus all shard boundaries."""
+    few seconds, otherwise a million sampled elements plus every shard and
+    bucket boundary."""
     T, seed = 5, 3
     stage, bucket = 2, BUCKET_25MIB
     full_compare = P * N <= 2**24
@@ -324,12 +325,13 @@ def test_sweep(orc, N, P):
         assert H.padding_is_zero(params, P, None)
         for a in (master, m, v):
             assert H.padding_is_zero(a, P, S)
-        bounds = [k * S + d for k in range(N + 1) for d in (-1, 0, 1)] + [P - 1]
-        idx = sample_indices(P, bounds, 200_000 if N >= 16 else 1_000_000, seed=N)
+        # every shard and 25 MiB bucket (= chained launch) boundary and its neighbours
+        edges = [k * S for k in range(N + 1)] + list(range(bucket, u.n_padded, bucket))
+        bounds = [e + d for e in edges for d in (-1, 0, 1)] + [P - 1]
+        idx = sample_indices(P, bounds, 1_000_000, seed=N)
         gp = H.at_flat(params, idx, None)
         gw, gm, gv = (H.at_flat(a, idx, S) for a in (master, m, v))
-        rp, rw, rm, rv = orc.sample(N, seed, H.SIGMA_W, H.SIGMA_G, 1,
-                                    orc.hparams(**H.HP, step=1), T, idx)
+        rp, rw, rm, rv = H.oracle_sample(orc, N, seed, T, idx, outliers=1)
         H.assert_within_tolerance((gw, gm, gv), (rw, rm, rv), gp, rp)
         for name, g, r in (("params", gp, rp), ("master", gw, rw), ("m", gm, rm), ("v", gv, rv)):
             H.assert_bitwise(g, r, name)
