@@ -10,8 +10,9 @@ the oracle's fp64 norm within 1e-6: the norm's summation order is the GPU's
 own (fixed-grid partial sums), so its last bits are not the oracle's.  Each
 ZeRO-3 case draws unit sizes and runs the native scheduler with or without
 resharding after the forward pass, and checks the full-unit buffers hold the
-weights its last gathers had to read.  The seeds are fixed, so a failure
-repeats.
+weights its last gathers had to read; the timed-path cases also draw units of
+several chained launches and any form of the step the benchmark times.  The
+seeds are fixed, so a failure repeats.
 """
 import numpy as np
 import pytest
@@ -148,4 +149,37 @@ def test_random_zero3_cases_match_ddp(orc, i):
     before = orc.sim_ddp(N, sum(sizes), seed, H.SIGMA_W, H.SIGMA_G, 1,
                          orc.hparams(**H.HP, step=1), T - 1)[0]
     H.assert_gathered(units, sizes, before, fa, fb if reshard else None)
+    H.free()
+
+
+@pytest.mark.parametrize("i", range(12))
+def test_random_zero3_timed_path_cases(orc, i):
+    """Seeded random ZeRO-3 jobs through the calls the benchmark times: 1 to 4
+    units, some long enough for two or three chained launches, 1 to 64 ranks,
+    1 to 4 steps, and one of the step forms (native with resident, regenerated
+    or kept weights, accumulated, clipped from the rank gradients or through
+    the gradient shard, or any of them as a CUDA graph).  Every element is
+    compared when the job is small, else a third of a million sampled ones and
+    every unit, shard and chunk boundary."""
+    from zero3_job import CH, VARIANTS, Job, boundaries, check_clip, compare, references
+
+    rng = np.random.default_rng(5000 + i)
+    N = int(rng.choice([1, 2, 3, 4, 8, 16, 64]))
+    sizes = [int(rng.integers(CH + 1, 3 * CH)) if rng.random() < 0.3
+             else int(rng.integers(1, 300_000)) for _ in range(int(rng.integers(1, 5)))]
+    variant = str(rng.choice(VARIANTS))
+    steps, seed = int(rng.integers(1, 5)), 6000 + i
+    job = Job(sizes, N, seed, outliers=1)
+    P = sum(sizes)
+    if P <= 2_000_000:
+        idx = np.arange(P, dtype=np.int64)
+    else:
+        idx = np.unique(np.concatenate([rng.integers(0, P, size=300_000),
+                                        boundaries(job.units, N, P)]))
+    clipped = job.run(variant, steps)
+    if clipped is not None:
+        check_clip(clipped, {}, active=False)
+    ref_T, ref_before = references(orc, N, seed, 1, idx, variant, clipped, {}, steps)
+    compare(job, variant, idx, ref_T, ref_before)
+    del job
     H.free()
