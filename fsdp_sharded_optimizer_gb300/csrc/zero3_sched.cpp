@@ -19,10 +19,13 @@
 namespace zero {
 namespace {
 
-constexpr int kEvents = 5; // start, gathered[2], released[2]
+constexpr int kEvents = 7; // start, gathered[2], released[2], aux start, aux done
 constexpr int kMaxDevices = 64;
-constexpr int kEvStart = 0, kEvGathered = 1, kEvReleased = 3;
+constexpr int kEvStart = 0, kEvGathered = 1, kEvReleased = 3, kEvAuxStart = 5, kEvAuxDone = 6;
 constexpr int32_t kOwnRegion = 2; // GATHER/USE arg: the unit's region of the kept full buffer
+// Streams of a plan: the caller's main and side streams, and a second compute
+// stream of the library's own that takes every other backward unit.
+constexpr int32_t kMain = 0, kSide = 1, kAux = 2;
 
 // What a backward pass does with a unit's gradients of this micro-batch.
 enum class Reduce {
@@ -36,13 +39,20 @@ struct PlanBuilder {
     std::vector<zero_op_t> ops;
     bool released_recorded[2] = {false, false};
     Reduce reduce_mode = Reduce::kStep;
+    // The resharding backward pass runs the units of odd positions (those of
+    // full buffer 1) on the second compute stream: consecutive units' updates
+    // then overlap at their boundary, where one stream would separate them by
+    // an event wait and record.  Not with regeneration, whose units share one
+    // gradient buffer.
+    bool two_compute = false;
 
-    void reduce(int32_t u, bool clip)
+    void reduce(int32_t u, bool clip, int32_t stream)
     {
         if (reduce_mode == Reduce::kAccFirst || reduce_mode == Reduce::kAccLater)
-            add(ZERO_OP_ACCUMULATE, 0, u, reduce_mode == Reduce::kAccFirst ? 1 : 0);
+            add(ZERO_OP_ACCUMULATE, stream, u, reduce_mode == Reduce::kAccFirst ? 1 : 0);
         else
-            add(ZERO_OP_REDUCE_SCATTER, 0, u, reduce_mode == Reduce::kAccLast ? 2 : (clip ? 1 : 0));
+            add(ZERO_OP_REDUCE_SCATTER, stream, u,
+                reduce_mode == Reduce::kAccLast ? 2 : (clip ? 1 : 0));
     }
 
     void add(int32_t kind, int32_t stream, int32_t unit, int32_t arg)
@@ -67,13 +77,16 @@ struct PlanBuilder {
             const int32_t slot = pos % 2;
             const int32_t u = unit_at(pos);
             if (pos + 1 < n_units) gather(unit_at(pos + 1), pos + 1, 1 - slot); // prefetch
-            add(ZERO_OP_WAIT, 0, -1, kEvGathered + pos % 2);
-            add(ZERO_OP_USE, 0, u, slot);
+            // a unit's work, and the release of its full buffer, on the
+            // compute stream of that buffer
+            const int32_t cs = backward && two_compute && slot == 1 ? kAux : kMain;
+            add(ZERO_OP_WAIT, cs, -1, kEvGathered + pos % 2);
+            add(ZERO_OP_USE, cs, u, slot);
             if (backward) {
-                if (regen) add(ZERO_OP_REGEN, 0, u, 0);
-                reduce(u, clip);
+                if (regen) add(ZERO_OP_REGEN, cs, u, 0);
+                reduce(u, clip, cs);
             }
-            add(ZERO_OP_RECORD, 0, -1, kEvReleased + slot);
+            add(ZERO_OP_RECORD, cs, -1, kEvReleased + slot);
             released_recorded[slot] = true;
         }
     }
@@ -98,9 +111,9 @@ struct PlanBuilder {
     void backward_kept(int32_t n_units, bool regen, bool clip)
     {
         for (int32_t u = n_units - 1; u >= 0; --u) {
-            add(ZERO_OP_USE, 0, u, kOwnRegion);
-            if (regen) add(ZERO_OP_REGEN, 0, u, 0);
-            reduce(u, clip);
+            add(ZERO_OP_USE, kMain, u, kOwnRegion);
+            if (regen) add(ZERO_OP_REGEN, kMain, u, 0);
+            reduce(u, clip, kMain);
         }
     }
 
@@ -121,7 +134,20 @@ struct PlanBuilder {
         }
         if (reshard) {
             pass(n_units, false, regen, clip);
+            // the second compute stream starts after everything the main
+            // stream did before the backward pass (the caller's work, the
+            // clip coefficient) and hands its end back to the main stream
+            const bool aux = two_compute && !regen && n_units > 1;
+            two_compute = aux;
+            if (aux) {
+                add(ZERO_OP_RECORD, kMain, -1, kEvAuxStart);
+                add(ZERO_OP_WAIT, kAux, -1, kEvAuxStart);
+            }
             pass(n_units, true, regen, clip);
+            if (aux) {
+                add(ZERO_OP_RECORD, kAux, -1, kEvAuxDone);
+                add(ZERO_OP_WAIT, kMain, -1, kEvAuxDone);
+            }
         } else {
             forward_keep(n_units);
             backward_kept(n_units, regen, clip);
@@ -153,25 +179,29 @@ int copy_plan(const PlanBuilder& b, zero_op_t* ops, int32_t max_ops, int32_t* n_
     return ZERO_OK;
 }
 
-// Five timing-free events per host thread and device, created on first use.
-struct EventCache {
+// Seven timing-free events and the second compute stream (non-blocking) per
+// host thread and device, created on first use.
+struct StepResources {
     int device = -1;
     cudaEvent_t ev[kEvents] = {};
+    cudaStream_t aux = nullptr;
 };
-thread_local EventCache t_events[kMaxDevices];
+thread_local StepResources t_res[kMaxDevices];
 
-int events_for_current_device(cudaEvent_t** out)
+int resources_for_current_device(StepResources** out)
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ZERO_ECUDA;
-    EventCache& c = t_events[dev];
+    StepResources& c = t_res[dev];
     if (c.device != dev) {
         for (int i = 0; i < kEvents; ++i)
-            if (cudaEventCreateWithFlags(&c.ev[i], cudaEventDisableTiming) != cudaSuccess)
+            if (!c.ev[i] && cudaEventCreateWithFlags(&c.ev[i], cudaEventDisableTiming) != cudaSuccess)
                 return ZERO_ECUDA;
+        if (!c.aux && cudaStreamCreateWithFlags(&c.aux, cudaStreamNonBlocking) != cudaSuccess)
+            return ZERO_ECUDA;
         c.device = dev;
     }
-    *out = c.ev;
+    *out = &c;
     return ZERO_OK;
 }
 
@@ -186,8 +216,8 @@ bool unit_consistent(const zero_unit_t& u, int32_t n_ranks)
 
 int preload_step_events()
 {
-    cudaEvent_t* ev = nullptr;
-    return events_for_current_device(&ev);
+    StepResources* r = nullptr;
+    return resources_for_current_device(&r);
 }
 
 } // namespace zero
@@ -204,6 +234,7 @@ extern "C" int zero3_plan_microbatch(int32_t n_units, int32_t reshard_after_forw
     const AccumArgs acc{nullptr, micro_batch, micro_batches};
     PlanBuilder b;
     b.reduce_mode = reduce_mode(&acc);
+    b.two_compute = true;
     b.step(n_units, false, false, reshard_after_forward != 0);
     return copy_plan(b, ops, max_ops, n_ops);
 }
@@ -214,6 +245,7 @@ extern "C" int zero3_plan(int32_t n_units, int32_t regen, int32_t clip,
 {
     if (n_units < 1 || !ops || !n_ops || max_ops < 0) return ZERO_EINVAL;
     PlanBuilder b;
+    b.two_compute = true;
     b.step(n_units, regen != 0, clip != 0, reshard_after_forward != 0);
     return copy_plan(b, ops, max_ops, n_ops);
 }
@@ -261,10 +293,17 @@ int run_step(const zero_unit_t* units, int32_t n_units, int32_t n_ranks, const v
             return rc;
     }
 
-    cudaEvent_t* ev = nullptr;
-    if ((rc = events_for_current_device(&ev)) != ZERO_OK) return rc;
+    StepResources* res = nullptr;
+    if ((rc = resources_for_current_device(&res)) != ZERO_OK) return rc;
+    cudaEvent_t* ev = res->ev;
+    cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+    if ((rc = cuda_status(cudaStreamIsCapturing(main_stream, &capture))) != ZERO_OK) return rc;
     PlanBuilder plan;
     plan.reduce_mode = reduce_mode(acc);
+    // While the main stream is being captured the backward pass keeps one
+    // compute stream, and the graph builder joins its units with programmatic
+    // edges instead.
+    plan.two_compute = capture == cudaStreamCaptureStatusNone;
     plan.step(n_units, regen != nullptr, clip != nullptr, reshard);
 
     const uint16_t* unit_grads[ZERO_MAX_RANKS];
@@ -292,16 +331,16 @@ int run_step(const zero_unit_t* units, int32_t n_units, int32_t n_ranks, const v
     // pass) they are not chained: measured on GB300, chaining across the
     // events gained nothing.  While the stream is being captured, the graph
     // builder joins the units itself.
-    bool after_update = false;
-    cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
-    if ((rc = cuda_status(cudaStreamIsCapturing(main_stream, &capture))) != ZERO_OK) return rc;
+    // (tracked per stream: an update follows an update on its own stream)
+    bool after_update[3] = {false, false, false};
     for (const zero_op_t& op : plan.ops) {
-        cudaStream_t s = op.stream == 0 ? main_stream : side_stream;
+        cudaStream_t s = op.stream == kMain ? main_stream : op.stream == kSide ? side_stream : res->aux;
         const bool chain_norm = after_norm;
-        const bool chain_update = after_update && capture == cudaStreamCaptureStatusNone;
-        if (op.stream == 0) after_norm = op.kind == ZERO_OP_NORM;
-        if (op.stream == 0 && op.kind != ZERO_OP_USE) // USE issues nothing
-            after_update = op.kind == ZERO_OP_REDUCE_SCATTER && op.arg != 2;
+        const bool chain_update =
+            after_update[op.stream] && capture == cudaStreamCaptureStatusNone;
+        if (op.stream == kMain) after_norm = op.kind == ZERO_OP_NORM;
+        if (op.kind != ZERO_OP_USE) // USE issues nothing
+            after_update[op.stream] = op.kind == ZERO_OP_REDUCE_SCATTER && op.arg != 2;
         switch (op.kind) {
         case ZERO_OP_RECORD:
             rc = cuda_status(cudaEventRecord(ev[op.arg], s));

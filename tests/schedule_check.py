@@ -1,21 +1,36 @@
-"""Happens-before checks of a two-stream ZeRO-3 step trace (test helper).
+"""Happens-before checks of a ZeRO-3 step trace (test helper).
 
 A trace is a list of entries in host issue order:
   ("record", stream, event)   ("wait", stream, event)
   ("gather", stream, unit, buffer)   ("use", stream, unit, buffer, ...)
-  ("rs", stream, unit)   ("regen", stream, unit)
-with stream "main" or "side".  A wait orders the waiting stream's later
-operations after the operation that preceded the event's most recent record
-at the time of the wait (CUDA's semantics for a re-recorded event)."""
+  ("rs", stream, unit)   ("regen", stream, unit)   ("end", stream)
+with stream "main", "side" or "aux" (the second compute stream of the
+native scheduler), and "end" marking where a step returns (on "main").  A
+wait orders the waiting stream's later operations after the operation that
+preceded the event's most recent record at the time of the wait (CUDA's
+semantics for a re-recorded event); a record right after waits also carries
+them, as a CUDA event record carries everything before it on its stream."""
+from collections import defaultdict
+
+COMPUTE = ("main", "aux")
 
 
 def happens_before_graph(trace):
     pos, last_op, event_src, edges = {}, {}, {}, {}
-    count = {"main": 0, "side": 0}
-    pending = {"main": [], "side": []}
+    count = defaultdict(int)
+    pending = defaultdict(list)
     for e in trace:
         kind, stream = e[0], e[1]
         if kind == "record":
+            if pending[stream]:
+                # a record after waits captures them too: it becomes a node of
+                # its own, after the waited-for operations and the stream's last
+                node = (stream, count[stream])
+                count[stream] += 1
+                pos[node] = ("sync", stream)
+                edges[node] = list(pending[stream]) + ([last_op[stream]] if stream in last_op else [])
+                pending[stream].clear()
+                last_op[stream] = node
             event_src[e[2]] = last_op.get(stream)
             continue
         if kind == "wait":
@@ -58,9 +73,14 @@ def check_zero3_trace(trace, n_units, n_steps):
     gathers = by_issue([n for n, e in pos.items() if e[0] == "gather"])
     uses = by_issue([n for n, e in pos.items() if e[0] == "use"])
     rss = by_issue([n for n, e in pos.items() if e[0] == "rs"])
+    ends = by_issue([n for n, e in pos.items() if e[0] == "end"])
     assert len(gathers) == 2 * U * n_steps and len(uses) == 2 * U * n_steps
     assert len(rss) == U * n_steps
-    assert all(n[0] == "side" for n in gathers) and all(n[0] == "main" for n in uses + rss)
+    assert all(n[0] == "side" for n in gathers) and all(n[0] in COMPUTE for n in uses + rss)
+    # the forward pass runs on the main stream; a unit's backward use and
+    # reduce-scatter share one compute stream
+    fwd_uses = [u for k, u in enumerate(uses) if (k // U) % 2 == 0]
+    assert all(n[0] == "main" for n in fwd_uses)
     # forward 0..U-1, backward U-1..0, every step
     assert [pos[n][2] for n in gathers] == (list(range(U)) + list(range(U - 1, -1, -1))) * n_steps
     assert [pos[n][2] for n in uses] == (list(range(U)) + list(range(U - 1, -1, -1))) * n_steps
@@ -86,9 +106,17 @@ def check_zero3_trace(trace, n_units, n_steps):
                    and order_of[id(pos[g])] < order_of[id(pos[r])]]
             assert pre, "no prefetch of unit %d before unit %d's reduce-scatter" % (unit - 1, unit)
             assert not hb(edges, pre[-1], r)
-    # the next step's first gather sees the previous step's last reduce-scatter
+    # the next step's first gather sees every reduce-scatter of the step before
     for s in range(1, n_steps):
-        assert hb(edges, rss[s * U - 1], gathers[s * 2 * U])
+        for r in rss[(s - 1) * U:s * U]:
+            assert hb(edges, r, gathers[s * 2 * U]), "next step overtakes unit %d" % pos[r][2]
+    # where the trace marks the step's return on the main stream, every
+    # reduce-scatter of the step happens before it
+    if ends:
+        assert len(ends) == n_steps and all(n[0] == "main" for n in ends)
+        for s in range(n_steps):
+            for r in rss[s * U:(s + 1) * U]:
+                assert hb(edges, r, ends[s]), "step ends before unit %d's update" % pos[r][2]
     # at most two units gathered and not yet released at any time is implied by
     # the two buffers and the overwrite check above
     return True

@@ -101,9 +101,12 @@ def test_prefetch_order_and_buffer_safety(orc):
     check_zero3_trace(be.trace, len(units), 2)
 
 
+STREAMS = {0: "main", 1: "side", 2: "aux"}
+
+
 def _native_trace(n_units, n_steps, regen=False, clip=False, reshard=True):
     from fsdp_sharded_optimizer_gb300 import _binding as B
-    names = {0: "main", 1: "side"}
+    names = STREAMS
     trace = []
     for _ in range(n_steps):
         for kind, stream, unit, arg in B.zero3_plan(n_units, regen, clip, reshard):
@@ -118,6 +121,7 @@ def _native_trace(n_units, n_steps, regen=False, clip=False, reshard=True):
                 trace.append(("rs", st, unit))
             else:
                 trace.append((kind, st, unit))
+        trace.append(("end", "main"))
     return trace
 
 
@@ -139,6 +143,38 @@ def test_native_plan_is_safe(n_units, n_steps, regen, clip):
             norms = [i for i, k in enumerate(kinds) if k == "norm"]
             assert len(norms) == n_units and max(norms) < coef < first_rs
             assert all(e[1] == "main" for e in st if e[0] in ("norm", "clip_coef"))
+        _assert_rs_after_coef(trace)
+
+
+def _assert_rs_after_coef(trace):
+    """Every reduce-scatter, on either compute stream, happens after the
+    coefficient kernel of its step (it scales by the coefficient)."""
+    from schedule_check import happens_before_graph, hb
+    pos, edges = happens_before_graph(trace)
+    order_of = {id(e): i for i, e in enumerate(trace)}
+    nodes = sorted(pos, key=lambda n: order_of.get(id(pos[n]), 0))
+    coef = None
+    for n in nodes:
+        if pos[n][0] == "clip_coef":
+            coef = n
+        elif pos[n][0] == "rs":
+            assert coef is not None and hb(edges, coef, n), "update before its coefficient"
+
+
+def test_checks_catch_a_missing_join_of_the_second_compute_stream():
+    """The plan's second compute stream hands its end back to the main stream
+    (event 6): without that join the step could return, and the next step
+    start, before a unit's update, and the checks see it.  Its updates follow
+    the clip coefficient (through the side stream's waits on the forward
+    pass's releases, and explicitly through event 5)."""
+    trace = _native_trace(5, 2, clip=True)
+    assert any(e[:2] == ("wait", "main") and e[2] == "ev6" for e in trace)
+    assert any(e[:2] == ("wait", "aux") and e[2] == "ev5" for e in trace)
+    no_join = [e for e in trace if not (e[:2] == ("wait", "main") and e[2] == "ev6")]
+    with pytest.raises(AssertionError):
+        check_zero3_trace(no_join, 5, 2)
+    check_zero3_trace(trace, 5, 2)
+    _assert_rs_after_coef(trace)
 
 
 def test_native_plan_counts_and_regen():
@@ -146,16 +182,16 @@ def test_native_plan_counts_and_regen():
     ops = B.zero3_plan(2, False)
     kinds = [o[0] for o in ops]
     assert kinds.count("gather") == 4 and kinds.count("reduce_scatter") == 2
-    assert "regen" not in kinds and "norm" not in kinds and len(ops) <= 13 * 2 + 2
+    assert "regen" not in kinds and "norm" not in kinds and len(ops) <= 13 * 2 + 6
     assert all(o[3] == 0 for o in ops if o[0] == "reduce_scatter")
     ops = B.zero3_plan(3, True, True)
-    assert len(ops) <= 13 * 3 + 2 + 3 + 3 + 1 + 3
+    assert len(ops) <= 13 * 3 + 6 + 3 + 3 + 1 + 3
     assert all(o[3] == 1 for o in ops if o[0] == "reduce_scatter")
     norms = [o for o in ops if o[0] == "norm"]
     assert [o[3] for o in norms] == [0, 1, 1]  # the first unit overwrites the partials
     ops = B.zero3_plan(4, True)
     kinds = [o[0] for o in ops]
-    assert kinds.count("regen") == 4 and len(ops) <= 14 * 4 + 2
+    assert kinds.count("regen") == 4 and len(ops) <= 14 * 4 + 6
     # every regeneration immediately precedes its unit's reduce-scatter on the main stream
     for i, o in enumerate(ops):
         if o[0] == "regen":
@@ -224,13 +260,13 @@ def test_microbatch_plans_are_safe_and_accumulate(n_units, micro, reshard):
         for o, p in zip(ops, plain):
             if p[0] == "reduce_scatter":
                 if mb < micro - 1:
-                    assert o == ("accumulate", 0, p[2], 1 if mb == 0 else 0)
+                    assert o == ("accumulate", p[1], p[2], 1 if mb == 0 else 0)
                 else:
-                    assert o == ("reduce_scatter", 0, p[2], 2 if micro > 1 else 0)
+                    assert o == ("reduce_scatter", p[1], p[2], 2 if micro > 1 else 0)
             else:
                 assert o == p
         for kind, stream, unit, arg in ops:
-            st = {0: "main", 1: "side"}[stream]
+            st = STREAMS[stream]
             if kind in ("record", "wait"):
                 trace.append((kind, st, "ev%d" % arg))
             elif kind in ("gather", "use"):
