@@ -559,7 +559,9 @@ typedef struct {
  *                    updates then read instead of the gradients)
  * The library keeps seven timing-free CUDA events and one non-blocking CUDA
  * stream (stream 2 of zero3_plan) per host thread and device, created on
- * first use; no device memory is allocated.  While main_stream is being
+ * first use and kept for the thread's life (a cudaDeviceReset invalidates
+ * them: the step then fails with ZERO_ECUDA on that device and thread); no
+ * device memory is allocated.  While main_stream is being
  * captured the backward pass keeps to the main stream (zero3_graph_create
  * joins its units with programmatic edges instead).  Work is queued
  * asynchronously; on return main_stream carries the end of the step.  Kernels
