@@ -560,8 +560,8 @@ typedef struct {
  * The library keeps seven timing-free CUDA events and one non-blocking CUDA
  * stream (stream 2 of zero3_plan) per host thread and device, created on
  * first use and kept for the thread's life (a cudaDeviceReset invalidates
- * them: the step then fails with ZERO_ECUDA on that device and thread); no
- * device memory is allocated.  While main_stream is being
+ * them, so zero3_step must not be called on that device from that thread
+ * again); no device memory is allocated.  While main_stream is being
  * captured the backward pass keeps to the main stream (zero3_graph_create
  * joins its units with programmatic edges instead).  Work is queued
  * asynchronously; on return main_stream carries the end of the step.  Kernels
