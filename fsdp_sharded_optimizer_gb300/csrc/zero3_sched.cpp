@@ -6,6 +6,10 @@
 // in reverse unit order that gathers each unit again and reduce-scatters its
 // gradients, gathers on a separate stream, and the next unit's gather issued
 // before the current unit's work, with at most two units gathered at once.
+// Without a backward compute to hide them behind, the boundaries between
+// consecutive units' updates would be idle time on one stream, so the
+// backward units alternate between the caller's main stream and a second
+// compute stream of the library's own (see PlanBuilder::two_compute).
 //
 // The plan is built on the host as a list of operations and then executed,
 // so the same plan can be checked on a machine without a GPU.  Executing it
