@@ -477,7 +477,7 @@ def zero_clip_coef_units_noalloc(units, grads, max_norm, norm_coef, unit_norms=N
 def zero3_plan(n_units, regen=False, clip=False, reshard_after_forward=True):
     """The operations of one ZeRO-3 step (host only): a list of
     (kind name, stream 0=main/1=side, unit, arg)."""
-    cap = 17 * n_units + 3
+    cap = 18 * n_units + 8  # the header's bound (16 n + 7 with regeneration and clipping) and more
     ops = (zero_op_t * cap)()
     n = C.c_int32()
     _check("zero3_plan", lib.zero3_plan(n_units, 1 if regen else 0, 1 if clip else 0,
@@ -488,7 +488,7 @@ def zero3_plan(n_units, regen=False, clip=False, reshard_after_forward=True):
 def zero3_plan_microbatch(n_units, micro_batch, micro_batches, reshard_after_forward=True):
     """The operations of one micro-batch of a ZeRO-3 step with gradient
     accumulation (host only), as zero3_plan's list."""
-    cap = 17 * n_units + 3
+    cap = 18 * n_units + 8  # the header's bound (16 n + 7 with regeneration and clipping) and more
     ops = (zero_op_t * cap)()
     n = C.c_int32()
     _check("zero3_plan_microbatch", lib.zero3_plan_microbatch(
