@@ -254,3 +254,49 @@ def test_native_step_without_reshard_matches_ddp(orc, regen):
     got = [np.concatenate([sh[k_][u.shard_offset:u.shard_offset + u.shard_len]
                            for k_ in range(N)])[:u.n_params] for u in units]
     H.assert_bitwise(np.concatenate(got), ddp[T][0], "params")
+
+
+def test_native_steps_from_two_host_threads(orc):
+    """zero3_step keeps its events and its second compute stream per host
+    thread: two threads stepping two independent jobs at once, each on its
+    own streams, both equal DDP bit for bit."""
+    import threading
+
+    N, sizes, T = 4, [70_000, 333, 200_000, 64, 90_001], 3
+    results, errors = {}, []
+
+    def job(seed):
+        try:
+            units, total = B.zero_layout(sizes, N)
+            master, m, v, shards, grads, fa, fb = _native_buffers(units, total, N, True, seed)
+            main, side = torch.cuda.Stream(), torch.cuda.Stream()
+            main.wait_stream(torch.cuda.current_stream())  # the buffers' initial contents
+            with torch.cuda.stream(main):
+                for t in range(1, T + 1):
+                    for u in units:
+                        B.zero_gen_grads_unit(seed, t, H.SIGMA_G, 1, u,
+                                              [r[u.offset:u.offset + u.n_padded] for r in grads.rows],
+                                              stream=main)
+                    B.zero3_step(units, grads.rows, master.rows, m.rows, v.rows, shards.rows,
+                                 fa.rows[0], fb.rows[0], H.hp(t), main_stream=main,
+                                 side_stream=side)
+            main.synchronize()
+            for b_ in (master, m, v, shards, grads, fa, fb):
+                b_.check()
+            sh = shards.numpy()
+            results[seed] = np.concatenate([np.concatenate(
+                [sh[k][u.shard_offset:u.shard_offset + u.shard_len] for k in range(N)])[:u.n_params]
+                for u in units])
+        except Exception as e:  # reported below, on the test's thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=job, args=(s,)) for s in (21, 22)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    for seed in (21, 22):
+        ddp = orc.sim_ddp(N, sum(sizes), seed, H.SIGMA_W, H.SIGMA_G, 1,
+                          orc.hparams(**H.HP, step=1), T)
+        H.assert_bitwise(results[seed], ddp[0], "params of the job seeded %d" % seed)
