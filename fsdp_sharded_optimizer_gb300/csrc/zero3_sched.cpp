@@ -7,9 +7,11 @@
 // gradients, gathers on a separate stream, and the next unit's gather issued
 // before the current unit's work, with at most two units gathered at once.
 // Without a backward compute to hide them behind, the boundaries between
-// consecutive units' updates would be idle time on one stream, so the
-// backward units alternate between the caller's main stream and a second
-// compute stream of the library's own (see PlanBuilder::two_compute).
+// consecutive units' updates, and between consecutive gathers, would be idle
+// time on one stream, so the backward units alternate between the caller's
+// main stream and a second compute stream of the library's own, and the
+// gathers between the caller's side stream and a second side stream
+// (PlanBuilder::two_compute, two_side).
 //
 // The plan is built on the host as a list of operations and then executed,
 // so the same plan can be checked on a machine without a GPU.  Executing it
@@ -27,9 +29,10 @@ constexpr int kEvents = 7; // start, gathered[2], released[2], aux start, aux do
 constexpr int kMaxDevices = 64;
 constexpr int kEvStart = 0, kEvGathered = 1, kEvReleased = 3, kEvAuxStart = 5, kEvAuxDone = 6;
 constexpr int32_t kOwnRegion = 2; // GATHER/USE arg: the unit's region of the kept full buffer
-// Streams of a plan: the caller's main and side streams, and a second compute
-// stream of the library's own that takes every other backward unit.
-constexpr int32_t kMain = 0, kSide = 1, kAux = 2;
+// Streams of a plan: the caller's main and side streams, and two of the
+// library's own: a second compute stream that takes every other backward unit
+// and a second side stream that takes the gathers into full buffer 1.
+constexpr int32_t kMain = 0, kSide = 1, kAux = 2, kSide2 = 3;
 
 // What a backward pass does with a unit's gradients of this micro-batch.
 enum class Reduce {
@@ -49,6 +52,12 @@ struct PlanBuilder {
     // an event wait and record.  Not with regeneration, whose units share one
     // gradient buffer.
     bool two_compute = false;
+    // Likewise the gathers into full buffer 1 (into the units of odd positions
+    // without resharding) run on the second side stream, so that consecutive
+    // gathers overlap at their boundary too.
+    bool two_side = false;
+
+    int32_t side_of(int32_t pos) const { return two_side && pos % 2 == 1 ? kSide2 : kSide; }
 
     void reduce(int32_t u, bool clip, int32_t stream)
     {
@@ -68,9 +77,10 @@ struct PlanBuilder {
     // stream has released that buffer, then marks the unit gathered.
     void gather(int32_t u, int32_t pos, int32_t slot)
     {
-        if (released_recorded[slot]) add(ZERO_OP_WAIT, 1, -1, kEvReleased + slot);
-        add(ZERO_OP_GATHER, 1, u, slot);
-        add(ZERO_OP_RECORD, 1, -1, kEvGathered + pos % 2);
+        const int32_t ss = side_of(pos); // pos % 2 == slot: a buffer's gathers share a stream
+        if (released_recorded[slot]) add(ZERO_OP_WAIT, ss, -1, kEvReleased + slot);
+        add(ZERO_OP_GATHER, ss, u, slot);
+        add(ZERO_OP_RECORD, ss, -1, kEvGathered + pos % 2);
     }
 
     void pass(int32_t n_units, bool backward, bool regen, bool clip)
@@ -101,8 +111,8 @@ struct PlanBuilder {
     void forward_keep(int32_t n_units)
     {
         auto gather_own = [&](int32_t u, int32_t pos) {
-            add(ZERO_OP_GATHER, 1, u, kOwnRegion);
-            add(ZERO_OP_RECORD, 1, -1, kEvGathered + pos % 2);
+            add(ZERO_OP_GATHER, side_of(pos), u, kOwnRegion);
+            add(ZERO_OP_RECORD, side_of(pos), -1, kEvGathered + pos % 2);
         };
         gather_own(0, 0);
         for (int32_t pos = 0; pos < n_units; ++pos) {
@@ -123,9 +133,11 @@ struct PlanBuilder {
 
     void step(int32_t n_units, bool regen, bool clip, bool reshard = true)
     {
-        // the step's first gather must see everything the main stream did before
-        add(ZERO_OP_RECORD, 0, -1, kEvStart);
-        add(ZERO_OP_WAIT, 1, -1, kEvStart);
+        // the step's first gathers must see everything the main stream did before
+        two_side = two_side && n_units > 1;
+        add(ZERO_OP_RECORD, kMain, -1, kEvStart);
+        add(ZERO_OP_WAIT, kSide, -1, kEvStart);
+        if (two_side) add(ZERO_OP_WAIT, kSide2, -1, kEvStart);
         if (clip) {
             // the global norm before any unit's update: every unit's squared
             // norm on the main stream (overlapping the forward gathers), then
@@ -183,12 +195,13 @@ int copy_plan(const PlanBuilder& b, zero_op_t* ops, int32_t max_ops, int32_t* n_
     return ZERO_OK;
 }
 
-// Seven timing-free events and the second compute stream (non-blocking) per
-// host thread and device, created on first use.
+// Seven timing-free events and the second compute and side streams
+// (non-blocking) per host thread and device, created on first use.
 struct StepResources {
     int device = -1;
     cudaEvent_t ev[kEvents] = {};
     cudaStream_t aux = nullptr;
+    cudaStream_t side2 = nullptr;
 };
 thread_local StepResources t_res[kMaxDevices];
 
@@ -202,6 +215,8 @@ int resources_for_current_device(StepResources** out)
             if (!c.ev[i] && cudaEventCreateWithFlags(&c.ev[i], cudaEventDisableTiming) != cudaSuccess)
                 return ZERO_ECUDA;
         if (!c.aux && cudaStreamCreateWithFlags(&c.aux, cudaStreamNonBlocking) != cudaSuccess)
+            return ZERO_ECUDA;
+        if (!c.side2 && cudaStreamCreateWithFlags(&c.side2, cudaStreamNonBlocking) != cudaSuccess)
             return ZERO_ECUDA;
         c.device = dev;
     }
@@ -238,7 +253,7 @@ extern "C" int zero3_plan_microbatch(int32_t n_units, int32_t reshard_after_forw
     const AccumArgs acc{nullptr, micro_batch, micro_batches};
     PlanBuilder b;
     b.reduce_mode = reduce_mode(&acc);
-    b.two_compute = true;
+    b.two_compute = b.two_side = true;
     b.step(n_units, false, false, reshard_after_forward != 0);
     return copy_plan(b, ops, max_ops, n_ops);
 }
@@ -249,7 +264,7 @@ extern "C" int zero3_plan(int32_t n_units, int32_t regen, int32_t clip,
 {
     if (n_units < 1 || !ops || !n_ops || max_ops < 0) return ZERO_EINVAL;
     PlanBuilder b;
-    b.two_compute = true;
+    b.two_compute = b.two_side = true;
     b.step(n_units, regen != 0, clip != 0, reshard_after_forward != 0);
     return copy_plan(b, ops, max_ops, n_ops);
 }
@@ -304,10 +319,10 @@ int run_step(const zero_unit_t* units, int32_t n_units, int32_t n_ranks, const v
     if ((rc = cuda_status(cudaStreamIsCapturing(main_stream, &capture))) != ZERO_OK) return rc;
     PlanBuilder plan;
     plan.reduce_mode = reduce_mode(acc);
-    // While the main stream is being captured the backward pass keeps one
-    // compute stream, and the graph builder joins its units with programmatic
-    // edges instead.
-    plan.two_compute = capture == cudaStreamCaptureStatusNone;
+    // While the main stream is being captured the step keeps one compute and
+    // one side stream, and the graph builder joins consecutive units and
+    // gathers with programmatic edges instead.
+    plan.two_compute = plan.two_side = capture == cudaStreamCaptureStatusNone;
     plan.step(n_units, regen != nullptr, clip != nullptr, reshard);
 
     const uint16_t* unit_grads[ZERO_MAX_RANKS];
@@ -336,9 +351,11 @@ int run_step(const zero_unit_t* units, int32_t n_units, int32_t n_ranks, const v
     // events gained nothing.  While the stream is being captured, the graph
     // builder joins the units itself.
     // (tracked per stream: an update follows an update on its own stream)
-    bool after_update[3] = {false, false, false};
+    bool after_update[4] = {false, false, false, false};
     for (const zero_op_t& op : plan.ops) {
-        cudaStream_t s = op.stream == kMain ? main_stream : op.stream == kSide ? side_stream : res->aux;
+        cudaStream_t s = op.stream == kMain ? main_stream
+                         : op.stream == kSide ? side_stream
+                         : op.stream == kAux ? res->aux : res->side2;
         const bool chain_norm = after_norm;
         const bool chain_update =
             after_update[op.stream] && capture == cudaStreamCaptureStatusNone;

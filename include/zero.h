@@ -38,7 +38,7 @@
  *  - Arguments are checked on the host before anything is launched; a bad
  *    argument launches nothing.  ZERO_ECUDA reports a launch failure.
  *  - Stateless and re-entrant, with three documented exceptions: zero3_step
- *    keeps a per-thread cache of seven CUDA events and one CUDA stream,
+ *    keeps a per-thread cache of seven CUDA events and two CUDA streams,
  *    zero_clip_coef_units_noalloc
  *    works in a library-internal device array, and a zero3_graph_t holds the
  *    graph it captured.  1 <= n_ranks <= ZERO_MAX_RANKS.
@@ -444,7 +444,9 @@ int zero_clip_coef_units_noalloc(const zero_unit_t* units, int32_t n_units, int3
 /* One operation of a ZeRO-3 step plan.  stream: 0 = main (reduce-scatter,
  * regeneration, unit use), 1 = side (gathers), 2 = the library's second
  * compute stream (the backward units of full buffer 1 when resharding
- * without regeneration: their use, reduce-scatter and buffer release).
+ * without regeneration: their use, reduce-scatter and buffer release), 3 =
+ * the library's second side stream (the gathers into full buffer 1, or of
+ * the units of odd positions without resharding).
  * RECORD/WAIT name one of the plan's seven reusable events in `arg` (0 = step
  * start, 1..2 = "unit gathered", 3..4 = "full buffer released", 5 = "the
  * second compute stream may start", 6 = "the second compute stream is
@@ -483,7 +485,10 @@ typedef struct {
  * waits for stream 2's event 6 after it, so that consecutive units'
  * reduce-scatters overlap at their boundary instead of being separated by an
  * event wait and record on one stream (Llama-1.1B shapes on GB300: 7.94 ->
- * 7.77 ms a step).
+ * 7.77 ms a step).  With more than one unit the gathers into full buffer 1
+ * (without resharding: of the units at odd positions) run on stream 3, which
+ * also waits for event 0, so that consecutive gathers overlap as well (7.77
+ * -> 7.68 ms).
  *   regen      non-zero: a REGEN op precedes each REDUCE_SCATTER (and each
  *              NORM)
  *   reshard_after_forward  0: [DZF] "How FSDP implements ZeRO-3", step 6 --
@@ -494,7 +499,7 @@ typedef struct {
  *              CLIP_COEF on the main stream, and REDUCE_SCATTER ops carry
  *              arg = 1 (scale by the coefficient)
  *   ops        caller array of max_ops entries; *n_ops receives the count
- *              (13*n_units + 6, plus n_units with regen, plus n_units + 1
+ *              (13*n_units + 7, plus n_units with regen, plus n_units + 1
  *              with clip, plus n_units with both, at most)
  * ZERO_EINVAL on n_units < 1, null pointers or max_ops too small. */
 int zero3_plan(int32_t n_units, int32_t regen, int32_t clip, int32_t reshard_after_forward,
@@ -557,13 +562,13 @@ typedef struct {
  *                    pre-pass reads every unit's gradients once more; with
  *                    clip->grad_shard it also keeps their mean, which the
  *                    updates then read instead of the gradients)
- * The library keeps seven timing-free CUDA events and one non-blocking CUDA
- * stream (stream 2 of zero3_plan) per host thread and device, created on
+ * The library keeps seven timing-free CUDA events and two non-blocking CUDA
+ * streams (streams 2 and 3 of zero3_plan) per host thread and device, created on
  * first use and kept for the thread's life (a cudaDeviceReset invalidates
  * them, so zero3_step must not be called on that device from that thread
  * again); no device memory is allocated.  While main_stream is being
- * captured the backward pass keeps to the main stream (zero3_graph_create
- * joins its units with programmatic edges instead).  Work is queued
+ * captured the step keeps to main_stream and side_stream (zero3_graph_create
+ * joins consecutive units and gathers with programmatic edges instead).  Work is queued
  * asynchronously; on return main_stream carries the end of the step.  Kernels
  * that follow one another on the main stream with nothing else between them
  * are chained with programmatic dependent launch (each may start while the

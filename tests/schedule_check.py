@@ -4,8 +4,9 @@ A trace is a list of entries in host issue order:
   ("record", stream, event)   ("wait", stream, event)
   ("gather", stream, unit, buffer)   ("use", stream, unit, buffer, ...)
   ("rs", stream, unit)   ("regen", stream, unit)   ("end", stream)
-with stream "main", "side" or "aux" (the second compute stream of the
-native scheduler), and "end" marking where a step returns (on "main").  A
+with stream "main", "side", "aux" (the second compute stream of the native
+scheduler) or "side2" (its second side stream), and "end" marking where a
+step returns (on "main").  A
 wait orders the waiting stream's later operations after the operation that
 preceded the event's most recent record at the time of the wait (CUDA's
 semantics for a re-recorded event); a record right after waits also carries
@@ -13,6 +14,7 @@ them, as a CUDA event record carries everything before it on its stream."""
 from collections import defaultdict
 
 COMPUTE = ("main", "aux")
+SIDE = ("side", "side2")
 
 
 def happens_before_graph(trace):
@@ -76,7 +78,10 @@ def check_zero3_trace(trace, n_units, n_steps):
     ends = by_issue([n for n, e in pos.items() if e[0] == "end"])
     assert len(gathers) == 2 * U * n_steps and len(uses) == 2 * U * n_steps
     assert len(rss) == U * n_steps
-    assert all(n[0] == "side" for n in gathers) and all(n[0] in COMPUTE for n in uses + rss)
+    assert all(n[0] in SIDE for n in gathers) and all(n[0] in COMPUTE for n in uses + rss)
+    # each full buffer's gathers stay on one side stream
+    for b in {pos[n][3] for n in gathers}:
+        assert len({n[0] for n in gathers if pos[n][3] == b}) == 1
     # the forward pass runs on the main stream; a unit's backward use and
     # reduce-scatter share one compute stream
     fwd_uses = [u for k, u in enumerate(uses) if (k // U) % 2 == 0]
@@ -106,10 +111,14 @@ def check_zero3_trace(trace, n_units, n_steps):
                    and order_of[id(pos[g])] < order_of[id(pos[r])]]
             assert pre, "no prefetch of unit %d before unit %d's reduce-scatter" % (unit - 1, unit)
             assert not hb(edges, pre[-1], r)
-    # the next step's first gather sees every reduce-scatter of the step before
+    # the next step's first gather sees every reduce-scatter of the step before,
+    # and every gather of a unit sees that unit's update of the step before
     for s in range(1, n_steps):
         for r in rss[(s - 1) * U:s * U]:
             assert hb(edges, r, gathers[s * 2 * U]), "next step overtakes unit %d" % pos[r][2]
+            for g in gathers[s * 2 * U:(s + 1) * 2 * U]:
+                if pos[g][2] == pos[r][2]:
+                    assert hb(edges, r, g), "unit %d gathered before its update" % pos[r][2]
     # where the trace marks the step's return on the main stream, every
     # reduce-scatter of the step happens before it
     if ends:
@@ -135,7 +144,7 @@ def check_zero3_kept_trace(trace, n_units, n_steps):
     rss = by_issue([n for n, e in pos.items() if e[0] == "rs"])
     assert len(gathers) == U * n_steps and len(uses) == 2 * U * n_steps
     assert len(rss) == U * n_steps
-    assert all(n[0] == "side" for n in gathers) and all(n[0] == "main" for n in uses + rss)
+    assert all(n[0] in SIDE for n in gathers) and all(n[0] == "main" for n in uses + rss)
     assert [pos[n][2] for n in gathers] == list(range(U)) * n_steps
     assert [pos[n][2] for n in uses] == (list(range(U)) + list(range(U - 1, -1, -1))) * n_steps
     for s in range(n_steps):

@@ -101,7 +101,7 @@ def test_prefetch_order_and_buffer_safety(orc):
     check_zero3_trace(be.trace, len(units), 2)
 
 
-STREAMS = {0: "main", 1: "side", 2: "aux"}
+STREAMS = {0: "main", 1: "side", 2: "aux", 3: "side2"}
 
 
 def _native_trace(n_units, n_steps, regen=False, clip=False, reshard=True):
@@ -177,21 +177,36 @@ def test_checks_catch_a_missing_join_of_the_second_compute_stream():
     _assert_rs_after_coef(trace)
 
 
+def test_checks_catch_a_second_side_stream_that_does_not_wait_for_the_start():
+    """The second side stream's gathers read shards the previous step updated:
+    it waits for the step's start event like the first side stream, and
+    without that wait the checks see a gather overtake its unit's update."""
+    trace = _native_trace(5, 2)
+    assert any(e[:2] == ("wait", "side2") and e[2] == "ev0" for e in trace)
+    no_start = [e for e in trace if not (e[:2] == ("wait", "side2") and e[2] == "ev0")]
+    with pytest.raises(AssertionError):
+        check_zero3_trace(no_start, 5, 2)
+    kept = _native_trace(4, 2, reshard=False)
+    no_start = [e for e in kept if not (e[:2] == ("wait", "side2") and e[2] == "ev0")]
+    with pytest.raises(AssertionError):
+        check_zero3_kept_trace(no_start, 4, 2)
+
+
 def test_native_plan_counts_and_regen():
     from fsdp_sharded_optimizer_gb300 import _binding as B
     ops = B.zero3_plan(2, False)
     kinds = [o[0] for o in ops]
     assert kinds.count("gather") == 4 and kinds.count("reduce_scatter") == 2
-    assert "regen" not in kinds and "norm" not in kinds and len(ops) <= 13 * 2 + 6
+    assert "regen" not in kinds and "norm" not in kinds and len(ops) <= 13 * 2 + 7
     assert all(o[3] == 0 for o in ops if o[0] == "reduce_scatter")
     ops = B.zero3_plan(3, True, True)
-    assert len(ops) <= 13 * 3 + 6 + 3 + 3 + 1 + 3
+    assert len(ops) <= 13 * 3 + 7 + 3 + 3 + 1 + 3
     assert all(o[3] == 1 for o in ops if o[0] == "reduce_scatter")
     norms = [o for o in ops if o[0] == "norm"]
     assert [o[3] for o in norms] == [0, 1, 1]  # the first unit overwrites the partials
     ops = B.zero3_plan(4, True)
     kinds = [o[0] for o in ops]
-    assert kinds.count("regen") == 4 and len(ops) <= 14 * 4 + 6
+    assert kinds.count("regen") == 4 and len(ops) <= 14 * 4 + 7
     # every regeneration immediately precedes its unit's reduce-scatter on the main stream
     for i, o in enumerate(ops):
         if o[0] == "regen":
