@@ -107,6 +107,19 @@ def llama(name):
     return _jobs[name]
 
 
+def oracle_norm(orc, units, N, seed, step):
+    """The oracle's global gradient norm of one step over every unit (fp64
+    sum of the squared averaged gradient, unit by unit on host threads)."""
+    from concurrent.futures import ThreadPoolExecutor
+    import os
+
+    def unit_sumsq(u):
+        return orc.grad_sumsq(orc.gen_grads_unit(seed, step, H.SIGMA_G, 0, u, N))
+
+    with ThreadPoolExecutor(min(16, os.cpu_count() or 1)) as ex:
+        return float(np.sqrt(sum(ex.map(unit_sumsq, units))))
+
+
 @pytest.mark.parametrize("name,variant", [(n, v) for n in LLAMA for v in VARIANTS])
 def test_llama_full_size_timed_path_sampled(orc, name, variant):
     """Llama shapes, N_d = 8, 10 steps.  At 7B the job holds 203 GB: every
@@ -118,5 +131,12 @@ def test_llama_full_size_timed_path_sampled(orc, name, variant):
     clipped = job.run(variant, T)
     if clipped is not None:
         check_clip(clipped, seen)
+        if name == "llama-1.1b" and variant == "native-clip":
+            # the whole model's norm of step 1 against the oracle's fp64 sum
+            # (1.1 G parameters x 8 ranks; the bound of test_gpu_clip.py); the
+            # norm depends on the step's gradients only, not on the state
+            ounits, _ = orc.layout(LLAMA[name], 8)
+            want = oracle_norm(orc, ounits, 8, 0, 1)
+            assert abs(clipped[0][0] - want) <= 1e-6 * want, (clipped[0][0], want)
     ref_T, ref_before = references(orc, 8, 0, 0, idx, variant, clipped, cache, T)
     compare(job, variant, idx, ref_T, ref_before)
