@@ -60,3 +60,28 @@ def test_zero3_line_reports_the_step_its_graph_and_the_fused_kernel():
     assert d["graph"]["ms_per_step"] > 0 and d["gather"]["gbs"] > 0
     # the fused kernel alone moves fewer bytes than the step and takes less time
     assert r["kernel_ms_per_step"] < d["ms_per_step"]
+
+
+def test_zero3_summary_object_of_the_default_line():
+    """The default line's ZeRO-3 summaries (here the Llama-1.1B one, short):
+    the step, its graph form, the fused kernel alone against the roofline
+    with its traffic, the gathers alone and the clocks."""
+    import torch
+
+    import bench
+    import fsdp_sharded_optimizer_gb300 as Z
+
+    dev = torch.device("cuda", 0)
+    s = bench.zero3_summary(torch, Z, 1, dev, "llama-1.1b-zero3-n8", K=3, W=3)
+    for key in ("workload", "ms_per_step", "value", "hbm_bytes_per_step", "hbm_gbs", "graph",
+                "fused_kernel_alone", "gathers_alone", "clocks", "gpu_launches"):
+        assert key in s, key
+    assert s["units"] == 23 and s["steps"] == 3 and s["warmup"] == 3
+    P, Pp = 1_100_048_384, 1_100_048_384
+    assert s["hbm_bytes_per_step"] == (26 + 2 * 8 + 8) * Pp
+    assert abs(s["value"] - P / (s["ms_per_step"] * 1e-3)) <= 1e-6 * s["value"]
+    f = s["fused_kernel_alone"]
+    assert f["bytes_per_step"] == 42 * Pp and f["launches_per_step"] == 99
+    assert abs(f["frac"] - f["achieved_gbs"] / f["peak"]) < 1e-9 and 0.3 < f["frac"] < 1.3
+    assert f["ms_per_step"] < s["ms_per_step"] and s["graph"]["ms_per_step"] > 0
+    assert s["gpu_launches"] == 3 * (2 * 23 + 99)
