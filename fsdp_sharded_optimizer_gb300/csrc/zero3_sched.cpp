@@ -73,8 +73,8 @@ struct PlanBuilder {
         ops.push_back(zero_op_t{kind, stream, unit, arg});
     }
 
-    // The side stream fills full buffer `slot` with unit `u` once the main
-    // stream has released that buffer, then marks the unit gathered.
+    // The buffer's side stream fills full buffer `slot` with unit `u` once the
+    // compute stream using it has released it, then marks the unit gathered.
     void gather(int32_t u, int32_t pos, int32_t slot)
     {
         const int32_t ss = side_of(pos); // pos % 2 == slot: a buffer's gathers share a stream
