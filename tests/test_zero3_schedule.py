@@ -192,6 +192,32 @@ def test_checks_catch_a_second_side_stream_that_does_not_wait_for_the_start():
         check_zero3_kept_trace(no_start, 4, 2)
 
 
+def test_plan_length_stays_within_the_header_bound():
+    """include/zero.h sizes the caller's op array: 13 n + 7 operations, plus n
+    with regeneration, n + 1 with clipping and n more with both; a micro-batch
+    plan stays within 13 n + 7.  An array one entry short is rejected."""
+    import ctypes as C
+
+    from fsdp_sharded_optimizer_gb300 import _binding as B
+    for n in list(range(1, 41)) + [64, 257]:
+        for regen in (0, 1):
+            for clip in (0, 1):
+                for reshard in (0, 1):
+                    L = len(B.zero3_plan(n, regen, clip, reshard))
+                    bound = 13 * n + 7 + regen * n + clip * (n + 1) + regen * clip * n
+                    assert L <= bound, (n, regen, clip, reshard, L, bound)
+                    ops = (B.zero_op_t * L)()
+                    got = C.c_int32()
+                    assert B.lib.zero3_plan(n, regen, clip, reshard, ops, L, C.byref(got)) == 0
+                    assert got.value == L
+                    assert B.lib.zero3_plan(n, regen, clip, reshard, ops, L - 1,
+                                            C.byref(got)) == B.ZERO_EINVAL
+        for m in (1, 2, 4):
+            for mb in range(m):
+                for reshard in (True, False):
+                    assert len(B.zero3_plan_microbatch(n, mb, m, reshard)) <= 13 * n + 7
+
+
 def test_native_plan_counts_and_regen():
     from fsdp_sharded_optimizer_gb300 import _binding as B
     ops = B.zero3_plan(2, False)
