@@ -88,6 +88,8 @@ def lib():
             "or_sample": (None, [i32, u64, f64, f64, i32, P, i32, P, i64, P, P, P, P]),
             "or_sample_coef": (None, [i32, u64, f64, f64, i32, P, i32, P, P, i64, P, P, P, P]),
             "or_sample_accum": (None, [i32, u64, f64, f64, i32, P, i32, i32, P, i64, P, P, P, P]),
+            "or_sample_fixed_grads": (None, [i32, u64, f64, f64, i32, P, i32, i64, P, i64, P, P, P,
+                                             P]),
             "or_grad_sumsq": (f64, [i32, i64, P]),
             "or_grad_nonfinite": (None, [i32, i64, P, P]),
             "or_reduce_mean_f32": (f32, [P, i32, i64, f32]),
@@ -394,6 +396,19 @@ def sample_accum(n_ranks, seed, sigma_w, sigma_g, outliers, hp0, n_steps, micro_
            np.zeros(n, np.float32))
     lib().or_sample_accum(n_ranks, seed, sigma_w, sigma_g, outliers, C.byref(hp0), n_steps,
                           int(micro_batches), _ptr(idx), n, *[_ptr(a) for a in out])
+    return out
+
+
+def sample_fixed_grads(n_ranks, seed, sigma_w, sigma_g, outliers, hp0, n_steps, grad_step,
+                       param_index):
+    """sample() with the rank gradients of generator step `grad_step` in every
+    step (AdamW's step counter still advances from hp0.step)."""
+    idx = np.ascontiguousarray(np.asarray(param_index, dtype=np.int64))
+    n = idx.size
+    out = (np.zeros(n, np.uint16), np.zeros(n, np.float32), np.zeros(n, np.float32),
+           np.zeros(n, np.float32))
+    lib().or_sample_fixed_grads(n_ranks, seed, sigma_w, sigma_g, outliers, C.byref(hp0), n_steps,
+                                int(grad_step), _ptr(idx), n, *[_ptr(a) for a in out])
     return out
 
 

@@ -835,16 +835,16 @@ int or_sim_zero(int32_t stage, int32_t n_ranks, const int64_t* unit_sizes,
  * ==================================================================== */
 static void sample_steps(int32_t n_ranks, uint64_t seed, double sigma_w, double sigma_g,
                          int32_t outliers, const or_hparams_t* hp0, int32_t n_steps,
-                         const float* coef, int32_t micro_batches, const int64_t* param_index,
-                         int64_t n_index, uint16_t* out_params, float* out_master, float* out_m,
-                         float* out_v);
+                         const float* coef, int32_t micro_batches, int64_t grad_step,
+                         const int64_t* param_index, int64_t n_index, uint16_t* out_params,
+                         float* out_master, float* out_m, float* out_v);
 
 void or_sample(int32_t n_ranks, uint64_t seed, double sigma_w, double sigma_g,
                int32_t outliers, const or_hparams_t* hp0, int32_t n_steps,
                const int64_t* param_index, int64_t n_index, uint16_t* out_params,
                float* out_master, float* out_m, float* out_v)
 {
-    sample_steps(n_ranks, seed, sigma_w, sigma_g, outliers, hp0, n_steps, NULL, 0, param_index,
+    sample_steps(n_ranks, seed, sigma_w, sigma_g, outliers, hp0, n_steps, NULL, 0, 0, param_index,
                  n_index, out_params, out_master, out_m, out_v);
 }
 
@@ -857,7 +857,7 @@ void or_sample_coef(int32_t n_ranks, uint64_t seed, double sigma_w, double sigma
                     const float* coef, const int64_t* param_index, int64_t n_index,
                     uint16_t* out_params, float* out_master, float* out_m, float* out_v)
 {
-    sample_steps(n_ranks, seed, sigma_w, sigma_g, outliers, hp0, n_steps, coef, 0, param_index,
+    sample_steps(n_ranks, seed, sigma_w, sigma_g, outliers, hp0, n_steps, coef, 0, 0, param_index,
                  n_index, out_params, out_master, out_m, out_v);
 }
 
@@ -873,15 +873,29 @@ void or_sample_accum(int32_t n_ranks, uint64_t seed, double sigma_w, double sigm
                      uint16_t* out_params, float* out_master, float* out_m, float* out_v)
 {
     sample_steps(n_ranks, seed, sigma_w, sigma_g, outliers, hp0, n_steps, NULL,
-                 micro_batches < 1 ? 1 : micro_batches, param_index, n_index, out_params,
+                 micro_batches < 1 ? 1 : micro_batches, 0, param_index, n_index, out_params,
                  out_master, out_m, out_v);
+}
+
+/* or_sample with the same rank gradients in every step: those the generator
+ * gives for step grad_step (>= 1), while AdamW's step counter still advances
+ * from hp0->step.  This is a choice of inputs only: a job that keeps one
+ * gradient set resident and applies it again at every step. */
+void or_sample_fixed_grads(int32_t n_ranks, uint64_t seed, double sigma_w, double sigma_g,
+                           int32_t outliers, const or_hparams_t* hp0, int32_t n_steps,
+                           int64_t grad_step, const int64_t* param_index, int64_t n_index,
+                           uint16_t* out_params, float* out_master, float* out_m, float* out_v)
+{
+    sample_steps(n_ranks, seed, sigma_w, sigma_g, outliers, hp0, n_steps, NULL, 0,
+                 grad_step < 1 ? 1 : grad_step, param_index, n_index, out_params, out_master,
+                 out_m, out_v);
 }
 
 static void sample_steps(int32_t n_ranks, uint64_t seed, double sigma_w, double sigma_g,
                          int32_t outliers, const or_hparams_t* hp0, int32_t n_steps,
-                         const float* coef, int32_t micro_batches, const int64_t* param_index,
-                         int64_t n_index, uint16_t* out_params, float* out_master, float* out_m,
-                         float* out_v)
+                         const float* coef, int32_t micro_batches, int64_t grad_step,
+                         const int64_t* param_index, int64_t n_index, uint16_t* out_params,
+                         float* out_master, float* out_m, float* out_v)
 {
     float inv_m = micro_batches > 0 ? (float)(1.0 / (double)micro_batches) : 1.0f;
     uint64_t wkey = or_gen_key(seed, 0, 0, 0);
@@ -894,7 +908,8 @@ static void sample_steps(int32_t n_ranks, uint64_t seed, double sigma_w, double 
         hp.step = hp0->step + t;
         or_scalars(&hp, n_ranks, &sc[t]);
         for (int32_t r = 0; r < n_ranks; ++r)
-            keys[(size_t)t * n_ranks + r] = or_gen_key(seed, 1, (uint64_t)hp.step, (uint64_t)r);
+            keys[(size_t)t * n_ranks + r] =
+                or_gen_key(seed, 1, (uint64_t)(grad_step > 0 ? grad_step : hp.step), (uint64_t)r);
     }
     uint16_t* g1 = xcalloc((size_t)n_ranks, sizeof *g1);
     const uint16_t** gp = xcalloc((size_t)n_ranks, sizeof *gp);

@@ -198,6 +198,13 @@ void or_sample_accum(int32_t n_ranks, uint64_t seed, double sigma_w, double sigm
                      int32_t outliers, const or_hparams_t* hp0, int32_t n_steps,
                      int32_t micro_batches, const int64_t* param_index, int64_t n_index,
                      uint16_t* out_params, float* out_master, float* out_m, float* out_v);
+/* The same as or_sample with one gradient set for every step: the generated
+ * rank gradients of step grad_step (>= 1), applied at AdamW steps hp0->step,
+ * hp0->step + 1, ... (a job that keeps its gradients resident). */
+void or_sample_fixed_grads(int32_t n_ranks, uint64_t seed, double sigma_w, double sigma_g,
+                           int32_t outliers, const or_hparams_t* hp0, int32_t n_steps,
+                           int64_t grad_step, const int64_t* param_index, int64_t n_index,
+                           uint16_t* out_params, float* out_master, float* out_m, float* out_v);
 
 #ifdef __cplusplus
 }

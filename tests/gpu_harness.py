@@ -143,11 +143,13 @@ def padding_is_zero_unit(g, u):
     return True
 
 
-def oracle_sample(orc, N, seed, T, idx, outliers=0, threads=None, coefs=None, micro=0):
+def oracle_sample(orc, N, seed, T, idx, outliers=0, threads=None, coefs=None, micro=0,
+                  grad_step=0):
     """orc.sample (the oracle's element-by-element run of T steps from step 1;
     with coefs, orc.sample_coef: step t's mean gradient times coefs[t]; with
     micro > 0, orc.sample_accum: accumulation over micro identical
-    micro-batches) over
+    micro-batches; with grad_step > 0, orc.sample_fixed_grads: the gradients
+    of generator step grad_step at every step) over
     the true parameter indices idx, split across host threads.  Each call is
     independent and allocates its own buffers, and ctypes releases the GIL
     around it, so the pieces run concurrently; the values are those of one call."""
@@ -164,6 +166,9 @@ def oracle_sample(orc, N, seed, T, idx, outliers=0, threads=None, coefs=None, mi
         piece = idx[cuts[i]:cuts[i + 1]]
         if micro:
             return orc.sample_accum(N, seed, SIGMA_W, SIGMA_G, outliers, hp0, T, micro, piece)
+        if grad_step:
+            return orc.sample_fixed_grads(N, seed, SIGMA_W, SIGMA_G, outliers, hp0, T, grad_step,
+                                          piece)
         if coefs is None:
             return orc.sample(N, seed, SIGMA_W, SIGMA_G, outliers, hp0, T, piece)
         return orc.sample_coef(N, seed, SIGMA_W, SIGMA_G, outliers, hp0, T, coefs[:T], piece)

@@ -284,6 +284,51 @@ def test_gpt2_shaped_zero2_full_size_sampled(orc):
     H.free()
 
 
+@pytest.mark.parametrize("workload,stage,bucket", [
+    ("gpt2-small-flat-n8", 1, 0),               # the headline step
+    ("gpt2-small-flat-n8", 2, BUCKET_25MIB),    # its ZeRO-2 leg
+    ("flat-2p20-n2", 1, 0),                     # the N_d = 2, P = 2^20 case
+])
+def test_bench_job_matches_oracle(orc, workload, stage, bucket):
+    """The job bench.py times, as it times it: bench.Zero12State's buffers and
+    inputs (one generated gradient set, applied again at every step) through
+    its step call, 10 steps, against the oracle's run with the same gradients
+    at every step: every parameter up to 2^20, else a million sampled ones
+    plus every shard and chunk boundary, bit for bit; padding stays +0."""
+    import bench
+
+    assert bench.HP == H.HP and (bench.SIGMA_W, bench.SIGMA_G) == (H.SIGMA_W, H.SIGMA_G)
+    sizes, N = bench.workload(workload)[:2]
+    st = bench.Zero12State(B, torch, sizes, N, torch.device("cuda", 0))
+    T, P, S = 10, st.P, st.S
+    for _ in range(T):
+        st.step(stage, bucket)
+    torch.cuda.synchronize()
+    # padding [P, P') is +0 in the weights and in every rank's state
+    assert not bool(st.params[P:].view(torch.int16).any())
+    for a in (st.master, st.m, st.v):
+        for k in range(N):
+            lo = max(P - k * S, 0)
+            if lo < S:
+                assert not bool(a[k, lo:].view(torch.int32).any())
+    if P <= 2**20:
+        idx = np.arange(P, dtype=np.int64)
+    else:
+        edges = [k * S for k in range(N + 1)] + list(range(BUCKET_25MIB, st.unit.n_padded,
+                                                           BUCKET_25MIB))
+        bounds = [e + d for e in edges for d in (-1, 0, 1)] + [P - 1]
+        idx = sample_indices(P, bounds, 1_000_000, seed=stage)
+    ti = torch.from_numpy(idx).cuda()
+    gp = st.params[ti].cpu().numpy().view(np.uint16)
+    gw, gm, gv = (a[ti // S, ti % S].cpu().numpy() for a in (st.master, st.m, st.v))
+    rp, rw, rm, rv = H.oracle_sample(orc, N, 0, T, idx, grad_step=1)
+    H.assert_within_tolerance((gw, gm, gv), (rw, rm, rv), gp, rp)
+    for name, g, r in (("params", gp, rp), ("master", gw, rw), ("m", gm, rm), ("v", gv, rv)):
+        H.assert_bitwise(g, r, name)
+    del st, ti
+    H.free()
+
+
 # ---------------------------------------------------------------- sweep
 SWEEP_P = [2**16 + 37, 2**20 + 5, 2**24, 2**27 + 3, 2**30]
 SWEEP_N = [2, 4, 8, 16, 64]

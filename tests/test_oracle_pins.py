@@ -477,6 +477,36 @@ def test_sampled_accumulated_run_matches_the_accumulation_steps(orc, micro):
         np.testing.assert_array_equal(got.view(np.uint32), ref[k, j].view(np.uint32))
 
 
+@pytest.mark.parametrize("grad_step", [1, 3])
+def test_sampled_fixed_gradient_run_matches_resident_gradient_steps(orc, grad_step):
+    """The sampled run that applies one gradient set at every step (a job whose
+    gradients stay resident) equals, at every index, T whole-buffer ZeRO-1
+    steps fed the same generated gradients each time while AdamW's step
+    counter advances; with grad_step = 1 and one step it is the plain sampled
+    run, and the gradients are those of grad_step, not of the AdamW step."""
+    N, P, T, seed = 4, 3000, 5, 19
+    (u,), _ = orc.layout([P], N, 64)
+    master = orc.gen_master(seed, 0.02, [u], N)
+    m, v = np.zeros_like(master), np.zeros_like(master)
+    params = np.zeros(u.n_padded, np.uint16)
+    g = orc.gen_grads_unit(seed, grad_step, 1e-3, 1, u, N)
+    for t in range(1, T + 1):
+        orc.zero12_step(1, g, master, m, v, params, orc.hparams(**HP, step=t), 0)
+    idx = np.arange(P, dtype=np.int64)
+    hp0 = orc.hparams(**HP, step=1)
+    sp, sw, sm, sv = orc.sample_fixed_grads(N, seed, 0.02, 1e-3, 1, hp0, T, grad_step, idx)
+    k, j = idx // u.shard_len, idx % u.shard_len
+    np.testing.assert_array_equal(sp, params[idx])
+    for got, ref in ((sw, master), (sm, m), (sv, v)):
+        np.testing.assert_array_equal(got.view(np.uint32), ref[k, j].view(np.uint32))
+    one = orc.sample_fixed_grads(N, seed, 0.02, 1e-3, 1, hp0, 1, 1, idx)
+    plain = orc.sample(N, seed, 0.02, 1e-3, 1, hp0, 1, idx)
+    for a, b in zip(one, plain):
+        np.testing.assert_array_equal(a, b)
+    other = orc.sample_fixed_grads(N, seed, 0.02, 1e-3, 1, hp0, T, grad_step + 1, idx)
+    assert not np.array_equal(other[1], sw)
+
+
 def test_threaded_sampling_equals_the_full_run(orc):
     """The GPU tests split a large sample across host threads
     (gpu_harness.oracle_sample); the pieces, put back together, are the full
