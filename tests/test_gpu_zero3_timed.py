@@ -39,7 +39,7 @@ import numpy as np
 import pytest
 
 import gpu_harness as H
-from zero3_job import CH, VARIANTS, Job, boundaries, check_clip, compare, references
+from zero3_job import CH, VARIANTS, Job, boundaries, check_clip, compare, owner, references
 
 pytestmark = pytest.mark.gpu
 
@@ -140,3 +140,52 @@ def test_llama_full_size_timed_path_sampled(orc, name, variant):
             assert abs(clipped[0][0] - want) <= 1e-6 * want, (clipped[0][0], want)
     ref_T, ref_before = references(orc, 8, 0, 0, idx, variant, clipped, cache, T)
     compare(job, variant, idx, ref_T, ref_before)
+
+
+@pytest.mark.parametrize("name", list(LLAMA))
+def test_bench_zero3_job_matches_oracle(orc, name):
+    """The ZeRO-3 job bench.py times, through its own class (bench.Zero3Bench:
+    its buffers, its inputs -- one gradient set generated once and applied at
+    every step -- and its calls): 4 native steps (zero3_step), 3 replays of the
+    step captured as a CUDA graph, and 3 passes of the fused reduce-scatter +
+    AdamW launches alone, which update every unit as a step does.  After those
+    10 steps, a million sampled parameters plus every unit, shard and chunk
+    boundary equal the oracle's run with the same gradients at every step, bit
+    for bit."""
+    import torch
+
+    import bench
+    from fsdp_sharded_optimizer_gb300 import _binding as B
+
+    assert bench.HP == H.HP and (bench.SIGMA_W, bench.SIGMA_G) == (H.SIGMA_W, H.SIGMA_G)
+    _jobs.clear()
+    H.free()
+    sizes = LLAMA[name]
+    zb = bench.Zero3Bench(torch, B, sizes, 8, torch.device("cuda", 0))
+    for _ in range(4):
+        zb.native_step()
+    g = zb.graph()
+    try:
+        for _ in range(3):
+            zb.graph_step(g)
+        torch.cuda.synchronize()
+    finally:
+        g.close()
+    for _ in range(3):
+        zb.rs_only()
+    torch.cuda.synchronize()
+    assert zb.t == T
+    P = sum(sizes)
+    rng = np.random.default_rng(2)
+    idx = np.unique(np.concatenate([rng.integers(0, P, size=1_000_000),
+                                    boundaries(zb.units, 8, P)]))
+    k, pos = owner(zb.units, idx)
+    tk, tp = torch.from_numpy(k).cuda(), torch.from_numpy(pos).cuda()
+    gp = zb.shards[tk, tp].cpu().numpy().view(np.uint16)
+    gw, gm, gv = (a[tk, tp].cpu().numpy() for a in (zb.master, zb.m, zb.v))
+    rp, rw, rm, rv = H.oracle_sample(orc, 8, 0, T, idx, grad_step=1)
+    H.assert_within_tolerance((gw, gm, gv), (rw, rm, rv), gp, rp)
+    for what, got, ref in (("params", gp, rp), ("master", gw, rw), ("m", gm, rm), ("v", gv, rv)):
+        H.assert_bitwise(got, ref, what)
+    del zb, tk, tp
+    H.free()

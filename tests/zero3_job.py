@@ -133,13 +133,7 @@ class Job:
     # ---------------------------------------------------------------- reading
     def owner(self, idx):
         """True parameter indices -> (owner rank, position in its shard storage)."""
-        starts = np.array([u.param_offset for u in self.units], np.int64)
-        ui = np.searchsorted(starts, idx, side="right") - 1
-        local = idx - starts[ui]
-        S = np.array([u.shard_len for u in self.units], np.int64)[ui]
-        k = local // S
-        pos = np.array([u.shard_offset for u in self.units], np.int64)[ui] + local - k * S
-        return k, pos
+        return owner(self.units, idx)
 
     def state_at(self, idx):
         k, pos = self.owner(idx)
@@ -172,6 +166,18 @@ class Job:
             buf = bufs[(n - 1 - i) % 2]
             bits[here] = at_rows(buf, np.zeros(int(here.sum()), np.int64), local[sel][here])
         return mask, bits
+
+
+def owner(units, idx):
+    """True parameter indices -> (owner rank, position in the rank's shard
+    storage of every unit)."""
+    starts = np.array([u.param_offset for u in units], np.int64)
+    ui = np.searchsorted(starts, idx, side="right") - 1
+    local = idx - starts[ui]
+    S = np.array([u.shard_len for u in units], np.int64)[ui]
+    k = local // S
+    pos = np.array([u.shard_offset for u in units], np.int64)[ui] + local - k * S
+    return k, pos
 
 
 def at_rows(g, rows, cols):
