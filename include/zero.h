@@ -236,7 +236,8 @@ int zero3_reduce_scatter_unit_f32grads(const zero_unit_t* unit, int32_t n_ranks,
 int zero2_accumulate(int32_t n_ranks, int64_t n_padded, const uint16_t* const* grads,
                      float* const* grad_acc, int32_t first, cudaStream_t stream);
 
-/* zero2_step_accumulated -- the last micro-batch fused with the step: the
+/* zero2_step_accumulated -- the last micro-batch fused with the step ([DZF]
+ * "Gradient accumulation": one optimizer step per m micro-batches): the
  * fused kernel of zero_step_stage12 with g = (grad_acc + mean) * (1/m).
  * micro_batches = m >= 1; with m = 1 it is zero_step_stage12 (stage 2) and
  * grad_acc is not read.  Other arguments as zero_step_stage12. */
@@ -312,7 +313,8 @@ int64_t zero_clip_scratch_bytes(void);
 
 /* zero_grad_sqnorm -- adds the squared L2 norm of the averaged gradient of
  * one buffer (g[i] = fp32 rank-order mean of grads[r][i], exactly as the
- * fused step forms it) into per-block fp64 partials in scratch.
+ * fused step forms it) into per-block fp64 partials in scratch: the squared
+ * shard norms whose sum is the global norm ([DZF] "7. Common mistakes").
  *   n_elems      length of each rank's buffer (multiple of 8)
  *   grads        n_ranks device pointers (read only)
  *   accumulate   0: overwrite the partials (first buffer of the step);
@@ -326,7 +328,9 @@ int zero_grad_sqnorm(int32_t n_ranks, int64_t n_elems, const uint16_t* const* gr
                      cudaStream_t stream);
 
 /* zero_clip_coef -- sums the partials (fp64, fixed order) and writes
- * norm_coef[0] = (float)norm and norm_coef[1] = (float)coef on the device.
+ * norm_coef[0] = (float)norm and norm_coef[1] = (float)coef on the device,
+ * coef = min(1, max_norm / (norm + 1e-6)): the rule of the clip_grad_norm_
+ * call in [DDF]'s "A complete rank-aware DDP reference".
  *   max_norm   > 0, finite
  *   norm_coef  device float[2], 16-byte aligned */
 int zero_clip_coef(const double* scratch, int64_t scratch_bytes, double max_norm,
@@ -334,7 +338,8 @@ int zero_clip_coef(const double* scratch, int64_t scratch_bytes, double max_norm
 
 /* zero_step_stage12_clip / zero3_reduce_scatter_unit_clip -- the two fused
  * steps with the mean gradient multiplied (one fp32 multiply) by
- * norm_coef[1] before AdamW.  norm_coef: device float[2] written by
+ * norm_coef[1] before AdamW (clipping before the optimizer step, as in
+ * [DDF]'s "A complete rank-aware DDP reference").  norm_coef: device float[2] written by
  * zero_clip_coef earlier on the same stream.  Other arguments as the
  * unclipped calls. */
 int zero_step_stage12_clip(int32_t stage, int32_t n_ranks, int64_t n_padded,
@@ -350,8 +355,9 @@ int zero3_reduce_scatter_unit_clip(const zero_unit_t* unit, int32_t n_ranks,
 
 /* zero3_update_unit_reduced -- zero3_reduce_scatter_unit (or, with norm_coef,
  * its clipped form) reading the unit's mean gradient from the fp32 gradient
- * shard that zero_grad_reduce_sqnorm wrote, instead of reducing the rank
- * gradients: the same bits.
+ * shard that zero_grad_reduce_sqnorm wrote ([DZF] "How FSDP implements
+ * ZeRO-3", step 1: each rank keeps the fp32 shard of its gradient), instead of
+ * reducing the rank gradients: the same bits.
  *   grad_shard   n_ranks device pointers to each rank's fp32 gradient shard
  *                storage of all units (laid out like master: this unit at
  *                unit->shard_offset), read only
@@ -541,8 +547,9 @@ typedef struct {
     float* const* grad_shard; /* host table of n_ranks device pointers, or NULL */
 } zero_clip_t;
 
-/* zero3_step -- one whole ZeRO-3 step: executes zero3_plan's operations with
- * zero3_gather_unit, zero3_reduce_scatter_unit and (if regen != NULL)
+/* zero3_step -- one whole ZeRO-3 step ([DZF] "How FSDP implements ZeRO-3",
+ * steps 2-5, and step 6 without resharding): executes zero3_plan's operations
+ * with zero3_gather_unit, zero3_reduce_scatter_unit and (if regen != NULL)
  * zero_gen_grads_unit, on main_stream and side_stream, which must differ.
  *   units[n_units]   layouts from one zero_layout call (host array)
  *   grads            n_ranks device pointers.  grads_resident != 0: rank r's
@@ -599,7 +606,9 @@ int zero3_step_f32grads(const zero_unit_t* units, int32_t n_units, int32_t n_ran
                         cudaStream_t side_stream);
 
 /* zero3_step_microbatch -- one micro-batch of a ZeRO-3 step with gradient
- * accumulation: zero3_plan_microbatch's operations, issued like zero3_step's
+ * accumulation ([DZF] "Gradient accumulation", the 3mP row: both gathers and
+ * the reduce-scatter in every micro-batch): zero3_plan_microbatch's
+ * operations, issued like zero3_step's
  * (every unit's bf16 gradients of this micro-batch resident; no regeneration,
  * no clipping).  Call it for micro_batch = 0 .. m-1 in order, refilling the
  * gradients between calls; the update happens in the last call, with
@@ -689,7 +698,8 @@ int zero_grad_nonfinite(int32_t n_ranks, int64_t n_elems, const uint16_t* const*
  * buffers without a host round trip.
  * ------------------------------------------------------------------- */
 
-/* zero_gen_grads_unit -- rank r's bf16 gradient of one unit at step t.
+/* zero_gen_grads_unit -- rank r's bf16 gradient of one unit at step t (a
+ * harness input; no page defines it: SplitMix64, Steele, Lea and Flood 2014).
  * Element j < unit->n_params holds bf16_rne(z), z drawn by a SplitMix64
  * counter stream keyed by (seed, stream 1, step, r) at the true parameter
  * index unit->param_offset + j (an approximately normal value of standard
@@ -701,14 +711,16 @@ int zero_gen_grads_unit(uint64_t seed, int64_t step, double sigma, int32_t outli
                         uint16_t* const* unit_grads, cudaStream_t stream);
 
 /* zero_gen_grads_unit_f32 -- the same draws as zero_gen_grads_unit kept in
- * fp32 (no bf16 rounding): inputs of the fp32-gradient calls.
+ * fp32 (no bf16 rounding): inputs of the fp32-gradient calls (harness; the
+ * fp32 gradients of [DZF] "6. Where it shows up").
  *   unit_grads  n_ranks device pointers, each unit->n_padded fp32 (written) */
 int zero_gen_grads_unit_f32(uint64_t seed, int64_t step, double sigma, int32_t outliers,
                             const zero_unit_t* unit, int32_t n_ranks, float* const* unit_grads,
                             cudaStream_t stream);
 
-/* zero_gen_master -- initial fp32 master weights of every unit, written into
- * each owner's shard storage: true parameter p draws from (seed, stream 0,
+/* zero_gen_master -- initial fp32 master weights of every unit (harness: the
+ * fp32 master copy of [DDF] "Memory accounting", filled with synthetic
+ * values), written into each owner's shard storage: true parameter p draws from (seed, stream 0,
  * step 0, rank 0) at index p with standard deviation sigma; padding is +0.
  *   units[n_units]  layout from zero_layout (host array)
  *   master          n_ranks device pointers to fp32 shard storage */
@@ -717,16 +729,20 @@ int zero_gen_master(uint64_t seed, double sigma, const zero_unit_t* units,
                     cudaStream_t stream);
 
 /* zero_cast_bf16 -- dst[i] = bf16_rne(src[i]) for i < n (n a multiple of 8):
- * the initial bf16 replica or shard of fp32 master weights. */
+ * the initial bf16 replica or shard of fp32 master weights (the bf16
+ * parameters beside the fp32 master of [DDF] "Memory accounting"). */
 int zero_cast_bf16(const float* src, uint16_t* dst, int64_t n, cudaStream_t stream);
 
 /* zero_stream_wait -- host wait for all work on a stream, polling with a
- * wall-clock limit instead of blocking forever.  ZERO_ETIMEOUT if the work
+ * wall-clock limit instead of blocking forever, so that a stuck step is seen
+ * and rank progress can be compared ([DDF] "Failure investigation and
+ * recovery", a collective hang).  ZERO_ETIMEOUT if the work
  * has not finished after timeout_ms milliseconds (the work is left running),
  * ZERO_ECUDA if the stream reports an error. */
 int zero_stream_wait(cudaStream_t stream, int64_t timeout_ms);
 
-/* zero_strerror -- a static string naming a return code. */
+/* zero_strerror -- a static string naming a return code (no page defines
+ * it). */
 const char* zero_strerror(int code);
 
 #ifdef __cplusplus
