@@ -75,3 +75,28 @@ def test_reference_arm_prints_the_contract_line():
     assert d["impl"] == "reference" and d["steps"] == 2 and d["value"] > 0
     assert d["e2e"]["value"] == d["value"] and d["e2e"]["h2d_bytes_per_step"] == 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
+
+
+def test_reference_arm_under_torchrun_prints_once():
+    """Launched as the driver launches it for N > 1 (torchrun, two ranks on
+    127.0.0.1), the reference arm runs on rank 0 alone: one JSON line, the
+    other rank exits 0 without work."""
+    import json
+    import socket
+    import subprocess
+    import sys
+
+    from conftest import ROOT
+    with socket.socket() as sock:
+        sock.bind(("127.0.0.1", 0))
+        port = sock.getsockname()[1]
+    r = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+                        "--nproc-per-node", "2", "--master-addr", "127.0.0.1", "--master-port",
+                        str(port), "bench.py", "--impl", "reference", "--gpus", "2", "--steps",
+                        "1", "--warmup", "1"], cwd=ROOT, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip().startswith("{")]
+    assert len(lines) == 1, r.stdout[-2000:]
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
