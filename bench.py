@@ -386,6 +386,21 @@ def run_gpu(args):
         ms2, _ = timed(torch, world, dev, stream, lambda: st.step(2, BUCKET_25MIB), K)
         n_buckets = -(-Pp // BUCKET_25MIB)
 
+        # ZeRO-1 with the pre-reduction finite check fused in: per-rank flags of
+        # non-finite gradients, on the values the reduction loads anyway
+        flags = torch.zeros(2, dtype=torch.int32, device=dev)
+
+        def checked_step():
+            st.t += 1
+            Z.zero_step_stage12_checked(1, st.grads, st.master, st.m, st.v, st.params,
+                                        Z.hparams(**HP, step=st.t), flags)
+
+        for _ in range(min(W, 3)):
+            checked_step()
+        Kk = min(K, 200)
+        ms_k, _ = timed(torch, world, dev, stream, checked_step, Kk)
+        flag_words = [int(x) for x in flags.cpu().tolist()]
+
         # ZeRO-1 with global-norm clipping: norm pass + coefficient + clipped fused step
         scratch = torch.empty(Z.zero_clip_scratch_bytes() // 8, dtype=torch.float64, device=dev)
         norm_coef = torch.empty(4, dtype=torch.float32, device=dev)[:2]
@@ -492,6 +507,13 @@ def run_gpu(args):
                 "ms_per_step": ms2 / K, "value": world * P * K / (ms2 * 1e-3),
                 "launches_per_step": n_buckets, "bucket_elems": BUCKET_25MIB,
                 "hbm_gbs": bytes_per_step * K / (ms2 * 1e-3) / 1e9,
+            },
+            "checked": {
+                "ms_per_step": ms_k / Kk, "value": world * P * Kk / (ms_k * 1e-3), "steps": Kk,
+                "hbm_gbs": bytes_per_step * Kk / (ms_k * 1e-3) / 1e9,
+                "nonfinite_rank_words": flag_words,
+                "note": "ZeRO-1 with the pre-reduction finite check fused into the reduce-scatter "
+                        "(zero_step_stage12_checked): per-rank flags, the same bytes and bits",
             },
             "clip_reduced": {
                 "ms_per_step": ms_cr / Kc, "value": world * P * Kc / (ms_cr * 1e-3), "steps": Kc,

@@ -27,7 +27,8 @@ _PUBLIC = ("ZERO_DEFAULT_ALIGN", "ZERO_CHUNK_ELEMS", "ZERO_EALIGN", "ZERO_ECUDA"
            "Zero3Graph", "zero_grad_reduce_sqnorm", "zero_step_stage12_reduced",
            "zero3_update_unit_reduced", "zero3_step_f32grads", "zero3_accumulate_unit",
            "zero3_reduce_scatter_unit_accumulated", "zero_reshard_f32", "zero3_plan_microbatch",
-           "zero3_step_microbatch")
+           "zero3_step_microbatch", "zero_step_stage12_checked",
+           "zero3_reduce_scatter_unit_checked")
 
 __all__ = list(_PUBLIC)
 

@@ -110,6 +110,9 @@ SIGNATURES = {
                                             _P]),
     "zero_clip_coef_units_noalloc": (C.c_int, [_P, _I32, _I32, _P, _F64, _P, _P, _P]),
     "zero_grad_nonfinite": (C.c_int, [_I32, _I64, _P, _P, _I32, _P]),
+    "zero_step_stage12_checked": (C.c_int, [_I32, _I32, _I64, _P, _P, _P, _P, _P, _P, _I64, _P,
+                                            _P]),
+    "zero3_reduce_scatter_unit_checked": (C.c_int, [_P, _I32, _P, _P, _P, _P, _P, _P, _P, _P]),
     "zero_step_stage12_f32grads": (C.c_int, [_I32, _I32, _I64, _P, _P, _P, _P, _P, _P, _I64,
                                              _P]),
     "zero3_reduce_scatter_unit_f32grads": (C.c_int, [_P, _I32, _P, _P, _P, _P, _P, _P, _P]),
@@ -441,6 +444,41 @@ def zero_grad_nonfinite(grads, counts, reset=True, stream=None):
     g, rows = _rows(grads, 2, "grads")
     _check("zero_grad_nonfinite", lib.zero_grad_nonfinite(
         len(rows), rows[0].numel(), g, _dev(counts, 4, "counts"), 1 if reset else 0,
+        _stream(stream)))
+
+
+def _flags(nonfinite_ranks):
+    """The finite check's output: a device tensor of two 32-bit words (or more)."""
+    if nonfinite_ranks.numel() * nonfinite_ranks.element_size() < 8:
+        raise ValueError("nonfinite_ranks needs two 32-bit words")
+    return _dev(nonfinite_ranks, 4, "nonfinite_ranks")
+
+
+def zero_step_stage12_checked(stage, grads, master, m, v, params_bf16, hp, nonfinite_ranks,
+                              bucket_elems=0, stream=None):
+    """zero_step_stage12 with the pre-reduction finite check fused in: bit r of
+    nonfinite_ranks (device int32/uint32[2]; word r // 32) is OR-ed in when rank
+    r's gradient holds an infinity or a NaN.  Same results, no extra traffic."""
+    g, grows = _rows(grads, 2, "grads")
+    w, _ = _rows(master, 4, "master")
+    mm, _ = _rows(m, 4, "m")
+    vv, _ = _rows(v, 4, "v")
+    _check("zero_step_stage12_checked", lib.zero_step_stage12_checked(
+        stage, len(grows), grows[0].numel(), g, w, mm, vv, _dev(params_bf16, 2, "params_bf16"),
+        C.byref(hp), int(bucket_elems), _flags(nonfinite_ranks), _stream(stream)))
+
+
+def zero3_reduce_scatter_unit_checked(unit, unit_grads, master, m, v, shard_bf16, hp,
+                                      nonfinite_ranks, stream=None):
+    """zero3_reduce_scatter_unit with the fused finite check (as
+    zero_step_stage12_checked)."""
+    g, grows = _rows(unit_grads, 2, "unit_grads")
+    w, _ = _rows(master, 4, "master")
+    mm, _ = _rows(m, 4, "m")
+    vv, _ = _rows(v, 4, "v")
+    s, _ = _rows(shard_bf16, 2, "shard_bf16")
+    _check("zero3_reduce_scatter_unit_checked", lib.zero3_reduce_scatter_unit_checked(
+        C.byref(unit), len(grows), g, w, mm, vv, s, C.byref(hp), _flags(nonfinite_ranks),
         _stream(stream)))
 
 

@@ -53,12 +53,26 @@ __device__ __forceinline__ void st8_stream(float4* p, const float (&x)[8])
                  : "memory");
 }
 
+// Whether any of the 8 bf16 values in v is infinite or NaN (exponent all
+// ones).  Per 16-bit half, (h & 0x7F80) + 0x0080 reaches 0x8000 exactly when
+// the exponent field is all ones; a half's sum never carries into the other
+// half.
+__device__ __forceinline__ bool nonfinite_bf16x8(uint4 v)
+{
+    constexpr uint32_t kExp = 0x7F807F80u, kOne = 0x00800080u;
+    const uint32_t x = ((v.x & kExp) + kOne) | ((v.y & kExp) + kOne) | ((v.z & kExp) + kOne) |
+                       ((v.w & kExp) + kOne);
+    return (x & 0x80008000u) != 0;
+}
+
 // The reduce-scatter's sum for 8 consecutive elements of vector q: fp32 from
 // +0 over ranks 0..n_ranks-1 in order.  All loads of a batch of `kBatch`
-// ranks are issued before any of them is summed.
-template <int kBatch>
+// ranks are issued before any of them is summed.  kCheck: also set bit r of
+// *bad when rank r's 8 values hold an infinity or a NaN (the sums are the
+// same).
+template <int kBatch, bool kCheck = false>
 __device__ __forceinline__ void sum_ranks(const uint4* const* g, int n_ranks, int64_t q,
-                                          float (&acc)[8])
+                                          float (&acc)[8], uint64_t* bad = nullptr)
 {
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
@@ -70,6 +84,7 @@ __device__ __forceinline__ void sum_ranks(const uint4* const* g, int n_ranks, in
 #pragma unroll
         for (int i = 0; i < kBatch; ++i) {
             if (r0 + i < n_ranks) {
+                if (kCheck && nonfinite_bf16x8(G[i])) *bad |= 1ull << (r0 + i);
                 acc[0] = __fadd_rn(acc[0], bf16_lo(G[i].x));
                 acc[1] = __fadd_rn(acc[1], bf16_hi(G[i].x));
                 acc[2] = __fadd_rn(acc[2], bf16_lo(G[i].y));

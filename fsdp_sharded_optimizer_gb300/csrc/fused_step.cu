@@ -69,6 +69,9 @@ struct Range {
     int64_t step_k, step_j;
     int32_t n_ranks;
     float inv_m; // ZeRO-2 accumulation: 1/micro-batches
+    // kCheck: device uint32[2]; bit r is set when rank r's gradient holds an
+    // infinity or a NaN
+    uint32_t* nonfinite;
 };
 
 __device__ __forceinline__ void adamw(float g, float& w, float& m, float& v,
@@ -118,12 +121,17 @@ __device__ __forceinline__ float ld_coef(const float* clip)
 // kSmall: the four-block launch shape (every step that reads rank gradients);
 // without it the three-block shape of the 16-byte update from the gradient
 // shard.
-template <bool kClip, bool kAcc, bool kF32 = false, bool kG32 = false, bool kSmall = false>
+// kCheck: the pre-reduction finite check of each rank's bf16 gradient, on the
+// values the reduction loads anyway: bit r of R.nonfinite is set when rank r
+// contributed an infinity or a NaN.  The results are unchanged.
+template <bool kClip, bool kAcc, bool kF32 = false, bool kG32 = false, bool kSmall = false,
+          bool kCheck = false>
 __global__ void __launch_bounds__(kBlock, kSmall ? kMinBlocksPerSMSmall : kMinBlocksPerSM)
 fused_step_kernel(const __grid_constant__ Tables T, const StepScalars s, const Range R,
                   const float* __restrict__ clip)
 {
     static_assert(!(kAcc && (kF32 || kG32)), "accumulation reads bf16 rank gradients");
+    static_assert(!(kCheck && (kF32 || kG32)), "the finite check reads bf16 rank gradients");
     // Chained launches (programmatic dependent launch): the next chunk's grid
     // may start as soon as every block of this one is running, so its blocks
     // fill the SMs this grid's tail leaves idle.  Chunks touch disjoint
@@ -139,6 +147,7 @@ fused_step_kernel(const __grid_constant__ Tables T, const StepScalars s, const R
     int64_t k = q / R.shard_vec;     // owner
     int64_t j = q - k * R.shard_vec; // vector position inside the owner's shard
     const int N = R.n_ranks;
+    uint64_t bad = 0; // kCheck: ranks seen with a non-finite gradient
 
     for (; q < R.q1; q += stride) {
         // The gradient of the 8 elements is loaded, summed and scaled before
@@ -162,7 +171,7 @@ fused_step_kernel(const __grid_constant__ Tables T, const StepScalars s, const R
             dev::sum_ranks_f32<kSmall ? kRankBatchSmall / 2 : kRankBatch / 2>(
                 reinterpret_cast<const float4* const*>(T.g), N, q, acc);
         else
-            dev::sum_ranks<kSmall ? kRankBatchSmall : kRankBatch>(T.g, N, q, acc);
+            dev::sum_ranks<kSmall ? kRankBatchSmall : kRankBatch, kCheck>(T.g, N, q, acc, &bad);
         // g = mean (the shard already holds it), then for the last micro-batch
         // (earlier micro-batches + this mean) / m, then times the clip coefficient
         if (kAcc) {
@@ -211,6 +220,10 @@ fused_step_kernel(const __grid_constant__ Tables T, const StepScalars s, const R
             j -= R.shard_vec;
             ++k;
         }
+    }
+    if (kCheck && bad != 0) { // rare: only threads that met a non-finite value
+        if (static_cast<uint32_t>(bad) != 0) atomicOr(R.nonfinite, static_cast<uint32_t>(bad));
+        if ((bad >> 32) != 0) atomicOr(R.nonfinite + 1, static_cast<uint32_t>(bad >> 32));
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
@@ -378,7 +391,8 @@ void log_capture(const void* func, int blocks, const Tables& T, const StepScalar
 // serialization, so it may begin while the previous kernel on the stream (the
 // previous chunk or bucket of the same call, which touches other elements)
 // finishes.
-template <bool kClip, bool kAcc, bool kF32, bool kG32 = false, bool kSmall = false>
+template <bool kClip, bool kAcc, bool kF32, bool kG32 = false, bool kSmall = false,
+          bool kCheck = false>
 cudaError_t launch_fused(int blocks, cudaStream_t stream, bool chained, const Tables& T,
                          const StepScalars& s, const Range& R, const float* clip)
 {
@@ -393,11 +407,11 @@ cudaError_t launch_fused(int blocks, cudaStream_t stream, bool chained, const Ta
     cfg.attrs = attr;
     cfg.numAttrs = chained ? 1 : 0;
     const cudaError_t e = cudaLaunchKernelEx(
-        &cfg, fused_step_kernel<kClip, kAcc, kF32, kG32, kSmall>, T, s, R, clip);
+        &cfg, fused_step_kernel<kClip, kAcc, kF32, kG32, kSmall, kCheck>, T, s, R, clip);
     if (e == cudaSuccess)
-        log_capture(
-            reinterpret_cast<const void*>(fused_step_kernel<kClip, kAcc, kF32, kG32, kSmall>),
-            blocks, T, s, R, clip, stream);
+        log_capture(reinterpret_cast<const void*>(
+                        fused_step_kernel<kClip, kAcc, kF32, kG32, kSmall, kCheck>),
+                    blocks, T, s, R, clip, stream);
     return e;
 }
 
@@ -435,11 +449,23 @@ bool wide_aligned(const Tables& T, int32_t n)
 }
 
 // One launch of a bf16-gradient variant (plain, clipped, last micro-batch of an
-// accumulation), in the four-block shape.
+// accumulation, plain with the finite check), in the four-block shape.
 int launch_bf16(const Tables& T, const StepScalars& s, int64_t q0, int64_t q1, int64_t shard_vec,
-                int32_t n_ranks, const float* clip, cudaStream_t stream, float inv_m, bool chained)
+                int32_t n_ranks, const float* clip, cudaStream_t stream, float inv_m, bool chained,
+                uint32_t* nonfinite)
 {
     const bool acc = inv_m != 0.0f;
+    if (nonfinite) { // the plain step with the finite check
+        if (clip || acc) return ZERO_EINVAL;
+        const void* k =
+            reinterpret_cast<const void*>(fused_step_kernel<false, false, false, false, true, true>);
+        int blocks = 0;
+        Range R = make_range(k, q0, q1, shard_vec, n_ranks, &blocks);
+        if (blocks <= 0) return ZERO_ECUDA;
+        R.nonfinite = nonfinite;
+        return cuda_status(launch_fused<false, false, false, false, true, true>(
+            blocks, stream, chained, T, s, R, nullptr));
+    }
     const void* kernel =
         clip ? (acc ? reinterpret_cast<const void*>(fused_step_kernel<true, true, false, false, true>)
                     : reinterpret_cast<const void*>(fused_step_kernel<true, false, false, false, true>))
@@ -464,8 +490,9 @@ int launch_bf16(const Tables& T, const StepScalars& s, int64_t q0, int64_t q1, i
 // One launch over the vectors [q0, q1).
 int launch_range(const Tables& T, const StepScalars& s, int64_t q0, int64_t q1, int64_t shard_vec,
                  int32_t n_ranks, const float* clip, cudaStream_t stream, float inv_m, bool f32,
-                 bool chained, bool g32)
+                 bool chained, bool g32, uint32_t* nonfinite)
 {
+    if (nonfinite && (f32 || g32)) return ZERO_EINVAL; // the check reads bf16 rank gradients
     if (g32 && wide_aligned(T, n_ranks)) { // the reduced fp32 gradient shard, 32-byte accesses
         const void* k = clip ? reinterpret_cast<const void*>(fused_step_wide_kernel<true>)
                              : reinterpret_cast<const void*>(fused_step_wide_kernel<false>);
@@ -508,7 +535,7 @@ int launch_range(const Tables& T, const StepScalars& s, int64_t q0, int64_t q1, 
     // zero take a slower path through the IEEE division, which more resident
     // warps hide better: all-zero gradients 1.098 -> 0.989 ms, half of them
     // zero 0.921 -> 0.864.
-    return launch_bf16(T, s, q0, q1, shard_vec, n_ranks, clip, stream, inv_m, chained);
+    return launch_bf16(T, s, q0, q1, shard_vec, n_ranks, clip, stream, inv_m, chained, nonfinite);
 }
 
 // The fused step over the vectors [q0, q1), issued as chunk_count() chained
@@ -526,12 +553,12 @@ int launch_range(const Tables& T, const StepScalars& s, int64_t q0, int64_t q1, 
 // same step).
 int launch(const Tables& T, const StepScalars& s, int64_t q0, int64_t q1, int64_t shard_vec,
            int32_t n_ranks, const float* clip, cudaStream_t stream, float inv_m = 0.0f,
-           bool f32 = false, bool chained = false, bool g32 = false)
+           bool f32 = false, bool chained = false, bool g32 = false, uint32_t* nonfinite = nullptr)
 {
     for (int64_t a = q0; a < q1; a += kChunkVec) {
         const int64_t b = q1 - a > kChunkVec ? a + kChunkVec : q1;
         const int rc = launch_range(T, s, a, b, shard_vec, n_ranks, clip, stream, inv_m, f32,
-                                    chained || a > q0, g32);
+                                    chained || a > q0, g32, nonfinite);
         if (rc != ZERO_OK) return rc;
     }
     return ZERO_OK;
@@ -551,7 +578,8 @@ int check_state_tables(int32_t n, const uint16_t* const* grads, float* const* ma
 int step_stage12(int32_t stage, int32_t n_ranks, int64_t n_padded, const void* const* grads,
                  float* const* master, float* const* m, float* const* v, uint16_t* params_bf16,
                  const zero_hparams_t* hp, int64_t bucket_elems, const float* clip,
-                 cudaStream_t stream, bool f32 = false, bool g32 = false)
+                 cudaStream_t stream, bool f32 = false, bool g32 = false,
+                 uint32_t* nonfinite = nullptr)
 {
     // g32: `grads` holds the n_ranks fp32 gradient shards (S each) of the
     // reduced mean gradient instead of the rank gradients.
@@ -584,7 +612,7 @@ int step_stage12(int32_t stage, int32_t n_ranks, int64_t n_padded, const void* c
     for (int64_t q0 = 0; q0 < nvec; q0 += bucket_vec) {
         const int64_t q1 = q0 + bucket_vec < nvec ? q0 + bucket_vec : nvec;
         if ((rc = launch(T, s, q0, q1, shard_vec, n_ranks, clip, stream, 0.0f, f32, q0 > 0,
-                         g32)) != ZERO_OK)
+                         g32, nonfinite)) != ZERO_OK)
             return rc;
     }
     return ZERO_OK;
@@ -605,7 +633,7 @@ bool unit_valid(const zero_unit_t* unit, int32_t n_ranks)
 int rs_unit(const zero_unit_t* unit, int32_t n_ranks, const void* const* unit_grads,
             float* const* master, float* const* m, float* const* v, uint16_t* const* shard_bf16,
             const zero_hparams_t* hp, const float* clip, cudaStream_t stream, bool f32 = false,
-            bool g32 = false, bool chain_first = false)
+            bool g32 = false, bool chain_first = false, uint32_t* nonfinite = nullptr)
 {
     if (!unit_valid(unit, n_ranks) || !valid_hparams(hp)) return ZERO_EINVAL;
     int rc = check_state_tables(n_ranks, reinterpret_cast<const uint16_t* const*>(unit_grads), master, m,
@@ -628,13 +656,20 @@ int rs_unit(const zero_unit_t* unit, int32_t n_ranks, const void* const* unit_gr
     }
     const StepScalars s = make_scalars(hp, n_ranks);
     return launch(T, s, 0, unit->n_padded / 8, unit->shard_len / 8, n_ranks, clip, stream, 0.0f,
-                  f32, chain_first, g32);
+                  f32, chain_first, g32, nonfinite);
 }
 
 int check_clip(const float* norm_coef)
 {
     if (!norm_coef) return ZERO_EINVAL;
     return aligned16(norm_coef) ? ZERO_OK : ZERO_EALIGN;
+}
+
+// The finite check's output: a device uint32[2], 8-byte aligned.
+int check_flags(const uint32_t* nonfinite)
+{
+    if (!nonfinite) return ZERO_EINVAL;
+    return reinterpret_cast<uintptr_t>(nonfinite) % 8 == 0 ? ZERO_OK : ZERO_EALIGN;
 }
 
 } // namespace
@@ -723,6 +758,20 @@ extern "C" int zero_step_stage12(int32_t stage, int32_t n_ranks, int64_t n_padde
                         master, m, v, params_bf16, hp, bucket_elems, nullptr, stream);
 }
 
+extern "C" int zero_step_stage12_checked(int32_t stage, int32_t n_ranks, int64_t n_padded,
+                                         const uint16_t* const* grads, float* const* master,
+                                         float* const* m, float* const* v,
+                                         uint16_t* params_bf16, const zero_hparams_t* hp,
+                                         int64_t bucket_elems, uint32_t* nonfinite_ranks,
+                                         cudaStream_t stream)
+{
+    const int rc = check_flags(nonfinite_ranks);
+    if (rc != ZERO_OK) return rc;
+    return step_stage12(stage, n_ranks, n_padded, reinterpret_cast<const void* const*>(grads),
+                        master, m, v, params_bf16, hp, bucket_elems, nullptr, stream, false, false,
+                        nonfinite_ranks);
+}
+
 extern "C" int zero_step_stage12_clip(int32_t stage, int32_t n_ranks, int64_t n_padded,
                                       const uint16_t* const* grads, float* const* master,
                                       float* const* m, float* const* v, uint16_t* params_bf16,
@@ -772,6 +821,19 @@ extern "C" int zero3_reduce_scatter_unit(const zero_unit_t* unit, int32_t n_rank
 {
     return rs_unit(unit, n_ranks, reinterpret_cast<const void* const*>(unit_grads), master, m, v,
                    shard_bf16, hp, nullptr, stream);
+}
+
+extern "C" int zero3_reduce_scatter_unit_checked(const zero_unit_t* unit, int32_t n_ranks,
+                                                 const uint16_t* const* unit_grads,
+                                                 float* const* master, float* const* m,
+                                                 float* const* v, uint16_t* const* shard_bf16,
+                                                 const zero_hparams_t* hp,
+                                                 uint32_t* nonfinite_ranks, cudaStream_t stream)
+{
+    const int rc = check_flags(nonfinite_ranks);
+    if (rc != ZERO_OK) return rc;
+    return rs_unit(unit, n_ranks, reinterpret_cast<const void* const*>(unit_grads), master, m, v,
+                   shard_bf16, hp, nullptr, stream, false, false, false, nonfinite_ranks);
 }
 
 extern "C" int zero3_reduce_scatter_unit_clip(const zero_unit_t* unit, int32_t n_ranks,

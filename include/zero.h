@@ -692,6 +692,31 @@ int zero3_graph_destroy(zero3_graph_t* graph);
 int zero_grad_nonfinite(int32_t n_ranks, int64_t n_elems, const uint16_t* const* grads,
                         uint32_t* counts, int32_t reset, cudaStream_t stream);
 
+/* zero_step_stage12_checked / zero3_reduce_scatter_unit_checked -- the fused
+ * ZeRO-1/2 step and the ZeRO-3 unit reduce-scatter + AdamW with the same
+ * pre-reduction finite check done on the gradient values the reduction loads
+ * anyway, so it adds no memory traffic ([DDF] "Failure investigation and
+ * recovery": which rank a NaN came from).  The results are those of
+ * zero_step_stage12 / zero3_reduce_scatter_unit bit for bit (a non-finite
+ * gradient propagates by IEEE arithmetic as there; nothing is skipped).
+ *   nonfinite_ranks  device uint32[2], 8-byte aligned: bit r % 32 of word
+ *                    r / 32 is set (OR-ed in) when rank r's gradient of this
+ *                    call holds an infinity or a NaN; bits are never cleared,
+ *                    so the caller zeroes the words (e.g. before each step)
+ *   other arguments as zero_step_stage12 / zero3_reduce_scatter_unit
+ * Only the presence per rank is recorded; zero_grad_nonfinite counts.
+ * ZERO_EINVAL (also for a null nonfinite_ranks) / ZERO_EALIGN / ZERO_ECUDA. */
+int zero_step_stage12_checked(int32_t stage, int32_t n_ranks, int64_t n_padded,
+                              const uint16_t* const* grads, float* const* master,
+                              float* const* m, float* const* v, uint16_t* params_bf16,
+                              const zero_hparams_t* hp, int64_t bucket_elems,
+                              uint32_t* nonfinite_ranks, cudaStream_t stream);
+int zero3_reduce_scatter_unit_checked(const zero_unit_t* unit, int32_t n_ranks,
+                                      const uint16_t* const* unit_grads, float* const* master,
+                                      float* const* m, float* const* v,
+                                      uint16_t* const* shard_bf16, const zero_hparams_t* hp,
+                                      uint32_t* nonfinite_ranks, cudaStream_t stream);
+
 /* ---------------------------------------------------------------------
  * Harness calls: seeded synthetic inputs and helpers.  They are not part
  * of the method; the benchmark and the tests use them to fill device

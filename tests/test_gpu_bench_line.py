@@ -48,6 +48,9 @@ def test_default_line_has_the_contract_keys():
     assert e["h2d_bytes_per_step"] == 8 * 124_440_064 * 2 and e["d2h_bytes_per_step"] == 124_440_064 * 2
     assert 0 < e["value"] < d["value"]
     assert d["clocks"]["sm_mhz"] is None or d["clocks"]["sm_mhz"] > 0
+    # the step with the fused finite check: finite synthetic gradients, no rank flagged
+    k = d["checked"]
+    assert k["ms_per_step"] > 0 and k["nonfinite_rank_words"] == [0, 0]
 
 
 def test_zero3_line_reports_the_step_its_graph_and_the_fused_kernel():

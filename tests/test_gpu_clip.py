@@ -236,6 +236,108 @@ def test_nonfinite_counts_match_oracle(orc):
     np.testing.assert_array_equal(counts.cpu().numpy().astype(np.uint32), ref)
 
 
+def _nan_aware_equal(g, r, what):
+    """Bit for bit, except that any NaN matches any NaN (payloads are the
+    hardware's choice; the bf16 weight of a NaN is 0x7FC0 on both sides)."""
+    g, r = np.asarray(g), np.asarray(r)
+    assert np.array_equal(np.isnan(g), np.isnan(r)), what
+    keep = ~np.isnan(g)
+    np.testing.assert_array_equal(g.view(np.uint32)[keep], r.view(np.uint32)[keep], err_msg=what)
+
+
+@pytest.mark.parametrize("N,P,stage,bucket", [(8, 300_001, 1, 0), (64, 2**16 + 37, 2, 1024),
+                                              (3, 2 * B.ZERO_CHUNK_ELEMS + 1000, 1, 0),
+                                              (33, 100_003, 2, 0)])
+def test_checked_step_flags_the_ranks_and_keeps_the_bits(orc, N, P, stage, bucket):
+    """zero_step_stage12_checked over 3 steps, with infinities and NaNs planted
+    in some ranks' gradients from step 2 on: after each step the flag words
+    name exactly the ranks whose gradients of that step hold a non-finite
+    value (the oracle's per-rank count > 0), and the state and weights equal
+    the oracle's steps on the same gradients (any NaN matching any NaN) and the
+    unchecked GPU step's bit for bit."""
+    T, seed = 3, 21
+    (u,), _ = B.zero_layout([P], N)
+    S = u.shard_len
+    grads = torch.empty((N, u.n_padded), dtype=torch.int16, device="cuda")
+    master = torch.empty((N, S), dtype=torch.float32, device="cuda")
+    B.zero_gen_master(seed, H.SIGMA_W, [u], master)
+    m, v = torch.zeros_like(master), torch.zeros_like(master)
+    params = torch.zeros(u.n_padded, dtype=torch.int16, device="cuda")
+    plain = [master.clone(), m.clone(), v.clone(), params.clone()]  # the unchecked step's copy
+    (ou,), _ = orc.layout([P], N)
+    rw = orc.gen_master(seed, H.SIGMA_W, [ou], N)
+    rm, rv = np.zeros_like(rw), np.zeros_like(rw)
+    rp = np.zeros(ou.n_padded, np.uint16)
+    flags = torch.zeros(2, dtype=torch.int32, device="cuda")
+    rng = np.random.default_rng(N)
+    specials = np.array([0x7F80, 0xFF80, 0x7FC0, 0xFFC1, 0x7F81], np.uint16)
+    for t in range(1, T + 1):
+        B.zero_gen_grads_unit(seed, t, H.SIGMA_G, 1, u, grads)
+        torch.cuda.synchronize()
+        host = grads.cpu().numpy().view(np.uint16).copy()
+        if t > 1:
+            for r in rng.choice(N, size=min(N, 2 * t - 1), replace=False):
+                pos = rng.choice(P, size=int(rng.integers(1, 4)), replace=False)
+                host[r, pos] = rng.choice(specials, size=pos.size)
+            grads.copy_(torch.from_numpy(host.view(np.int16)))
+        flags.zero_()
+        B.zero_step_stage12_checked(stage, grads, master, m, v, params, H.hp(t), flags, bucket)
+        B.zero_step_stage12(stage, grads, *plain, H.hp(t), bucket)
+        orc.zero12_step(stage, host, rw, rm, rv, rp, orc.hparams(**H.HP, step=t), bucket)
+        torch.cuda.synchronize()
+        words = flags.cpu().numpy().view(np.uint32)
+        got = {r for r in range(N) if (int(words[r // 32]) >> (r % 32)) & 1}
+        want = set(np.flatnonzero(orc.grad_nonfinite(host)).tolist())
+        assert got == want, (t, sorted(got), sorted(want))
+        assert (t == 1) == (not want)
+    for name, g, r, q in (("master", master, rw, plain[0]), ("m", m, rm, plain[1]),
+                          ("v", v, rv, plain[2])):
+        g = g.cpu().numpy()
+        _nan_aware_equal(g, r, name)
+        H.assert_bitwise(g, q.cpu().numpy(), name + " (unchecked)")
+    gp = params.cpu().numpy().view(np.uint16)
+    H.assert_bitwise(gp, rp, "params")
+    H.assert_bitwise(gp, plain[3].cpu().numpy().view(np.uint16), "params (unchecked)")
+    del grads, master, m, v, params, plain
+    H.free()
+
+
+def test_checked_unit_update_flags_the_ranks(orc):
+    """zero3_reduce_scatter_unit_checked on two units of a ZeRO-3 layout: the
+    flags OR over the calls, and the unit's shards and state equal the
+    unchecked call's bit for bit."""
+    N, sizes, seed = 8, [40_000, 3 * B.ZERO_CHUNK_ELEMS // 2 + 77], 5
+    units, total = B.zero_layout(sizes, N)
+    St = total // N
+    g = torch.empty((N, total), dtype=torch.int16, device="cuda")
+    for u in units:
+        B.zero_gen_grads_unit(seed, 1, H.SIGMA_G, 0, u, [g[r, u.offset:u.offset + u.n_padded]
+                                                        for r in range(N)])
+    torch.cuda.synchronize()
+    host = g.cpu().numpy().view(np.uint16).copy()
+    host[2, units[0].offset + 17] = 0x7FC0                        # rank 2, unit 0
+    host[5, units[1].offset + units[1].n_params - 1] = 0xFF80     # rank 5, unit 1, its last one
+    g.copy_(torch.from_numpy(host.view(np.int16)))
+    w = torch.empty((N, St), dtype=torch.float32, device="cuda")
+    B.zero_gen_master(seed, H.SIGMA_W, units, w)
+    state = [w, torch.zeros_like(w), torch.zeros_like(w), torch.zeros((N, St), dtype=torch.int16,
+                                                                      device="cuda")]
+    plain = [x.clone() for x in state]
+    flags = torch.zeros(2, dtype=torch.int32, device="cuda")
+    seen = []
+    for u in units:
+        rows = [g[r, u.offset:u.offset + u.n_padded] for r in range(N)]
+        B.zero3_reduce_scatter_unit_checked(u, rows, *state, H.hp(1), flags)
+        B.zero3_reduce_scatter_unit(u, rows, *plain, H.hp(1))
+        torch.cuda.synchronize()
+        seen.append(int(flags.cpu().numpy().view(np.uint32)[0]))
+    assert seen == [1 << 2, (1 << 2) | (1 << 5)]
+    for name, a, b in zip(("master", "m", "v", "shards"), state, plain):
+        H.assert_bitwise(a.cpu().numpy(), b.cpu().numpy(), name)
+    del g, state, plain
+    H.free()
+
+
 @pytest.mark.parametrize("stage,N,P,bucket,max_norm", [(1, 2, 2**20, 0, 1e-3), (2, 8, 300_001, 104, 2e-3),
                                                        (1, 64, 2**16 + 37, 0, 1e-4),
                                                        (1, 4, 2 * B.ZERO_CHUNK_ELEMS + 1000, 0, 1e-3),

@@ -153,6 +153,45 @@ def test_step_rejects_before_launch(B):
 
 
 @host_only
+def test_checked_step_rejects_before_launch(B):
+    """The steps with the fused finite check validate like the plain ones and
+    also need their two-word output, 8-byte aligned."""
+    hp = B.hparams()
+    g = _table(A16[:8])
+    w, m, v = _table(A16[8:16]), _table(A16[16:24]), _table(A16[24:32])
+    p = C.c_void_p(0x900000)
+    flags = C.c_void_p(0xA00000)
+    call = B.lib.zero_step_stage12_checked
+    assert call(1, 8, 1024, g, w, m, v, p, C.byref(hp), 0, None, None) == B.ZERO_EINVAL
+    assert call(1, 8, 1024, g, w, m, v, p, C.byref(hp), 0, C.c_void_p(0xA00004),
+                None) == B.ZERO_EALIGN
+    assert call(3, 8, 1024, g, w, m, v, p, C.byref(hp), 0, flags, None) == B.ZERO_EINVAL
+    assert call(1, 8, 1000, g, w, m, v, p, C.byref(hp), 0, flags, None) == B.ZERO_EINVAL
+    assert call(1, 8, 1024, None, w, m, v, p, C.byref(hp), 0, flags, None) == B.ZERO_EINVAL
+    assert call(1, 8, 1024, g, w, m, v, p, C.byref(B.hparams(step=0)), 0, flags,
+                None) == B.ZERO_EINVAL
+    odd = _table(A16[:7] + [A16[7] + 8])
+    assert call(1, 8, 1024, odd, w, m, v, p, C.byref(hp), 0, flags, None) == B.ZERO_EALIGN
+    (u,), _ = B.zero_layout([1000], 8)
+    s16 = _table(A16[32:40])
+    ucall = B.lib.zero3_reduce_scatter_unit_checked
+    assert ucall(C.byref(u), 8, g, w, m, v, s16, C.byref(hp), None, None) == B.ZERO_EINVAL
+    assert ucall(C.byref(u), 8, g, w, m, v, s16, C.byref(hp), C.c_void_p(0xA00004),
+                 None) == B.ZERO_EALIGN
+    assert ucall(C.byref(u), 4, g, w, m, v, s16, C.byref(hp), flags, None) == B.ZERO_EINVAL
+    assert ucall(None, 8, g, w, m, v, s16, C.byref(hp), flags, None) == B.ZERO_EINVAL
+
+
+def test_checked_step_wrapper_needs_two_words(B):
+    """The Python wrapper rejects an output of fewer than two 32-bit words
+    before calling the library."""
+    import torch
+    one = torch.zeros(1, dtype=torch.int32, pin_memory=False)
+    with pytest.raises(ValueError):
+        B._flags(one)
+
+
+@host_only
 def test_zero3_calls_reject_before_launch(B):
     (u,), _ = B.zero_layout([1000], 4)
     hp = B.hparams()
