@@ -302,6 +302,46 @@ def test_checked_step_flags_the_ranks_and_keeps_the_bits(orc, N, P, stage, bucke
     H.free()
 
 
+def test_checked_step_classifies_every_bf16_pattern():
+    """The fused check against every bf16 bit pattern: all 65,536 spread over
+    64 ranks (1,024 each) flag exactly the two ranks that hold the patterns
+    with an all-ones exponent (infinities and NaNs, both signs), and each of
+    those 256 patterns alone, at a random position of rank i % 64's gradient,
+    flags exactly that rank."""
+    N = 64
+    (u,), _ = B.zero_layout([65_536], N)
+    P = u.n_padded
+    pats = np.arange(65_536, dtype=np.uint32).astype(np.uint16)
+    nonfinite = (pats & 0x7F80) == 0x7F80
+    assert nonfinite.sum() == 256
+    host = np.zeros((N, P), np.uint16)
+    for r in range(N):
+        host[r, :1024] = pats[r * 1024:(r + 1) * 1024]
+    grads = torch.from_numpy(host.view(np.int16)).cuda()
+    w = torch.zeros((N, u.shard_len), dtype=torch.float32, device="cuda")
+    m, v = torch.zeros_like(w), torch.zeros_like(w)
+    params = torch.zeros(P, dtype=torch.int16, device="cuda")
+    flags = torch.zeros(2, dtype=torch.int32, device="cuda")
+    B.zero_step_stage12_checked(1, grads, w, m, v, params, H.hp(1), flags)
+    words = flags.cpu().numpy().view(np.uint32)
+    got = {r for r in range(N) if (int(words[r // 32]) >> (r % 32)) & 1}
+    want = {int(i) // 1024 for i in np.flatnonzero(nonfinite)}
+    assert got == want == {31, 63}
+    rng = np.random.default_rng(7)
+    for i, pat in enumerate(pats[nonfinite]):
+        r = i % N
+        host[:] = 0
+        host[r, rng.integers(0, P)] = pat
+        grads.copy_(torch.from_numpy(host.view(np.int16)))
+        flags.zero_()
+        B.zero_step_stage12_checked(1, grads, w, m, v, params, H.hp(1), flags)
+        words = flags.cpu().numpy().view(np.uint32)
+        assert [int(words[0]), int(words[1])] == [(1 << r) if r < 32 else 0,
+                                                  (1 << (r - 32)) if r >= 32 else 0], hex(pat)
+    del grads, w, m, v, params
+    H.free()
+
+
 def test_checked_unit_update_flags_the_ranks(orc):
     """zero3_reduce_scatter_unit_checked on two units of a ZeRO-3 layout: the
     flags OR over the calls, and the unit's shards and state equal the
