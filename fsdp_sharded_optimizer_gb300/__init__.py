@@ -28,7 +28,7 @@ _PUBLIC = ("ZERO_DEFAULT_ALIGN", "ZERO_CHUNK_ELEMS", "ZERO_EALIGN", "ZERO_ECUDA"
            "zero3_update_unit_reduced", "zero3_step_f32grads", "zero3_accumulate_unit",
            "zero3_reduce_scatter_unit_accumulated", "zero_reshard_f32", "zero3_plan_microbatch",
            "zero3_step_microbatch", "zero_step_stage12_checked",
-           "zero3_reduce_scatter_unit_checked")
+           "zero3_reduce_scatter_unit_checked", "zero3_step_checked")
 
 __all__ = list(_PUBLIC)
 

@@ -113,6 +113,8 @@ SIGNATURES = {
     "zero_step_stage12_checked": (C.c_int, [_I32, _I32, _I64, _P, _P, _P, _P, _P, _P, _I64, _P,
                                             _P]),
     "zero3_reduce_scatter_unit_checked": (C.c_int, [_P, _I32, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "zero3_step_checked": (C.c_int, [_P, _I32, _I32, _P, _I32, _P, _P, _P, _P, _P, _P, _P, _P,
+                                     _I32, _P, _P, _P]),
     "zero_step_stage12_f32grads": (C.c_int, [_I32, _I32, _I64, _P, _P, _P, _P, _P, _P, _I64,
                                              _P]),
     "zero3_reduce_scatter_unit_f32grads": (C.c_int, [_P, _I32, _P, _P, _P, _P, _P, _P, _P]),
@@ -572,6 +574,26 @@ def zero3_step(units, grads, master, m, v, shard_bf16, full_a, full_b, hp, grads
         C.byref(hp),
         C.byref(regen) if regen is not None else None, C.byref(clip) if clip is not None else None,
         1 if reshard_after_forward else 0, _stream(main_stream), _stream(side_stream)))
+
+
+def zero3_step_checked(units, grads, master, m, v, shard_bf16, full_a, full_b, hp,
+                       nonfinite_ranks, grads_resident=True, regen=None,
+                       reshard_after_forward=True, main_stream=None, side_stream=None):
+    """zero3_step (no clipping) with the fused pre-reduction finite check:
+    bit r of nonfinite_ranks (device int32/uint32[2], word r // 32) is OR-ed in
+    when rank r's gradient of any unit holds an infinity or a NaN."""
+    g, rows = _rows(grads, 2, "grads")
+    w, _ = _rows(master, 4, "master")
+    mm, _ = _rows(m, 4, "m")
+    vv, _ = _rows(v, 4, "v")
+    s, _ = _rows(shard_bf16, 2, "shard_bf16")
+    arr = (zero_unit_t * len(units))(*units)
+    _check("zero3_step_checked", lib.zero3_step_checked(
+        arr, len(units), len(rows), g, 1 if grads_resident else 0, w, mm, vv, s,
+        _dev(full_a, 2, "full_a"), _dev(full_b, 2, "full_b") if full_b is not None else None,
+        C.byref(hp), C.byref(regen) if regen is not None else None,
+        1 if reshard_after_forward else 0, _flags(nonfinite_ranks), _stream(main_stream),
+        _stream(side_stream)))
 
 
 def zero3_step_f32grads(units, grads, master, m, v, shard_bf16, full_a, full_b, hp,

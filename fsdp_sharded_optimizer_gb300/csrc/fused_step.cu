@@ -677,14 +677,18 @@ int check_flags(const uint32_t* nonfinite)
 int unit_update(const zero_unit_t* unit, int32_t n_ranks, const void* const* grads,
                 float* const* master, float* const* m, float* const* v,
                 uint16_t* const* shard_bf16, const zero_hparams_t* hp, const float* clip,
-                cudaStream_t stream, bool f32, bool g32, bool chain_first)
+                cudaStream_t stream, bool f32, bool g32, bool chain_first, uint32_t* nonfinite)
 {
     if (clip) {
         const int rc = check_clip(clip);
         if (rc != ZERO_OK) return rc;
     }
+    if (nonfinite) {
+        const int rc = check_flags(nonfinite);
+        if (rc != ZERO_OK) return rc;
+    }
     return rs_unit(unit, n_ranks, grads, master, m, v, shard_bf16, hp, clip, stream, f32, g32,
-                   chain_first);
+                   chain_first, nonfinite);
 }
 
 StepNodeList* step_nodes_begin()

@@ -278,7 +278,7 @@ int run_step(const zero_unit_t* units, int32_t n_units, int32_t n_ranks, const v
              float* const* v, uint16_t* const* shard_bf16, uint16_t* full_a, uint16_t* full_b,
              const zero_hparams_t* hp, const zero_regen_t* regen, const zero_clip_t* clip,
              int32_t reshard_after_forward, cudaStream_t main_stream, cudaStream_t side_stream,
-             const AccumArgs* acc = nullptr)
+             const AccumArgs* acc = nullptr, uint32_t* nonfinite = nullptr)
 {
     const bool reshard = reshard_after_forward != 0;
     if (!units || n_units < 1 || n_ranks < 1 || n_ranks > ZERO_MAX_RANKS || !valid_hparams(hp) ||
@@ -303,6 +303,8 @@ int run_step(const zero_unit_t* units, int32_t n_units, int32_t n_ranks, const v
             return rc;
     }
 
+    // the fused finite check: the plain step from bf16 rank gradients only
+    if (nonfinite && (f32 || clip || acc)) return ZERO_EINVAL;
     if (acc) {
         // accumulation: bf16 rank gradients, no clipping
         if (f32 || clip || acc->micro_batches < 1 || acc->micro_batch < 0 ||
@@ -406,7 +408,7 @@ int run_step(const zero_unit_t* units, int32_t n_units, int32_t n_ranks, const v
                 rc = unit_update(&units[op.unit], n_ranks,
                                  reinterpret_cast<const void* const*>(unit_grads), master, m, v,
                                  shard_bf16, hp, op.arg ? clip->norm_coef : nullptr, s, false,
-                                 false, chain_update);
+                                 false, chain_update, nonfinite);
             break;
         case ZERO_OP_NORM:
             grads_of(op.unit);
@@ -447,6 +449,22 @@ extern "C" int zero3_step(const zero_unit_t* units, int32_t n_units, int32_t n_r
     return run_step(units, n_units, n_ranks, reinterpret_cast<const void* const*>(grads), false,
                     grads_resident, master, m, v, shard_bf16, full_a, full_b, hp, regen, clip,
                     reshard_after_forward, main_stream, side_stream);
+}
+
+extern "C" int zero3_step_checked(const zero_unit_t* units, int32_t n_units, int32_t n_ranks,
+                                  const uint16_t* const* grads, int32_t grads_resident,
+                                  float* const* master, float* const* m, float* const* v,
+                                  uint16_t* const* shard_bf16, uint16_t* full_a,
+                                  uint16_t* full_b, const zero_hparams_t* hp,
+                                  const zero_regen_t* regen, int32_t reshard_after_forward,
+                                  uint32_t* nonfinite_ranks, cudaStream_t main_stream,
+                                  cudaStream_t side_stream)
+{
+    if (!nonfinite_ranks) return ZERO_EINVAL;
+    if (reinterpret_cast<uintptr_t>(nonfinite_ranks) % 8 != 0) return ZERO_EALIGN;
+    return run_step(units, n_units, n_ranks, reinterpret_cast<const void* const*>(grads), false,
+                    grads_resident, master, m, v, shard_bf16, full_a, full_b, hp, regen, nullptr,
+                    reshard_after_forward, main_stream, side_stream, nullptr, nonfinite_ranks);
 }
 
 extern "C" int zero3_step_microbatch(const zero_unit_t* units, int32_t n_units, int32_t n_ranks,

@@ -78,10 +78,13 @@ int grad_reduce_sqnorm(int32_t n_ranks, int64_t n_elems, const uint16_t* const* 
 // `stream` was another unit's update and nothing else has been issued on it
 // since (no event record or wait); the first chunk is then chained to it
 // (programmatic dependent launch; the units touch disjoint elements).
+// nonfinite: nullptr, or the device flag words of the fused finite check
+// (bf16 rank gradients without clipping only).
 int unit_update(const zero_unit_t* unit, int32_t n_ranks, const void* const* grads,
                 float* const* master, float* const* m, float* const* v,
                 uint16_t* const* shard_bf16, const zero_hparams_t* hp, const float* clip,
-                cudaStream_t stream, bool f32, bool g32, bool chain_first);
+                cudaStream_t stream, bool f32, bool g32, bool chain_first,
+                uint32_t* nonfinite = nullptr);
 
 // CUDA-graph support (zero3_graph).  Between step_nodes_begin and
 // step_nodes_end, every fused-step launch made on this thread into a stream

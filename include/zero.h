@@ -605,6 +605,22 @@ int zero3_step_f32grads(const zero_unit_t* units, int32_t n_units, int32_t n_ran
                         int32_t reshard_after_forward, cudaStream_t main_stream,
                         cudaStream_t side_stream);
 
+/* zero3_step_checked -- zero3_step (without clipping) whose per-unit
+ * reduce-scatters carry the fused pre-reduction finite check of
+ * zero_step_stage12_checked ([DDF] "Failure investigation and recovery"):
+ * bit r of nonfinite_ranks (device uint32[2], 8-byte aligned, zeroed by the
+ * caller) is OR-ed in when rank r's gradient of any unit holds an infinity or
+ * a NaN.  The results are zero3_step's bit for bit.  Arguments as zero3_step;
+ * ZERO_EINVAL also for a null nonfinite_ranks, ZERO_EALIGN when it is not
+ * 8-byte aligned (both before anything is issued). */
+int zero3_step_checked(const zero_unit_t* units, int32_t n_units, int32_t n_ranks,
+                       const uint16_t* const* grads, int32_t grads_resident,
+                       float* const* master, float* const* m, float* const* v,
+                       uint16_t* const* shard_bf16, uint16_t* full_a, uint16_t* full_b,
+                       const zero_hparams_t* hp, const zero_regen_t* regen,
+                       int32_t reshard_after_forward, uint32_t* nonfinite_ranks,
+                       cudaStream_t main_stream, cudaStream_t side_stream);
+
 /* zero3_step_microbatch -- one micro-batch of a ZeRO-3 step with gradient
  * accumulation ([DZF] "Gradient accumulation", the 3mP row: both gathers and
  * the reduce-scatter in every micro-batch): zero3_plan_microbatch's

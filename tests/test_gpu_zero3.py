@@ -187,6 +187,66 @@ def test_native_zero3_step_matches_ddp(orc, resident):
     H.assert_gathered(units, sizes, before, fa, fb)
 
 
+@pytest.mark.parametrize("reshard", [True, False])
+def test_native_zero3_step_checked_flags_the_ranks(orc, reshard):
+    """zero3_step_checked over 3 steps with infinities and NaNs planted in some
+    (unit, rank) gradients from step 2 on: after each step the flag words name
+    exactly the ranks whose gradient of any unit holds a non-finite value (the
+    oracle's per-rank count > 0), and the shards, state and full-unit buffers
+    equal zero3_step's on the same inputs bit for bit, with resharding after
+    the forward pass and without."""
+    N, sizes, T, seed = 40, [70_000, 333, B.ZERO_CHUNK_ELEMS + 4_321, 90_001], 3, 6
+    units, total = B.zero_layout(sizes, N)
+    bufs = _native_buffers(units, total, N, True, seed)
+    plain = [H.Guarded(N, total // N, torch.float32) for _ in range(3)] + \
+        [H.Guarded(N, total // N, torch.int16)]
+    for dst, src in zip(plain, bufs[:4]):
+        dst.full.copy_(src.full)
+    master, m, v, shards, grads, fa, fb = bufs
+    kept = [H.Guarded(1, total, torch.int16) for _ in range(2)] if not reshard else None
+    full = (kept[0].rows[0], None, kept[1].rows[0], None) if kept else \
+        (fa.rows[0], fb.rows[0], H.Guarded(1, fa.length, torch.int16).rows[0],
+         H.Guarded(1, fb.length, torch.int16).rows[0])
+    side = torch.cuda.Stream()
+    flags = torch.zeros(2, dtype=torch.int32, device="cuda")
+    rng = np.random.default_rng(11)
+    specials = np.array([0x7F80, 0xFF80, 0x7FC0, 0xFFC1], np.uint16)
+    for t in range(1, T + 1):
+        for u in units:
+            B.zero_gen_grads_unit(seed, t, H.SIGMA_G, 1, u,
+                                  [r[u.offset:u.offset + u.n_padded] for r in grads.rows])
+        torch.cuda.synchronize()
+        host = grads.numpy().copy()
+        want = set()
+        if t > 1:
+            for _ in range(3):
+                ui, r = int(rng.integers(len(units))), int(rng.integers(N))
+                u = units[ui]
+                host[r, u.offset + int(rng.integers(u.n_params))] = rng.choice(specials)
+                want.add(r)
+            for r in range(N):
+                grads.rows[r].copy_(torch.from_numpy(host[r].view(np.int16)))
+        assert set(np.flatnonzero(orc.grad_nonfinite(host)).tolist()) == want
+        flags.zero_()
+        B.zero3_step_checked(units, grads.rows, master.rows, m.rows, v.rows, shards.rows,
+                             full[0], full[1], H.hp(t), flags, reshard_after_forward=reshard,
+                             side_stream=side)
+        B.zero3_step(units, grads.rows, *(b.rows for b in plain), full[2], full[3], H.hp(t),
+                     reshard_after_forward=reshard, side_stream=side)
+        torch.cuda.synchronize()
+        words = flags.cpu().numpy().view(np.uint32)
+        got = {r for r in range(N) if (int(words[r // 32]) >> (r % 32)) & 1}
+        assert got == want, (t, sorted(got), sorted(want))
+    for name, a, b in zip(("master", "m", "v", "shards"), (master, m, v, shards), plain):
+        a.check()
+        H.assert_bitwise(a.numpy(), b.numpy(), name)
+    H.assert_bitwise(full[0].cpu().numpy(), full[2].cpu().numpy(), "full buffer a")
+    if reshard:
+        H.assert_bitwise(full[1].cpu().numpy(), full[3].cpu().numpy(), "full buffer b")
+    del bufs, plain, kept
+    H.free()
+
+
 def test_native_zero3_step_rejects():
     units, total = B.zero_layout([1000, 64], 2)
     master, m, v, shards, grads, fa, fb = _native_buffers(units, total, 2, True)

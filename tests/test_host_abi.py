@@ -288,6 +288,18 @@ def test_zero3_step_rejects_before_launch(B):
     assert mb(arr, 2, 4, t, _table(A16[:3] + [A16[3] + 4]), 1, 3, t, t, t, t, fa, fb,
               C.byref(hp), 1, s1, s2) == B.ZERO_EALIGN
     assert mb(arr, 2, 4, t, t, 0, 2, t, t, t, t, fa, fb, C.byref(hp), 1, s1, s1) == B.ZERO_EINVAL
+    # the ZeRO-3 step with the fused finite check: units, n, ranks, grads, resident, w, m, v,
+    # shards, full_a, full_b, hp, regen, reshard, flags, main, side
+    ck = B.lib.zero3_step_checked
+    flags = C.c_void_p(0xB00000)
+    assert ck(arr, 2, 4, t, 1, t, t, t, t, fa, fb, C.byref(hp), None, 1, None, s1,
+              s2) == B.ZERO_EINVAL
+    assert ck(arr, 2, 4, t, 1, t, t, t, t, fa, fb, C.byref(hp), None, 1, C.c_void_p(0xB00004), s1,
+              s2) == B.ZERO_EALIGN
+    assert ck(arr, 2, 4, t, 0, t, t, t, t, fa, fb, C.byref(hp), None, 1, flags, s1,
+              s2) == B.ZERO_EINVAL   # nothing fills grads
+    assert ck(arr, 2, 4, t, 1, t, t, t, t, fa, fb, C.byref(hp), None, 1, flags, s1,
+              s1) == B.ZERO_EINVAL   # one stream
 
 
 @host_only
